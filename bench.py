@@ -1,0 +1,333 @@
+"""Benchmark: U-Net denoise megapixels/s at 1080p fp16 on GB300.
+
+Workload: full OIDN-shaped U-Net denoise of a 1920x1080 image (colour,
+albedo, normal; HDR, log transfer, inputScale 1), fp16 storage with fp32
+accumulation, whole image as one 1920x1088 tile.  Inputs are seeded
+synthetic images (see synth/).  One step = one oidnx_filter_execute (input
+pass, 16 conv kernels, output pass).  L2 is flushed (a 256 MiB write)
+before every timed step; the flush is outside the per-step CUDA events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank denoises its own frame:
+replicas, weak scaling, no collective on the data path.
+`--impl reference` times the CPU oracle (the pages' computation restated in
+numpy float64) on a bounded crop of the same workload.
+"""
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "U-Net denoise megapixels/s at 1080p fp16 on 1 GB300; conv TFLOP/s vs FP16 peak"
+WIDTH, HEIGHT = 1920, 1080
+WORKLOAD = "OIDN-shaped U-Net denoise, 1920x1080 HDR colour+albedo+normal (9 ch), fp16, single tile"
+CPU_CROP = 768          # oracle sample: a 768x768 crop denoised as one tile
+FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def cpu_oracle_sample(steps=1):
+    """Oracle denoise of a CPU_CROP x CPU_CROP crop of the bench inputs."""
+    import synth
+    from oracle import unet
+    imgs = [im[:CPU_CROP, :CPU_CROP].copy() for im in synth.denoise_inputs(WIDTH, HEIGHT, 3, hdr=True)]
+    weights = synth.unet_weights(9)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        unet.denoise(imgs, weights, hdr=True, input_scale=1.0, precision="fp16")
+        times.append(time.perf_counter() - t0)
+    px = CPU_CROP * CPU_CROP
+    return {"value": px / 1e6 / float(np.mean(times)), "unit": "MP/s", "cores": _cpu_threads(),
+            "kind": "oracle",
+            "sample": f"oracle (numpy float64) denoise of one {CPU_CROP}x{CPU_CROP} crop of the "
+                      f"1920x1080 inputs as one tile, fp16 storage; {steps} run(s)",
+            "seconds": float(np.mean(times))}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(ms_per_rank, px_per_rank):
+    """Whole-job throughput: all ranks' pixels over the slowest rank's time."""
+    slowest = max(ms_per_rank)
+    return sum(px_per_rank) / 1e6 / (slowest / 1e3), slowest
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; warm-up steps do no work
+    cpu = cpu_oracle_sample(args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "MP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": cpu["seconds"] * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": f"{CPU_CROP}x{CPU_CROP} crop per step",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": cpu["value"], "unit": "MP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    import conv2d_implicit_gemm_gb300 as ox
+    import synth
+
+    imgs = synth.denoise_inputs(WIDTH, HEIGHT, 3, hdr=True)
+    weights = synth.unet_weights(9)
+    f = ox.oidnx_filter_create(ox.write_weight_blob(weights), ox.PRECISION_FP16)
+    d_imgs = [torch.from_numpy(im).cuda() for im in imgs]
+    d_out = torch.zeros((HEIGHT, WIDTH, 4), dtype=torch.float32, device="cuda")
+    for i, t in enumerate(d_imgs):
+        ox.oidnx_filter_set_image(f, i, t.data_ptr(), 0)
+    ox.oidnx_filter_set_image(f, ox.IMAGE_OUTPUT, d_out.data_ptr(), 0)
+    ox.oidnx_filter_set_int(f, "width", WIDTH)
+    ox.oidnx_filter_set_int(f, "height", HEIGHT)
+    ox.oidnx_filter_set_int(f, "hdr", 1)
+    ox.oidnx_filter_set_int(f, "transfer", ox.TRANSFER_LOG)
+    ox.oidnx_filter_set_float(f, "inputScale", 1.0)
+    ox.oidnx_filter_set_int(f, "profile", 1)   # per-kernel events inside the graph
+    ox.oidnx_filter_commit(f)
+    tiles = ox.oidnx_filter_get_int(f, "tiles")
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        ox.oidnx_filter_execute(f, sptr)
+    ox.oidnx_filter_sync_status(f)
+
+    layer_ms, layer_flop, layer_bytes = {}, {}, {}
+    step_ms = []
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clocks:
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            starts[k].record(stream)
+            ox.oidnx_filter_execute(f, sptr)
+            ends[k].record(stream)
+            prof = ox.oidnx_get_profile(f)   # waits for this step's events
+            for l in prof["layers"]:
+                layer_ms[l["id"]] = layer_ms.get(l["id"], 0.0) + l["ms"]
+                layer_flop[l["id"]] = l["flop"]
+                layer_bytes[l["id"]] = l["bytes"]
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ox.oidnx_filter_sync_status(f)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_ms = float(np.mean(step_ms))
+
+    # end to end through the host-buffer call: H2D inputs, denoise, D2H output
+    pinned = [torch.from_numpy(im).pin_memory() for im in imgs]
+    host_out = torch.empty((HEIGHT, WIDTH, 4), dtype=torch.float32).pin_memory()
+    ox.oidnx_filter_set_int(f, "profile", 0)
+    host_ptr = [p.data_ptr() for p in pinned]
+    for _ in range(3):
+        ox._check(ox._lib.oidnx_filter_execute_host(f, *host_ptr, host_out.data_ptr(), sptr))
+    e2e_ms = []
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ox._check(ox._lib.oidnx_filter_execute_host(f, *host_ptr, host_out.data_ptr(), sptr))
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    ox.oidnx_filter_release(f)
+
+    px = WIDTH * HEIGHT
+    if world > 1:
+        t = torch.tensor([mean_ms, float(np.mean(e2e_ms))], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_ms, e2e_mean = float(t[0]), float(t[1])
+    else:
+        e2e_mean = float(np.mean(e2e_ms))
+    value, _ = aggregate([mean_ms] * world, [px] * world)
+    e2e_value, _ = aggregate([e2e_mean] * world, [px] * world)
+
+    steps = args.steps
+    avg = {k: v / steps for k, v in layer_ms.items()}
+    conv_ids = [k for k in avg if k not in ("input-pack", "output")]
+    conv_ms = sum(avg[k] for k in conv_ids)
+    conv_flop = sum(layer_flop[k] for k in conv_ids)
+    peaks = _peaks()
+    tensor_peak = peaks["bf16_tflops_sustained"]   # fp16 dense rate = bf16 dense rate
+    top = max(conv_ids, key=lambda k: avg[k])
+    top_flop, top_bytes = layer_flop[top], layer_bytes[top]
+    ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if top_flop / max(top_bytes, 1) >= ridge:
+        roof = {"kernel": top, "bound": "tensor", "achieved": top_flop / (avg[top] * 1e-3) / 1e12,
+                "peak": tensor_peak, "unit": "TFLOP/s"}
+    else:
+        roof = {"kernel": top, "bound": "hbm", "achieved": top_bytes / (avg[top] * 1e-3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = TRAFFIC.get(top)
+    roof["peak_source"] = peaks["source"] + (" sustained bf16 (dense fp16 = bf16 rate)"
+                                             if roof["bound"] == "tensor" else " HBM copy")
+    roof["launch_ms"] = avg[top] / tiles
+    layers = {k: {"ms": round(avg[k], 5),
+                  "tflops": round(layer_flop[k] / (avg[k] * 1e-3) / 1e12, 2) if layer_flop[k] else None,
+                  "gbs": round(layer_bytes[k] / (avg[k] * 1e-3) / 1e9, 1)} for k in avg}
+
+    if rank == 0:
+        cpu = cpu_oracle_sample(1) if world == 1 else None
+        line = {
+            "metric": METRIC, "value": value, "unit": "MP/s", "n_gpus": world,
+            "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": mean_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "width": WIDTH, "height": HEIGHT, "tiles": tiles,
+                       "precision": "fp16 storage, fp32 accumulate", "hdr": True,
+                       "transfer": "log", "l2": "flushed (256 MiB write) before every step",
+                       "parallelism": f"replicas x{world}"},
+            "conv_tflops": conv_flop / (conv_ms * 1e-3) / 1e12,
+            "conv_frac_of_peak": conv_flop / (conv_ms * 1e-3) / 1e12 / tensor_peak,
+            "roofline": roof,
+            "layers": layers,
+            "e2e": {"value": e2e_value, "unit": "MP/s", "h2d_bytes_per_step": 3 * px * 16,
+                    "d2h_bytes_per_step": px * 16, "ms_per_step": e2e_mean},
+            "gpu_launches": steps * tiles * 18,
+            "clocks": clocks.summary(),
+        }
+        if cpu:
+            line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# DRAM traffic per launch of each kernel from one ncu capture of this workload
+# (dram__bytes_read.sum + dram__bytes_write.sum); None until captured for the
+# current kernels.
+TRAFFIC = {}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

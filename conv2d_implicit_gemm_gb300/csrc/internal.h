@@ -1,0 +1,104 @@
+// Internal interfaces between the host runtime (oidnx.cpp) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace oidnx {
+
+// Pixels of one output row per tensor-core M tile and halo geometry.
+constexpr int kTileM = 128;
+constexpr int kHaloPx = kTileM + 2;        // input pixels of one halo row
+constexpr int kLowPx = kTileM / 2 + 2;     // low-resolution pixels for one M tile
+constexpr int kChunkBytes = 16;            // one 16-byte channel block
+constexpr int kTcThreads = 192;            // 6 warps: TMA, MMA, 4 x epilogue
+
+enum EpilogueMode : int {
+  kEpiRelu = 0,      // bias + ReLU, fp16 store
+  kEpiReluPool = 1,  // bias + ReLU + 2x2 max-pool, fp16 store
+  kEpiFinal = 2,     // bias only, fp32 [H][W][4] store
+};
+
+// Parameters of one tensor-core conv launch (one layer).
+struct TcConvParams {
+  const __half* weights;   // packed B operand, [kb][tap][2][N][8] halves
+  const float* bias;       // [N] (zero padded)
+  void* out;               // fp16 [Ho][N/8][Wo][8] or f32 [H][W][4]
+  int* status;             // device error word
+  int W, H;                // conv (full-resolution) extent of this layer
+  int N;                   // Cout rounded up to 16
+  int KB0, KB1;            // 16-lane K blocks from source 0 / source 1
+  int R;                   // output rows per CTA
+  int S;                   // pipeline stages
+  int mode;                // EpilogueMode
+  int upsample0;           // source 0 is at half resolution (decoder)
+  uint32_t tmem_cols;      // power of two >= max(32, R*N)
+  uint32_t a_stage;        // bytes per A stage (1024-aligned)
+  uint32_t b_stage;        // bytes per B stage (1024-aligned)
+  uint32_t st_stage;       // bytes per low-res staging stage (0 if none)
+  uint32_t a_tx, b_tx, st_tx;  // transaction bytes per stage
+};
+
+struct TcConvLaunch {
+  CUtensorMap map0;        // source 0 (full-res halo box, or low-res box)
+  CUtensorMap map1;        // source 1 (full-res halo box); unused if KB1 == 0
+  TcConvParams p;
+  dim3 grid;
+  size_t smem;
+};
+
+cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream);
+cudaError_t conv_tc_set_smem_limit(size_t bytes);
+cudaError_t conv_tc_occupancy(size_t smem, int* blocks_per_sm);
+
+// Parameters of one fp32 CUDA-core conv launch (one layer).
+struct SimtConvParams {
+  const float* src0;       // [H0][C40][W0][4]
+  const float* src1;       // [H][C41][W][4] or null
+  const float* weights;    // [groups][9][K4*4][8]
+  const float* bias;       // [groups*8]
+  float* out;              // [Ho][Cout4][Wo][4] or [H][W][4] (final)
+  int W, H;                // conv extent
+  int W0, H0;              // source 0 extent
+  int C40, C41;            // 4-lane chunks per source
+  int cout4;               // output chunks
+  int groups;              // output groups of 8 lanes
+  int mode;                // EpilogueMode
+  int upsample0;
+};
+cudaError_t launch_conv_simt(const SimtConvParams& p, cudaStream_t stream);
+
+// Input pass of one tile.
+struct PackParams {
+  const float4* img[3];    // colour, albedo, normal (device)
+  size_t stride[3];        // row stride in float4 elements
+  int sources;             // 1..3
+  int width, height;       // image extent
+  int tx, ty, tw, th;      // tile input rect
+  int hdr;
+  float scale;             // effective inputScale (HDR)
+  int fp16;                // storage precision
+  void* out;               // [th][chunks][tw][lanes]
+  int chunks;              // 16-byte chunks per pixel
+};
+cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
+
+// Output pass of one tile.
+struct UnpackParams {
+  const float4* net;       // [th][tw] network output of the tile
+  int tw;                  // tile input width (row stride of net)
+  int in_x, in_y;          // output rect offset inside the tile
+  const float4* color;     // input colour image
+  size_t color_stride;     // in float4
+  float4* out;             // output image
+  size_t out_stride;       // in float4
+  int ox, oy, ow, oh;      // output rect in the image
+  int hdr;
+  float scale;
+};
+cudaError_t launch_unpack(const UnpackParams& p, cudaStream_t stream);
+
+}  // namespace oidnx

@@ -1,0 +1,1465 @@
+// Host runtime of the oidnx C ABI: weight blob parsing and packing, the tile
+// planner, per-tile-shape network plans (activation arena from value
+// liveness, tensor maps, launch parameters), CUDA-graph replay, profiling and
+// the extern "C" entry points declared in include/oidnx.h.
+//
+// Structure follows "oidn-web 0.3.4 -> 0.4.0, package/src/nativeUNet.ts"
+// (NativeUNetExecutor: constructor validation and weight packing,
+// _createExecution liveness + best-fit slot reuse, _execution LRU shape cache
+// with deferred destruction of evicted plans, profileNextExecution) and
+// "oidn-webgpu 0.0.0-stage -> 0.6.0, src/native/denoise.ts"
+// (recordDenoiseExecution: overlap, tile grid, per-tile input pass ->
+// network -> output pass in order on one queue).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <functional>
+#include <list>
+#include <map>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "../../include/oidnx.h"
+#include "internal.h"
+
+using namespace oidnx;
+
+// ======================================================================
+// errors
+// ======================================================================
+namespace {
+
+thread_local std::string g_last_error;
+
+oidnx_status fail(oidnx_status s, const char* fmt, ...) {
+  char buf[1024];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+oidnx_status ok() {
+  g_last_error.clear();
+  return OIDNX_OK;
+}
+
+#define OIDNX_CUDA(call)                                                               \
+  do {                                                                                 \
+    cudaError_t e_ = (call);                                                           \
+    if (e_ != cudaSuccess) {                                                           \
+      if (e_ == cudaErrorMemoryAllocation)                                             \
+        return fail(OIDNX_ERR_OUT_OF_MEMORY, "%s: %s", #call, cudaGetErrorString(e_)); \
+      return fail(OIDNX_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_));            \
+    }                                                                                  \
+  } while (0)
+
+#define OIDNX_TRY(expr)               \
+  do {                                \
+    oidnx_status s_ = (expr);         \
+    if (s_ != OIDNX_OK) return s_;    \
+  } while (0)
+
+// ======================================================================
+// model
+// ======================================================================
+constexpr int kLayers = 16;
+const char* const kLayerNames[kLayers] = {
+    "enc_conv0",  "enc_conv1",  "enc_conv2",  "enc_conv3",  "enc_conv4",  "enc_conv5a",
+    "enc_conv5b", "dec_conv4a", "dec_conv4b", "dec_conv3a", "dec_conv3b", "dec_conv2a",
+    "dec_conv2b", "dec_conv1a", "dec_conv1b", "dec_conv0"};
+
+struct ConvTensors {
+  int cout = 0, cin = 0;
+  std::vector<float> w;  // OIHW
+  std::vector<float> b;  // [cout]
+};
+
+enum Kind { kPlain, kPool, kDecoder, kFinal };
+
+// Values of the network dataflow.
+enum Val {
+  V_IN, V_E0, V_P1, V_P2, V_P3, V_P4, V_E5A, V_E5B, V_D4A, V_D4B,
+  V_D3A, V_D3B, V_D2A, V_D2B, V_D1A, V_D1B, V_OUT, V_COUNT
+};
+
+struct LayerDef {
+  int src0, src1, dst, kind, level;  // level of the conv (full-resolution) extent
+};
+
+// enc_conv0 -> enc_conv1+pool -> (enc_convK+pool)x3 -> enc_conv5a/5b ->
+// per decoder level up+concat(skip) conv, conv -> dec_conv0 (no ReLU, fp32).
+const LayerDef kDefs[kLayers] = {
+    {V_IN, -1, V_E0, kPlain, 0},     {V_E0, -1, V_P1, kPool, 0},
+    {V_P1, -1, V_P2, kPool, 1},      {V_P2, -1, V_P3, kPool, 2},
+    {V_P3, -1, V_P4, kPool, 3},      {V_P4, -1, V_E5A, kPlain, 4},
+    {V_E5A, -1, V_E5B, kPlain, 4},   {V_E5B, V_P3, V_D4A, kDecoder, 3},
+    {V_D4A, -1, V_D4B, kPlain, 3},   {V_D4B, V_P2, V_D3A, kDecoder, 2},
+    {V_D3A, -1, V_D3B, kPlain, 2},   {V_D3B, V_P1, V_D2A, kDecoder, 1},
+    {V_D2A, -1, V_D2B, kPlain, 1},   {V_D2B, V_IN, V_D1A, kDecoder, 0},
+    {V_D1A, -1, V_D1B, kPlain, 0},   {V_D1B, -1, V_OUT, kFinal, 0},
+};
+
+int round_up(int v, int a) { return (v + a - 1) / a * a; }
+size_t round_up_sz(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Half-precision bits of a float, round to nearest even (host side).
+uint16_t to_half_bits(float f) {
+  __half h = __float2half_rn(f);
+  uint16_t b;
+  std::memcpy(&b, &h, 2);
+  return b;
+}
+
+float half_bits_to_float(uint16_t bits) {
+  __half h;
+  std::memcpy(&h, &bits, 2);
+  return __half2float(h);
+}
+
+// ---------------------------------------------------------------- blob
+struct BlobReader {
+  const uint8_t* p;
+  size_t n, off = 0;
+  bool u32(uint32_t* v) {
+    if (off + 4 > n) return false;
+    std::memcpy(v, p + off, 4);
+    off += 4;
+    return true;
+  }
+  bool bytes(const uint8_t** v, size_t len) {
+    if (len > n || off + len > n) return false;
+    *v = p + off;
+    off += len;
+    return true;
+  }
+};
+
+oidnx_status parse_blob(const void* blob, size_t bytes, ConvTensors (&layers)[kLayers],
+                        int* in_channels) {
+  BlobReader r{static_cast<const uint8_t*>(blob), bytes};
+  const uint8_t* magic;
+  uint32_t version, count;
+  if (!r.bytes(&magic, 4) || std::memcmp(magic, "OXW1", 4) != 0)
+    return fail(OIDNX_ERR_INVALID_MODEL, "weight blob: bad magic (expected OXW1)");
+  if (!r.u32(&version) || version != 1)
+    return fail(OIDNX_ERR_INVALID_MODEL, "weight blob: unsupported version");
+  if (!r.u32(&count) || count > 4096)
+    return fail(OIDNX_ERR_INVALID_MODEL, "weight blob: bad tensor count");
+  bool have_w[kLayers] = {}, have_b[kLayers] = {};
+  for (uint32_t t = 0; t < count; ++t) {
+    uint32_t name_len, ndim, dtype;
+    const uint8_t* name_p;
+    if (!r.u32(&name_len) || name_len > 256 || !r.bytes(&name_p, name_len) ||
+        !r.bytes(&name_p, 0))
+      return fail(OIDNX_ERR_INVALID_MODEL, "weight blob: truncated tensor name");
+    std::string name(reinterpret_cast<const char*>(r.p + r.off - name_len), name_len);
+    const uint8_t* skip;
+    if (!r.bytes(&skip, (4 - name_len % 4) % 4))
+      return fail(OIDNX_ERR_INVALID_MODEL, "weight blob: truncated");
+    if (!r.u32(&ndim) || ndim < 1 || ndim > 4)
+      return fail(OIDNX_ERR_INVALID_MODEL, "weight blob: tensor %s: bad rank", name.c_str());
+    uint32_t dims[4] = {1, 1, 1, 1};
+    uint64_t elems = 1;
+    for (uint32_t d = 0; d < ndim; ++d) {
+      if (!r.u32(&dims[d]) || dims[d] == 0 || dims[d] > 65536)
+        return fail(OIDNX_ERR_INVALID_MODEL, "weight blob: tensor %s: bad dims", name.c_str());
+      elems *= dims[d];
+    }
+    if (!r.u32(&dtype) || dtype > 1)
+      return fail(OIDNX_ERR_INVALID_MODEL, "weight blob: tensor %s: bad dtype", name.c_str());
+    const size_t data_bytes = elems * (dtype == 0 ? 4 : 2);
+    const uint8_t* data;
+    if (!r.bytes(&data, data_bytes) || !r.bytes(&skip, (4 - data_bytes % 4) % 4))
+      return fail(OIDNX_ERR_INVALID_MODEL, "weight blob: tensor %s: truncated data",
+                  name.c_str());
+    std::vector<float> vals(elems);
+    for (uint64_t i = 0; i < elems; ++i) {
+      if (dtype == 0) {
+        std::memcpy(&vals[i], data + 4 * i, 4);
+      } else {
+        uint16_t b;
+        std::memcpy(&b, data + 2 * i, 2);
+        vals[i] = half_bits_to_float(b);
+      }
+    }
+    int layer = -1;
+    bool is_weight = false;
+    for (int l = 0; l < kLayers; ++l) {
+      if (name == std::string(kLayerNames[l]) + ".weight") { layer = l; is_weight = true; }
+      if (name == std::string(kLayerNames[l]) + ".bias") { layer = l; is_weight = false; }
+    }
+    if (layer < 0) continue;  // unknown tensors are ignored
+    ConvTensors& L = layers[layer];
+    if (is_weight) {
+      if (ndim != 4 || dims[2] != 3 || dims[3] != 3)
+        return fail(OIDNX_ERR_INVALID_MODEL, "%s: expected a 3x3 OIHW weight", name.c_str());
+      L.cout = static_cast<int>(dims[0]);
+      L.cin = static_cast<int>(dims[1]);
+      L.w = std::move(vals);
+      have_w[layer] = true;
+    } else {
+      if (ndim != 1)
+        return fail(OIDNX_ERR_INVALID_MODEL, "%s: expected a 1-D bias", name.c_str());
+      L.b = std::move(vals);
+      have_b[layer] = true;
+    }
+  }
+  for (int l = 0; l < kLayers; ++l) {
+    if (!have_w[l] || !have_b[l])
+      return fail(OIDNX_ERR_INVALID_MODEL, "weight blob: missing %s weight or bias",
+                  kLayerNames[l]);
+    if (static_cast<int>(layers[l].b.size()) != layers[l].cout)
+      return fail(OIDNX_ERR_INVALID_MODEL, "%s: bias size %zu != %d outputs", kLayerNames[l],
+                  layers[l].b.size(), layers[l].cout);
+  }
+  // Topology checks (channel counts must chain as the U-Net's dataflow).
+  const int cin = layers[0].cin;
+  if (cin != 3 && cin != 6 && cin != 9)
+    return fail(OIDNX_ERR_INVALID_MODEL, "expects 3, 6, or 9 input channels, got %d", cin);
+  auto out_ch = [&](int v) -> int {
+    if (v == V_IN) return cin;
+    for (int l = 0; l < kLayers; ++l)
+      if (kDefs[l].dst == v) return layers[l].cout;
+    return -1;
+  };
+  for (int l = 0; l < kLayers; ++l) {
+    int need = out_ch(kDefs[l].src0) + (kDefs[l].src1 >= 0 ? out_ch(kDefs[l].src1) : 0);
+    if (layers[l].cin != need)
+      return fail(OIDNX_ERR_INVALID_MODEL, "%s: %d input channels, the U-Net needs %d",
+                  kLayerNames[l], layers[l].cin, need);
+    if (layers[l].cout > 256)
+      return fail(OIDNX_ERR_UNSUPPORTED, "%s: more than 256 output channels", kLayerNames[l]);
+  }
+  if (layers[15].cout != 3)
+    return fail(OIDNX_ERR_INVALID_MODEL, "dec_conv0 must have 3 outputs");
+  *in_channels = cin;
+  return ok();
+}
+
+// ---------------------------------------------------------------- packing
+// fp16 tensor-core B operand: per 16-lane K block kb, per tap, per 8-lane
+// half j, N rows of 8 halves ([kb][tap][j][n][8]).  K lanes enumerate the
+// concatenated sources, each padded to a multiple of 16 lanes; padded rows
+// and lanes are zero.
+std::vector<uint16_t> pack_weights_tc(const ConvTensors& L, int c0, int c1, int* KB0,
+                                      int* KB1, int* N) {
+  const int p0 = round_up(c0, 16), p1 = c1 > 0 ? round_up(c1, 16) : 0;
+  *KB0 = p0 / 16;
+  *KB1 = p1 / 16;
+  *N = round_up(L.cout, 16);
+  const int KB = *KB0 + *KB1;
+  std::vector<uint16_t> out(static_cast<size_t>(KB) * 9 * 2 * (*N) * 8, 0);
+  for (int kb = 0; kb < KB; ++kb)
+    for (int t = 0; t < 9; ++t)
+      for (int j = 0; j < 2; ++j)
+        for (int n = 0; n < L.cout; ++n)
+          for (int l = 0; l < 8; ++l) {
+            const int v = kb * 16 + j * 8 + l;
+            int ch = -1;
+            if (v < p0) ch = v < c0 ? v : -1;
+            else ch = (v - p0) < c1 ? c0 + (v - p0) : -1;
+            if (ch < 0) continue;
+            const float w = L.w[(static_cast<size_t>(n) * L.cin + ch) * 9 + t];
+            out[((((static_cast<size_t>(kb) * 9 + t) * 2 + j) * (*N) + n) * 8) + l] =
+                to_half_bits(w);
+          }
+  return out;
+}
+
+// fp32 CUDA-core weights: [group of 8 outputs][tap][K lane][8 outputs], K lanes
+// enumerate the concatenated sources each padded to a multiple of 4.
+std::vector<float> pack_weights_simt(const ConvTensors& L, int c0, int c1, int* C40, int* C41,
+                                     int* groups) {
+  const int p0 = round_up(c0, 4), p1 = c1 > 0 ? round_up(c1, 4) : 0;
+  *C40 = p0 / 4;
+  *C41 = p1 / 4;
+  *groups = (L.cout + 7) / 8;
+  const int K = p0 + p1;
+  std::vector<float> out(static_cast<size_t>(*groups) * 9 * K * 8, 0.0f);
+  for (int g = 0; g < *groups; ++g)
+    for (int t = 0; t < 9; ++t)
+      for (int v = 0; v < K; ++v) {
+        int ch = -1;
+        if (v < p0) ch = v < c0 ? v : -1;
+        else ch = (v - p0) < c1 ? c0 + (v - p0) : -1;
+        if (ch < 0) continue;
+        for (int o = 0; o < 8; ++o) {
+          const int n = g * 8 + o;
+          if (n >= L.cout) continue;
+          out[((static_cast<size_t>(g) * 9 + t) * K + v) * 8 + o] =
+              L.w[(static_cast<size_t>(n) * L.cin + ch) * 9 + t];
+        }
+      }
+  return out;
+}
+
+// ---------------------------------------------------------------- tiles
+struct AxisTile {
+  int in_start, in_size, out_start, out_size;
+};
+
+// Per-axis tile plan on the 16-aligned extent; see oidnx_plan_tiles.
+bool plan_axis(int extent, int limit, int overlap, std::vector<AxisTile>* tiles) {
+  tiles->clear();
+  if (extent <= 0 || overlap < 0 || overlap % 16) return false;
+  const int ea = round_up(extent, 16);
+  const int tmax = limit / 16 * 16;
+  if (ea <= tmax) {
+    tiles->push_back({0, ea, 0, extent});
+    return true;
+  }
+  int n = 2, c = 0;
+  for (;; ++n) {
+    c = round_up((ea + n - 1) / n, 16);
+    if (c + 2 * overlap <= tmax) break;
+    if (c <= 16) return false;
+  }
+  const int size = c + 2 * overlap;
+  for (int i = 0; i < n; ++i) {
+    const int o = i * c;
+    const int o_next = i + 1 < n ? (i + 1) * c : ea;
+    const int s = std::min(std::max(o - overlap, 0), ea - size);
+    const int osz = std::min(o_next, extent) - o;
+    if (osz > 0) tiles->push_back({s, size, o, osz});
+  }
+  return true;
+}
+
+// One-sided dependency radius of the 4-level U-Net output on its input,
+// by interval propagation (conv: +-1, pool source: [2a, 2b+1], nearest
+// upsample source: [a>>1, b>>1], concat: union), worst over residues mod 16.
+int dependency_radius() {
+  struct Iv { long a, b; };
+  auto conv = [](Iv v) { return Iv{v.a - 1, v.b + 1}; };
+  auto pool_src = [](Iv v) { return Iv{2 * v.a, 2 * v.b + 1}; };
+  auto up_src = [](Iv v) { return Iv{v.a >> 1, v.b >> 1}; };
+  const int levels = 4;
+  // input interval of a pooled value at `level` (0 = the input itself)
+  auto pooled = [&](Iv v, int level) {
+    while (level > 0) {
+      v = conv(pool_src(v));
+      if (level == 1) v = conv(v);
+      --level;
+    }
+    return v;
+  };
+  // input interval of the decoder output at `level`
+  std::function<Iv(Iv, int)> decoded;
+  decoded = [&](Iv v, int level) -> Iv {
+    if (level == levels) return pooled(conv(conv(v)), levels);
+    Iv cat = conv(conv(v));
+    Iv low = decoded(up_src(cat), level + 1);
+    Iv skip = pooled(cat, level);
+    return Iv{std::min(low.a, skip.a), std::max(low.b, skip.b)};
+  };
+  long r = 0;
+  for (int res = 0; res < 16; ++res) {
+    const long p = 16L * 64 * 10 + res;
+    Iv d = decoded(conv(Iv{p, p}), 0);
+    r = std::max(r, std::max(p - d.a, d.b - p));
+  }
+  return static_cast<int>(r);
+}
+
+int default_overlap_value() { return round_up(dependency_radius(), 16); }
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// fp16 activation [H][C8][W][8] as a 4-D tensor {8 lanes, W, C8, H}; box
+// {8, box_w, 2, box_h}; zero fill outside.
+oidnx_status encode_act_map(CUtensorMap* map, const void* base, int W, int H, int C8, int box_w,
+                            int box_h) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[4] = {8, static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(C8),
+                        static_cast<cuuint64_t>(H)};
+  cuuint64_t strides[3] = {16, static_cast<cuuint64_t>(W) * 16,
+                           static_cast<cuuint64_t>(W) * 16 * C8};
+  cuuint32_t box[4] = {8, static_cast<cuuint32_t>(box_w), 2, static_cast<cuuint32_t>(box_h)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %dx%dx%d", int(r), W, H,
+                C8);
+  return ok();
+}
+
+// ======================================================================
+// device-side model and plans
+// ======================================================================
+struct DeviceLayer {
+  int cout = 0, cin = 0, c0 = 0, c1 = 0;
+  // fp16 path
+  void* w16 = nullptr;  // packed B operand
+  int KB0 = 0, KB1 = 0, N = 0;
+  // fp32 path
+  float* w32 = nullptr;
+  int C40 = 0, C41 = 0, groups = 0;
+  float* bias = nullptr;  // [max(N, groups*8)]
+  size_t weight_bytes = 0;
+};
+
+struct Extent {
+  int w, h;
+};
+
+struct LayerLaunch {
+  int layer;
+  bool tc;
+  TcConvLaunch tcl;
+  SimtConvParams sp;
+  double flop;   // logical conv FLOPs
+  double bytes;  // algorithmic bytes: inputs read once, output written once
+};
+
+struct Plan {
+  int w = 0, h = 0;
+  Extent lvl[5];
+  size_t value_off[V_COUNT] = {};
+  size_t value_bytes[V_COUNT] = {};
+  Extent value_ext[V_COUNT];
+  int value_ch[V_COUNT] = {};
+  void* arena = nullptr;
+  size_t arena_bytes = 0;
+  std::vector<LayerLaunch> launches;
+  uint64_t last_used = 0;
+  cudaEvent_t done = nullptr;  // recorded after each use
+  bool used = false;
+  void* ptr(int v) const { return static_cast<uint8_t*>(arena) + value_off[v]; }
+};
+
+// Per-kernel timing events of one execution.
+struct Profile {
+  std::vector<cudaEvent_t> ev;        // ev[0] = start, one per launch after it
+  std::vector<int> label;             // layer id per launch: -1 pack, 0..15, 16 unpack
+  int used = 0;
+  bool valid = false;
+};
+
+}  // namespace
+
+struct oidnx_filter {
+  bool released = false;
+  int precision = OIDNX_PRECISION_FP16;  // resolved: 1 or 2
+  int in_channels = 9;
+  DeviceLayer layers[kLayers];
+  size_t weight_bytes = 0;
+  int* status = nullptr;  // device error word
+  // parameters
+  int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
+      overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0;
+  float input_scale = 1.0f;
+  void* img[4] = {};
+  size_t img_stride[4] = {};
+  // committed state
+  bool committed = false;
+  std::vector<AxisTile> tx, ty;
+  Plan* current = nullptr;
+  std::list<std::unique_ptr<Plan>> plans;    // LRU cache
+  std::list<std::unique_ptr<Plan>> retired;  // evicted, maybe still in flight
+  uint64_t clock = 0;
+  // graph of the committed denoise
+  cudaGraphExec_t graph = nullptr;
+  bool graph_profiled = false;
+  void* graph_img[4] = {};
+  cudaStream_t capture_stream = nullptr;
+  // profiling
+  bool profile_next = false;
+  Profile prof;
+  // host-path staging images
+  void* host_img[4] = {};
+  size_t host_img_bytes = 0;
+  // last network run (for debug reads)
+  Plan* last_plan = nullptr;
+};
+
+struct oidnx_conv {
+  DeviceLayer L;
+  int precision = OIDNX_PRECISION_FP16;
+  int* status = nullptr;
+};
+
+namespace {
+
+oidnx_status upload(const void* host, size_t bytes, void** dev) {
+  OIDNX_CUDA(cudaMalloc(dev, bytes));
+  OIDNX_CUDA(cudaMemcpy(*dev, host, bytes, cudaMemcpyHostToDevice));
+  return ok();
+}
+
+void free_layer(DeviceLayer& L) {
+  cudaFree(L.w16);
+  cudaFree(L.w32);
+  cudaFree(L.bias);
+  L.w16 = nullptr;
+  L.w32 = nullptr;
+  L.bias = nullptr;
+}
+
+oidnx_status make_device_layer(const ConvTensors& T, int c0, int c1, int precision,
+                               DeviceLayer* L) {
+  L->cout = T.cout;
+  L->cin = T.cin;
+  L->c0 = c0;
+  L->c1 = c1;
+  if (precision == OIDNX_PRECISION_FP16) {
+    std::vector<uint16_t> w = pack_weights_tc(T, c0, c1, &L->KB0, &L->KB1, &L->N);
+    if (L->N > 256) return fail(OIDNX_ERR_UNSUPPORTED, "more than 256 output channels");
+    OIDNX_TRY(upload(w.data(), w.size() * 2, &L->w16));
+    std::vector<float> b(L->N, 0.0f);
+    std::copy(T.b.begin(), T.b.end(), b.begin());
+    OIDNX_TRY(upload(b.data(), b.size() * 4, reinterpret_cast<void**>(&L->bias)));
+    L->weight_bytes = w.size() * 2 + b.size() * 4;
+  } else {
+    std::vector<float> w = pack_weights_simt(T, c0, c1, &L->C40, &L->C41, &L->groups);
+    OIDNX_TRY(upload(w.data(), w.size() * 4, reinterpret_cast<void**>(&L->w32)));
+    std::vector<float> b(L->groups * 8, 0.0f);
+    std::copy(T.b.begin(), T.b.end(), b.begin());
+    OIDNX_TRY(upload(b.data(), b.size() * 4, reinterpret_cast<void**>(&L->bias)));
+    L->weight_bytes = w.size() * 4 + b.size() * 4;
+  }
+  return ok();
+}
+
+// Bytes of one stored activation: fp16 rounds channels up to 16 lanes, fp32
+// to 4; the network output is [h][w][4] floats.
+size_t act_bytes(int precision, int w, int h, int c, bool final_out) {
+  if (final_out) return static_cast<size_t>(w) * h * 16;
+  if (precision == OIDNX_PRECISION_FP16) return static_cast<size_t>(w) * h * round_up(c, 16) * 2;
+  return static_cast<size_t>(w) * h * round_up(c, 4) * 4;
+}
+
+int act_chunks(int precision, int c) {
+  return precision == OIDNX_PRECISION_FP16 ? round_up(c, 16) / 8 : round_up(c, 4) / 4;
+}
+
+int g_num_sms = 0;
+
+int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        g_num_sms <= 0)
+      g_num_sms = 148;
+  }
+  return g_num_sms;
+}
+
+// Build the tensor-core launch of one conv.  src0/src1: device pointers of the
+// sources (fp16 layout), ext0: extent of source 0, (W, H): conv extent.
+oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, Extent ext0,
+                             const void* src1, int W, int H, void* out, int* status,
+                             TcConvLaunch* T) {
+  const bool up = kind == kDecoder;
+  const int N = L.N;
+  const int minR = (kind == kPool || kind == kDecoder) ? 2 : 1;
+  int R = 4;
+  while (R > minR && R * N > 512) R /= 2;
+  const long tiles_x = (W + kTileM - 1) / kTileM;
+  while (R > minR && tiles_x * ((H + R - 1) / R) < 2L * num_sms()) R /= 2;
+  if (R * N > 512) return fail(OIDNX_ERR_UNSUPPORTED, "accumulators exceed tensor memory");
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < static_cast<uint32_t>(R * N)) tmem_cols *= 2;
+
+  TcConvParams& p = T->p;
+  std::memset(&p, 0, sizeof(p));
+  p.weights = static_cast<const __half*>(L.w16);
+  p.bias = L.bias;
+  p.out = out;
+  p.status = status;
+  p.W = W;
+  p.H = H;
+  p.N = N;
+  p.KB0 = L.KB0;
+  p.KB1 = L.KB1;
+  p.R = R;
+  p.mode = kind == kPool ? kEpiReluPool : (kind == kFinal ? kEpiFinal : kEpiRelu);
+  p.upsample0 = up ? 1 : 0;
+  p.tmem_cols = tmem_cols;
+  p.a_tx = static_cast<uint32_t>((R + 2) * 2 * kHaloPx * kChunkBytes);
+  p.b_tx = static_cast<uint32_t>(9 * 2 * N * kChunkBytes);
+  p.st_tx = up ? static_cast<uint32_t>((R / 2 + 2) * 2 * kLowPx * kChunkBytes) : 0u;
+  p.a_stage = static_cast<uint32_t>(round_up_sz(p.a_tx, 1024));
+  p.b_stage = static_cast<uint32_t>(round_up_sz(p.b_tx, 1024));
+  p.st_stage = static_cast<uint32_t>(round_up_sz(p.st_tx, 1024));
+  const size_t stage = static_cast<size_t>(p.a_stage) + p.b_stage + p.st_stage;
+  const int KB = L.KB0 + L.KB1;
+  const int per_sm_target = std::max(1, std::min(2, static_cast<int>(512 / tmem_cols)));
+  const size_t fixed = 1024 + 512;  // alignment slack + barriers
+  const size_t max_smem = 227 * 1024;
+  const size_t budget = (per_sm_target == 2 ? 112 * 1024 : max_smem) - fixed;
+  int S = static_cast<int>(budget / stage);
+  S = std::max(1, std::min(S, std::min(KB, 6)));
+  if (S < 2 && KB > 1) S = 2;
+  p.S = S;
+  size_t smem = fixed + S * stage;
+  if (smem > max_smem) return fail(OIDNX_ERR_UNSUPPORTED, "conv stage does not fit shared memory");
+  // Keep the CTAs resident on one SM within the 512 TMEM columns: pad the
+  // shared-memory request until the occupancy allows no more than that.
+  static size_t limit_set = 0;
+  if (limit_set < max_smem) {
+    cudaError_t e = conv_tc_set_smem_limit(max_smem);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
+    limit_set = max_smem;
+  }
+  const int allowed = static_cast<int>(512 / tmem_cols);
+  for (;;) {
+    int blocks = 0;
+    cudaError_t e = conv_tc_occupancy(smem, &blocks);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "occupancy: %s", cudaGetErrorString(e));
+    if (blocks <= allowed) break;
+    smem += 4096;
+    if (smem > max_smem) return fail(OIDNX_ERR_UNSUPPORTED, "cannot bound CTAs per SM");
+  }
+  T->smem = smem;
+  T->grid = dim3(static_cast<unsigned>(tiles_x), static_cast<unsigned>((H + R - 1) / R), 1);
+
+  const int c8_0 = round_up(L.c0, 16) / 8;
+  if (up)
+    OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.h, c8_0, kLowPx, R / 2 + 2));
+  else
+    OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.h, c8_0, kHaloPx, R + 2));
+  if (L.KB1 > 0) {
+    const int c8_1 = round_up(L.c1, 16) / 8;
+    OIDNX_TRY(encode_act_map(&T->map1, src1, W, H, c8_1, kHaloPx, R + 2));
+  } else {
+    T->map1 = T->map0;
+  }
+  return ok();
+}
+
+void build_simt_launch(const DeviceLayer& L, int kind, const void* src0, Extent ext0,
+                       const void* src1, int W, int H, void* out, SimtConvParams* p) {
+  std::memset(p, 0, sizeof(*p));
+  p->src0 = static_cast<const float*>(src0);
+  p->src1 = static_cast<const float*>(src1);
+  p->weights = L.w32;
+  p->bias = L.bias;
+  p->out = static_cast<float*>(out);
+  p->W = W;
+  p->H = H;
+  p->W0 = ext0.w;
+  p->H0 = ext0.h;
+  p->C40 = L.C40;
+  p->C41 = L.C41;
+  p->cout4 = (L.cout + 3) / 4;
+  p->groups = L.groups;
+  p->mode = kind == kPool ? kEpiReluPool : (kind == kFinal ? kEpiFinal : kEpiRelu);
+  p->upsample0 = kind == kDecoder ? 1 : 0;
+}
+
+oidnx_status run_launch(const LayerLaunch& L, cudaStream_t s) {
+  cudaError_t e = L.tc ? launch_conv_tc(L.tcl, s) : launch_conv_simt(L.sp, s);
+  if (e != cudaSuccess)
+    return fail(OIDNX_ERR_CUDA, "%s launch: %s", kLayerNames[L.layer], cudaGetErrorString(e));
+  return ok();
+}
+
+void destroy_plan(Plan* p) {
+  if (!p) return;
+  if (p->done) {
+    cudaEventSynchronize(p->done);
+    cudaEventDestroy(p->done);
+  }
+  cudaFree(p->arena);
+  p->arena = nullptr;
+}
+
+// Liveness-based activation plan for a w x h network input
+// ("nativeUNet.ts", _createExecution: a value's slot is free after its last
+// use; each new value takes the smallest free slot that fits, else a new one).
+oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* out) {
+  std::unique_ptr<Plan> P(new Plan());
+  P->w = w;
+  P->h = h;
+  P->lvl[0] = {w, h};
+  for (int l = 1; l < 5; ++l) P->lvl[l] = {(P->lvl[l - 1].w + 1) / 2, (P->lvl[l - 1].h + 1) / 2};
+  // value shapes
+  P->value_ext[V_IN] = P->lvl[0];
+  P->value_ch[V_IN] = f->in_channels;
+  for (int l = 0; l < kLayers; ++l) {
+    const LayerDef& d = kDefs[l];
+    const int lvl = d.kind == kPool ? d.level + 1 : d.level;
+    P->value_ext[d.dst] = P->lvl[lvl];
+    P->value_ch[d.dst] = f->layers[l].cout;
+  }
+  // last use of each value
+  int last_use[V_COUNT];
+  for (int v = 0; v < V_COUNT; ++v) last_use[v] = -1;
+  for (int l = 0; l < kLayers; ++l) {
+    last_use[kDefs[l].src0] = l;
+    if (kDefs[l].src1 >= 0) last_use[kDefs[l].src1] = l;
+  }
+  last_use[V_OUT] = kLayers;
+  struct Slot {
+    size_t cap, off;
+    int active;
+  };
+  std::vector<Slot> slots;
+  size_t total = 0;
+  auto allocate = [&](int v, int index) {
+    if (!f->keep_acts)
+      for (Slot& s : slots)
+        if (s.active >= 0 && last_use[s.active] < index) s.active = -1;
+    const size_t need = act_bytes(f->precision, P->value_ext[v].w, P->value_ext[v].h,
+                                  P->value_ch[v], v == V_OUT);
+    int best = -1;
+    for (size_t i = 0; i < slots.size(); ++i)
+      if (slots[i].active < 0 && slots[i].cap >= need &&
+          (best < 0 || slots[i].cap < slots[best].cap))
+        best = static_cast<int>(i);
+    if (best < 0) {
+      slots.push_back({round_up_sz(need, 1024), total, -1});
+      total += round_up_sz(need, 1024);
+      best = static_cast<int>(slots.size()) - 1;
+    }
+    slots[best].active = v;
+    P->value_off[v] = slots[best].off;
+    P->value_bytes[v] = need;
+  };
+  allocate(V_IN, -1);
+  for (int l = 0; l < kLayers; ++l) allocate(kDefs[l].dst, l);
+  P->arena_bytes = total;
+  cudaError_t e = cudaMalloc(&P->arena, total);
+  if (e != cudaSuccess)
+    return fail(OIDNX_ERR_OUT_OF_MEMORY, "activation arena of %zu bytes: %s", total,
+                cudaGetErrorString(e));
+  // Zero once so that padded lanes read as zero before any write.
+  e = cudaMemset(P->arena, 0, total);
+  if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "arena memset: %s", cudaGetErrorString(e));
+  e = cudaEventCreateWithFlags(&P->done, cudaEventDisableTiming);
+  if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "event: %s", cudaGetErrorString(e));
+
+  for (int l = 0; l < kLayers; ++l) {
+    const LayerDef& d = kDefs[l];
+    const DeviceLayer& L = f->layers[l];
+    LayerLaunch LL;
+    std::memset(&LL, 0, sizeof(LL));
+    LL.layer = l;
+    const Extent conv = P->lvl[d.level];
+    const void* s1 = d.src1 >= 0 ? P->ptr(d.src1) : nullptr;
+    if (f->precision == OIDNX_PRECISION_FP16) {
+      LL.tc = true;
+      OIDNX_TRY(build_tc_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, conv.w,
+                                conv.h, P->ptr(d.dst), f->status, &LL.tcl));
+    } else {
+      LL.tc = false;
+      build_simt_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, conv.w, conv.h,
+                        P->ptr(d.dst), &LL.sp);
+    }
+    const double px = static_cast<double>(conv.w) * conv.h;
+    LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
+    const int bpe = f->precision == OIDNX_PRECISION_FP16 ? 2 : 4;
+    double in_bytes = static_cast<double>(P->value_ext[d.src0].w) * P->value_ext[d.src0].h *
+                      P->value_ch[d.src0] * bpe;
+    if (d.src1 >= 0)
+      in_bytes += static_cast<double>(P->value_ext[d.src1].w) * P->value_ext[d.src1].h *
+                  P->value_ch[d.src1] * bpe;
+    const Extent oe = P->value_ext[d.dst];
+    const double out_bytes = d.kind == kFinal ? static_cast<double>(oe.w) * oe.h * 16
+                                              : static_cast<double>(oe.w) * oe.h * L.cout * bpe;
+    LL.bytes = in_bytes + out_bytes + static_cast<double>(L.weight_bytes);
+    P->launches.push_back(LL);
+  }
+  *out = std::move(P);
+  return ok();
+}
+
+// LRU lookup/creation of the plan for a w x h network input ("nativeUNet.ts",
+// _execution): evicted plans are destroyed once their last use has finished.
+oidnx_status get_plan(oidnx_filter* f, int w, int h, Plan** out) {
+  for (auto it = f->retired.begin(); it != f->retired.end();) {
+    if (cudaEventQuery((*it)->done) == cudaSuccess) {
+      destroy_plan(it->get());
+      it = f->retired.erase(it);
+    } else {
+      ++it;
+    }
+  }
+  for (auto& p : f->plans)
+    if (p->w == w && p->h == h) {
+      p->last_used = ++f->clock;
+      *out = p.get();
+      return ok();
+    }
+  std::unique_ptr<Plan> P;
+  OIDNX_TRY(create_plan(f, w, h, &P));
+  P->last_used = ++f->clock;
+  Plan* raw = P.get();
+  f->plans.push_back(std::move(P));
+  while (static_cast<int>(f->plans.size()) > f->shape_cache) {
+    auto oldest = f->plans.end();
+    for (auto it = f->plans.begin(); it != f->plans.end(); ++it)
+      if (it->get() != raw && (oldest == f->plans.end() || (*it)->last_used < (*oldest)->last_used))
+        oldest = it;
+    if (oldest == f->plans.end()) break;
+    if (f->current == oldest->get()) {
+      f->current = nullptr;
+      if (f->graph) {
+        cudaGraphExecDestroy(f->graph);
+        f->graph = nullptr;
+      }
+    }
+    if (f->last_plan == oldest->get()) f->last_plan = nullptr;
+    f->retired.push_back(std::move(*oldest));
+    f->plans.erase(oldest);
+  }
+  *out = raw;
+  return ok();
+}
+
+// ---------------------------------------------------------------- profiling
+oidnx_status prof_begin(oidnx_filter* f, size_t launches) {
+  Profile& P = f->prof;
+  while (P.ev.size() < launches + 1) {
+    cudaEvent_t e;
+    OIDNX_CUDA(cudaEventCreate(&e));
+    P.ev.push_back(e);
+  }
+  P.label.assign(launches, 0);
+  P.used = 0;
+  P.valid = true;
+  return ok();
+}
+
+oidnx_status prof_mark(oidnx_filter* f, bool on, int label, cudaStream_t s) {
+  if (!on) return ok();
+  Profile& P = f->prof;
+  if (P.used > 0) P.label[P.used - 1] = label;
+  OIDNX_CUDA(cudaEventRecord(P.ev[P.used], s));
+  P.used++;
+  return ok();
+}
+
+// ---------------------------------------------------------------- enqueue
+oidnx_status enqueue_network(oidnx_filter* f, Plan* P, bool prof, cudaStream_t s) {
+  for (const LayerLaunch& L : P->launches) {
+    OIDNX_TRY(run_launch(L, s));
+    OIDNX_TRY(prof_mark(f, prof, L.layer, s));
+  }
+  return ok();
+}
+
+// All tiles: input pass -> network -> output pass, on stream s.
+oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t stride[4],
+                             bool prof, cudaStream_t s) {
+  Plan* P = f->current;
+  const int sources = f->in_channels / 3;
+  const float scale = f->input_scale == 0.0f ? 1.0f : f->input_scale;
+  OIDNX_TRY(prof_mark(f, prof, -2, s));
+  for (const AxisTile& ty : f->ty)
+    for (const AxisTile& tx : f->tx) {
+      PackParams pp;
+      std::memset(&pp, 0, sizeof(pp));
+      for (int i = 0; i < 3; ++i) {
+        pp.img[i] = static_cast<const float4*>(img[i]);
+        pp.stride[i] = stride[i] / 16;
+      }
+      pp.sources = sources;
+      pp.width = f->width;
+      pp.height = f->height;
+      pp.tx = tx.in_start;
+      pp.ty = ty.in_start;
+      pp.tw = tx.in_size;
+      pp.th = ty.in_size;
+      pp.hdr = f->hdr;
+      pp.scale = scale;
+      pp.fp16 = f->precision == OIDNX_PRECISION_FP16;
+      pp.out = P->ptr(V_IN);
+      pp.chunks = act_chunks(f->precision, f->in_channels);
+      cudaError_t e = launch_pack(pp, s);
+      if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
+      OIDNX_TRY(prof_mark(f, prof, -1, s));
+      OIDNX_TRY(enqueue_network(f, P, prof, s));
+      UnpackParams up;
+      std::memset(&up, 0, sizeof(up));
+      up.net = static_cast<const float4*>(P->ptr(V_OUT));
+      up.tw = tx.in_size;
+      up.in_x = tx.out_start - tx.in_start;
+      up.in_y = ty.out_start - ty.in_start;
+      up.color = static_cast<const float4*>(img[0]);
+      up.color_stride = stride[0] / 16;
+      up.out = static_cast<float4*>(img[3]);
+      up.out_stride = stride[3] / 16;
+      up.ox = tx.out_start;
+      up.oy = ty.out_start;
+      up.ow = tx.out_size;
+      up.oh = ty.out_size;
+      up.hdr = f->hdr;
+      up.scale = scale;
+      e = launch_unpack(up, s);
+      if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "output pass: %s", cudaGetErrorString(e));
+      OIDNX_TRY(prof_mark(f, prof, kLayers, s));
+    }
+  return ok();
+}
+
+size_t denoise_launches(const oidnx_filter* f) {
+  return f->tx.size() * f->ty.size() * (kLayers + 2);
+}
+
+bool filter_alive(oidnx_filter* f, oidnx_status* st) {
+  if (!f) {
+    *st = fail(OIDNX_ERR_INVALID_ARGUMENT, "filter is NULL");
+    return false;
+  }
+  if (f->released) {
+    *st = fail(OIDNX_ERR_RELEASED, "filter was released");
+    return false;
+  }
+  return true;
+}
+
+void invalidate(oidnx_filter* f) {
+  f->committed = false;
+  if (f->graph) {
+    cudaGraphExecDestroy(f->graph);
+    f->graph = nullptr;
+  }
+}
+
+oidnx_status execute_images(oidnx_filter* f, void* const img[4], const size_t stride[4],
+                            cudaStream_t s) {
+  if (!f->committed) return fail(OIDNX_ERR_NOT_COMMITTED, "execute before a successful commit");
+  const bool prof = f->profile_next || f->profile_always;
+  if (f->profile_next) {
+    // One-shot profile: a plain (eager) run with events between the kernels.
+    f->profile_next = false;
+    OIDNX_TRY(prof_begin(f, denoise_launches(f)));
+    OIDNX_TRY(enqueue_denoise(f, img, stride, true, s));
+  } else {
+    bool same = f->graph && f->graph_profiled == prof;
+    for (int i = 0; i < 4 && same; ++i) same = f->graph_img[i] == img[i];
+    if (!same) {
+      if (f->graph) {
+        cudaGraphExecDestroy(f->graph);
+        f->graph = nullptr;
+      }
+      if (!f->capture_stream)
+        OIDNX_CUDA(cudaStreamCreateWithFlags(&f->capture_stream, cudaStreamNonBlocking));
+      if (prof) OIDNX_TRY(prof_begin(f, denoise_launches(f)));
+      OIDNX_CUDA(cudaStreamBeginCapture(f->capture_stream, cudaStreamCaptureModeThreadLocal));
+      oidnx_status st = enqueue_denoise(f, img, stride, prof, f->capture_stream);
+      cudaGraph_t g = nullptr;
+      cudaError_t e = cudaStreamEndCapture(f->capture_stream, &g);
+      if (st != OIDNX_OK) {
+        if (g) cudaGraphDestroy(g);
+        return st;
+      }
+      if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
+      e = cudaGraphInstantiate(&f->graph, g, 0);
+      cudaGraphDestroy(g);
+      if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+      f->graph_profiled = prof;
+      for (int i = 0; i < 4; ++i) f->graph_img[i] = img[i];
+    }
+    OIDNX_CUDA(cudaGraphLaunch(f->graph, s));
+  }
+  OIDNX_CUDA(cudaEventRecord(f->current->done, s));
+  f->last_plan = f->current;
+  return ok();
+}
+
+}  // namespace
+
+// ======================================================================
+// C ABI
+// ======================================================================
+extern "C" {
+
+const char* oidnx_last_error(void) { return g_last_error.c_str(); }
+
+const char* oidnx_version(void) { return "oidnx 0.1 (sm_103a)"; }
+
+int oidnx_default_overlap(void) { return default_overlap_value(); }
+
+oidnx_status oidnx_plan_tiles(int width, int height, int max_tile_size, int overlap, int* rects,
+                              int cap, int* count) {
+  if (width <= 0 || height <= 0 || !count || cap < 0 || (cap > 0 && !rects))
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "plan_tiles: bad arguments");
+  if (overlap < 0) overlap = default_overlap_value();
+  const int limit = max_tile_size > 0 ? max_tile_size : round_up(std::max(width, height), 16);
+  std::vector<AxisTile> xs, ys;
+  if (!plan_axis(width, limit, overlap, &xs) || !plan_axis(height, limit, overlap, &ys))
+    return fail(OIDNX_ERR_INVALID_ARGUMENT,
+                "maxTileSize %d too small for overlap %d (or bad overlap)", max_tile_size, overlap);
+  *count = static_cast<int>(xs.size() * ys.size());
+  int i = 0;
+  for (const AxisTile& y : ys)
+    for (const AxisTile& x : xs) {
+      if (i < cap) {
+        int* r = rects + 8 * i;
+        r[0] = x.in_start; r[1] = y.in_start; r[2] = x.in_size; r[3] = y.in_size;
+        r[4] = x.out_start; r[5] = y.out_start; r[6] = x.out_size; r[7] = y.out_size;
+      }
+      ++i;
+    }
+  return ok();
+}
+
+oidnx_status oidnx_filter_create(const void* blob, size_t bytes, int precision,
+                                 oidnx_filter** out) {
+  if (!blob || !out) return fail(OIDNX_ERR_INVALID_ARGUMENT, "filter_create: NULL argument");
+  *out = nullptr;
+  if (precision < 0 || precision > 2)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "precision must be 0 (auto), 1 (fp32) or 2 (fp16)");
+  ConvTensors T[kLayers];
+  int cin = 0;
+  OIDNX_TRY(parse_blob(blob, bytes, T, &cin));
+  std::unique_ptr<oidnx_filter> f(new oidnx_filter());
+  f->precision = precision == OIDNX_PRECISION_FP32 ? OIDNX_PRECISION_FP32 : OIDNX_PRECISION_FP16;
+  f->in_channels = cin;
+  auto out_ch = [&](int v) -> int {
+    if (v == V_IN) return cin;
+    for (int l = 0; l < kLayers; ++l)
+      if (kDefs[l].dst == v) return T[l].cout;
+    return 0;
+  };
+  oidnx_status st = OIDNX_OK;
+  for (int l = 0; l < kLayers && st == OIDNX_OK; ++l) {
+    const int c0 = out_ch(kDefs[l].src0);
+    const int c1 = kDefs[l].src1 >= 0 ? out_ch(kDefs[l].src1) : 0;
+    st = make_device_layer(T[l], c0, c1, f->precision, &f->layers[l]);
+    f->weight_bytes += f->layers[l].weight_bytes;
+  }
+  if (st == OIDNX_OK) {
+    cudaError_t e = cudaMalloc(&f->status, 256);
+    if (e == cudaSuccess) e = cudaMemset(f->status, 0, 256);
+    if (e != cudaSuccess) st = fail(OIDNX_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+  }
+  if (st != OIDNX_OK) {
+    std::string msg = g_last_error;
+    for (DeviceLayer& L : f->layers) free_layer(L);
+    cudaFree(f->status);
+    g_last_error = msg;
+    return st;
+  }
+  *out = f.release();
+  return ok();
+}
+
+oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr,
+                                    size_t row_stride_bytes) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  if (which < 0 || which > 3) return fail(OIDNX_ERR_INVALID_ARGUMENT, "bad image slot %d", which);
+  if (reinterpret_cast<uintptr_t>(device_ptr) % 16)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "image pointer must be 16-byte aligned");
+  if (row_stride_bytes % 16)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "row stride must be a multiple of 16 bytes");
+  f->img[which] = device_ptr;
+  f->img_stride[which] = row_stride_bytes;
+  invalidate(f);
+  return ok();
+}
+
+oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  if (!name) return fail(OIDNX_ERR_INVALID_ARGUMENT, "NULL parameter name");
+  const std::string n(name);
+  if (n == "width" || n == "height") {
+    if (value <= 0) return fail(OIDNX_ERR_INVALID_ARGUMENT, "Image dimensions must be positive");
+    (n == "width" ? f->width : f->height) = value;
+  } else if (n == "hdr") {
+    if (value != 0 && value != 1) return fail(OIDNX_ERR_INVALID_ARGUMENT, "hdr must be 0 or 1");
+    f->hdr = value;
+  } else if (n == "transfer") {
+    if (value != OIDNX_TRANSFER_PU && value != OIDNX_TRANSFER_LOG)
+      return fail(OIDNX_ERR_INVALID_ARGUMENT, "transfer must be 0 (pu) or 1 (log)");
+    f->transfer = value;
+  } else if (n == "maxTileSize") {
+    if (value < 0) return fail(OIDNX_ERR_INVALID_ARGUMENT, "maxTileSize must be >= 0");
+    f->max_tile = value;
+  } else if (n == "overlap") {
+    if (value < -1 || (value >= 0 && value % 16))
+      return fail(OIDNX_ERR_INVALID_ARGUMENT, "overlap must be -1 or a multiple of 16");
+    f->overlap = value;
+  } else if (n == "shapeCacheSize") {
+    if (value < 1) return fail(OIDNX_ERR_INVALID_ARGUMENT, "shapeCacheSize must be >= 1");
+    f->shape_cache = value;
+  } else if (n == "keepActivations") {
+    f->keep_acts = value ? 1 : 0;
+    for (auto& p : f->plans) f->retired.push_back(std::move(p));
+    f->plans.clear();
+    f->current = nullptr;
+    f->last_plan = nullptr;
+  } else if (n == "profile") {
+    f->profile_always = value ? 1 : 0;  // the graph is re-recorded on demand
+    return ok();
+  } else {
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "unknown integer parameter '%s'", name);
+  }
+  invalidate(f);
+  return ok();
+}
+
+oidnx_status oidnx_filter_get_int(oidnx_filter* f, const char* name, int* value) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  if (!name || !value) return fail(OIDNX_ERR_INVALID_ARGUMENT, "NULL argument");
+  const std::string n(name);
+  if (n == "width") *value = f->width;
+  else if (n == "height") *value = f->height;
+  else if (n == "hdr") *value = f->hdr;
+  else if (n == "transfer") *value = f->transfer;
+  else if (n == "maxTileSize") *value = f->max_tile;
+  else if (n == "overlap") *value = f->overlap < 0 ? default_overlap_value() : f->overlap;
+  else if (n == "shapeCacheSize") *value = f->shape_cache;
+  else if (n == "keepActivations") *value = f->keep_acts;
+  else if (n == "profile") *value = f->profile_always;
+  else if (n == "inputChannels") *value = f->in_channels;
+  else if (n == "precision") *value = f->precision;
+  else if (n == "tiles") *value = f->committed ? static_cast<int>(f->tx.size() * f->ty.size()) : 0;
+  else return fail(OIDNX_ERR_INVALID_ARGUMENT, "unknown integer parameter '%s'", name);
+  return ok();
+}
+
+oidnx_status oidnx_filter_set_float(oidnx_filter* f, const char* name, float value) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  if (!name) return fail(OIDNX_ERR_INVALID_ARGUMENT, "NULL parameter name");
+  if (std::string(name) != "inputScale")
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "unknown float parameter '%s'", name);
+  if (!std::isfinite(value) || value < 0.0f)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "inputScale must be finite and >= 0");
+  f->input_scale = value;
+  invalidate(f);
+  return ok();
+}
+
+oidnx_status oidnx_filter_commit(oidnx_filter* f) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  invalidate(f);
+  if (f->width <= 0 || f->height <= 0)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "Image dimensions must be positive");
+  if (f->hdr && f->transfer == OIDNX_TRANSFER_PU)
+    return fail(OIDNX_ERR_UNSUPPORTED, "the 'pu' transfer is not defined by this build");
+  const int sources = f->in_channels / 3;
+  if (!f->img[OIDNX_IMAGE_COLOR] || !f->img[OIDNX_IMAGE_OUTPUT] ||
+      (sources > 1 && !f->img[OIDNX_IMAGE_ALBEDO]) || (sources > 2 && !f->img[OIDNX_IMAGE_NORMAL]))
+    return fail(OIDNX_ERR_INVALID_ARGUMENT,
+                "expected %d input image(s) (colour%s) and an output image", sources,
+                sources == 3 ? ", albedo, normal" : sources == 2 ? ", albedo" : "");
+  for (int i = 0; i < 4; ++i)
+    if (f->img[i] && f->img_stride[i] != 0 && f->img_stride[i] < static_cast<size_t>(f->width) * 16)
+      return fail(OIDNX_ERR_INVALID_ARGUMENT, "row stride of image %d below width*16", i);
+  const int overlap = f->overlap < 0 ? default_overlap_value() : f->overlap;
+  const int limit = f->max_tile > 0 ? f->max_tile : round_up(std::max(f->width, f->height), 16);
+  if (!plan_axis(f->width, limit, overlap, &f->tx) || !plan_axis(f->height, limit, overlap, &f->ty))
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "maxTileSize %d too small for overlap %d",
+                f->max_tile, overlap);
+  Plan* P = nullptr;
+  OIDNX_TRY(get_plan(f, f->tx[0].in_size, f->ty[0].in_size, &P));
+  f->current = P;
+  f->committed = true;
+  return ok();
+}
+
+oidnx_status oidnx_filter_execute(oidnx_filter* f, void* stream) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  void* img[4];
+  size_t stride[4];
+  for (int i = 0; i < 4; ++i) {
+    img[i] = f->img[i];
+    stride[i] = f->img_stride[i] ? f->img_stride[i] : static_cast<size_t>(f->width) * 16;
+  }
+  return execute_images(f, img, stride, static_cast<cudaStream_t>(stream));
+}
+
+oidnx_status oidnx_filter_execute_host(oidnx_filter* f, const float* color, const float* albedo,
+                                       const float* normal, float* output, void* stream) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  if (!f->committed) return fail(OIDNX_ERR_NOT_COMMITTED, "execute before a successful commit");
+  const int sources = f->in_channels / 3;
+  if (!color || !output || (sources > 1 && !albedo) || (sources > 2 && !normal))
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "missing host image");
+  const size_t bytes = static_cast<size_t>(f->width) * f->height * 16;
+  if (f->host_img_bytes != bytes) {
+    for (int i = 0; i < 4; ++i) {
+      cudaFree(f->host_img[i]);
+      f->host_img[i] = nullptr;
+    }
+    f->host_img_bytes = 0;
+    for (int i = 0; i < 4; ++i) OIDNX_CUDA(cudaMalloc(&f->host_img[i], bytes));
+    f->host_img_bytes = bytes;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float* src[3] = {color, albedo, normal};
+  for (int i = 0; i < sources; ++i)
+    OIDNX_CUDA(cudaMemcpyAsync(f->host_img[i], src[i], bytes, cudaMemcpyHostToDevice, s));
+  size_t stride[4];
+  for (int i = 0; i < 4; ++i) stride[i] = static_cast<size_t>(f->width) * 16;
+  OIDNX_TRY(execute_images(f, f->host_img, stride, s));
+  OIDNX_CUDA(cudaMemcpyAsync(output, f->host_img[3], bytes, cudaMemcpyDeviceToHost, s));
+  OIDNX_CUDA(cudaStreamSynchronize(s));
+  return ok();
+}
+
+oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w, int h,
+                                   void* out, void* stream) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  if (!packed_in || !out || w <= 0 || h <= 0)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "network_execute: bad arguments");
+  if ((reinterpret_cast<uintptr_t>(packed_in) | reinterpret_cast<uintptr_t>(out)) % 16)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "network_execute: pointers must be 16-byte aligned");
+  Plan* P = nullptr;
+  OIDNX_TRY(get_plan(f, w, h, &P));
+  if (f->current != P && f->graph) {
+    // the denoise graph stays valid: it refers to its own plan
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool prof = f->profile_next || f->profile_always;
+  f->profile_next = false;
+  if (prof) OIDNX_TRY(prof_begin(f, kLayers));
+  OIDNX_CUDA(cudaMemcpyAsync(P->ptr(V_IN), packed_in, P->value_bytes[V_IN],
+                             cudaMemcpyDeviceToDevice, s));
+  OIDNX_TRY(prof_mark(f, prof, -2, s));
+  OIDNX_TRY(enqueue_network(f, P, prof, s));
+  OIDNX_CUDA(cudaMemcpyAsync(out, P->ptr(V_OUT), P->value_bytes[V_OUT], cudaMemcpyDeviceToDevice, s));
+  OIDNX_CUDA(cudaEventRecord(P->done, s));
+  f->last_plan = P;
+  return ok();
+}
+
+oidnx_status oidnx_filter_sync_status(oidnx_filter* f) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  OIDNX_CUDA(cudaDeviceSynchronize());
+  int word = 0;
+  OIDNX_CUDA(cudaMemcpy(&word, f->status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (word) {
+    OIDNX_CUDA(cudaMemset(f->status, 0, sizeof(int)));
+    return fail(OIDNX_ERR_TIMEOUT, "a device-side wait gave up (status bits 0x%x)", word);
+  }
+  return ok();
+}
+
+oidnx_status oidnx_profile_next(oidnx_filter* f) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  f->profile_next = true;
+  return ok();
+}
+
+oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  Profile& P = f->prof;
+  if (!P.valid || P.used < 2 || !json)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "nothing profiled");
+  OIDNX_CUDA(cudaEventSynchronize(P.ev[P.used - 1]));
+  double ms[kLayers + 3] = {};  // index label + 2: -2 unused, -1 pack, 0..15, 16 unpack
+  int count[kLayers + 3] = {};
+  for (int i = 1; i < P.used; ++i) {
+    float t = 0;
+    OIDNX_CUDA(cudaEventElapsedTime(&t, P.ev[i - 1], P.ev[i]));
+    const int idx = P.label[i - 1] + 2;
+    if (idx >= 0 && idx < kLayers + 3) {
+      ms[idx] += t;
+      count[idx] += 1;
+    }
+  }
+  float total = 0;
+  OIDNX_CUDA(cudaEventElapsedTime(&total, P.ev[0], P.ev[P.used - 1]));
+  const Plan* plan = f->last_plan;
+  std::string s = "{\"totalMs\":" + std::to_string(total) + ",\"layers\":[";
+  bool first = true;
+  auto add = [&](const char* id, int idx, double flop, double bytes) {
+    if (count[idx] == 0) return;
+    char buf[256];
+    snprintf(buf, sizeof(buf), "%s{\"id\":\"%s\",\"ms\":%.6f,\"launches\":%d,\"flop\":%.0f,\"bytes\":%.0f}",
+             first ? "" : ",", id, ms[idx], count[idx], flop * count[idx], bytes * count[idx]);
+    s += buf;
+    first = false;
+  };
+  const int sources = f->in_channels / 3;
+  const int bpe = f->precision == OIDNX_PRECISION_FP16 ? 2 : 4;
+  const double tile_px = plan ? static_cast<double>(plan->w) * plan->h : 0;
+  add("input-pack", 1, 0, tile_px * (16.0 * sources + f->in_channels * bpe));
+  for (int l = 0; l < kLayers; ++l)
+    add(kLayerNames[l], l + 2, plan ? plan->launches[l].flop : 0,
+        plan ? plan->launches[l].bytes : 0);
+  double out_px = 0;
+  for (const AxisTile& y : f->ty)
+    for (const AxisTile& x : f->tx) out_px += static_cast<double>(x.out_size) * y.out_size;
+  const int tiles = static_cast<int>(std::max<size_t>(1, f->tx.size() * f->ty.size()));
+  add("output", kLayers + 2, 0, out_px / tiles * 48.0);
+  s += "]}";
+  if (s.size() + 1 > cap) return fail(OIDNX_ERR_INVALID_ARGUMENT, "profile buffer too small");
+  std::memcpy(json, s.c_str(), s.size() + 1);
+  return ok();
+}
+
+oidnx_status oidnx_get_resource_info(oidnx_filter* f, char* json, size_t cap) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  if (!json) return fail(OIDNX_ERR_INVALID_ARGUMENT, "NULL buffer");
+  size_t arena = 0;
+  for (auto& p : f->plans) arena += p->arena_bytes;
+  char buf[512];
+  snprintf(buf, sizeof(buf),
+           "{\"weightBytes\":%zu,\"arenaBytes\":%zu,\"plans\":%zu,\"retiredPlans\":%zu,"
+           "\"graphs\":%d,\"hostImageBytes\":%zu,\"precision\":\"%s\",\"inputChannels\":%d}",
+           f->weight_bytes, arena, f->plans.size(), f->retired.size(), f->graph ? 1 : 0,
+           f->host_img_bytes * 4, f->precision == OIDNX_PRECISION_FP16 ? "fp16" : "fp32",
+           f->in_channels);
+  if (strlen(buf) + 1 > cap) return fail(OIDNX_ERR_INVALID_ARGUMENT, "buffer too small");
+  std::memcpy(json, buf, strlen(buf) + 1);
+  return ok();
+}
+
+oidnx_status oidnx_debug_read_activation(oidnx_filter* f, int layer, void* host_dst, size_t cap,
+                                         size_t* bytes_needed) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  const Plan* P = f->last_plan;
+  if (!P) return fail(OIDNX_ERR_INVALID_ARGUMENT, "no network run to read from");
+  if (layer < 0 || layer > kLayers) return fail(OIDNX_ERR_INVALID_ARGUMENT, "bad layer %d", layer);
+  const int v = layer == 0 ? V_IN : kDefs[layer - 1].dst;
+  const Extent e = P->value_ext[v];
+  const int C = v == V_OUT ? 3 : P->value_ch[v];
+  const size_t need = static_cast<size_t>(e.w) * e.h * C * 4;
+  if (bytes_needed) *bytes_needed = need;
+  if (!host_dst) return ok();
+  if (cap < need) return fail(OIDNX_ERR_INVALID_ARGUMENT, "need %zu bytes", need);
+  std::vector<uint8_t> raw(P->value_bytes[v]);
+  OIDNX_CUDA(cudaDeviceSynchronize());
+  OIDNX_CUDA(cudaMemcpy(raw.data(), P->ptr(v), raw.size(), cudaMemcpyDeviceToHost));
+  float* dst = static_cast<float*>(host_dst);
+  if (v == V_OUT) {
+    const float* src = reinterpret_cast<const float*>(raw.data());
+    for (size_t p = 0; p < static_cast<size_t>(e.w) * e.h; ++p)
+      for (int c = 0; c < 3; ++c) dst[p * 3 + c] = src[p * 4 + c];
+    return ok();
+  }
+  const int lanes = f->precision == OIDNX_PRECISION_FP16 ? 8 : 4;
+  const int chunks = act_chunks(f->precision, C);
+  for (int y = 0; y < e.h; ++y)
+    for (int x = 0; x < e.w; ++x)
+      for (int c = 0; c < C; ++c) {
+        const size_t idx = ((static_cast<size_t>(y) * chunks + c / lanes) * e.w + x) * lanes + c % lanes;
+        float val;
+        if (lanes == 8) {
+          uint16_t b;
+          std::memcpy(&b, raw.data() + idx * 2, 2);
+          val = half_bits_to_float(b);
+        } else {
+          std::memcpy(&val, raw.data() + idx * 4, 4);
+        }
+        dst[(static_cast<size_t>(y) * e.w + x) * C + c] = val;
+      }
+  return ok();
+}
+
+void oidnx_filter_release(oidnx_filter* f) {
+  if (!f || f->released) return;
+  f->released = true;
+  cudaDeviceSynchronize();
+  if (f->graph) cudaGraphExecDestroy(f->graph);
+  for (auto& p : f->plans) destroy_plan(p.get());
+  for (auto& p : f->retired) destroy_plan(p.get());
+  f->plans.clear();
+  f->retired.clear();
+  for (DeviceLayer& L : f->layers) free_layer(L);
+  for (int i = 0; i < 4; ++i) cudaFree(f->host_img[i]);
+  for (cudaEvent_t e : f->prof.ev) cudaEventDestroy(e);
+  if (f->capture_stream) cudaStreamDestroy(f->capture_stream);
+  cudaFree(f->status);
+  delete f;
+}
+
+oidnx_status oidnx_conv_create(const float* weight, const float* bias, int cout, int cin,
+                               int precision, oidnx_conv** out) {
+  if (!weight || !bias || !out || cout <= 0 || cin <= 0)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "conv_create: bad arguments");
+  if (precision != OIDNX_PRECISION_FP16 && precision != OIDNX_PRECISION_FP32)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "conv_create: precision must be fp16 or fp32");
+  if (cout > 256) return fail(OIDNX_ERR_UNSUPPORTED, "conv_create: more than 256 outputs");
+  ConvTensors T;
+  T.cout = cout;
+  T.cin = cin;
+  T.w.assign(weight, weight + static_cast<size_t>(cout) * cin * 9);
+  T.b.assign(bias, bias + cout);
+  std::unique_ptr<oidnx_conv> c(new oidnx_conv());
+  c->precision = precision;
+  oidnx_status st = make_device_layer(T, cin, 0, precision, &c->L);
+  if (st == OIDNX_OK) {
+    cudaError_t e = cudaMalloc(&c->status, 256);
+    if (e == cudaSuccess) e = cudaMemset(c->status, 0, 256);
+    if (e != cudaSuccess) st = fail(OIDNX_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+  }
+  if (st != OIDNX_OK) {
+    std::string msg = g_last_error;
+    free_layer(c->L);
+    cudaFree(c->status);
+    g_last_error = msg;
+    return st;
+  }
+  *out = c.release();
+  return ok();
+}
+
+oidnx_status oidnx_conv_execute(oidnx_conv* c, const void* in, void* out, int w, int h, int relu,
+                                void* stream) {
+  if (!c || !in || !out || w <= 0 || h <= 0)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "conv_execute: bad arguments");
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "conv_execute: pointers must be 16-byte aligned");
+  if (!relu) return fail(OIDNX_ERR_UNSUPPORTED, "conv_execute: only relu=1 for hidden layers");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LayerLaunch LL;
+  std::memset(&LL, 0, sizeof(LL));
+  LL.layer = 0;
+  if (c->precision == OIDNX_PRECISION_FP16) {
+    LL.tc = true;
+    OIDNX_TRY(build_tc_launch(c->L, kPlain, in, Extent{w, h}, nullptr, w, h, out, c->status,
+                              &LL.tcl));
+  } else {
+    LL.tc = false;
+    build_simt_launch(c->L, kPlain, in, Extent{w, h}, nullptr, w, h, out, &LL.sp);
+  }
+  return run_launch(LL, s);
+}
+
+void oidnx_conv_release(oidnx_conv* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  free_layer(c->L);
+  cudaFree(c->status);
+  delete c;
+}
+
+}  // extern "C"

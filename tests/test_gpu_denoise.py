@@ -1,0 +1,115 @@
+"""Whole denoise on the GPU against the oracle for the four image workloads:
+128x128 fp32 (full image), 1920x1080 fp16 (single tile), 3840x2160 fp16
+tiled (maxTileSize 1024, overlap 96), 3840x2160 fp32 LDR colour-only with 5%
+NaN/Inf.  Full-size runs are checked on 16-aligned crops that the oracle can
+afford: with a margin of the default overlap (96 >= the network's dependency
+radius 94) the oracle's output on a crop equals the full-frame output in the
+crop's interior, so the interior is compared pixel by pixel."""
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+import synth
+from oracle import passes, unet
+from oracle.numerics import FLT_MAX, sanitize
+from tests._gpu import Denoiser, rel_l2
+
+import conv2d_implicit_gemm_gb300 as ox
+
+MARGIN = 96
+
+
+def _crop_check(net_gpu, imgs, weights, precision, hdr, scale, crop, tile_w, tile_h, tol):
+    cx, cy, cw, ch = crop
+    packed = passes.pack_tile(imgs, crop, hdr, scale, precision)
+    ref = unet.forward(packed, weights, precision)
+    ml = 0 if cx == 0 else MARGIN
+    mt = 0 if cy == 0 else MARGIN
+    mr = 0 if cx + cw == tile_w else MARGIN
+    mb = 0 if cy + ch == tile_h else MARGIN
+    r = ref[mt:ch - mb, ml:cw - mr]
+    g = net_gpu[cy + mt:cy + ch - mb, cx + ml:cx + cw - mr]
+    assert r.size > 0
+    if precision == "fp16":
+        top = FLT_MAX if hdr else 1.0
+        diff = np.abs(sanitize(g, 0, top).astype(np.float64) - sanitize(r, 0, top))
+        assert diff.max() <= tol, diff.max()
+    else:
+        assert rel_l2(g, r) <= tol
+
+
+def test_config_128x128_fp32_full_image():
+    w = h = 128
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    weights = synth.unet_weights(9)
+    d = Denoiser(weights, ox.PRECISION_FP32, imgs, True, keep=True)
+    try:
+        out = d.run()
+        net = d.activation(16, h, w, 3)
+    finally:
+        d.close()
+    ref = unet.denoise(imgs, weights, hdr=True, precision="fp32")
+    ref_net = unet.forward(passes.pack_tile(imgs, (0, 0, w, h), True, 1.0, "fp32"),
+                           weights, "fp32")
+    assert rel_l2(net, ref_net) <= 1e-4
+    assert rel_l2(out[..., :3], ref[..., :3]) <= 1e-4
+    assert np.array_equal(out[..., 3].view(np.uint32), imgs[0][..., 3].view(np.uint32))
+
+
+def test_config_1080p_fp16_single_tile():
+    w, h = 1920, 1080
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    weights = synth.unet_weights(9)
+    d = Denoiser(weights, ox.PRECISION_FP16, imgs, True)
+    try:
+        out = d.run()
+        assert ox.oidnx_filter_get_int(d.f, "tiles") == 1
+        net = d.activation(16, 1088, 1920, 3)
+    finally:
+        d.close()
+    assert np.isfinite(out[..., :3]).all()
+    for crop in [(0, 0, 256, 256), (832, 416, 256, 256), (1664, 832, 256, 256)]:
+        _crop_check(net, imgs, weights, "fp16", True, 1.0, crop, 1920, 1088, 2e-2)
+    # final HDR image on one interior window
+    ref = unet.denoise([im[400:656, 800:1056] for im in imgs], weights, hdr=True)
+    got = out[400 + MARGIN:656 - MARGIN, 800 + MARGIN:1056 - MARGIN, :3]
+    assert rel_l2(got, ref[MARGIN:-MARGIN, MARGIN:-MARGIN, :3]) <= 2e-2
+
+
+def test_config_4k_fp16_tiled_equals_single_tile():
+    w, h = 3840, 2160
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    weights = synth.unet_weights(9)
+    d = Denoiser(weights, ox.PRECISION_FP16, imgs, True, max_tile_size=1024)
+    try:
+        tiled = d.run()
+        assert ox.oidnx_filter_get_int(d.f, "tiles") == 15
+    finally:
+        d.close()
+    d = Denoiser(weights, ox.PRECISION_FP16, imgs, True, max_tile_size=0)
+    try:
+        whole = d.run()
+        net = d.activation(16, 2160 + 16, 3840, 3)
+    finally:
+        d.close()
+    assert np.array_equal(tiled.view(np.uint32), whole.view(np.uint32))
+    _crop_check(net, imgs, weights, "fp16", True, 1.0, (2144, 1008, 256, 256), 3840, 2176, 2e-2)
+
+
+def test_config_4k_fp32_ldr_color_only_nan_inf():
+    w, h = 3840, 2160
+    imgs = synth.denoise_inputs(w, h, 1, hdr=False, nan_fraction=0.05)
+    weights = synth.unet_weights(3)
+    d = Denoiser(weights, ox.PRECISION_FP32, imgs, False)
+    try:
+        out = d.run()
+        net = d.activation(16, 2176, 3840, 3)
+    finally:
+        d.close()
+    assert np.isfinite(out).sum() == out[..., :3].size + np.isfinite(imgs[0][..., 3]).sum()
+    assert (out[..., :3] >= 0).all() and (out[..., :3] <= 1).all()
+    _crop_check(net, imgs, weights, "fp32", False, 1.0, (3584, 1920, 256, 256), 3840, 2176, 1e-4)
+    ref = passes.unpack_rect(net[:h, :w], imgs[0], False, 1.0)
+    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))

@@ -1,0 +1,99 @@
+"""The 16-layer network on the GPU against the oracle: every stored
+activation checked in isolation (the oracle's layer applied to the GPU's own
+input activations) and the chained output checked end to end."""
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+import synth
+from oracle import layers, unet
+from oracle.numerics import round_storage
+from tests import _layout
+from tests._gpu import empty_dev, rel_l2, stream, to_dev, to_host
+
+import conv2d_implicit_gemm_gb300 as ox
+
+# activation index (0 = input, k = output of layer k-1) -> its sources and op
+LAYER_OPS = {
+    1: (0, None, "plain"), 2: (1, None, "pool"), 3: (2, None, "pool"),
+    4: (3, None, "pool"), 5: (4, None, "pool"), 6: (5, None, "plain"),
+    7: (6, None, "plain"), 8: (7, 4, "dec"), 9: (8, None, "plain"),
+    10: (9, 3, "dec"), 11: (10, None, "plain"), 12: (11, 2, "dec"),
+    13: (12, None, "plain"), 14: (13, 0, "dec"), 15: (14, None, "plain"),
+    16: (15, None, "final"),
+}
+VALUE_NAMES = ["input", "enc_conv0", "pool1", "pool2", "pool3", "pool4",
+               "enc_conv5a", "enc_conv5b", "dec_conv4a", "dec_conv4b",
+               "dec_conv3a", "dec_conv3b", "dec_conv2a", "dec_conv2b",
+               "dec_conv1a", "dec_conv1b", "dec_conv0"]
+
+
+def _isolated(k, acts, weights, precision):
+    s0, s1, op = LAYER_OPS[k]
+    name = ox.LAYER_NAMES[k - 1]
+    w, b = weights[name]
+    wq = round_storage(w, precision).astype(np.float64)
+    x = acts[s0].astype(np.float64)
+    if op == "dec":
+        x = layers.decoder_input(x, acts[s1].astype(np.float64))
+    y = layers.conv3x3(x, wq, b.astype(np.float64), relu=op != "final")
+    y = round_storage(y, "fp32" if op == "final" else precision).astype(np.float64)
+    if op == "pool":
+        y = layers.maxpool2x2(y)
+    return y
+
+
+def _run_network(weights, packed_logical, precision):
+    h, w, c = packed_logical.shape
+    prec = ox.PRECISION_FP16 if precision == "fp16" else ox.PRECISION_FP32
+    f = ox.oidnx_filter_create(ox.write_weight_blob(weights), prec)
+    try:
+        ox.oidnx_filter_set_int(f, "keepActivations", 1)
+        src = to_dev(_layout.to_internal(packed_logical, precision))
+        out = empty_dev(w * h * 16)
+        ox.oidnx_network_execute(f, src.data_ptr(), w, h, out.data_ptr(), stream())
+        ox.oidnx_filter_sync_status(f)
+        acts = [ox.oidnx_debug_read_activation(f, k) for k in range(17)]
+        final = to_host(out, np.float32, (h, w, 4)).copy()
+    finally:
+        ox.oidnx_filter_release(f)
+    return acts, final
+
+
+@pytest.mark.parametrize("precision", ["fp16", "fp32"])
+@pytest.mark.parametrize("w,h", [(64, 48), (80, 34), (130, 20)])
+def test_network_layers_match_oracle(precision, w, h):
+    weights = synth.unet_weights(9, bias_scale=0.05)
+    x = synth.uniform_activations(h, w, 9, seed=w + h, low=0.0, high=1.0)
+    x = round_storage(x, precision)
+    acts_flat, final = _run_network(weights, x, precision)
+    ref = unet.forward(x, weights, precision, keep=True)
+    acts = []
+    for k, name in enumerate(VALUE_NAMES):
+        shape = ref[name].shape if k < 16 else ref["dec_conv0"].shape
+        acts.append(acts_flat[k].reshape(shape))
+    assert np.array_equal(acts[0], np.asarray(x, np.float32))
+    tol = 1e-2 if precision == "fp16" else 1e-4
+    for k in range(1, 17):
+        iso = _isolated(k, acts, weights, precision)
+        err = rel_l2(acts[k], iso)
+        assert err <= tol, (VALUE_NAMES[k], err)
+    # chained end to end
+    out = ref["dec_conv0"]
+    assert np.array_equal(final[..., :3], acts[16].astype(np.float32))
+    assert not final[..., 3].any()
+    if precision == "fp16":
+        assert np.abs(final[..., :3] - out).max() <= 2e-2
+    else:
+        assert rel_l2(final[..., :3], out) <= 1e-4
+
+
+def test_network_one_pixel_and_tiny_inputs():
+    weights = synth.unet_weights(9, bias_scale=0.05)
+    for (w, h) in [(1, 1), (3, 2), (17, 5)]:
+        x = round_storage(synth.uniform_activations(h, w, 9, seed=w, low=0, high=1), "fp16")
+        _, final = _run_network(weights, x, "fp16")
+        ref = unet.forward(x, weights, "fp16")
+        assert np.abs(final[..., :3] - ref).max() <= 2e-2

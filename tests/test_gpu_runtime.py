@@ -1,0 +1,107 @@
+"""Runtime behaviour on the GPU: graph replay is bit-identical to the eager
+(profiled) run, the host-buffer path equals the device path, the LRU shape
+cache evicts safely, the profile and resource reports are well formed."""
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+import synth
+from oracle.numerics import round_storage
+from tests import _layout
+from tests._gpu import Denoiser, empty_dev, stream, to_dev, to_host
+
+import conv2d_implicit_gemm_gb300 as ox
+
+
+@pytest.fixture(scope="module")
+def weights():
+    return synth.unet_weights(9, bias_scale=0.05)
+
+
+def test_graph_replay_equals_eager_and_host_path(weights):
+    w, h = 300, 120        # 10 tiles of 224 x 128 (maxTileSize 224, overlap 96)
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    d = Denoiser(weights, ox.PRECISION_FP16, imgs, True, max_tile_size=224, overlap=96)
+    try:
+        ox.oidnx_profile_next(d.f)
+        eager = d.run()
+        prof = ox.oidnx_get_profile(d.f)
+        graph1 = d.run()
+        graph2 = d.run()
+        host_out = np.zeros((h, w, 4), np.float32)
+        ox.oidnx_filter_execute_host(d.f, imgs[0], imgs[1], imgs[2], host_out, stream())
+        info = ox.oidnx_get_resource_info(d.f)
+    finally:
+        d.close()
+    assert np.array_equal(eager.view(np.uint32), graph1.view(np.uint32))
+    assert np.array_equal(graph1.view(np.uint32), graph2.view(np.uint32))
+    assert np.array_equal(graph1.view(np.uint32), host_out.view(np.uint32))
+    ids = [l["id"] for l in prof["layers"]]
+    assert ids[0] == "input-pack" and ids[-1] == "output" and len(ids) == 18
+    assert all(l["launches"] == 10 for l in prof["layers"])
+    assert all(l["ms"] > 0 for l in prof["layers"])
+    assert prof["totalMs"] >= sum(l["ms"] for l in prof["layers"]) * 0.99
+    assert info["graphs"] == 1 and info["plans"] >= 1 and info["weightBytes"] > 0
+
+
+def test_profile_every_execution_through_the_graph(weights):
+    w, h = 96, 64
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    d = Denoiser(weights, ox.PRECISION_FP16, imgs, True)
+    try:
+        plain = d.run()
+        ox.oidnx_filter_set_int(d.f, "profile", 1)
+        profiled = d.run()
+        prof = ox.oidnx_get_profile(d.f)
+    finally:
+        d.close()
+    assert np.array_equal(plain.view(np.uint32), profiled.view(np.uint32))
+    assert len(prof["layers"]) == 18
+
+
+def test_shape_cache_eviction_with_work_in_flight(weights):
+    f = ox.oidnx_filter_create(ox.write_weight_blob(weights), ox.PRECISION_FP16)
+    try:
+        ox.oidnx_filter_set_int(f, "shapeCacheSize", 1)
+        shapes = [(64, 48), (96, 32), (64, 48), (40, 40)]
+        bufs, outs = [], []
+        for (w, h) in shapes:
+            x = round_storage(synth.uniform_activations(h, w, 9, seed=w * h, low=0, high=1), "fp16")
+            src = to_dev(_layout.to_internal(x, "fp16"))
+            out = empty_dev(w * h * 16)
+            ox.oidnx_network_execute(f, src.data_ptr(), w, h, out.data_ptr(), stream())
+            bufs.append(src)
+            outs.append((out, w, h))
+        ox.oidnx_filter_sync_status(f)
+        results = [to_host(o, np.float32, (h, w, 4)).copy() for (o, w, h) in outs]
+        info = ox.oidnx_get_resource_info(f)
+        assert info["plans"] == 1
+        # same shape, same input -> same bits, even across an eviction
+        assert np.array_equal(results[0].view(np.uint32), results[2].view(np.uint32))
+    finally:
+        ox.oidnx_filter_release(f)
+
+
+def test_execute_requires_commit_and_release_is_final(weights):
+    f = ox.oidnx_filter_create(ox.write_weight_blob(weights), ox.PRECISION_FP16)
+    with pytest.raises(ox.OidnxError) as e:
+        ox.oidnx_filter_execute(f, stream())
+    assert e.value.status == ox.ERR_NOT_COMMITTED
+    with pytest.raises(ox.OidnxError) as e:
+        ox.oidnx_filter_commit(f)                 # no images bound
+    assert e.value.status == ox.ERR_INVALID_ARGUMENT
+    ox.oidnx_filter_set_int(f, "hdr", 1)
+    ox.oidnx_filter_set_int(f, "transfer", ox.TRANSFER_PU)
+    ox.oidnx_filter_set_int(f, "width", 8)
+    ox.oidnx_filter_set_int(f, "height", 8)
+    img = empty_dev(8 * 8 * 16)
+    for i in range(4):
+        ox.oidnx_filter_set_image(f, i, img.data_ptr(), 0)
+    with pytest.raises(ox.OidnxError) as e:
+        ox.oidnx_filter_commit(f)
+    assert e.value.status == ox.ERR_UNSUPPORTED
+    ox.oidnx_filter_release(f)
+    torch.cuda.synchronize()
