@@ -677,6 +677,7 @@ void build_simt_launch(const DeviceLayer& L, int kind, const void* src0, Extent 
 }
 
 oidnx_status run_launch(const LayerLaunch& L, cudaStream_t s) {
+  (void)cudaGetLastError();  // drop a stale, non-sticky error of an earlier call
   cudaError_t e = L.tc ? launch_conv_tc(L.tcl, s) : launch_conv_simt(L.sp, s);
   if (e != cudaSuccess)
     return fail(OIDNX_ERR_CUDA, "%s launch: %s", kLayerNames[L.layer], cudaGetErrorString(e));
@@ -854,7 +855,14 @@ oidnx_status prof_mark(oidnx_filter* f, bool on, int label, cudaStream_t s) {
   if (!on) return ok();
   Profile& P = f->prof;
   if (P.used > 0) P.label[P.used - 1] = label;
-  OIDNX_CUDA(cudaEventRecord(P.ev[P.used], s));
+  // Inside stream capture an event becomes a graph node only when recorded
+  // as an external event; otherwise it would only order captured work.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  OIDNX_CUDA(cudaStreamIsCapturing(s, &cap));
+  if (cap == cudaStreamCaptureStatusActive)
+    OIDNX_CUDA(cudaEventRecordWithFlags(P.ev[P.used], s, cudaEventRecordExternal));
+  else
+    OIDNX_CUDA(cudaEventRecord(P.ev[P.used], s));
   P.used++;
   return ok();
 }
@@ -895,6 +903,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
       pp.fp16 = f->precision == OIDNX_PRECISION_FP16;
       pp.out = P->ptr(V_IN);
       pp.chunks = act_chunks(f->precision, f->in_channels);
+      (void)cudaGetLastError();
       cudaError_t e = launch_pack(pp, s);
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
       OIDNX_TRY(prof_mark(f, prof, -1, s));

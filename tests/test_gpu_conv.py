@@ -45,6 +45,14 @@ def _fp16_code_diff(a, b):
     return np.abs(ai - bi)
 
 
+def _assert_near_fp16(got, ref):
+    """fp32 accumulation vs the exact sum: every stored fp16 value is within
+    one fp16 step of the oracle's, or within 1e-4 absolute where the sum
+    cancels to a value whose fp16 spacing is finer than the fp32 rounding."""
+    close = (_fp16_code_diff(got, ref) <= 1) | (np.abs(got - ref) <= 1e-4)
+    assert close.all(), (np.abs(got - ref)[~close].max(), (~close).sum())
+
+
 CASES = [  # (width, height, cin, cout)
     (128, 4, 16, 16), (130, 5, 32, 32), (1, 1, 16, 16), (37, 9, 9, 32),
     (257, 3, 64, 48), (64, 20, 80, 96), (200, 7, 112, 112), (50, 6, 160, 96),
@@ -65,9 +73,7 @@ def test_conv_layer_matches_oracle(w, h, cin, cout, precision):
     err = rel_l2(got, ref)
     if precision == "fp16":
         assert err <= 1e-2, err
-        # fp32 accumulation vs exact sum: the stored fp16 codes differ by at
-        # most one step except where cancellation is extreme
-        assert (_fp16_code_diff(got, ref) > 1).mean() < 1e-3
+        _assert_near_fp16(got, ref)
     else:
         assert err <= 1e-4, err
 
@@ -88,4 +94,4 @@ def test_single_conv_512x512_64_to_64_full_size():
     got, _ = _run_conv(x, wt, b, "fp16")
     ref = _oracle_conv(x, wt, b, "fp16")
     assert rel_l2(got, ref) <= 1e-2
-    assert (_fp16_code_diff(got, ref) > 1).mean() < 1e-4
+    _assert_near_fp16(got, ref)
