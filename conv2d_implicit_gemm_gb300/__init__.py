@@ -7,7 +7,7 @@ and streams are plain integers (e.g. ``tensor.data_ptr()`` and
 ``OidnxError`` carrying the status code and ``oidnx_last_error()``.
 
 Importing fails loudly when the library has not been built (there is no
-fallback): build it with ``python -m conv2d_implicit_gemm_gb300.build``.
+fallback): build it with ``python conv2d_implicit_gemm_gb300/build.py``.
 """
 
 import ctypes
@@ -21,7 +21,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liboidnx.s
 if not os.path.exists(_LIB_PATH):
     raise ImportError(
         f"{_LIB_PATH} is missing: build the CUDA library first "
-        "(python -m conv2d_implicit_gemm_gb300.build)")
+        "(python conv2d_implicit_gemm_gb300/build.py)")
 _lib = ctypes.CDLL(_LIB_PATH)
 
 OK = 0
@@ -67,6 +67,7 @@ _sig("oidnx_filter_commit", _st, _vp)
 _sig("oidnx_filter_execute", _st, _vp, _vp)
 _sig("oidnx_filter_execute_host", _st, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("oidnx_network_execute", _st, _vp, _vp, _i, _i, _vp, _vp)
+_sig("oidnx_network_execute_noalloc", _st, _vp, _vp, _i, _i, _vp, _vp)
 _sig("oidnx_filter_sync_status", _st, _vp)
 _sig("oidnx_profile_next", _st, _vp)
 _sig("oidnx_get_profile", _st, _vp, ctypes.c_char_p, _sz)
@@ -156,6 +157,12 @@ def oidnx_filter_execute_host(f, color, albedo, normal, output, stream=0):
 
 def oidnx_network_execute(f, packed_in, w, h, out, stream=0):
     _check(_lib.oidnx_network_execute(f, packed_in, w, h, out, stream))
+
+
+def oidnx_network_execute_noalloc(f, packed_in, w, h, out, stream=0):
+    """Network forward without device allocation (intermediates in the
+    library's fixed 40 MiB device array; see oidnx.h)."""
+    _check(_lib.oidnx_network_execute_noalloc(f, packed_in, w, h, out, stream))
 
 
 def oidnx_filter_sync_status(f):

@@ -1,6 +1,7 @@
 """Build liboidnx.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-Usage: python -m conv2d_implicit_gemm_gb300.build   (or build() from Python)
+Usage: python conv2d_implicit_gemm_gb300/build.py   (run as a script: importing the
+package would load the library it is about to rebuild)
 
 Translation units compile in parallel; the result is
 conv2d_implicit_gemm_gb300/liboidnx.so.  Nothing here is imported at run time.
@@ -16,7 +17,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liboidnx.so")
-SOURCES = ["oidnx_host.cpp", "conv_tc.cu", "conv_simt.cu", "io_passes.cu"]
+SOURCES = ["oidnx_host.cpp", "conv_tc.cu", "conv_simt.cu", "io_passes.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

@@ -1000,6 +1000,103 @@ oidnx_status execute_images(oidnx_filter* f, void* const img[4], const size_t st
 }  // namespace
 
 // ======================================================================
+// network in caller-given scratch (no device allocation)
+// ======================================================================
+namespace oidnx {
+
+oidnx_status report_error(oidnx_status status, const char* message) {
+  return fail(status, "%s", message);
+}
+
+// Plan the network for a w x h input with every intermediate activation
+// placed in `arena` (cap bytes) by the same liveness best-fit rule as the
+// plan cache, the input read from `in` and the output written to `out`, then
+// enqueue the 16 conv kernels on `s`.  No device memory is allocated and no
+// plan is cached; the launch descriptors live on the stack.
+oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, int h, void* out,
+                                      void* arena, size_t cap, cudaStream_t s) {
+  if (!f) return fail(OIDNX_ERR_INVALID_ARGUMENT, "filter is NULL");
+  if (f->released) return fail(OIDNX_ERR_RELEASED, "filter was released");
+  if (!in || !out || w <= 0 || h <= 0)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "network_execute_noalloc: bad arguments");
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT,
+                "network_execute_noalloc: pointers must be 16-byte aligned");
+  Extent lvl[5];
+  lvl[0] = {w, h};
+  for (int l = 1; l < 5; ++l) lvl[l] = {(lvl[l - 1].w + 1) / 2, (lvl[l - 1].h + 1) / 2};
+  Extent ext[V_COUNT];
+  int ch[V_COUNT] = {};
+  ext[V_IN] = lvl[0];
+  ch[V_IN] = f->in_channels;
+  for (int l = 0; l < kLayers; ++l) {
+    const LayerDef& d = kDefs[l];
+    ext[d.dst] = lvl[d.kind == kPool ? d.level + 1 : d.level];
+    ch[d.dst] = f->layers[l].cout;
+  }
+  int last_use[V_COUNT];
+  for (int v = 0; v < V_COUNT; ++v) last_use[v] = -1;
+  for (int l = 0; l < kLayers; ++l) {
+    last_use[kDefs[l].src0] = l;
+    if (kDefs[l].src1 >= 0) last_use[kDefs[l].src1] = l;
+  }
+  struct Slot { size_t cap, off; int active; };
+  Slot slots[V_COUNT];
+  int nslots = 0;
+  size_t total = 0, off[V_COUNT] = {};
+  for (int l = 0; l < kLayers; ++l) {
+    const int v = kDefs[l].dst;
+    if (v == V_OUT) continue;  // written straight into the caller's output
+    for (int i = 0; i < nslots; ++i)
+      if (slots[i].active >= 0 && last_use[slots[i].active] < l) slots[i].active = -1;
+    const size_t need = round_up_sz(act_bytes(f->precision, ext[v].w, ext[v].h, ch[v], false), 1024);
+    int best = -1;
+    for (int i = 0; i < nslots; ++i)
+      if (slots[i].active < 0 && slots[i].cap >= need && (best < 0 || slots[i].cap < slots[best].cap))
+        best = i;
+    if (best < 0) {
+      slots[nslots] = {need, total, -1};
+      total += need;
+      best = nslots++;
+    }
+    slots[best].active = v;
+    off[v] = slots[best].off;
+  }
+  if (total > cap)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT,
+                "network_execute_noalloc: a %dx%d input needs %zu bytes of activation scratch; "
+                "the static arena holds %zu bytes",
+                w, h, total, cap);
+  auto ptr = [&](int v) -> void* {
+    if (v == V_IN) return const_cast<void*>(in);
+    if (v == V_OUT) return out;
+    return static_cast<uint8_t*>(arena) + off[v];
+  };
+  for (int l = 0; l < kLayers; ++l) {
+    const LayerDef& d = kDefs[l];
+    const DeviceLayer& L = f->layers[l];
+    LayerLaunch LL;
+    std::memset(&LL, 0, sizeof(LL));
+    LL.layer = l;
+    const Extent conv = lvl[d.level];
+    const void* s1 = d.src1 >= 0 ? ptr(d.src1) : nullptr;
+    if (f->precision == OIDNX_PRECISION_FP16) {
+      LL.tc = true;
+      OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, conv.w, conv.h,
+                                ptr(d.dst), f->status, &LL.tcl));
+    } else {
+      LL.tc = false;
+      build_simt_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, conv.w, conv.h, ptr(d.dst),
+                        &LL.sp);
+    }
+    OIDNX_TRY(run_launch(LL, s));
+  }
+  return ok();
+}
+
+}  // namespace oidnx
+
+// ======================================================================
 // C ABI
 // ======================================================================
 extern "C" {

@@ -134,6 +134,35 @@ oidnx_status oidnx_filter_execute_host(oidnx_filter* f, const float* color,
 oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w,
                                    int h, void* out, void* stream);
 
+/* The same network forward as oidnx_network_execute, for callers that must
+ * not allocate device memory once set-up is over: a renderer whose device
+ * memory budget is fixed after start-up (an allocation can synchronise the
+ * device and stall the frame), a plug-in whose host application owns all
+ * device memory, or any path where an allocation may not fail or wait.
+ * The pages have no counterpart of this call; it is an addition of this
+ * library.
+ *   - Allocates nothing: no cudaMalloc/cudaFree, no plan is created or
+ *     cached.  The intermediate activations live in one library-owned
+ *     device array of 40 MiB (41943040 bytes), present on every GPU that
+ *     loads the library until the process exits.
+ *   - Limit: the input must fit that array: fp16 up to 384 x 384 pixels,
+ *     fp32 up to 256 x 256 (other shapes: whatever the liveness plan of
+ *     the activations fits in 40 MiB).  Larger inputs fail with
+ *     INVALID_ARGUMENT and a message stating the bytes needed.
+ *   - packed_in / out: as for oidnx_network_execute (the kernels read the
+ *     input and write the output in place, without copies).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls on a device share the one array, and it keeps the previous
+ *     call's contents (every activation is fully written before it is
+ *     read, so nothing is cleared).  Calls that overlap on the GPU (on
+ *     different streams, or from several threads) race on the array and
+ *     give undefined results: serialise them.
+ *   - Device-side timeouts are reported by oidnx_filter_sync_status.
+ * Errors: INVALID_ARGUMENT, RELEASED, UNSUPPORTED, CUDA.  */
+oidnx_status oidnx_network_execute_noalloc(oidnx_filter* f, const void* packed_in, int w,
+                                           int h, void* out, void* stream);
+
 /* Wait for the filter's work, then report and clear the device error word:
  * OK, or TIMEOUT if a kernel's bounded wait gave up (its output is then
  * undefined).  Errors: CUDA.  */

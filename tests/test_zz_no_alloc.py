@@ -1,0 +1,66 @@
+"""oidnx_network_execute_noalloc: the network forward for callers that may
+not allocate device memory after set-up (fixed-budget renderers, plug-ins
+whose host owns all device memory).  Its intermediate activations live in
+the library's fixed device array instead of a filter-allocated arena.
+
+Checked against oidnx_network_execute on two calls in a row with different
+shapes and data, so that contents left in the shared array by the first call
+cannot leak into the second.  This file is collected last on purpose."""
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+import synth
+from oracle.numerics import round_storage
+from tests import _layout
+from tests._gpu import empty_dev, stream, to_dev, to_host
+
+import conv2d_implicit_gemm_gb300 as ox
+
+
+def _packed(w, h, seed, precision):
+    x = synth.uniform_activations(h, w, 9, seed=seed, low=0.0, high=1.0)
+    return to_dev(_layout.to_internal(round_storage(x, precision), precision))
+
+
+@pytest.mark.parametrize("precision", ["fp16", "fp32"])
+def test_noalloc_matches_network_execute_two_calls_in_a_row(precision):
+    prec = ox.PRECISION_FP16 if precision == "fp16" else ox.PRECISION_FP32
+    f = ox.oidnx_filter_create(ox.write_weight_blob(synth.unet_weights(9, bias_scale=0.05)), prec)
+    try:
+        for (w, h, seed) in [(200, 136, 1), (96, 72, 2)]:
+            src = _packed(w, h, seed, precision)
+            ref = empty_dev(w * h * 16)
+            got = empty_dev(w * h * 16)
+            got.fill_(0xFF)   # NaN pattern: every output value must be written
+            ox.oidnx_network_execute(f, src.data_ptr(), w, h, ref.data_ptr(), stream())
+            ox.oidnx_network_execute_noalloc(f, src.data_ptr(), w, h, got.data_ptr(), stream())
+            ox.oidnx_filter_sync_status(f)
+            r = to_host(ref, np.float32, (h, w, 4))
+            g = to_host(got, np.float32, (h, w, 4))
+            assert np.isfinite(g).all()
+            if precision == "fp16":
+                np.testing.assert_allclose(g, r, rtol=0, atol=2e-2)
+            else:
+                num = np.linalg.norm((g - r).ravel())
+                assert num <= 1e-4 * np.linalg.norm(r.ravel())
+            # same kernels with the same launch parameters: the bits agree too
+            assert np.array_equal(g.view(np.uint32), r.view(np.uint32))
+    finally:
+        ox.oidnx_filter_release(f)
+
+
+def test_noalloc_rejects_inputs_beyond_the_array():
+    f = ox.oidnx_filter_create(ox.write_weight_blob(synth.unet_weights(9)), ox.PRECISION_FP16)
+    try:
+        src = empty_dev(16)
+        with pytest.raises(ox.OidnxError) as e:
+            ox.oidnx_network_execute_noalloc(f, src.data_ptr(), 512, 512, src.data_ptr(), stream())
+        assert e.value.status == ox.ERR_INVALID_ARGUMENT
+        assert "bytes of activation scratch" in str(e.value)
+    finally:
+        ox.oidnx_filter_release(f)
+    torch.cuda.synchronize()
