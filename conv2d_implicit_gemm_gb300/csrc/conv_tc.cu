@@ -10,8 +10,10 @@
 // the 2x2 max of ReLU(conv) before the store.
 //
 // GB300 design (not the pages'):
-//  * CTA = R output rows x 128 pixels; one M=128 UMMA tile per row, each
-//    with its own fp32 accumulator of N columns in TMEM.
+//  * Persistent CTAs (one per SM) walk the output tiles of R rows x 128
+//    pixels.  One M=128 UMMA tile per output row; the R accumulators of a
+//    tile (N fp32 columns each) live in tensor memory, double-buffered so the
+//    epilogue of one tile runs while the MMAs of the next are issued.
 //  * K is walked in blocks of 16 input channels.  For one block the CTA
 //    stages, by one TMA box, the whole input halo: (R+2) rows x 130 pixels x
 //    16 channels, zero-filled outside the image (the same padding).  Stored
@@ -19,13 +21,22 @@
 //    matrix is a contiguous 128 B run, so the 9 taps of all R rows are just
 //    9R shared-memory descriptors into the same halo: a kx shift is +16 B, a
 //    ky shift selects the next halo row.  No im2col copy, no re-load per tap.
+//  * The three ky taps are stacked along N: halo row h feeds output rows h,
+//    h-1 and h-2 through ky = 0, 1, 2, so one MMA with B = [W(ky=2); W(ky=1);
+//    W(ky=0)] (N = 3 x Cout <= 256) updates three row accumulators that sit
+//    next to each other in TMEM.  An M=128, K=16 MMA costs at least ~46
+//    cycles of operand fetch whatever N is, so small-Cout layers reach the
+//    tensor rate only with N stacked this way; it also cuts the MMA count
+//    per K block from 9R to 3(R+2).
 //  * Weights are pre-packed on the host into the exact shared-memory image
-//    of the B operand ([tap][8-channel half][N][8] per K block) and fetched
-//    with one bulk copy per stage.
+//    of the B operand ([kx][8-channel half][ky stack][Cout][8] per K block).
+//    When they fit they are loaded once per CTA and stay resident; otherwise
+//    one block per pipeline stage is streamed with the A halo.
 //  * Warp roles: warp 0 issues TMA, warp 1 allocates TMEM and issues the
-//    MMAs from one thread, warps 2-5 run the epilogue (and, for decoders,
-//    build the upsampled halo in shared memory from a low-resolution TMA
-//    box, since nearest upsampling is not an affine TMA box).
+//    MMAs from one thread, warps 2-5 run the epilogue (bias, ReLU, pool,
+//    fp16/fp32 stores), warps 6-9 (decoders only) build the upsampled halo
+//    in shared memory from a low-resolution TMA box, since nearest
+//    upsampling is not an affine TMA box.
 //  * Every wait is bounded: on timeout the kernel records a bit in the
 //    status word, lets its in-flight copies land, frees TMEM and returns.
 #include "internal.h"
@@ -33,7 +44,71 @@
 
 namespace oidnx {
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+namespace {
+
+__device__ __forceinline__ void tile_origin(const TcConvParams& p, int tile, int* x0, int* y0) {
+  const int ty = tile / p.tiles_x;
+  *x0 = (tile - ty * p.tiles_x) * kTileM;
+  *y0 = ty * p.R;
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// All MMAs of one K block for a tile of R rows, fully unrolled so that the
+// single issuing thread spends a handful of instructions per MMA (its
+// instruction stream, not the tensor core, is otherwise the bottleneck).
+// Halo row h updates output rows lo..hi = max(0,h-2)..min(R-1,h) with the
+// ky-stacked B block; rows are grouped G at a time (N = rows x Cout <= 256).
+// In K block 0, kx 0 the row first reached by halo row h (row h itself,
+// through ky = 0) gets its own MMA that overwrites the accumulator.
+template <int R, int G>
+__device__ __forceinline__ void issue_kblock(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
+                                             uint32_t kx_b16, uint32_t id1, uint32_t id2,
+                                             uint32_t id3, bool first) {
+  const uint32_t idn[4] = {0u, id1, id2, id3};
+#pragma unroll
+  for (int kx = 0; kx < 3; ++kx) {
+    const uint64_t adk = ad + kx;
+    const uint64_t bdk = bd + kx * kx_b16;
+#pragma unroll
+    for (int h = 0; h < R + 2; ++h) {
+      const int lo = h - 2 > 0 ? h - 2 : 0;
+      const int hi = h < R - 1 ? h : R - 1;
+      const uint64_t a = adk + static_cast<uint32_t>(h * 2 * kHaloPx);
+#pragma unroll
+      for (int c = lo; c <= hi; c += G) {
+        const int e = c + G - 1 < hi ? c + G - 1 : hi;
+        if (kx == 0 && h <= R - 1 && e == h) {
+          if (first) {
+            if (e > c)
+              mma_f16_ss(dbase + c * N, a, bdk + (2 - h + c) * N, idn[e - c], 1u);
+            mma_f16_ss(dbase + h * N, a, bdk + 2 * N, idn[1], 0u);
+            continue;
+          }
+        }
+        mma_f16_ss(dbase + c * N, a, bdk + (2 - h + c) * N, idn[e - c + 1], 1u);
+      }
+    }
+  }
+}
+
+template <int G>
+__device__ __forceinline__ void issue_kblock_r(int R, uint64_t ad, uint64_t bd, uint32_t dbase,
+                                               uint32_t N, uint32_t kx_b16, uint32_t id1,
+                                               uint32_t id2, uint32_t id3, bool first) {
+  switch (R) {
+    case 1: issue_kblock<1, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3, first); break;
+    case 2: issue_kblock<2, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3, first); break;
+    case 4: issue_kblock<4, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3, first); break;
+    default: issue_kblock<8, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3, first); break;
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kTcThreadsDecoder, 1)
     conv3x3_tc_kernel(const __grid_constant__ CUtensorMap map0,
                       const __grid_constant__ CUtensorMap map1, const TcConvParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -42,19 +117,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int S = p.S, R = p.R, N = p.N, KB0 = p.KB0;
   const int KB = p.KB0 + p.KB1;
-  uint8_t* A = smem;
+  const int num_tiles = p.tiles_x * p.tiles_y;
+  // shared memory: [resident weights][A stages][B stages][staging][bias][barriers]
+  uint8_t* Wres = smem;
+  uint8_t* A = Wres + (p.resident ? static_cast<size_t>(KB) * p.b_stage : 0);
   uint8_t* B = A + static_cast<size_t>(S) * p.a_stage;
-  uint8_t* ST = B + static_cast<size_t>(S) * p.b_stage;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ST + static_cast<size_t>(S) * p.st_stage);
+  uint8_t* ST = B + (p.resident ? 0 : static_cast<size_t>(S) * p.b_stage);
+  float* bias_s = reinterpret_cast<float*>(ST + static_cast<size_t>(S) * p.st_stage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(bias_s + ((N + 31) / 32) * 32);
   uint64_t* empty = full + S;
   uint64_t* xdone = empty + S;
-  uint64_t* accum = xdone + S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* tfull = xdone + S;   // [2] accumulator set ready
+  uint64_t* tempty = tfull + 2;  // [2] accumulator set drained
+  uint64_t* wbar = tempty + 2;   // resident weights landed
+  uint64_t* done = wbar + 1;     // every MMA finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int x0 = blockIdx.x * kTileM;
-  const int y0 = blockIdx.y * R;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -62,7 +142,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&empty[s], 1);
       mbar_init(&xdone[s], 128);
     }
-    mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(wbar, 1);
+    mbar_init(done, 1);
     fence_mbarrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, p.tmem_cols);
@@ -76,179 +161,243 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&map0);
       if (p.KB1 > 0) prefetch_tmap(&map1);
-      int issued = 0;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % S;
-        const uint32_t round = static_cast<uint32_t>(kb / S);
-        if (!mbar_wait_bounded(&empty[s], (round & 1u) ^ 1u, p.status, kErrTimeoutProducer)) break;
-        const bool low = p.upsample0 && kb < KB0;
-        mbar_arrive_expect_tx(&full[s], (low ? p.st_tx : p.a_tx) + p.b_tx);
-        if (kb < KB0) {
-          if (low)
-            tma_load_4d(ST + static_cast<size_t>(s) * p.st_stage, &map0, &full[s], 0,
-                        (x0 >> 1) - 1, 2 * kb, (y0 >> 1) - 1);
-          else
-            tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map0, &full[s], 0, x0 - 1,
-                        2 * kb, y0 - 1);
-        } else {
-          tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map1, &full[s], 0, x0 - 1,
-                      2 * (kb - KB0), y0 - 1);
+      if (p.resident) {
+        mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(KB) * p.b_tx);
+        for (int kb = 0; kb < KB; ++kb)
+          bulk_load(Wres + static_cast<size_t>(kb) * p.b_stage,
+                    reinterpret_cast<const uint8_t*>(p.weights) + static_cast<size_t>(kb) * p.b_tx,
+                    p.b_tx, wbar);
+      }
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int x0, y0;
+        tile_origin(p, tile, &x0, &y0);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const uint32_t s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kErrTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          const bool low = p.upsample0 && kb < KB0;
+          mbar_arrive_expect_tx(&full[s], (low ? p.st_tx : p.a_tx) + (p.resident ? 0u : p.b_tx));
+          if (kb < KB0) {
+            if (low)
+              tma_load_4d(ST + static_cast<size_t>(s) * p.st_stage, &map0, &full[s], 0,
+                          (x0 >> 1) - 1, 2 * kb, (y0 >> 1) - 1);
+            else
+              tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map0, &full[s], 0, x0 - 1,
+                          2 * kb, y0 - 1);
+          } else {
+            tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map1, &full[s], 0, x0 - 1,
+                        2 * (kb - KB0), y0 - 1);
+          }
+          if (!p.resident)
+            bulk_load(B + static_cast<size_t>(s) * p.b_stage,
+                      reinterpret_cast<const uint8_t*>(p.weights) + static_cast<size_t>(kb) * p.b_tx,
+                      p.b_tx, &full[s]);
         }
-        bulk_load(B + static_cast<size_t>(s) * p.b_stage,
-                  reinterpret_cast<const uint8_t*>(p.weights) + static_cast<size_t>(kb) * p.b_tx,
-                  p.b_tx, &full[s]);
-        issued = kb + 1;
       }
       // Every copy issued must have landed before this CTA may exit.
-      for (int kb = issued > S ? issued - S : 0; kb < issued; ++kb)
-        mbar_wait_bounded(&full[kb % S], static_cast<uint32_t>(kb / S) & 1u, p.status,
-                          kErrTimeoutDrain);
+      for (uint32_t k = it > static_cast<uint32_t>(S) ? it - S : 0u; k < it; ++k)
+        mbar_wait_bounded(&full[k % S], (k / S) & 1u, p.status, kErrTimeoutDrain);
+      if (p.resident) mbar_wait_bounded(wbar, 0, p.status, kErrTimeoutDrain);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(kTileM, N);
-      const uint32_t a_base = smem_u32(A);
-      const uint32_t b_base = smem_u32(B);
-      const uint32_t b_tap = 2u * N * kChunkBytes;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % S;
-        const uint32_t par = static_cast<uint32_t>(kb / S) & 1u;
-        bool ok = mbar_wait_bounded(&full[s], par, p.status, kErrTimeoutMma);
-        if (ok && p.upsample0 && kb < KB0)
-          ok = mbar_wait_bounded(&xdone[s], par, p.status, kErrTimeoutMma);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t a_s = a_base + s * p.a_stage;
-        const uint32_t b_s = b_base + s * p.b_stage;
-#pragma unroll 1
-        for (int t = 0; t < 9; ++t) {
-          const int ky = t / 3, kx = t - 3 * (t / 3);
-          const uint64_t bdesc =
-              smem_desc_noswizzle(b_s + t * b_tap, static_cast<uint32_t>(N) * kChunkBytes, 128);
-#pragma unroll 1
-          for (int r = 0; r < R; ++r) {
-            const uint32_t a_off = (static_cast<uint32_t>(r + ky) * 2u * kHaloPx + kx) * kChunkBytes;
-            const uint64_t adesc = smem_desc_noswizzle(a_s + a_off, kHaloPx * kChunkBytes, 128);
-            mma_f16_ss(tmem + static_cast<uint32_t>(r * N), adesc, bdesc, idesc,
-                       (kb | t) != 0 ? 1u : 0u);
-          }
+      const int g = min(3, 256 / N);
+      const uint32_t id1 = idesc_f16_f32(kTileM, N);
+      const uint32_t id2 = idesc_f16_f32(kTileM, min(2 * N, 256));
+      const uint32_t id3 = idesc_f16_f32(kTileM, min(3 * N, 256));
+      const uint64_t a_desc0 = smem_desc_noswizzle(smem_u32(A), kHaloPx * kChunkBytes, 128);
+      const uint64_t b_desc0 =
+          smem_desc_noswizzle(smem_u32(p.resident ? Wres : B), 3u * N * kChunkBytes, 128);
+      const uint32_t kx_b16 = 6u * N;  // one kx block of B = 2 x 3N rows x 16 B
+      const uint32_t set_cols = static_cast<uint32_t>(R * N);
+      bool ok = !p.resident || mbar_wait_bounded(wbar, 0, p.status, kErrTimeoutMma);
+      uint32_t it = 0, tcount = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tcount) {
+        const uint32_t buf = tcount & 1u;
+        if (!mbar_wait_bounded(&tempty[buf], ((tcount >> 1) & 1u) ^ 1u, p.status, kErrTimeoutMma)) {
+          ok = false;
+          break;
         }
-        mma_commit(&empty[s]);
+        tc_fence_after();
+        const uint32_t d_base = tmem + buf * set_cols;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const uint32_t s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          ok = mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutMma);
+          if (ok && p.upsample0) ok = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t ad = a_desc0 + ((s * p.a_stage) >> 4);
+          const uint64_t bd = b_desc0 + ((static_cast<uint32_t>(p.resident ? kb : s) * p.b_stage) >> 4);
+          if (g == 3) issue_kblock_r<3>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, kb == 0);
+          else if (g == 2) issue_kblock_r<2>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, kb == 0);
+          else issue_kblock_r<1>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, kb == 0);
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&tfull[buf]);
       }
-      mma_commit(accum);
       // TMEM is freed only after every MMA issued above has completed.
-      mbar_wait_bounded(accum, 0, p.status, kErrTimeoutMma);
+      mma_commit(done);
+      mbar_wait_bounded(done, 0, p.status, kErrTimeoutMma);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int et = threadIdx.x - 64;  // 0..127
-    if (p.upsample0) {
-      // Build the full-resolution halo of the upsampled source in the A stage.
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ upsampled halo
+    const int et = threadIdx.x - 192;  // 0..127
+    const int total = (R + 2) * 2 * kHaloPx;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      int x0, y0;
+      tile_origin(p, tile, &x0, &y0);
       const int ly0 = (y0 >> 1) - 1, lx0 = (x0 >> 1) - 1;
-      const int total = (R + 2) * 2 * kHaloPx;
-      for (int kb = 0; kb < KB0; ++kb) {
-        const int s = kb % S;
-        const uint32_t par = static_cast<uint32_t>(kb / S) & 1u;
-        if (!mbar_wait_bounded(&full[s], par, p.status, kErrTimeoutEpilogue)) break;
-        const uint4* src = reinterpret_cast<const uint4*>(ST + static_cast<size_t>(s) * p.st_stage);
-        uint4* dst = reinterpret_cast<uint4*>(A + static_cast<size_t>(s) * p.a_stage);
-        for (int i = et; i < total; i += 128) {
-          const int px = i % kHaloPx;
-          const int rc = i / kHaloPx;
-          const int j = rc & 1, rr = rc >> 1;
-          const int iy = y0 - 1 + rr, ix = x0 - 1 + px;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (iy >= 0 && iy < p.H && ix >= 0 && ix < p.W) {
-            const int sr = (iy >> 1) - ly0, sc = (ix >> 1) - lx0;
-            v = src[(sr * 2 + j) * kLowPx + sc];
-          }
-          dst[i] = v;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const uint32_t s = it % S;
+        const uint32_t ph = (it / S) & 1u;
+        // Waiting on every stage keeps this warp group at most one use of a
+        // stage ahead of the MMA issuer, so the xdone phases stay paired.
+        if (!mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutEpilogue)) {
+          ok = false;
+          break;
         }
-        fence_proxy_async_smem();
+        if (kb < KB0) {
+          const uint4* src = reinterpret_cast<const uint4*>(ST + static_cast<size_t>(s) * p.st_stage);
+          uint4* dst = reinterpret_cast<uint4*>(A + static_cast<size_t>(s) * p.a_stage);
+          for (int i = et; i < total; i += 128) {
+            const int px = i % kHaloPx;
+            const int rc = i / kHaloPx;
+            const int j = rc & 1, rr = rc >> 1;
+            const int iy = y0 - 1 + rr, ix = x0 - 1 + px;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (iy >= 0 && iy < p.H && ix >= 0 && ix < p.W) {
+              const int sr = (iy >> 1) - ly0, sc = (ix >> 1) - lx0;
+              v = src[(sr * 2 + j) * kLowPx + sc];
+            }
+            dst[i] = v;
+          }
+          fence_proxy_async_smem();
+        }
         mbar_arrive(&xdone[s]);
       }
     }
-
-    mbar_wait_bounded(accum, 0, p.status, kErrTimeoutEpilogue);
-    tc_fence_after();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;  // 0..127
+    for (int i = et; i < N; i += 128) bias_s[i] = p.bias[i];
+    named_barrier_sync(1, 128);
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int m = q * 32 + lane;     // pixel in the M tile = TMEM lane
-    const int x = x0 + m;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int nc = N / 16;
+    const int C8 = N / 8;
+    const uint32_t set_cols = static_cast<uint32_t>(R * N);
+    uint32_t tcount = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
+      const uint32_t buf = tcount & 1u;
+      if (!mbar_wait_bounded(&tfull[buf], (tcount >> 1) & 1u, p.status, kErrTimeoutEpilogue)) break;
+      tc_fence_after();
+      int x0, y0;
+      tile_origin(p, tile, &x0, &y0);
+      const int x = x0 + m;
+      const uint32_t tl = tmem + lane_off + buf * set_cols;
 
-    if (p.mode == kEpiRelu) {
-      __half* out = static_cast<__half*>(p.out);
-      const int C8 = N / 8;
-      for (int r = 0; r < R; ++r) {
-        const int y = y0 + r;
-        const bool valid = x < p.W && y < p.H;
-        for (int c = 0; c < nc; ++c) {
-          float v[16];
-          tmem_ld16(tl + static_cast<uint32_t>(r * N + c * 16), v);
-          uint32_t h[8];
+      if (p.mode == kEpiRelu) {
+        __half* out = static_cast<__half*>(p.out);
+        for (int r = 0; r < R; ++r) {
+          const int y = y0 + r;
+          const bool valid = x < p.W && y < p.H;
+          for (int c0 = 0; c0 < nc; c0 += 4) {
+            uint32_t v[4][16];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float a = fmaxf(v[2 * k] + __ldg(&p.bias[c * 16 + 2 * k]), 0.0f);
-            const float b = fmaxf(v[2 * k + 1] + __ldg(&p.bias[c * 16 + 2 * k + 1]), 0.0f);
-            h[k] = pack_half2(a, b);
+            for (int b = 0; b < 4; ++b)
+              if (c0 + b < nc) tmem_ld16_nowait(tl + static_cast<uint32_t>(r * N + (c0 + b) * 16), v[b]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              if (c0 + b >= nc) break;
+              const int c = c0 + b;
+              uint32_t h[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float a = fmaxf(__uint_as_float(v[b][2 * k]) + bias_s[c * 16 + 2 * k], 0.0f);
+                const float bb = fmaxf(__uint_as_float(v[b][2 * k + 1]) + bias_s[c * 16 + 2 * k + 1], 0.0f);
+                h[k] = pack_half2(a, bb);
+              }
+              if (valid) {
+                const size_t base0 = ((static_cast<size_t>(y) * C8 + 2 * c) * p.W + x) * 8;
+                const size_t base1 = base0 + static_cast<size_t>(p.W) * 8;
+                *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
+              }
+            }
           }
-          if (valid) {
-            const size_t base0 = ((static_cast<size_t>(y) * C8 + 2 * c) * p.W + x) * 8;
-            const size_t base1 = ((static_cast<size_t>(y) * C8 + 2 * c + 1) * p.W + x) * 8;
-            *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+      } else if (p.mode == kEpiReluPool) {
+        __half* out = static_cast<__half*>(p.out);
+        const int Wp = (p.W + 1) >> 1, Hp = (p.H + 1) >> 1;
+        for (int i = 0; i < R / 2; ++i) {
+          const int ya = y0 + 2 * i;
+          const bool va = x < p.W && ya < p.H;
+          const bool vb = x < p.W && ya + 1 < p.H;
+          const int yp = ya >> 1, xp = x >> 1;
+          const bool store = ((lane & 1) == 0) && xp < Wp && yp < Hp;
+          for (int c0 = 0; c0 < nc; ++c0) {
+            uint32_t v[2][16];  // chunk c0 of the two rows of the pooling window
+            tmem_ld16_nowait(tl + static_cast<uint32_t>((2 * i) * N + c0 * 16), v[0]);
+            tmem_ld16_nowait(tl + static_cast<uint32_t>((2 * i + 1) * N + c0 * 16), v[1]);
+            tmem_wait_ld();
+            {
+              const int c = c0;
+              float mx[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                const float bk = bias_s[c * 16 + k];
+                const float a = va ? fmaxf(__uint_as_float(v[0][k]) + bk, 0.0f) : -INFINITY;
+                const float bb = vb ? fmaxf(__uint_as_float(v[1][k]) + bk, 0.0f) : -INFINITY;
+                float t = fmaxf(a, bb);
+                t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 1));
+                mx[k] = t;
+              }
+              if (store) {
+                uint32_t h[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) h[k] = pack_half2(mx[2 * k], mx[2 * k + 1]);
+                const size_t base0 = ((static_cast<size_t>(yp) * C8 + 2 * c) * Wp + xp) * 8;
+                const size_t base1 = base0 + static_cast<size_t>(Wp) * 8;
+                *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
+              }
+            }
+          }
+        }
+      } else {
+        float4* out = static_cast<float4*>(p.out);
+        const float b0 = bias_s[0], b1 = bias_s[1], b2 = bias_s[2], b3 = bias_s[3];
+        for (int r0 = 0; r0 < R; r0 += 4) {
+          uint32_t v[4][16];
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            if (r0 + b < R) tmem_ld16_nowait(tl + static_cast<uint32_t>((r0 + b) * N), v[b]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int y = y0 + r0 + b;
+            if (r0 + b < R && x < p.W && y < p.H)
+              out[static_cast<size_t>(y) * p.W + x] =
+                  make_float4(__uint_as_float(v[b][0]) + b0, __uint_as_float(v[b][1]) + b1,
+                              __uint_as_float(v[b][2]) + b2, __uint_as_float(v[b][3]) + b3);
           }
         }
       }
-    } else if (p.mode == kEpiReluPool) {
-      __half* out = static_cast<__half*>(p.out);
-      const int C8 = N / 8;
-      const int Wp = (p.W + 1) >> 1, Hp = (p.H + 1) >> 1;
-      for (int i = 0; i < R / 2; ++i) {
-        const int ya = y0 + 2 * i;
-        const bool va = x < p.W && ya < p.H;
-        const bool vb = x < p.W && ya + 1 < p.H;
-        const int yp = ya >> 1, xp = x >> 1;
-        const bool store = ((lane & 1) == 0) && xp < Wp && yp < Hp;
-        for (int c = 0; c < nc; ++c) {
-          float va16[16], vb16[16];
-          tmem_ld16(tl + static_cast<uint32_t>((2 * i) * N + c * 16), va16);
-          tmem_ld16(tl + static_cast<uint32_t>((2 * i + 1) * N + c * 16), vb16);
-          float mx[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float bk = __ldg(&p.bias[c * 16 + k]);
-            const float a = va ? fmaxf(va16[k] + bk, 0.0f) : -INFINITY;
-            const float b = vb ? fmaxf(vb16[k] + bk, 0.0f) : -INFINITY;
-            float t = fmaxf(a, b);
-            t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 1));
-            mx[k] = t;
-          }
-          if (store) {
-            uint32_t h[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) h[k] = pack_half2(mx[2 * k], mx[2 * k + 1]);
-            const size_t base0 = ((static_cast<size_t>(yp) * C8 + 2 * c) * Wp + xp) * 8;
-            const size_t base1 = ((static_cast<size_t>(yp) * C8 + 2 * c + 1) * Wp + xp) * 8;
-            *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
-          }
-        }
-      }
-    } else {
-      float4* out = static_cast<float4*>(p.out);
-      const float b0 = __ldg(&p.bias[0]), b1 = __ldg(&p.bias[1]);
-      const float b2 = __ldg(&p.bias[2]), b3 = __ldg(&p.bias[3]);
-      for (int r = 0; r < R; ++r) {
-        const int y = y0 + r;
-        float v[16];
-        tmem_ld16(tl + static_cast<uint32_t>(r * N), v);
-        if (x < p.W && y < p.H)
-          out[static_cast<size_t>(y) * p.W + x] = make_float4(v[0] + b0, v[1] + b1, v[2] + b2, v[3] + b3);
-      }
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
     }
   }
 
@@ -261,7 +410,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
-  conv3x3_tc_kernel<<<L.grid, kTcThreads, L.smem, stream>>>(L.map0, L.map1, L.p);
+  const int threads = L.p.upsample0 ? kTcThreadsDecoder : kTcThreads;
+  conv3x3_tc_kernel<<<L.grid, threads, L.smem, stream>>>(L.map0, L.map1, L.p);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ constexpr int kHaloPx = kTileM + 2;        // input pixels of one halo row
 constexpr int kLowPx = kTileM / 2 + 2;     // low-resolution pixels for one M tile
 constexpr int kChunkBytes = 16;            // one 16-byte channel block
 constexpr int kTcThreads = 192;            // 6 warps: TMA, MMA, 4 x epilogue
+constexpr int kTcThreadsDecoder = 320;     // + 4 warps building the upsampled halo
 
 enum EpilogueMode : int {
   kEpiRelu = 0,      // bias + ReLU, fp16 store
@@ -35,9 +36,11 @@ struct TcConvParams {
   int S;                   // pipeline stages
   int mode;                // EpilogueMode
   int upsample0;           // source 0 is at half resolution (decoder)
-  uint32_t tmem_cols;      // power of two >= max(32, R*N)
+  int tiles_x, tiles_y;    // output tiles of 128 pixels x R rows
+  int resident;            // all weights held in shared memory for the CTA's life
+  uint32_t tmem_cols;      // power of two >= max(32, 2*R*N): two accumulator sets
   uint32_t a_stage;        // bytes per A stage (1024-aligned)
-  uint32_t b_stage;        // bytes per B stage (1024-aligned)
+  uint32_t b_stage;        // bytes per B block (1024-aligned)
   uint32_t st_stage;       // bytes per low-res staging stage (0 if none)
   uint32_t a_tx, b_tx, st_tx;  // transaction bytes per stage
 };

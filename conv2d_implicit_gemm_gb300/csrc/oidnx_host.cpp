@@ -247,6 +247,11 @@ oidnx_status parse_blob(const void* blob, size_t bytes, ConvTensors (&layers)[kL
 // half j, N rows of 8 halves ([kb][tap][j][n][8]).  K lanes enumerate the
 // concatenated sources, each padded to a multiple of 16 lanes; padded rows
 // and lanes are zero.
+// fp16 tensor-core B operand, per 16-lane K block kb: [kx][8-lane half j]
+// [ky stack pos][N][8] halves with pos = 2 - ky, so that rows pos*N .. of one
+// (kx, j) slice are W(ky=2), W(ky=1), W(ky=0) one after the other.  K lanes
+// enumerate the concatenated sources, each padded to a multiple of 16 lanes;
+// padded rows and lanes are zero.
 std::vector<uint16_t> pack_weights_tc(const ConvTensors& L, int c0, int c1, int* KB0,
                                       int* KB1, int* N) {
   const int p0 = round_up(c0, 16), p1 = c1 > 0 ? round_up(c1, 16) : 0;
@@ -256,19 +261,22 @@ std::vector<uint16_t> pack_weights_tc(const ConvTensors& L, int c0, int c1, int*
   const int KB = *KB0 + *KB1;
   std::vector<uint16_t> out(static_cast<size_t>(KB) * 9 * 2 * (*N) * 8, 0);
   for (int kb = 0; kb < KB; ++kb)
-    for (int t = 0; t < 9; ++t)
+    for (int kx = 0; kx < 3; ++kx)
       for (int j = 0; j < 2; ++j)
-        for (int n = 0; n < L.cout; ++n)
-          for (int l = 0; l < 8; ++l) {
-            const int v = kb * 16 + j * 8 + l;
-            int ch = -1;
-            if (v < p0) ch = v < c0 ? v : -1;
-            else ch = (v - p0) < c1 ? c0 + (v - p0) : -1;
-            if (ch < 0) continue;
-            const float w = L.w[(static_cast<size_t>(n) * L.cin + ch) * 9 + t];
-            out[((((static_cast<size_t>(kb) * 9 + t) * 2 + j) * (*N) + n) * 8) + l] =
-                to_half_bits(w);
-          }
+        for (int pos = 0; pos < 3; ++pos)
+          for (int n = 0; n < L.cout; ++n)
+            for (int l = 0; l < 8; ++l) {
+              const int v = kb * 16 + j * 8 + l;
+              int ch = -1;
+              if (v < p0) ch = v < c0 ? v : -1;
+              else ch = (v - p0) < c1 ? c0 + (v - p0) : -1;
+              if (ch < 0) continue;
+              const int ky = 2 - pos;
+              const float w = L.w[(static_cast<size_t>(n) * L.cin + ch) * 9 + ky * 3 + kx];
+              const size_t idx =
+                  (((((static_cast<size_t>(kb) * 3 + kx) * 2 + j) * 3 + pos) * (*N) + n) * 8) + l;
+              out[idx] = to_half_bits(w);
+            }
   return out;
 }
 
@@ -581,13 +589,14 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   const bool up = kind == kDecoder;
   const int N = L.N;
   const int minR = (kind == kPool || kind == kDecoder) ? 2 : 1;
-  int R = 4;
-  while (R > minR && R * N > 512) R /= 2;
-  const long tiles_x = (W + kTileM - 1) / kTileM;
-  while (R > minR && tiles_x * ((H + R - 1) / R) < 2L * num_sms()) R /= 2;
-  if (R * N > 512) return fail(OIDNX_ERR_UNSUPPORTED, "accumulators exceed tensor memory");
+  // Two accumulator sets of R x N fp32 columns must fit the 512 TMEM columns.
+  int R = 8;
+  while (R > minR && R * N > 256) R /= 2;
+  if (2 * R * N > 512) return fail(OIDNX_ERR_UNSUPPORTED, "accumulators exceed tensor memory");
+  const int tiles_x = (W + kTileM - 1) / kTileM;
+  while (R > minR && static_cast<long>(tiles_x) * ((H + R - 1) / R) < num_sms()) R /= 2;
   uint32_t tmem_cols = 32;
-  while (tmem_cols < static_cast<uint32_t>(R * N)) tmem_cols *= 2;
+  while (tmem_cols < static_cast<uint32_t>(2 * R * N)) tmem_cols *= 2;
 
   TcConvParams& p = T->p;
   std::memset(&p, 0, sizeof(p));
@@ -603,6 +612,8 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   p.R = R;
   p.mode = kind == kPool ? kEpiReluPool : (kind == kFinal ? kEpiFinal : kEpiRelu);
   p.upsample0 = up ? 1 : 0;
+  p.tiles_x = tiles_x;
+  p.tiles_y = (H + R - 1) / R;
   p.tmem_cols = tmem_cols;
   p.a_tx = static_cast<uint32_t>((R + 2) * 2 * kHaloPx * kChunkBytes);
   p.b_tx = static_cast<uint32_t>(9 * 2 * N * kChunkBytes);
@@ -610,29 +621,36 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   p.a_stage = static_cast<uint32_t>(round_up_sz(p.a_tx, 1024));
   p.b_stage = static_cast<uint32_t>(round_up_sz(p.b_tx, 1024));
   p.st_stage = static_cast<uint32_t>(round_up_sz(p.st_tx, 1024));
-  const size_t stage = static_cast<size_t>(p.a_stage) + p.b_stage + p.st_stage;
   const int KB = L.KB0 + L.KB1;
-  const int per_sm_target = std::max(1, std::min(2, static_cast<int>(512 / tmem_cols)));
-  const size_t fixed = 1024 + 512;  // alignment slack + barriers
   const size_t max_smem = 227 * 1024;
-  const size_t budget = (per_sm_target == 2 ? 112 * 1024 : max_smem) - fixed;
-  int S = static_cast<int>(budget / stage);
-  S = std::max(1, std::min(S, std::min(KB, 6)));
-  if (S < 2 && KB > 1) S = 2;
-  p.S = S;
-  size_t smem = fixed + S * stage;
-  if (smem > max_smem) return fail(OIDNX_ERR_UNSUPPORTED, "conv stage does not fit shared memory");
-  // Keep the CTAs resident on one SM within the 512 TMEM columns: pad the
-  // shared-memory request until the occupancy allows no more than that.
+  // alignment slack + bias + barriers
+  const size_t fixed = 1024 + static_cast<size_t>((N + 31) / 32) * 32 * 4 + 256;
+  const size_t wbytes = static_cast<size_t>(KB) * p.b_stage;
+  const size_t a_st = static_cast<size_t>(p.a_stage) + p.st_stage;
+  const int min_stages = std::min(KB, 3) < 2 ? 2 : std::min(KB, 3);
+  size_t smem;
+  if (fixed + wbytes + min_stages * a_st <= max_smem) {
+    p.resident = 1;
+    p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed - wbytes) / a_st));
+    smem = fixed + wbytes + p.S * a_st;
+  } else {
+    p.resident = 0;
+    const size_t stage = a_st + p.b_stage;
+    p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed) / stage));
+    if (p.S < 2) return fail(OIDNX_ERR_UNSUPPORTED, "conv stage does not fit shared memory");
+    smem = fixed + p.S * stage;
+  }
   static size_t limit_set = 0;
   if (limit_set < max_smem) {
     cudaError_t e = conv_tc_set_smem_limit(max_smem);
     if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
     limit_set = max_smem;
   }
+  // CTAs resident on one SM must share the 512 TMEM columns without waiting:
+  // pad the shared-memory request until the occupancy allows no more.
   const int allowed = static_cast<int>(512 / tmem_cols);
+  int blocks = 0;
   for (;;) {
-    int blocks = 0;
     cudaError_t e = conv_tc_occupancy(smem, &blocks);
     if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "occupancy: %s", cudaGetErrorString(e));
     if (blocks <= allowed) break;
@@ -640,7 +658,8 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
     if (smem > max_smem) return fail(OIDNX_ERR_UNSUPPORTED, "cannot bound CTAs per SM");
   }
   T->smem = smem;
-  T->grid = dim3(static_cast<unsigned>(tiles_x), static_cast<unsigned>((H + R - 1) / R), 1);
+  const long tiles = static_cast<long>(p.tiles_x) * p.tiles_y;
+  T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, static_cast<long>(num_sms()) * blocks)), 1, 1);
 
   const int c8_0 = round_up(L.c0, 16) / 8;
   if (up)
