@@ -63,7 +63,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -82,6 +82,11 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+
+    def wait_first_sample(self, timeout=10.0):
+        t0 = time.time()
+        while self.proc and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.05)
 
     def summary(self):
         sm, smax, reasons = [], None, set()
@@ -195,7 +200,6 @@ def run_ours(args):
     ox.oidnx_filter_set_int(f, "hdr", 1)
     ox.oidnx_filter_set_int(f, "transfer", ox.TRANSFER_LOG)
     ox.oidnx_filter_set_float(f, "inputScale", 1.0)
-    ox.oidnx_filter_set_int(f, "profile", 1)   # per-kernel events inside the graph
     ox.oidnx_filter_commit(f)
     tiles = ox.oidnx_filter_get_int(f, "tiles")
     stream = torch.cuda.current_stream()
@@ -208,34 +212,50 @@ def run_ours(args):
     ox.oidnx_filter_sync_status(f)
 
     layer_ms, layer_flop, layer_bytes = {}, {}, {}
-    step_ms = []
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(dev) as clocks:
+        clocks.wait_first_sample()
+        # Timed region: K denoise steps, L2 flushed before each, CUDA events on
+        # the launching stream around each step (the flush is outside them).
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         for k in range(args.steps):
             flush.fill_(k & 0xFF)
             starts[k].record(stream)
             ox.oidnx_filter_execute(f, sptr)
             ends[k].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ox.oidnx_filter_sync_status(f)
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        # Profiled steps: the same execution with a CUDA event after every
+        # kernel (recorded inside the graph on the launching stream).  Events
+        # between kernels stop the next kernel's prologue from overlapping the
+        # previous one, so these per-kernel times are slightly pessimistic.
+        ox.oidnx_filter_set_int(f, "profile", 1)
+        ox.oidnx_filter_execute(f, sptr)
+        ox.oidnx_get_profile(f)
+        prof_steps = []
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            ox.oidnx_filter_execute(f, sptr)
             prof = ox.oidnx_get_profile(f)   # waits for this step's events
+            prof_steps.append(prof["totalMs"])
             for l in prof["layers"]:
                 layer_ms[l["id"]] = layer_ms.get(l["id"], 0.0) + l["ms"]
                 layer_flop[l["id"]] = l["flop"]
                 layer_bytes[l["id"]] = l["bytes"]
+        ox.oidnx_filter_set_int(f, "profile", 0)
         torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
     ox.oidnx_filter_sync_status(f)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     mean_ms = float(np.mean(step_ms))
 
     # end to end through the host-buffer call: H2D inputs, denoise, D2H output
     pinned = [torch.from_numpy(im).pin_memory() for im in imgs]
     host_out = torch.empty((HEIGHT, WIDTH, 4), dtype=torch.float32).pin_memory()
-    ox.oidnx_filter_set_int(f, "profile", 0)
     host_ptr = [p.data_ptr() for p in pinned]
     for _ in range(3):
         ox._check(ox._lib.oidnx_filter_execute_host(f, *host_ptr, host_out.data_ptr(), sptr))
@@ -301,6 +321,8 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": "MP/s", "h2d_bytes_per_step": 3 * px * 16,
                     "d2h_bytes_per_step": px * 16, "ms_per_step": e2e_mean},
             "gpu_launches": steps * tiles * 18,
+            "profiled_ms_per_step": float(np.mean(prof_steps)),
+            "layers_note": "per-kernel times from the profiled steps (event after every kernel)",
             "clocks": clocks.summary(),
         }
         if cpu:
@@ -319,7 +341,7 @@ TRAFFIC = {}
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     args = ap.parse_args()

@@ -14,6 +14,7 @@
 // consecutive pixels of one row (or pooled pixels) and one group of 8 output
 // channels, whose weights it stages in shared memory.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace oidnx {
 
@@ -64,6 +65,8 @@ __global__ void __launch_bounds__(128) conv3x3_simt_kernel(const SimtConvParams 
   const float* wsrc = p.weights + static_cast<size_t>(g) * wcount;
   for (int i = threadIdx.x; i < wcount; i += blockDim.x) wsm[i] = wsrc[i];
   __syncthreads();
+  griddep_wait();  // activations come from the previous kernel in the stream
+  griddep_launch_dependents();
   float bias[8];
 #pragma unroll
   for (int o = 0; o < 8; ++o) bias[o] = p.bias[g * 8 + o];
@@ -130,8 +133,7 @@ cudaError_t launch_variant(const SimtConvParams& p, cudaStream_t stream) {
   const int wide = MODE == kEpiReluPool ? (p.W + 1) / 2 : p.W;
   const int rows = MODE == kEpiReluPool ? (p.H + 1) / 2 : p.H;
   dim3 grid((wide + 127) / 128, rows, p.groups);
-  conv3x3_simt_kernel<MODE, UP><<<grid, 128, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(conv3x3_simt_kernel<MODE, UP>, grid, dim3(128), smem, stream, p);
 }
 
 }  // namespace

@@ -108,7 +108,8 @@ __device__ __forceinline__ void issue_kblock_r(int R, uint64_t ad, uint64_t bd, 
 
 }  // namespace
 
-__global__ void __launch_bounds__(kTcThreadsDecoder, 1)
+template <bool DEC>
+__global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
     conv3x3_tc_kernel(const __grid_constant__ CUtensorMap map0,
                       const __grid_constant__ CUtensorMap map1, const TcConvParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kTcThreadsDecoder, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 32 * kTcEpilogueWarps);
     }
     mbar_init(wbar, 1);
     mbar_init(done, 1);
@@ -155,6 +156,9 @@ __global__ void __launch_bounds__(kTcThreadsDecoder, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Every CTA of this persistent grid is resident: the next layer's kernel
+  // may start its prologue on SMs as they free up.
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -168,6 +172,9 @@ __global__ void __launch_bounds__(kTcThreadsDecoder, 1)
                     reinterpret_cast<const uint8_t*>(p.weights) + static_cast<size_t>(kb) * p.b_tx,
                     p.b_tx, wbar);
       }
+      // Weights and bias are constants; the activations come from the
+      // previous kernel in the stream.
+      griddep_wait();
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(kTcThreadsDecoder, 1)
           const uint32_t s = it % S;
           const uint32_t ph = (it / S) & 1u;
           ok = mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutMma);
-          if (ok && p.upsample0) ok = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
+          if (ok && DEC) ok = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
           const uint64_t ad = a_desc0 + ((s * p.a_stage) >> 4);
@@ -248,9 +255,9 @@ __global__ void __launch_bounds__(kTcThreadsDecoder, 1)
       mbar_wait_bounded(done, 0, p.status, kErrTimeoutMma);
     }
     __syncwarp();
-  } else if (warp >= 6) {
+  } else if (warp >= 2 + kTcEpilogueWarps) {
     // ------------------------------------------------------------ upsampled halo
-    const int et = threadIdx.x - 192;  // 0..127
+    const int et = threadIdx.x - 32 * (2 + kTcEpilogueWarps);  // 0..127
     const int total = (R + 2) * 2 * kHaloPx;
     uint32_t it = 0;
     bool ok = true;
@@ -289,11 +296,14 @@ __global__ void __launch_bounds__(kTcThreadsDecoder, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int et = threadIdx.x - 64;  // 0..127
-    for (int i = et; i < N; i += 128) bias_s[i] = p.bias[i];
-    named_barrier_sync(1, 128);
-    const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int m = q * 32 + lane;     // pixel in the M tile = TMEM lane
+    // Eight warps: warp w reads TMEM lane quarter w % 4 (pixels 32q..32q+31
+    // of the M tile); the two warps of a quarter split the tile's rows.
+    const int et = threadIdx.x - 64;  // 0..255
+    for (int i = et; i < N; i += 32 * kTcEpilogueWarps) bias_s[i] = p.bias[i];
+    named_barrier_sync(1, 32 * kTcEpilogueWarps);
+    const int q = warp & 3;
+    const int sub = (warp - 2) >> 2;  // 0 or 1
+    const int m = q * 32 + lane;      // pixel in the M tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int nc = N / 16;
     const int C8 = N / 8;
@@ -310,31 +320,33 @@ __global__ void __launch_bounds__(kTcThreadsDecoder, 1)
 
       if (p.mode == kEpiRelu) {
         __half* out = static_cast<__half*>(p.out);
-        for (int r = 0; r < R; ++r) {
-          const int y = y0 + r;
-          const bool valid = x < p.W && y < p.H;
-          for (int c0 = 0; c0 < nc; c0 += 4) {
-            uint32_t v[4][16];
+        for (int c0 = 0; c0 < nc; c0 += 2) {
+          const bool two = c0 + 1 < nc;
+          float bv[32];
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-              if (c0 + b < nc) tmem_ld16_nowait(tl + static_cast<uint32_t>(r * N + (c0 + b) * 16), v[b]);
+          for (int k = 0; k < 16; ++k) {
+            bv[k] = bias_s[c0 * 16 + k];
+            bv[16 + k] = two ? bias_s[c0 * 16 + 16 + k] : 0.0f;
+          }
+          for (int r = sub; r < R; r += 2) {
+            const int y = y0 + r;
+            uint32_t v[2][16];
+            tmem_ld16_nowait(tl + static_cast<uint32_t>(r * N + c0 * 16), v[0]);
+            if (two) tmem_ld16_nowait(tl + static_cast<uint32_t>(r * N + c0 * 16 + 16), v[1]);
             tmem_wait_ld();
+            if (x < p.W && y < p.H) {
+              __half* row = out + (static_cast<size_t>(y) * C8 * p.W + x) * 8;
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              if (c0 + b >= nc) break;
-              const int c = c0 + b;
-              uint32_t h[8];
+              for (int b = 0; b < 2; ++b) {
+                if (b == 1 && !two) break;
+                uint32_t h[8];
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const float a = fmaxf(__uint_as_float(v[b][2 * k]) + bias_s[c * 16 + 2 * k], 0.0f);
-                const float bb = fmaxf(__uint_as_float(v[b][2 * k + 1]) + bias_s[c * 16 + 2 * k + 1], 0.0f);
-                h[k] = pack_half2(a, bb);
-              }
-              if (valid) {
-                const size_t base0 = ((static_cast<size_t>(y) * C8 + 2 * c) * p.W + x) * 8;
-                const size_t base1 = base0 + static_cast<size_t>(p.W) * 8;
-                *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
+                for (int k = 0; k < 8; ++k)
+                  h[k] = pack_half2(fmaxf(__uint_as_float(v[b][2 * k]) + bv[16 * b + 2 * k], 0.0f),
+                                    fmaxf(__uint_as_float(v[b][2 * k + 1]) + bv[16 * b + 2 * k + 1], 0.0f));
+                const size_t c8 = 2 * (c0 + b);
+                *reinterpret_cast<uint4*>(row + c8 * p.W * 8) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(row + (c8 + 1) * p.W * 8) = make_uint4(h[4], h[5], h[6], h[7]);
               }
             }
           }
@@ -342,54 +354,53 @@ __global__ void __launch_bounds__(kTcThreadsDecoder, 1)
       } else if (p.mode == kEpiReluPool) {
         __half* out = static_cast<__half*>(p.out);
         const int Wp = (p.W + 1) >> 1, Hp = (p.H + 1) >> 1;
-        for (int i = 0; i < R / 2; ++i) {
-          const int ya = y0 + 2 * i;
-          const bool va = x < p.W && ya < p.H;
-          const bool vb = x < p.W && ya + 1 < p.H;
-          const int yp = ya >> 1, xp = x >> 1;
-          const bool store = ((lane & 1) == 0) && xp < Wp && yp < Hp;
-          for (int c0 = 0; c0 < nc; ++c0) {
-            uint32_t v[2][16];  // chunk c0 of the two rows of the pooling window
-            tmem_ld16_nowait(tl + static_cast<uint32_t>((2 * i) * N + c0 * 16), v[0]);
-            tmem_ld16_nowait(tl + static_cast<uint32_t>((2 * i + 1) * N + c0 * 16), v[1]);
+        const int xp = x >> 1;
+        for (int c = 0; c < nc; ++c) {
+          float bv[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) bv[k] = bias_s[c * 16 + k];
+          for (int i = sub; i < R / 2; i += 2) {
+            const int ya = y0 + 2 * i;
+            const bool va = x < p.W && ya < p.H;
+            const bool vb = x < p.W && ya + 1 < p.H;
+            const int yp = ya >> 1;
+            uint32_t v[2][16];
+            tmem_ld16_nowait(tl + static_cast<uint32_t>((2 * i) * N + c * 16), v[0]);
+            tmem_ld16_nowait(tl + static_cast<uint32_t>((2 * i + 1) * N + c * 16), v[1]);
             tmem_wait_ld();
-            {
-              const int c = c0;
-              float mx[16];
+            float mx[16];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                const float bk = bias_s[c * 16 + k];
-                const float a = va ? fmaxf(__uint_as_float(v[0][k]) + bk, 0.0f) : -INFINITY;
-                const float bb = vb ? fmaxf(__uint_as_float(v[1][k]) + bk, 0.0f) : -INFINITY;
-                float t = fmaxf(a, bb);
-                t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 1));
-                mx[k] = t;
-              }
-              if (store) {
-                uint32_t h[8];
+            for (int k = 0; k < 16; ++k) {
+              const float a = va ? fmaxf(__uint_as_float(v[0][k]) + bv[k], 0.0f) : -INFINITY;
+              const float bb = vb ? fmaxf(__uint_as_float(v[1][k]) + bv[k], 0.0f) : -INFINITY;
+              float t = fmaxf(a, bb);
+              t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 1));
+              mx[k] = t;
+            }
+            if (((lane & 1) == 0) && xp < Wp && yp < Hp) {
+              uint32_t h[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) h[k] = pack_half2(mx[2 * k], mx[2 * k + 1]);
-                const size_t base0 = ((static_cast<size_t>(yp) * C8 + 2 * c) * Wp + xp) * 8;
-                const size_t base1 = base0 + static_cast<size_t>(Wp) * 8;
-                *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
-              }
+              for (int k = 0; k < 8; ++k) h[k] = pack_half2(mx[2 * k], mx[2 * k + 1]);
+              const size_t base0 = ((static_cast<size_t>(yp) * C8 + 2 * c) * Wp + xp) * 8;
+              const size_t base1 = base0 + static_cast<size_t>(Wp) * 8;
+              *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
+              *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
             }
           }
         }
       } else {
         float4* out = static_cast<float4*>(p.out);
         const float b0 = bias_s[0], b1 = bias_s[1], b2 = bias_s[2], b3 = bias_s[3];
-        for (int r0 = 0; r0 < R; r0 += 4) {
+        for (int r0 = sub; r0 < R; r0 += 8) {
           uint32_t v[4][16];
 #pragma unroll
           for (int b = 0; b < 4; ++b)
-            if (r0 + b < R) tmem_ld16_nowait(tl + static_cast<uint32_t>((r0 + b) * N), v[b]);
+            if (r0 + 2 * b < R) tmem_ld16_nowait(tl + static_cast<uint32_t>((r0 + 2 * b) * N), v[b]);
           tmem_wait_ld();
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
-            const int y = y0 + r0 + b;
-            if (r0 + b < R && x < p.W && y < p.H)
+            const int y = y0 + r0 + 2 * b;
+            if (r0 + 2 * b < R && x < p.W && y < p.H)
               out[static_cast<size_t>(y) * p.W + x] =
                   make_float4(__uint_as_float(v[b][0]) + b0, __uint_as_float(v[b][1]) + b1,
                               __uint_as_float(v[b][2]) + b2, __uint_as_float(v[b][3]) + b3);
@@ -410,18 +421,25 @@ __global__ void __launch_bounds__(kTcThreadsDecoder, 1)
 }
 
 cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
-  const int threads = L.p.upsample0 ? kTcThreadsDecoder : kTcThreads;
-  conv3x3_tc_kernel<<<L.grid, threads, L.smem, stream>>>(L.map0, L.map1, L.p);
-  return cudaGetLastError();
+  if (L.p.upsample0)
+    return launch_pdl(conv3x3_tc_kernel<true>, L.grid, dim3(kTcThreadsDecoder), L.smem, stream,
+                      L.map0, L.map1, L.p);
+  return launch_pdl(conv3x3_tc_kernel<false>, L.grid, dim3(kTcThreads), L.smem, stream, L.map0,
+                    L.map1, L.p);
 }
 
 cudaError_t conv_tc_set_smem_limit(size_t bytes) {
-  return cudaFuncSetAttribute(conv3x3_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(bytes));
+  cudaError_t e = cudaFuncSetAttribute(conv3x3_tc_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(conv3x3_tc_kernel<false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
 cudaError_t conv_tc_occupancy(size_t smem, int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, conv3x3_tc_kernel,
+  // the plain variant has fewer threads and so the higher occupancy bound
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, conv3x3_tc_kernel<false>,
                                                        kTcThreads, smem);
 }
 

@@ -14,8 +14,9 @@ constexpr int kTileM = 128;
 constexpr int kHaloPx = kTileM + 2;        // input pixels of one halo row
 constexpr int kLowPx = kTileM / 2 + 2;     // low-resolution pixels for one M tile
 constexpr int kChunkBytes = 16;            // one 16-byte channel block
-constexpr int kTcThreads = 192;            // 6 warps: TMA, MMA, 4 x epilogue
-constexpr int kTcThreadsDecoder = 320;     // + 4 warps building the upsampled halo
+constexpr int kTcEpilogueWarps = 8;        // two per TMEM lane quarter
+constexpr int kTcThreads = 320;            // 10 warps: TMA, MMA, 8 x epilogue
+constexpr int kTcThreadsDecoder = 448;     // + 4 warps building the upsampled halo
 
 enum EpilogueMode : int {
   kEpiRelu = 0,      // bias + ReLU, fp16 store
@@ -52,6 +53,25 @@ struct TcConvLaunch {
   dim3 grid;
   size_t smem;
 };
+
+// Launch with programmatic stream serialization, so that the kernel's
+// prologue overlaps the previous kernel in the stream (each kernel calls
+// griddepcontrol.wait before touching data the previous one produced).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream);
 cudaError_t conv_tc_set_smem_limit(size_t bytes);

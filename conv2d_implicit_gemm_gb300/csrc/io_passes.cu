@@ -8,12 +8,14 @@
 // Readings of the helpers the page imports without showing them:
 //  * sanitize(v, lo, hi): NaN becomes 0, then clamp by comparison;
 //  * 'log' transfer: F(x) = log2(1 + x), F^-1(y) = 2^y - 1.
-// The fp16 input pass stores F correctly rounded: a float estimate decides
-// the fp16 code unless it lies within 2^-19 (relative) of a rounding
-// boundary, in which case the value is recomputed in double precision.
+// The input pass stores F correctly rounded to the storage precision (see
+// hdr_forward_f16: float estimate, exact decision near rounding boundaries
+// through the inverse, double precision only when that decision is too
+// close to call; fp32 storage evaluates F in double precision).
 #include <cfloat>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace oidnx {
 
@@ -29,11 +31,21 @@ __device__ __forceinline__ float sanitize(float v, float lo, float hi) {
 constexpr double kLn2 = 0.69314718055994530942;
 
 // F(s) = log2(1 + s), s in [0, FLT_MAX], correctly rounded to fp16.
+// The float estimate y (log1pf is within 1 ulp, so y is within 3 ulp of
+// F(s)) decides the code unless y(1 -+ 2^-20) round differently.  Then the
+// rounding boundary b between the two candidate codes (exact in float) is
+// compared through the monotone inverse instead: F(s) >= b <=> s >= 2^b - 1,
+// with 2^b - 1 from exp2f/expm1f (a few ulp).  Only when s lies within
+// 2^-18 (relative) of that value is F evaluated in double precision.
 __device__ __forceinline__ __half hdr_forward_f16(float s) {
-  const float y = log1pf(s) * 1.44269504088896341f;  // within a few ulp
-  const __half lo = __float2half_rn(y * (1.0f - 0x1p-19f));
-  const __half hi = __float2half_rn(y * (1.0f + 0x1p-19f));
+  const float y = log1pf(s) * 1.44269504088896341f;
+  const __half lo = __float2half_rn(y * (1.0f - 0x1p-20f));
+  const __half hi = __float2half_rn(y * (1.0f + 0x1p-20f));
   if (__half_as_ushort(lo) == __half_as_ushort(hi)) return lo;
+  const float b = 0.5f * (__half2float(lo) + __half2float(hi));
+  const float c = b < 1.0f ? expm1f(b * 0.693147180559945309f) : exp2f(b) - 1.0f;
+  if (s > c * (1.0f + 0x1p-18f)) return hi;
+  if (s < c * (1.0f - 0x1p-18f)) return lo;
   return __double2half(log1p(static_cast<double>(s)) / kLn2);
 }
 
@@ -47,63 +59,75 @@ __device__ __forceinline__ float hdr_inverse(float d) {
   return d < 1.0f ? expm1f(d * 0.693147180559945309f) : exp2f(d) - 1.0f;
 }
 
+template <int SOURCES, bool FP16, bool HDR>
 __global__ void pack_kernel(const PackParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int tx = blockIdx.x * blockDim.x + threadIdx.x;
   const int ty = blockIdx.y;
   if (tx >= p.tw) return;
   const int ix = min(max(p.tx + tx, 0), p.width - 1);
   const int iy = min(max(p.ty + ty, 0), p.height - 1);
-
-  float ch[9];
-  __half hch[9];
+  constexpr int kCh = 3 * SOURCES;
+  float ch[kCh];
   const float4 c = p.img[0][static_cast<size_t>(iy) * p.stride[0] + ix];
-  const float rgb[3] = {c.x, c.y, c.z};
-  for (int k = 0; k < 3; ++k) {
-    if (p.hdr) {
-      const float s = sanitize(__fmul_rn(rgb[k], p.scale), 0.0f, FLT_MAX);
-      if (p.fp16) hch[k] = hdr_forward_f16(s);
-      else ch[k] = hdr_forward_f32(s);
-    } else {
-      ch[k] = sanitize(rgb[k], 0.0f, 1.0f);
-      hch[k] = __float2half_rn(ch[k]);
-    }
+  if (HDR) {
+    ch[0] = sanitize(__fmul_rn(c.x, p.scale), 0.0f, FLT_MAX);
+    ch[1] = sanitize(__fmul_rn(c.y, p.scale), 0.0f, FLT_MAX);
+    ch[2] = sanitize(__fmul_rn(c.z, p.scale), 0.0f, FLT_MAX);
+  } else {
+    ch[0] = sanitize(c.x, 0.0f, 1.0f);
+    ch[1] = sanitize(c.y, 0.0f, 1.0f);
+    ch[2] = sanitize(c.z, 0.0f, 1.0f);
   }
-  if (p.sources > 1) {
+  if (SOURCES > 1) {
     const float4 a = p.img[1][static_cast<size_t>(iy) * p.stride[1] + ix];
-    ch[3] = sanitize(a.x, 0.0f, 1.0f);
-    ch[4] = sanitize(a.y, 0.0f, 1.0f);
-    ch[5] = sanitize(a.z, 0.0f, 1.0f);
+    ch[3 % kCh] = sanitize(a.x, 0.0f, 1.0f);
+    ch[4 % kCh] = sanitize(a.y, 0.0f, 1.0f);
+    ch[5 % kCh] = sanitize(a.z, 0.0f, 1.0f);
   }
-  if (p.sources > 2) {
+  if (SOURCES > 2) {
     const float4 n = p.img[2][static_cast<size_t>(iy) * p.stride[2] + ix];
-    ch[6] = __fadd_rn(__fmul_rn(sanitize(n.x, -1.0f, 1.0f), 0.5f), 0.5f);
-    ch[7] = __fadd_rn(__fmul_rn(sanitize(n.y, -1.0f, 1.0f), 0.5f), 0.5f);
-    ch[8] = __fadd_rn(__fmul_rn(sanitize(n.z, -1.0f, 1.0f), 0.5f), 0.5f);
+    ch[6 % kCh] = __fadd_rn(__fmul_rn(sanitize(n.x, -1.0f, 1.0f), 0.5f), 0.5f);
+    ch[7 % kCh] = __fadd_rn(__fmul_rn(sanitize(n.y, -1.0f, 1.0f), 0.5f), 0.5f);
+    ch[8 % kCh] = __fadd_rn(__fmul_rn(sanitize(n.z, -1.0f, 1.0f), 0.5f), 0.5f);
   }
-  const int nch = 3 * p.sources;
   const size_t pixel = static_cast<size_t>(ty) * p.chunks * p.tw + tx;
-  uint4* out = static_cast<uint4*>(p.out);
-  if (p.fp16) {
-    for (int k = 3; k < nch; ++k) hch[k] = __float2half_rn(ch[k]);
-    unsigned short bits[16];
-    for (int k = 0; k < 16; ++k) bits[k] = k < nch ? __half_as_ushort(hch[k]) : 0;
-    for (int j = 0; j < p.chunks; ++j) {
-      uint32_t w[4];
-      for (int k = 0; k < 4; ++k)
-        w[k] = static_cast<uint32_t>(bits[8 * j + 2 * k]) |
-               (static_cast<uint32_t>(bits[8 * j + 2 * k + 1]) << 16);
-      out[pixel + static_cast<size_t>(j) * p.tw] = make_uint4(w[0], w[1], w[2], w[3]);
+  if (FP16) {
+    // 16 lanes = 2 chunks of 8 halves; lanes past 3*SOURCES are zero
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint32_t pair = 0;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int lane = 2 * k + e;
+        if (lane < kCh) {
+          const __half hv = (HDR && lane < 3) ? hdr_forward_f16(ch[lane]) : __float2half_rn(ch[lane]);
+          pair |= static_cast<uint32_t>(__half_as_ushort(hv)) << (16 * e);
+        }
+      }
+      w[k] = pair;
     }
+    uint4* out = static_cast<uint4*>(p.out);
+    out[pixel] = make_uint4(w[0], w[1], w[2], w[3]);
+    out[pixel + p.tw] = make_uint4(w[4], w[5], w[6], w[7]);
   } else {
     float v[12];
-    for (int k = 0; k < 12; ++k) v[k] = k < nch ? ch[k] : 0.0f;
-    for (int j = 0; j < p.chunks; ++j)
-      reinterpret_cast<float4*>(out)[pixel + static_cast<size_t>(j) * p.tw] =
+#pragma unroll
+    for (int k = 0; k < 12; ++k)
+      v[k] = k < kCh ? ((HDR && k < 3) ? hdr_forward_f32(ch[k]) : ch[k]) : 0.0f;
+    float4* out = static_cast<float4*>(p.out);
+#pragma unroll
+    for (int j = 0; j < (kCh + 3) / 4; ++j)
+      out[pixel + static_cast<size_t>(j) * p.tw] =
           make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
   }
 }
 
 __global__ void unpack_kernel(const UnpackParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int x = blockIdx.x * blockDim.x + threadIdx.x;
   const int y = blockIdx.y;
   if (x >= p.ow) return;
@@ -124,16 +148,27 @@ __global__ void unpack_kernel(const UnpackParams p) {
 
 }  // namespace
 
-cudaError_t launch_pack(const PackParams& p, cudaStream_t stream) {
+template <int S, bool F16, bool HDR>
+cudaError_t launch_pack_t(const PackParams& p, cudaStream_t stream) {
   dim3 grid((p.tw + 127) / 128, p.th);
-  pack_kernel<<<grid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(pack_kernel<S, F16, HDR>, grid, dim3(128), 0, stream, p);
+}
+
+template <int S>
+cudaError_t launch_pack_s(const PackParams& p, cudaStream_t stream) {
+  if (p.fp16) return p.hdr ? launch_pack_t<S, true, true>(p, stream) : launch_pack_t<S, true, false>(p, stream);
+  return p.hdr ? launch_pack_t<S, false, true>(p, stream) : launch_pack_t<S, false, false>(p, stream);
+}
+
+cudaError_t launch_pack(const PackParams& p, cudaStream_t stream) {
+  if (p.sources == 1) return launch_pack_s<1>(p, stream);
+  if (p.sources == 2) return launch_pack_s<2>(p, stream);
+  return launch_pack_s<3>(p, stream);
 }
 
 cudaError_t launch_unpack(const UnpackParams& p, cudaStream_t stream) {
   dim3 grid((p.ow + 127) / 128, p.oh);
-  unpack_kernel<<<grid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(unpack_kernel, grid, dim3(128), 0, stream, p);
 }
 
 }  // namespace oidnx
