@@ -152,6 +152,18 @@ def aggregate(ms_per_rank, px_per_rank):
     return sum(px_per_rank) / 1e6 / (slowest / 1e3), slowest
 
 
+def max_over_ranks(values):
+    """Element-wise max of per-rank timings (identity on a single process)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(values)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(list(values), dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
@@ -269,12 +281,7 @@ def run_ours(args):
     ox.oidnx_filter_release(f)
 
     px = WIDTH * HEIGHT
-    if world > 1:
-        t = torch.tensor([mean_ms, float(np.mean(e2e_ms))], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_ms, e2e_mean = float(t[0]), float(t[1])
-    else:
-        e2e_mean = float(np.mean(e2e_ms))
+    mean_ms, e2e_mean = max_over_ranks([mean_ms, float(np.mean(e2e_ms))])
     value, _ = aggregate([mean_ms] * world, [px] * world)
     e2e_value, _ = aggregate([e2e_mean] * world, [px] * world)
 
