@@ -52,6 +52,23 @@ __device__ __forceinline__ void tile_origin(const TcConvParams& p, int tile, int
   *y0 = ty * p.R;
 }
 
+// Tile origin; sub-pixel decoder tiles span 256 columns and hold one column
+// parity px (tile index = 2 * 256-column block + px).
+template <int KIND>
+__device__ __forceinline__ void tile_origin_k(const TcConvParams& p, int tile, int* x0, int* y0,
+                                              int* px) {
+  const int ty = tile / p.tiles_x;
+  const int tx = tile - ty * p.tiles_x;
+  *y0 = ty * p.R;
+  if (KIND == kTcSubpixel) {
+    *x0 = (tx >> 1) * (2 * kTileM);
+    *px = tx & 1;
+  } else {
+    *x0 = tx * kTileM;
+    *px = 0;
+  }
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -106,10 +123,101 @@ __device__ __forceinline__ void issue_kblock_r(int R, uint64_t ad, uint64_t bd, 
   }
 }
 
+// Sub-pixel decoder, upsampled part: the tile holds 128 outputs of column
+// parity px (x = xb + 2m + px) in R rows.  Nearest upsampling folds the 3x3
+// taps over the upsampled source into 2x2 taps over the low-resolution halo:
+// low-res row hl feeds output rows 2hl-3 .. 2hl of the tile (parity classes
+// (1,+1), (0,0), (1,0), (0,-1) in (row parity, row offset)), whose summed
+// weights are stacked along N in that order; the column offset dx runs over
+// two values selected by px (A shifted by d + px pixels).  In K block 0, d 0
+// the rows first reached at hl (2hl-1 and 2hl) are overwritten.
+template <int R, int G, bool FIRST>
+__device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
+                                         int px, int pxb, uint32_t id1, uint32_t id2,
+                                         uint32_t id3, uint32_t id4) {
+#pragma unroll
+  for (int d = 0; d < 2; ++d) {
+    const uint64_t adk = ad + static_cast<uint32_t>(d + px);
+    const uint64_t bdk = bd + static_cast<uint32_t>(pxb * 2 + d) * 8u * N;
+#pragma unroll
+    for (int hl = 0; hl < R / 2 + 2; ++hl) {
+      const int lo = 2 * hl - 3 > 0 ? 2 * hl - 3 : 0;
+      const int hi = 2 * hl < R - 1 ? 2 * hl : R - 1;
+      const uint64_t a = adk + static_cast<uint32_t>(hl * 2 * kHaloPx);
+      const int newlo = (FIRST && d == 0) ? (2 * hl - 1 > lo ? 2 * hl - 1 : lo) : hi + 1;
+#pragma unroll
+      for (int c = lo; c <= hi; c += G) {
+        const int e = c + G - 1 < hi ? c + G - 1 : hi;
+        const int ea = e < newlo - 1 ? e : newlo - 1;
+        if (c <= ea) {
+          const int n = ea - c + 1;
+          mma_f16_ss(dbase + c * N, a, bdk + static_cast<uint32_t>(c - 2 * hl + 3) * N,
+                     n == 1 ? id1 : n == 2 ? id2 : n == 3 ? id3 : id4, 1u);
+        }
+        const int c2 = c > newlo ? c : newlo;
+        if (c2 <= e) {
+          const int n = e - c2 + 1;
+          mma_f16_ss(dbase + c2 * N, a, bdk + static_cast<uint32_t>(c2 - 2 * hl + 3) * N,
+                     n == 1 ? id1 : n == 2 ? id2 : n == 3 ? id3 : id4, 0u);
+        }
+      }
+    }
+  }
+}
+
+// Sub-pixel decoder, skip part for one kx: the halo box of one column-parity
+// plane of the skip source holds the skip pixels xb + px + kx - 1 + 2m (A
+// shifted by one element for kx = 2 in the outer plane); ky stacked along N
+// as in issue_kblock.
+template <int R, int G>
+__device__ __forceinline__ void issue_skip(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
+                                           uint32_t id1, uint32_t id2, uint32_t id3) {
+#pragma unroll
+  for (int h = 0; h < R + 2; ++h) {
+    const int lo = h - 2 > 0 ? h - 2 : 0;
+    const int hi = h < R - 1 ? h : R - 1;
+    const uint64_t a = ad + static_cast<uint32_t>(h * 2 * kHaloPx);
+#pragma unroll
+    for (int c = lo; c <= hi; c += G) {
+      const int e = c + G - 1 < hi ? c + G - 1 : hi;
+      const int n = e - c + 1;
+      mma_f16_ss(dbase + c * N, a, bd + static_cast<uint32_t>(2 - h + c) * N,
+                 n == 1 ? id1 : n == 2 ? id2 : id3, 1u);
+    }
+  }
+}
+
+template <int R, int G4, int G3>
+__device__ __forceinline__ void issue_subpixel_r(bool up, bool first, uint64_t ad, uint64_t bd,
+                                                 uint32_t dbase, uint32_t N, int px, int pxb,
+                                                 uint32_t id1, uint32_t id2, uint32_t id3,
+                                                 uint32_t id4) {
+  if (!up) {
+    // bd: first kx slice; pxb (reused): 16-byte units to the second slice, 0 if none
+    issue_skip<R, G3>(ad, bd, dbase, N, id1, id2, id3);
+    if (pxb) issue_skip<R, G3>(ad + 1, bd + static_cast<uint32_t>(pxb), dbase, N, id1, id2, id3);
+  } else if (first)
+    issue_up<R, G4, true>(ad, bd, dbase, N, px, pxb, id1, id2, id3, id4);
+  else
+    issue_up<R, G4, false>(ad, bd, dbase, N, px, pxb, id1, id2, id3, id4);
+}
+
+template <int G4, int G3>
+__device__ __forceinline__ void issue_subpixel_item(int R, bool up, uint64_t ad, uint64_t bd,
+                                                    uint32_t dbase, uint32_t N, int px, int pxb,
+                                                    uint32_t id1, uint32_t id2, uint32_t id3,
+                                                    uint32_t id4, bool first) {
+  switch (R) {
+    case 2: issue_subpixel_r<2, G4, G3>(up, first, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
+    case 4: issue_subpixel_r<4, G4, G3>(up, first, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
+    default: issue_subpixel_r<8, G4, G3>(up, first, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
+  }
+}
+
 }  // namespace
 
-template <bool DEC>
-__global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
+template <int KIND>
+__global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThreads, 1)
     conv3x3_tc_kernel(const __grid_constant__ CUtensorMap map0,
                       const __grid_constant__ CUtensorMap map1, const TcConvParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -119,9 +227,13 @@ __global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
   const int S = p.S, R = p.R, N = p.N, KB0 = p.KB0;
   const int KB = p.KB0 + p.KB1;
   const int num_tiles = p.tiles_x * p.tiles_y;
+  constexpr bool SP = KIND == kTcSubpixel;
+  // pipeline items per tile: K blocks, or (sub-pixel) upsampled K blocks plus
+  // one item per (skip K block, kx)
+  const int items = SP ? KB0 + 2 * p.KB1 : KB;
   // shared memory: [resident weights][A stages][B stages][staging][bias][barriers]
   uint8_t* Wres = smem;
-  uint8_t* A = Wres + (p.resident ? static_cast<size_t>(KB) * p.b_stage : 0);
+  uint8_t* A = Wres + (p.resident ? ((p.wres_bytes + 1023u) & ~1023u) : 0u);
   uint8_t* B = A + static_cast<size_t>(S) * p.a_stage;
   uint8_t* ST = B + (p.resident ? 0 : static_cast<size_t>(S) * p.b_stage);
   float* bias_s = reinterpret_cast<float*>(ST + static_cast<size_t>(S) * p.st_stage);
@@ -166,11 +278,18 @@ __global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
       prefetch_tmap(&map0);
       if (p.KB1 > 0) prefetch_tmap(&map1);
       if (p.resident) {
-        mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(KB) * p.b_tx);
-        for (int kb = 0; kb < KB; ++kb)
-          bulk_load(Wres + static_cast<size_t>(kb) * p.b_stage,
-                    reinterpret_cast<const uint8_t*>(p.weights) + static_cast<size_t>(kb) * p.b_tx,
-                    p.b_tx, wbar);
+        if (SP) {
+          mbar_arrive_expect_tx(wbar, p.wres_bytes);
+          for (uint32_t off = 0; off < p.wres_bytes; off += 65536u)
+            bulk_load(Wres + off, reinterpret_cast<const uint8_t*>(p.weights) + off,
+                      min(65536u, p.wres_bytes - off), wbar);
+        } else {
+          mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(KB) * p.b_tx);
+          for (int kb = 0; kb < KB; ++kb)
+            bulk_load(Wres + static_cast<size_t>(kb) * p.b_stage,
+                      reinterpret_cast<const uint8_t*>(p.weights) + static_cast<size_t>(kb) * p.b_tx,
+                      p.b_tx, wbar);
+        }
       }
       // Weights and bias are constants; the activations come from the
       // previous kernel in the stream.
@@ -178,14 +297,50 @@ __global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        int x0, y0;
-        tile_origin(p, tile, &x0, &y0);
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        int x0, y0, px;
+        tile_origin_k<KIND>(p, tile, &x0, &y0, &px);
+        for (int kb = 0; kb < items; ++kb, ++it) {
           const uint32_t s = it % S;
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kErrTimeoutProducer)) {
             ok = false;
             break;
+          }
+          if (SP) {
+            const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(p.weights);
+            if (kb < KB0) {
+              const uint32_t half = p.b_tx / 2;  // one column parity of the block
+              mbar_arrive_expect_tx(&full[s], p.a_tx + (p.resident ? 0u : half));
+              tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map0, &full[s], 0,
+                          (x0 >> 1) - 1, 2 * kb, (y0 >> 1) - 1);
+              if (!p.resident)
+                bulk_load(B + static_cast<size_t>(s) * p.b_stage,
+                          wsrc + static_cast<size_t>(kb) * p.b_tx + static_cast<size_t>(px) * half,
+                          half, &full[s]);
+            } else {
+              // skip source, column-parity split: the outer plane (parity
+              // px ^ 1, serving kx = 0 and kx = 2) or the centre plane
+              // (parity px, kx = 1) of one 16-channel block
+              const int j = (kb - KB0) >> 1, part = (kb - KB0) & 1;
+              const int plane = part ? px : (px ^ 1);
+              const int i0 = (x0 >> 1) - (part == 0 && px == 0 ? 1 : 0);
+              const uint32_t wb = part ? p.b_tx2 : 2u * p.b_tx2;
+              mbar_arrive_expect_tx(&full[s], p.st_tx + (p.resident ? 0u : wb));
+              tma_load_5d(A + static_cast<size_t>(s) * p.a_stage, &map1, &full[s], 0, i0, plane,
+                          2 * j, y0 - 1);
+              if (!p.resident) {
+                const size_t kb_off = static_cast<size_t>(KB0) * p.b_tx + static_cast<size_t>(3 * j) * p.b_tx2;
+                if (part) {
+                  bulk_load(B + static_cast<size_t>(s) * p.b_stage, wsrc + kb_off + p.b_tx2, p.b_tx2,
+                            &full[s]);
+                } else {  // kx = 0 and kx = 2 slices, one after the other
+                  bulk_load(B + static_cast<size_t>(s) * p.b_stage, wsrc + kb_off, p.b_tx2, &full[s]);
+                  bulk_load(B + static_cast<size_t>(s) * p.b_stage + p.b_tx2,
+                            wsrc + kb_off + 2 * static_cast<size_t>(p.b_tx2), p.b_tx2, &full[s]);
+                }
+              }
+            }
+            continue;
           }
           const bool low = p.upsample0 && kb < KB0;
           mbar_arrive_expect_tx(&full[s], (low ? p.st_tx : p.a_tx) + (p.resident ? 0u : p.b_tx));
@@ -215,9 +370,15 @@ __global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const int g = min(3, 256 / N);
+      const int g4 = min(4, 256 / N);
       const uint32_t id1 = idesc_f16_f32(kTileM, N);
       const uint32_t id2 = idesc_f16_f32(kTileM, min(2 * N, 256));
       const uint32_t id3 = idesc_f16_f32(kTileM, min(3 * N, 256));
+      const uint32_t id4 = idesc_f16_f32(kTileM, min(4 * N, 256));
+      const uint64_t a_up0 = smem_desc_noswizzle(smem_u32(A), kHaloPx * kChunkBytes, 128);
+      const uint32_t wbase = smem_u32(p.resident ? Wres : B);
+      const uint64_t b_up0 = smem_desc_noswizzle(wbase, 4u * N * kChunkBytes, 128);
+      const uint64_t b_sk0 = smem_desc_noswizzle(wbase, 3u * N * kChunkBytes, 128);
       const uint64_t a_desc0 = smem_desc_noswizzle(smem_u32(A), kHaloPx * kChunkBytes, 128);
       const uint64_t b_desc0 =
           smem_desc_noswizzle(smem_u32(p.resident ? Wres : B), 3u * N * kChunkBytes, 128);
@@ -233,13 +394,42 @@ __global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_base = tmem + buf * set_cols;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        int tx0, ty0, tpx;
+        tile_origin_k<KIND>(p, tile, &tx0, &ty0, &tpx);
+        for (int kb = 0; kb < items; ++kb, ++it) {
           const uint32_t s = it % S;
           const uint32_t ph = (it / S) & 1u;
           ok = mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutMma);
-          if (ok && DEC) ok = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
+          if (ok && KIND == kTcExpand) ok = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
           if (!ok) break;
           tc_fence_after();
+          if (SP) {
+            const bool up = kb < KB0;
+            const uint32_t soff = (s * p.a_stage) >> 4;
+            uint32_t woff;
+            int pxb;
+            if (up) {
+              woff = p.resident ? static_cast<uint32_t>(kb) * p.b_tx : s * p.b_stage;
+              // streamed stages hold only this tile's parity half of an upsampled block
+              pxb = p.resident ? tpx : 0;
+            } else {
+              const int j = (kb - KB0) >> 1, part = (kb - KB0) & 1;
+              if (p.resident)
+                woff = static_cast<uint32_t>(KB0) * p.b_tx + static_cast<uint32_t>(3 * j + part) * p.b_tx2;
+              else
+                woff = s * p.b_stage;
+              // outer plane: kx = 0 then kx = 2 (two slices apart when resident,
+              // adjacent when streamed); centre plane: kx = 1 only
+              pxb = part ? 0 : static_cast<int>((p.resident ? 2u * p.b_tx2 : p.b_tx2) >> 4);
+            }
+            const uint64_t ad = a_up0 + soff;
+            const uint64_t bd = (up ? b_up0 : b_sk0) + (woff >> 4);
+            if (g4 == 4) issue_subpixel_item<4, 3>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4, kb == 0);
+            else if (g4 == 2) issue_subpixel_item<2, 2>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4, kb == 0);
+            else issue_subpixel_item<1, 1>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4, kb == 0);
+            mma_commit(&empty[s]);
+            continue;
+          }
           const uint64_t ad = a_desc0 + ((s * p.a_stage) >> 4);
           const uint64_t bd = b_desc0 + ((static_cast<uint32_t>(p.resident ? kb : s) * p.b_stage) >> 4);
           if (g == 3) issue_kblock_r<3>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, kb == 0);
@@ -256,6 +446,7 @@ __global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
     }
     __syncwarp();
   } else if (warp >= 2 + kTcEpilogueWarps) {
+    // (only launched with these warps for KIND == kTcExpand)
     // ------------------------------------------------------------ upsampled halo
     const int et = threadIdx.x - 32 * (2 + kTcEpilogueWarps);  // 0..127
     const int total = (R + 2) * 2 * kHaloPx;
@@ -313,9 +504,10 @@ __global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
       const uint32_t buf = tcount & 1u;
       if (!mbar_wait_bounded(&tfull[buf], (tcount >> 1) & 1u, p.status, kErrTimeoutEpilogue)) break;
       tc_fence_after();
-      int x0, y0;
-      tile_origin(p, tile, &x0, &y0);
-      const int x = x0 + m;
+      int x0, y0, px;
+      tile_origin_k<KIND>(p, tile, &x0, &y0, &px);
+      // sub-pixel tiles hold every other output column
+      const int x = SP ? x0 + 2 * m + px : x0 + m;
       const uint32_t tl = tmem + lane_off + buf * set_cols;
 
       if (p.mode == kEpiRelu) {
@@ -385,6 +577,15 @@ __global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
               const size_t base1 = base0 + static_cast<size_t>(Wp) * 8;
               *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
               *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
+              if (p.out_split) {
+                // plane xp & 1, index xp >> 1 (Wp even whenever the copy exists)
+                __half* o2 = static_cast<__half*>(p.out_split);
+                const size_t s0 =
+                    ((((static_cast<size_t>(yp) * C8 + 2 * c) * 2 + (xp & 1)) * (Wp >> 1)) + (xp >> 1)) * 8;
+                const size_t s1 = s0 + static_cast<size_t>(Wp) * 8;
+                *reinterpret_cast<uint4*>(o2 + s0) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(o2 + s1) = make_uint4(h[4], h[5], h[6], h[7]);
+              }
             }
           }
         }
@@ -421,25 +622,31 @@ __global__ void __launch_bounds__(DEC ? kTcThreadsDecoder : kTcThreads, 1)
 }
 
 cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
-  if (L.p.upsample0)
-    return launch_pdl(conv3x3_tc_kernel<true>, L.grid, dim3(kTcThreadsDecoder), L.smem, stream,
+  if (L.kind == kTcExpand)
+    return launch_pdl(conv3x3_tc_kernel<kTcExpand>, L.grid, dim3(kTcThreadsDecoder), L.smem,
+                      stream, L.map0, L.map1, L.p);
+  if (L.kind == kTcSubpixel)
+    return launch_pdl(conv3x3_tc_kernel<kTcSubpixel>, L.grid, dim3(kTcThreads), L.smem, stream,
                       L.map0, L.map1, L.p);
-  return launch_pdl(conv3x3_tc_kernel<false>, L.grid, dim3(kTcThreads), L.smem, stream, L.map0,
+  return launch_pdl(conv3x3_tc_kernel<kTcPlain>, L.grid, dim3(kTcThreads), L.smem, stream, L.map0,
                     L.map1, L.p);
 }
 
 cudaError_t conv_tc_set_smem_limit(size_t bytes) {
-  cudaError_t e = cudaFuncSetAttribute(conv3x3_tc_kernel<true>,
+  cudaError_t e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcExpand>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(conv3x3_tc_kernel<false>,
+  e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcSubpixel>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(conv3x3_tc_kernel<kTcPlain>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
 cudaError_t conv_tc_occupancy(size_t smem, int* blocks_per_sm) {
   // the plain variant has fewer threads and so the higher occupancy bound
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, conv3x3_tc_kernel<false>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, conv3x3_tc_kernel<kTcPlain>,
                                                        kTcThreads, smem);
 }
 

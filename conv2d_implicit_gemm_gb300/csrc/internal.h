@@ -44,12 +44,26 @@ struct TcConvParams {
   uint32_t b_stage;        // bytes per B block (1024-aligned)
   uint32_t st_stage;       // bytes per low-res staging stage (0 if none)
   uint32_t a_tx, b_tx, st_tx;  // transaction bytes per stage
+  // sub-pixel decoder: b_tx = upsampled B block (512 N), b_tx2 = skip B kx
+  // slice (96 N), st_tx = strided skip box; wres_bytes = resident weights
+  uint32_t b_tx2;
+  uint32_t wres_bytes;
+  // pool epilogue: optional second copy of the output, column-parity split
+  // [Ho][N/8][2][Wo/2][8] (read by the sub-pixel decoder as its skip source)
+  void* out_split;
+};
+
+enum TcKind : int {
+  kTcPlain = 0,     // plain conv (also pool / final epilogues)
+  kTcExpand = 1,    // decoder, upsampled halo built in shared memory
+  kTcSubpixel = 2,  // decoder, upsampled part as parity-class 2x2 taps
 };
 
 struct TcConvLaunch {
   CUtensorMap map0;        // source 0 (full-res halo box, or low-res box)
-  CUtensorMap map1;        // source 1 (full-res halo box); unused if KB1 == 0
+  CUtensorMap map1;        // source 1 (full-res halo box, or stride-2 box); unused if KB1 == 0
   TcConvParams p;
+  int kind;                // TcKind
   dim3 grid;
   size_t smem;
 };
@@ -106,6 +120,7 @@ struct PackParams {
   int fp16;                // storage precision
   void* out;               // [th][chunks][tw][lanes]
   int chunks;              // 16-byte chunks per pixel
+  void* out_split;         // optional parity-split copy [th][chunks][2][tw/2][lanes]
 };
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 
@@ -123,5 +138,10 @@ struct UnpackParams {
   float scale;
 };
 cudaError_t launch_unpack(const UnpackParams& p, cudaStream_t stream);
+
+// Column-parity split copy of an fp16 activation: [h][chunks][w][8] ->
+// [h][chunks][2][w/2][8] (w even).
+cudaError_t launch_split_copy(const void* src, void* dst, int w, int h, int chunks,
+                              cudaStream_t stream);
 
 }  // namespace oidnx

@@ -112,6 +112,14 @@ __global__ void pack_kernel(const PackParams p) {
     uint4* out = static_cast<uint4*>(p.out);
     out[pixel] = make_uint4(w[0], w[1], w[2], w[3]);
     out[pixel + p.tw] = make_uint4(w[4], w[5], w[6], w[7]);
+    if (p.out_split) {
+      // column-parity split copy: plane tx & 1, index tx >> 1 (tw even)
+      uint4* o2 = static_cast<uint4*>(p.out_split);
+      const size_t half = static_cast<size_t>(p.tw) >> 1;
+      const size_t s0 = (static_cast<size_t>(ty) * p.chunks * 2 + (tx & 1)) * half + (tx >> 1);
+      o2[s0] = make_uint4(w[0], w[1], w[2], w[3]);
+      o2[s0 + 2 * half] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
   } else {
     float v[12];
 #pragma unroll
@@ -146,7 +154,24 @@ __global__ void unpack_kernel(const UnpackParams p) {
   p.out[static_cast<size_t>(y + p.oy) * p.out_stride + x + p.ox] = make_float4(r, g, b, a);
 }
 
+__global__ void split_copy_kernel(const uint4* src, uint4* dst, int w, int h, int chunks) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  const int row = blockIdx.y;  // y * chunks + chunk
+  if (x >= w) return;
+  const size_t half = static_cast<size_t>(w) >> 1;
+  dst[(static_cast<size_t>(row) * 2 + (x & 1)) * half + (x >> 1)] = src[static_cast<size_t>(row) * w + x];
+}
+
 }  // namespace
+
+cudaError_t launch_split_copy(const void* src, void* dst, int w, int h, int chunks,
+                              cudaStream_t stream) {
+  dim3 grid((w + 127) / 128, h * chunks);
+  return launch_pdl(split_copy_kernel, grid, dim3(128), 0, stream, static_cast<const uint4*>(src),
+                    static_cast<uint4*>(dst), w, h, chunks);
+}
 
 template <int S, bool F16, bool HDR>
 cudaError_t launch_pack_t(const PackParams& p, cudaStream_t stream) {

@@ -85,8 +85,19 @@ enum Kind { kPlain, kPool, kDecoder, kFinal };
 // Values of the network dataflow.
 enum Val {
   V_IN, V_E0, V_P1, V_P2, V_P3, V_P4, V_E5A, V_E5B, V_D4A, V_D4B,
-  V_D3A, V_D3B, V_D2A, V_D2B, V_D1A, V_D1B, V_OUT, V_COUNT
+  V_D3A, V_D3B, V_D2A, V_D2B, V_D1A, V_D1B, V_OUT,
+  // column-parity split copies of the decoders' skip sources (fp16 only)
+  V_INS, V_P1S, V_P2S, V_P3S, V_COUNT
 };
+
+// A split copy is written by the producer of `base` (layer index, -1 for the
+// input pass) next to the normal copy and read by decoder `consumer` when
+// that decoder runs in sub-pixel mode.
+struct SplitCopy {
+  int split, base, producer, consumer;
+};
+const SplitCopy kSplits[4] = {
+    {V_INS, V_IN, -1, 13}, {V_P1S, V_P1, 1, 11}, {V_P2S, V_P2, 2, 9}, {V_P3S, V_P3, 3, 7}};
 
 struct LayerDef {
   int src0, src1, dst, kind, level;  // level of the conv (full-resolution) extent
@@ -280,6 +291,71 @@ std::vector<uint16_t> pack_weights_tc(const ConvTensors& L, int c0, int c1, int*
   return out;
 }
 
+// Sub-pixel decoder B operand.  Upsampled K blocks (source 0): per block
+// [px][d][j][pos][N][8] where, for output column parity px, d selects the
+// low-resolution column offset dx = d - 1 + px and pos the (row parity py,
+// row offset dy) class (1,+1), (0,0), (1,0), (0,-1); each entry is the sum of
+// the fp16-rounded 3x3 weights whose taps land on that low-resolution pixel
+// (ky in Ky(py,dy), kx in Kx(px,dx)), rounded once more to fp16.  Skip K
+// blocks follow in the plain layout.  Returns bytes of the upsampled part per
+// K block in *ub.
+std::vector<uint16_t> pack_weights_subpixel(const ConvTensors& L, int c0, int c1, int N,
+                                            size_t* ub) {
+  const int p0 = round_up(c0, 16), p1 = round_up(c1, 16);
+  const int KB0 = p0 / 16, KB1 = p1 / 16;
+  // taps of the 3x3 kernel (row or column) that fall on low-res offset d for parity p
+  auto taps = [](int parity, int off, int* t) -> int {
+    if (parity == 0) {
+      if (off == -1) { t[0] = 0; return 1; }
+      t[0] = 1; t[1] = 2; return 2;       // off 0
+    }
+    if (off == 0) { t[0] = 0; t[1] = 1; return 2; }
+    t[0] = 2; return 1;                    // off +1
+  };
+  const int pos_py[4] = {1, 0, 1, 0}, pos_dy[4] = {1, 0, 0, -1};
+  const size_t up_halves = static_cast<size_t>(2) * 2 * 2 * 4 * N * 8;   // per K block
+  const size_t sk_halves = static_cast<size_t>(3) * 2 * 3 * N * 8;
+  *ub = up_halves * 2;
+  std::vector<uint16_t> out(KB0 * up_halves + KB1 * sk_halves, 0);
+  auto q = [](float w) { return half_bits_to_float(to_half_bits(w)); };
+  for (int kb = 0; kb < KB0; ++kb)
+    for (int px = 0; px < 2; ++px)
+      for (int d = 0; d < 2; ++d)
+        for (int j = 0; j < 2; ++j)
+          for (int pos = 0; pos < 4; ++pos) {
+            int kys[2], kxs[2];
+            const int nky = taps(pos_py[pos], pos_dy[pos], kys);
+            const int nkx = taps(px, d - 1 + px, kxs);
+            for (int n = 0; n < L.cout; ++n)
+              for (int l = 0; l < 8; ++l) {
+                const int ch = kb * 16 + j * 8 + l;
+                if (ch >= c0) continue;
+                float sum = 0.0f;
+                for (int a = 0; a < nky; ++a)
+                  for (int b = 0; b < nkx; ++b)
+                    sum += q(L.w[(static_cast<size_t>(n) * L.cin + ch) * 9 + kys[a] * 3 + kxs[b]]);
+                const size_t idx = kb * up_halves +
+                                   ((((static_cast<size_t>(px) * 2 + d) * 2 + j) * 4 + pos) * N + n) * 8 + l;
+                out[idx] = to_half_bits(sum);
+              }
+          }
+  for (int kb = 0; kb < KB1; ++kb)
+    for (int kx = 0; kx < 3; ++kx)
+      for (int j = 0; j < 2; ++j)
+        for (int pos = 0; pos < 3; ++pos)
+          for (int n = 0; n < L.cout; ++n)
+            for (int l = 0; l < 8; ++l) {
+              const int v = kb * 16 + j * 8 + l;
+              if (v >= c1) continue;
+              const int ky = 2 - pos;
+              const float w = L.w[(static_cast<size_t>(n) * L.cin + c0 + v) * 9 + ky * 3 + kx];
+              const size_t idx = KB0 * up_halves +
+                                 ((((static_cast<size_t>(kb) * 3 + kx) * 2 + j) * 3 + pos) * N + n) * 8 + l;
+              out[idx] = to_half_bits(w);
+            }
+  return out;
+}
+
 // fp32 CUDA-core weights: [group of 8 outputs][tap][K lane][8 outputs], K lanes
 // enumerate the concatenated sources each padded to a multiple of 4.
 std::vector<float> pack_weights_simt(const ConvTensors& L, int c0, int c1, int* C40, int* C41,
@@ -401,7 +477,7 @@ EncodeTiledFn get_encode_fn() {
 // fp16 activation [H][C8][W][8] as a 4-D tensor {8 lanes, W, C8, H}; box
 // {8, box_w, 2, box_h}; zero fill outside.
 oidnx_status encode_act_map(CUtensorMap* map, const void* base, int W, int H, int C8, int box_w,
-                            int box_h) {
+                            int box_h, int x_stride = 1) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   cuuint64_t dims[4] = {8, static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(C8),
@@ -409,13 +485,32 @@ oidnx_status encode_act_map(CUtensorMap* map, const void* base, int W, int H, in
   cuuint64_t strides[3] = {16, static_cast<cuuint64_t>(W) * 16,
                            static_cast<cuuint64_t>(W) * 16 * C8};
   cuuint32_t box[4] = {8, static_cast<cuuint32_t>(box_w), 2, static_cast<cuuint32_t>(box_h)};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
+  cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(x_stride), 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %dx%dx%d", int(r), W, H,
                 C8);
+  return ok();
+}
+
+// fp16 column-parity split activation [H][C8][2][W/2][8] as a 5-D tensor
+// {8 lanes, W/2, 2 planes, C8, H}; box {8, box_w, 1, 2, box_h}.
+oidnx_status encode_split_map(CUtensorMap* map, const void* base, int W, int H, int C8, int box_w,
+                              int box_h) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t half = static_cast<cuuint64_t>(W / 2);
+  cuuint64_t dims[5] = {8, half, 2, static_cast<cuuint64_t>(C8), static_cast<cuuint64_t>(H)};
+  cuuint64_t strides[4] = {16, half * 16, half * 32, half * 32 * C8};
+  cuuint32_t box[5] = {8, static_cast<cuuint32_t>(box_w), 1, 2, static_cast<cuuint32_t>(box_h)};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled (split) failed (%d)", int(r));
   return ok();
 }
 
@@ -427,6 +522,8 @@ struct DeviceLayer {
   // fp16 path
   void* w16 = nullptr;  // packed B operand
   int KB0 = 0, KB1 = 0, N = 0;
+  void* w16_sub = nullptr;  // sub-pixel decoder B operand (decoders only)
+  size_t sub_bytes = 0, sub_ub = 0;
   // fp32 path
   float* w32 = nullptr;
   int C40 = 0, C41 = 0, groups = 0;
@@ -457,6 +554,7 @@ struct Plan {
   void* arena = nullptr;
   size_t arena_bytes = 0;
   std::vector<LayerLaunch> launches;
+  bool split_on[4] = {};  // kSplits[i] in use (its decoder runs in sub-pixel mode)
   uint64_t last_used = 0;
   cudaEvent_t done = nullptr;  // recorded after each use
   bool used = false;
@@ -482,7 +580,7 @@ struct oidnx_filter {
   int* status = nullptr;  // device error word
   // parameters
   int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
-      overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0;
+      overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 0;
   float input_scale = 1.0f;
   void* img[4] = {};
   size_t img_stride[4] = {};
@@ -523,6 +621,8 @@ oidnx_status upload(const void* host, size_t bytes, void** dev) {
 }
 
 void free_layer(DeviceLayer& L) {
+  cudaFree(L.w16_sub);
+  L.w16_sub = nullptr;
   cudaFree(L.w16);
   cudaFree(L.w32);
   cudaFree(L.bias);
@@ -541,10 +641,15 @@ oidnx_status make_device_layer(const ConvTensors& T, int c0, int c1, int precisi
     std::vector<uint16_t> w = pack_weights_tc(T, c0, c1, &L->KB0, &L->KB1, &L->N);
     if (L->N > 256) return fail(OIDNX_ERR_UNSUPPORTED, "more than 256 output channels");
     OIDNX_TRY(upload(w.data(), w.size() * 2, &L->w16));
+    if (c1 > 0) {
+      std::vector<uint16_t> ws = pack_weights_subpixel(T, c0, c1, L->N, &L->sub_ub);
+      L->sub_bytes = ws.size() * 2;
+      OIDNX_TRY(upload(ws.data(), L->sub_bytes, &L->w16_sub));
+    }
     std::vector<float> b(L->N, 0.0f);
     std::copy(T.b.begin(), T.b.end(), b.begin());
     OIDNX_TRY(upload(b.data(), b.size() * 4, reinterpret_cast<void**>(&L->bias)));
-    L->weight_bytes = w.size() * 2 + b.size() * 4;
+    L->weight_bytes = w.size() * 2 + b.size() * 4 + L->sub_bytes;
   } else {
     std::vector<float> w = pack_weights_simt(T, c0, c1, &L->C40, &L->C41, &L->groups);
     OIDNX_TRY(upload(w.data(), w.size() * 4, reinterpret_cast<void**>(&L->w32)));
@@ -583,10 +688,109 @@ int num_sms() {
 
 // Build the tensor-core launch of one conv.  src0/src1: device pointers of the
 // sources (fp16 layout), ext0: extent of source 0, (W, H): conv extent.
+// Pad the shared-memory request until at most `allowed` CTAs fit one SM, so
+// that CTAs sharing an SM never wait for tensor memory.
+oidnx_status bound_ctas_per_sm(size_t* smem, uint32_t tmem_cols, int* blocks) {
+  const size_t max_smem = 227 * 1024;
+  static size_t limit_set = 0;
+  if (limit_set < max_smem) {
+    cudaError_t e = conv_tc_set_smem_limit(max_smem);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
+    limit_set = max_smem;
+  }
+  const int allowed = static_cast<int>(512 / tmem_cols);
+  for (;;) {
+    cudaError_t e = conv_tc_occupancy(*smem, blocks);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "occupancy: %s", cudaGetErrorString(e));
+    if (*blocks <= allowed) return ok();
+    *smem += 4096;
+    if (*smem > max_smem) return fail(OIDNX_ERR_UNSUPPORTED, "cannot bound CTAs per SM");
+  }
+}
+
+// Sub-pixel decoder launch (even W and H): tiles of R rows x 128 outputs of
+// one column parity; the upsampled source is read as a low-resolution halo
+// box, the skip source (src1) from its column-parity split copy.
+oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Extent ext0,
+                                      const void* src1, int W, int H, void* out, int* status,
+                                      TcConvLaunch* T) {
+  const int N = L.N;
+  int R = 8;
+  while (R > 2 && R * N > 256) R /= 2;
+  if (2 * R * N > 512) return fail(OIDNX_ERR_UNSUPPORTED, "accumulators exceed tensor memory");
+  const int tiles_x = 2 * ((W + 2 * kTileM - 1) / (2 * kTileM));
+  while (R > 2 && static_cast<long>(tiles_x) * ((H + R - 1) / R) < num_sms()) R /= 2;
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < static_cast<uint32_t>(2 * R * N)) tmem_cols *= 2;
+  TcConvParams& p = T->p;
+  std::memset(&p, 0, sizeof(p));
+  T->kind = kTcSubpixel;
+  p.weights = static_cast<const __half*>(L.w16_sub);
+  p.bias = L.bias;
+  p.out = out;
+  p.status = status;
+  p.W = W;
+  p.H = H;
+  p.N = N;
+  p.KB0 = L.KB0;
+  p.KB1 = L.KB1;
+  p.R = R;
+  p.mode = kEpiRelu;
+  p.upsample0 = 1;
+  p.tiles_x = tiles_x;
+  p.tiles_y = (H + R - 1) / R;
+  p.tmem_cols = tmem_cols;
+  p.a_tx = static_cast<uint32_t>((R / 2 + 2) * 2 * kHaloPx * kChunkBytes);   // low-res box
+  p.st_tx = static_cast<uint32_t>((R + 2) * 2 * kHaloPx * kChunkBytes);      // skip plane box
+  p.b_tx = static_cast<uint32_t>(L.sub_ub);                                  // 512 N
+  p.b_tx2 = static_cast<uint32_t>(6 * N * kChunkBytes);                      // 96 N
+  p.a_stage = static_cast<uint32_t>(round_up_sz(std::max(p.a_tx, p.st_tx), 1024));
+  p.b_stage = static_cast<uint32_t>(round_up_sz(std::max(p.b_tx / 2, 2 * p.b_tx2), 1024));
+  p.st_stage = 0;
+  const int items = L.KB0 + 2 * L.KB1;
+  const size_t max_smem = 227 * 1024;
+  const size_t fixed = 1024 + static_cast<size_t>((N + 31) / 32) * 32 * 4 + 256;
+  const size_t wbytes = round_up_sz(L.sub_bytes, 1024);
+  const int min_stages = std::max(2, std::min(items, 3));
+  size_t smem;
+  if (fixed + wbytes + min_stages * static_cast<size_t>(p.a_stage) <= max_smem) {
+    p.resident = 1;
+    p.wres_bytes = static_cast<uint32_t>(L.sub_bytes);  // bytes loaded; the layout rounds up to 1 KB
+    p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed - wbytes) / p.a_stage));
+    smem = fixed + wbytes + p.S * static_cast<size_t>(p.a_stage);
+  } else {
+    p.resident = 0;
+    const size_t stage = static_cast<size_t>(p.a_stage) + p.b_stage;
+    p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed) / stage));
+    if (p.S < 2) return fail(OIDNX_ERR_UNSUPPORTED, "conv stage does not fit shared memory");
+    smem = fixed + p.S * stage;
+  }
+  int blocks = 0;
+  OIDNX_TRY(bound_ctas_per_sm(&smem, tmem_cols, &blocks));
+  T->smem = smem;
+  const long tiles = static_cast<long>(p.tiles_x) * p.tiles_y;
+  T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, static_cast<long>(num_sms()) * blocks)), 1, 1);
+  const int c8_0 = round_up(L.c0, 16) / 8;
+  const int c8_1 = round_up(L.c1, 16) / 8;
+  OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.h, c8_0, kHaloPx, R / 2 + 2));
+  OIDNX_TRY(encode_split_map(&T->map1, src1, W, H, c8_1, kHaloPx, R + 2));
+  return ok();
+}
+
+// Whether a decoder with conv extent (W, H) and low-resolution source ext0
+// runs in sub-pixel mode (then its skip source must be the split copy).
+bool use_subpixel(int precision, int W, int H, Extent ext0) {
+  return precision == OIDNX_PRECISION_FP16 && W % 2 == 0 && H % 2 == 0 && ext0.w * 2 == W &&
+         ext0.h * 2 == H;
+}
+
 oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, Extent ext0,
                              const void* src1, int W, int H, void* out, int* status,
-                             TcConvLaunch* T) {
+                             TcConvLaunch* T, bool subpixel = false, void* out_split = nullptr) {
+  if (kind == kDecoder && subpixel && L.w16_sub)
+    return build_tc_launch_subpixel(L, src0, ext0, src1, W, H, out, status, T);
   const bool up = kind == kDecoder;
+  T->kind = up ? kTcExpand : kTcPlain;
   const int N = L.N;
   const int minR = (kind == kPool || kind == kDecoder) ? 2 : 1;
   // Two accumulator sets of R x N fp32 columns must fit the 512 TMEM columns.
@@ -612,6 +816,7 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   p.R = R;
   p.mode = kind == kPool ? kEpiReluPool : (kind == kFinal ? kEpiFinal : kEpiRelu);
   p.upsample0 = up ? 1 : 0;
+  p.out_split = kind == kPool ? out_split : nullptr;
   p.tiles_x = tiles_x;
   p.tiles_y = (H + R - 1) / R;
   p.tmem_cols = tmem_cols;
@@ -631,6 +836,7 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   size_t smem;
   if (fixed + wbytes + min_stages * a_st <= max_smem) {
     p.resident = 1;
+    p.wres_bytes = static_cast<uint32_t>(wbytes);
     p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed - wbytes) / a_st));
     smem = fixed + wbytes + p.S * a_st;
   } else {
@@ -739,6 +945,15 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
     if (kDefs[l].src1 >= 0) last_use[kDefs[l].src1] = l;
   }
   last_use[V_OUT] = kLayers;
+  for (int i = 0; i < 4; ++i) {
+    const SplitCopy& sc = kSplits[i];
+    const LayerDef& d = kDefs[sc.consumer];
+    P->split_on[i] = f->subpixel && use_subpixel(f->precision, P->lvl[d.level].w,
+                                                 P->lvl[d.level].h, P->value_ext[d.src0]);
+    P->value_ext[sc.split] = P->value_ext[sc.base];
+    P->value_ch[sc.split] = P->value_ch[sc.base];
+    last_use[sc.split] = sc.consumer;
+  }
   struct Slot {
     size_t cap, off;
     int active;
@@ -766,7 +981,12 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
     P->value_bytes[v] = need;
   };
   allocate(V_IN, -1);
-  for (int l = 0; l < kLayers; ++l) allocate(kDefs[l].dst, l);
+  if (P->split_on[0]) allocate(V_INS, -1);
+  for (int l = 0; l < kLayers; ++l) {
+    allocate(kDefs[l].dst, l);
+    for (int i = 0; i < 4; ++i)
+      if (P->split_on[i] && kSplits[i].producer == l) allocate(kSplits[i].split, l);
+  }
   P->arena_bytes = total;
   cudaError_t e = cudaMalloc(&P->arena, total);
   if (e != cudaSuccess)
@@ -786,10 +1006,20 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
     LL.layer = l;
     const Extent conv = P->lvl[d.level];
     const void* s1 = d.src1 >= 0 ? P->ptr(d.src1) : nullptr;
+    bool subpixel = false;
+    void* out_split = nullptr;
+    for (int i = 0; i < 4; ++i) {
+      if (!P->split_on[i]) continue;
+      if (kSplits[i].consumer == l) {
+        subpixel = true;
+        s1 = P->ptr(kSplits[i].split);
+      }
+      if (kSplits[i].producer == l) out_split = P->ptr(kSplits[i].split);
+    }
     if (f->precision == OIDNX_PRECISION_FP16) {
       LL.tc = true;
       OIDNX_TRY(build_tc_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, conv.w,
-                                conv.h, P->ptr(d.dst), f->status, &LL.tcl));
+                                conv.h, P->ptr(d.dst), f->status, &LL.tcl, subpixel, out_split));
     } else {
       LL.tc = false;
       build_simt_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, conv.w, conv.h,
@@ -921,6 +1151,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
       pp.scale = scale;
       pp.fp16 = f->precision == OIDNX_PRECISION_FP16;
       pp.out = P->ptr(V_IN);
+      pp.out_split = P->split_on[0] ? P->ptr(V_INS) : nullptr;
       pp.chunks = act_chunks(f->precision, f->in_channels);
       (void)cudaGetLastError();
       cudaError_t e = launch_pack(pp, s);
@@ -1059,13 +1290,21 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     last_use[kDefs[l].src0] = l;
     if (kDefs[l].src1 >= 0) last_use[kDefs[l].src1] = l;
   }
+  bool split_on[4];
+  for (int i = 0; i < 4; ++i) {
+    const SplitCopy& sc = kSplits[i];
+    const LayerDef& d = kDefs[sc.consumer];
+    split_on[i] = f->subpixel && use_subpixel(f->precision, lvl[d.level].w, lvl[d.level].h,
+                                              ext[d.src0]);
+    ext[sc.split] = ext[sc.base];
+    ch[sc.split] = ch[sc.base];
+    last_use[sc.split] = sc.consumer;
+  }
   struct Slot { size_t cap, off; int active; };
   Slot slots[V_COUNT];
   int nslots = 0;
   size_t total = 0, off[V_COUNT] = {};
-  for (int l = 0; l < kLayers; ++l) {
-    const int v = kDefs[l].dst;
-    if (v == V_OUT) continue;  // written straight into the caller's output
+  auto place = [&](int v, int l) {
     for (int i = 0; i < nslots; ++i)
       if (slots[i].active >= 0 && last_use[slots[i].active] < l) slots[i].active = -1;
     const size_t need = round_up_sz(act_bytes(f->precision, ext[v].w, ext[v].h, ch[v], false), 1024);
@@ -1080,6 +1319,13 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     }
     slots[best].active = v;
     off[v] = slots[best].off;
+  };
+  if (split_on[0]) place(V_INS, -1);
+  for (int l = 0; l < kLayers; ++l) {
+    const int v = kDefs[l].dst;
+    if (v != V_OUT) place(v, l);  // V_OUT is written straight into the caller's output
+    for (int i = 0; i < 4; ++i)
+      if (split_on[i] && kSplits[i].producer == l) place(kSplits[i].split, l);
   }
   if (total > cap)
     return fail(OIDNX_ERR_INVALID_ARGUMENT,
@@ -1091,6 +1337,10 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     if (v == V_OUT) return out;
     return static_cast<uint8_t*>(arena) + off[v];
   };
+  if (split_on[0]) {
+    cudaError_t e = launch_split_copy(in, ptr(V_INS), w, h, act_chunks(f->precision, f->in_channels), s);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "split copy: %s", cudaGetErrorString(e));
+  }
   for (int l = 0; l < kLayers; ++l) {
     const LayerDef& d = kDefs[l];
     const DeviceLayer& L = f->layers[l];
@@ -1099,10 +1349,20 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     LL.layer = l;
     const Extent conv = lvl[d.level];
     const void* s1 = d.src1 >= 0 ? ptr(d.src1) : nullptr;
+    bool subpixel = false;
+    void* out_split = nullptr;
+    for (int i = 0; i < 4; ++i) {
+      if (!split_on[i]) continue;
+      if (kSplits[i].consumer == l) {
+        subpixel = true;
+        s1 = ptr(kSplits[i].split);
+      }
+      if (kSplits[i].producer == l) out_split = ptr(kSplits[i].split);
+    }
     if (f->precision == OIDNX_PRECISION_FP16) {
       LL.tc = true;
       OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, conv.w, conv.h,
-                                ptr(d.dst), f->status, &LL.tcl));
+                                ptr(d.dst), f->status, &LL.tcl, subpixel, out_split));
     } else {
       LL.tc = false;
       build_simt_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, conv.w, conv.h, ptr(d.dst),
@@ -1231,8 +1491,8 @@ oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value) 
   } else if (n == "shapeCacheSize") {
     if (value < 1) return fail(OIDNX_ERR_INVALID_ARGUMENT, "shapeCacheSize must be >= 1");
     f->shape_cache = value;
-  } else if (n == "keepActivations") {
-    f->keep_acts = value ? 1 : 0;
+  } else if (n == "keepActivations" || n == "subpixelDecoder") {
+    (n == "keepActivations" ? f->keep_acts : f->subpixel) = value ? 1 : 0;
     for (auto& p : f->plans) f->retired.push_back(std::move(p));
     f->plans.clear();
     f->current = nullptr;
@@ -1260,6 +1520,7 @@ oidnx_status oidnx_filter_get_int(oidnx_filter* f, const char* name, int* value)
   else if (n == "overlap") *value = f->overlap < 0 ? default_overlap_value() : f->overlap;
   else if (n == "shapeCacheSize") *value = f->shape_cache;
   else if (n == "keepActivations") *value = f->keep_acts;
+  else if (n == "subpixelDecoder") *value = f->subpixel;
   else if (n == "profile") *value = f->profile_always;
   else if (n == "inputChannels") *value = f->in_channels;
   else if (n == "precision") *value = f->precision;
@@ -1371,6 +1632,11 @@ oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w
   if (prof) OIDNX_TRY(prof_begin(f, kLayers));
   OIDNX_CUDA(cudaMemcpyAsync(P->ptr(V_IN), packed_in, P->value_bytes[V_IN],
                              cudaMemcpyDeviceToDevice, s));
+  if (P->split_on[0]) {
+    cudaError_t e = launch_split_copy(P->ptr(V_IN), P->ptr(V_INS), w, h,
+                                      act_chunks(f->precision, f->in_channels), s);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "split copy: %s", cudaGetErrorString(e));
+  }
   OIDNX_TRY(prof_mark(f, prof, -2, s));
   OIDNX_TRY(enqueue_network(f, P, prof, s));
   OIDNX_CUDA(cudaMemcpyAsync(out, P->ptr(V_OUT), P->value_bytes[V_OUT], cudaMemcpyDeviceToDevice, s));

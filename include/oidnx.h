@@ -92,6 +92,12 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *   "overlap"            -1 = alignUp(receptive field / 2, 16) (default)
  *   "shapeCacheSize"     number of per-shape plans kept (LRU, default 2)
  *   "keepActivations"    1 = no activation-slot reuse (for debug reads)
+ *   "subpixelDecoder"    1 = fp16 decoder convs with even extents compute the
+ *                        upsampled part as parity-class 2x2 taps on the
+ *                        low-resolution source (fewer MMAs; weights of one
+ *                        class are summed, then rounded to fp16), reading
+ *                        parity-split copies of the skip sources; 0 (default)
+ *                        builds the upsampled halo in shared memory
  *   "profile"            1 = record per-kernel events on every execute
  * Errors: INVALID_ARGUMENT for unknown names or out-of-range values.  */
 oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value);

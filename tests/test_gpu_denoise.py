@@ -113,3 +113,25 @@ def test_config_4k_fp32_ldr_color_only_nan_inf():
     _crop_check(net, imgs, weights, "fp32", False, 1.0, (3584, 1904, 256, 256), 3840, 2160, 1e-4)
     ref = passes.unpack_rect(net[:h, :w], imgs[0], False, 1.0)
     assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))
+
+
+def test_subpixel_decoder_denoise_matches_oracle():
+    """Opt-in sub-pixel decoder mode through the whole filter path (the input
+    pass and the pool epilogues also write the parity-split skip copies)."""
+    w, h = 400, 272
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    weights = synth.unet_weights(9, bias_scale=0.05)
+    outs = []
+    for mode in (0, 1):
+        d = Denoiser(weights, ox.PRECISION_FP16, imgs, True)
+        try:
+            ox.oidnx_filter_set_int(d.f, "subpixelDecoder", mode)
+            ox.oidnx_filter_commit(d.f)
+            outs.append(d.run())
+            net = d.activation(16, 272, 400, 3)
+        finally:
+            d.close()
+    ref = unet.forward(passes.pack_tile(imgs, (0, 0, w, h), True, 1.0, "fp16"), weights, "fp16")
+    diff = np.abs(sanitize(net, 0, FLT_MAX).astype(np.float64) - sanitize(ref, 0, FLT_MAX))
+    assert diff.max() <= 2e-2
+    assert rel_l2(outs[1][..., :3], outs[0][..., :3]) <= 2e-2

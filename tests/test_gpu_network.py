@@ -45,12 +45,13 @@ def _isolated(k, acts, weights, precision):
     return y
 
 
-def _run_network(weights, packed_logical, precision):
+def _run_network(weights, packed_logical, precision, subpixel=0):
     h, w, c = packed_logical.shape
     prec = ox.PRECISION_FP16 if precision == "fp16" else ox.PRECISION_FP32
     f = ox.oidnx_filter_create(ox.write_weight_blob(weights), prec)
     try:
         ox.oidnx_filter_set_int(f, "keepActivations", 1)
+        ox.oidnx_filter_set_int(f, "subpixelDecoder", subpixel)
         src = to_dev(_layout.to_internal(packed_logical, precision))
         out = empty_dev(w * h * 16)
         ox.oidnx_network_execute(f, src.data_ptr(), w, h, out.data_ptr(), stream())
@@ -62,13 +63,13 @@ def _run_network(weights, packed_logical, precision):
     return acts, final
 
 
-@pytest.mark.parametrize("precision", ["fp16", "fp32"])
-@pytest.mark.parametrize("w,h", [(64, 48), (80, 34), (130, 20)])
-def test_network_layers_match_oracle(precision, w, h):
+@pytest.mark.parametrize("precision,subpixel", [("fp16", 0), ("fp16", 1), ("fp32", 0)])
+@pytest.mark.parametrize("w,h", [(64, 48), (80, 34), (130, 20), (512, 64)])
+def test_network_layers_match_oracle(precision, subpixel, w, h):
     weights = synth.unet_weights(9, bias_scale=0.05)
     x = synth.uniform_activations(h, w, 9, seed=w + h, low=0.0, high=1.0)
     x = round_storage(x, precision)
-    acts_flat, final = _run_network(weights, x, precision)
+    acts_flat, final = _run_network(weights, x, precision, subpixel)
     ref = unet.forward(x, weights, precision, keep=True)
     acts = []
     for k, name in enumerate(VALUE_NAMES):
