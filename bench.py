@@ -303,6 +303,7 @@ def run_ours(args):
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = TRAFFIC.get(top)
+    roof["traffic_unit"] = "bytes per launch (ncu dram read + write)"
     roof["peak_source"] = peaks["source"] + (" sustained bf16 (dense fp16 = bf16 rate)"
                                              if roof["bound"] == "tensor" else " HBM copy")
     roof["launch_ms"] = avg[top] / tiles
@@ -339,10 +340,11 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-# DRAM traffic per launch of each kernel from one ncu capture of this workload
-# (dram__bytes_read.sum + dram__bytes_write.sum); None until captured for the
-# current kernels.
-TRAFFIC = {}
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of this workload with the current kernels, see
+# profiles/conv3x3_tc_dec_conv1a_dec_conv1b_1080p_fp16.md.
+TRAFFIC = {"dec_conv1a": 134.152192e6 + 210.334208e6,
+           "dec_conv1b": 267.553024e6 + 100.923904e6}
 
 
 def main():
