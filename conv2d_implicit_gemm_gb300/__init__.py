@@ -69,6 +69,7 @@ _sig("oidnx_filter_execute_host", _st, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("oidnx_network_execute", _st, _vp, _vp, _i, _i, _vp, _vp)
 _sig("oidnx_network_execute_noalloc", _st, _vp, _vp, _i, _i, _vp, _vp)
 _sig("oidnx_filter_sync_status", _st, _vp)
+_sig("oidnx_debug_wait_probe", _st, _vp, ctypes.c_uint, _vp)
 _sig("oidnx_profile_next", _st, _vp)
 _sig("oidnx_get_profile", _st, _vp, ctypes.c_char_p, _sz)
 _sig("oidnx_get_resource_info", _st, _vp, ctypes.c_char_p, _sz)
@@ -167,6 +168,10 @@ def oidnx_network_execute_noalloc(f, packed_in, w, h, out, stream=0):
 
 def oidnx_filter_sync_status(f):
     _check(_lib.oidnx_filter_sync_status(f))
+
+
+def oidnx_debug_wait_probe(f, limit_us, stream=0):
+    _check(_lib.oidnx_debug_wait_probe(f, int(limit_us), stream))
 
 
 def oidnx_profile_next(f):

@@ -21,6 +21,12 @@
 //    matrix is a contiguous 128 B run, so the 9 taps of all R rows are just
 //    9R shared-memory descriptors into the same halo: a kx shift is +16 B, a
 //    ky shift selects the next halo row.  No im2col copy, no re-load per tap.
+//  * The box is widened to 144 pixels starting 8 left of the tile, so that
+//    with activation rows padded to a multiple of 8 pixels the tensor map's
+//    innermost box dimension is 8 pixels x 8 lanes (128 B).  With a 16-byte
+//    innermost dimension the TMA unit moves one pixel per request and
+//    delivered ~4.6 TB/s from L2 over the whole GPU; 128-byte rows deliver
+//    ~21 TB/s, which takes the loads off the critical path.
 //  * The three ky taps are stacked along N: halo row h feeds output rows h,
 //    h-1 and h-2 through ky = 0, 1, 2, so one MMA with B = [W(ky=2); W(ky=1);
 //    W(ky=0)] (N = 3 x Cout <= 256) updates three row accumulators that sit
@@ -33,8 +39,8 @@
 //    When they fit they are loaded once per CTA and stay resident; otherwise
 //    one block per pipeline stage is streamed with the A halo.
 //  * Warp roles: warp 0 issues TMA, warp 1 allocates TMEM and issues the
-//    MMAs from one thread, warps 2-5 run the epilogue (bias, ReLU, pool,
-//    fp16/fp32 stores), warps 6-9 (decoders only) build the upsampled halo
+//    MMAs from one thread, warps 2-9 run the epilogue (bias, ReLU, pool,
+//    fp16/fp32 stores), warps 10-13 (decoders only) build the upsampled halo
 //    in shared memory from a low-resolution TMA box, since nearest
 //    upsampling is not an affine TMA box.
 //  * Every wait is bounded: on timeout the kernel records a bit in the
@@ -69,21 +75,43 @@ __device__ __forceinline__ void tile_origin_k(const TcConvParams& p, int tile, i
   }
 }
 
+// Refill 16 accumulator columns (32 lanes) with the bias values bias16[0..15]
+// (16-byte aligned shared memory).
+__device__ __forceinline__ void tmem_fill_bias(uint32_t taddr, const float* bias16) {
+  uint32_t r[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 b = reinterpret_cast<const float4*>(bias16)[k];
+    r[4 * k] = __float_as_uint(b.x);
+    r[4 * k + 1] = __float_as_uint(b.y);
+    r[4 * k + 2] = __float_as_uint(b.z);
+    r[4 * k + 3] = __float_as_uint(b.w);
+  }
+  tmem_st16(taddr, r);
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// One MMA issued by the elected lane of the (converged) MMA warp.  Every MMA
+// accumulates: the epilogue refills each accumulator with the bias after
+// reading it (and before the first tile), so no MMA has to overwrite one.
+// An overwriting MMA issued amid accumulating ones stalled the tensor pipe
+// (~200 cycles each in a microbenchmark of this issue sequence).
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+  if (elect_one()) mma_f16_ss(d, a, b, idesc, 1u);
+}
+
 // All MMAs of one K block for a tile of R rows, fully unrolled so that the
-// single issuing thread spends a handful of instructions per MMA (its
-// instruction stream, not the tensor core, is otherwise the bottleneck).
-// Halo row h updates output rows lo..hi = max(0,h-2)..min(R-1,h) with the
-// ky-stacked B block; rows are grouped G at a time (N = rows x Cout <= 256).
-// In K block 0, kx 0 the row first reached by halo row h (row h itself,
-// through ky = 0) gets its own MMA that overwrites the accumulator.
+// issuing warp spends a handful of instructions per MMA (its instruction
+// stream, not the tensor core, is otherwise the bottleneck).  Halo row h
+// updates output rows lo..hi = max(0,h-2)..min(R-1,h) with the ky-stacked B
+// block; rows are grouped G at a time (N = rows x Cout <= 256).
 template <int R, int G>
 __device__ __forceinline__ void issue_kblock(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
                                              uint32_t kx_b16, uint32_t id1, uint32_t id2,
-                                             uint32_t id3, bool first) {
+                                             uint32_t id3) {
   const uint32_t idn[4] = {0u, id1, id2, id3};
 #pragma unroll
   for (int kx = 0; kx < 3; ++kx) {
@@ -93,19 +121,11 @@ __device__ __forceinline__ void issue_kblock(uint64_t ad, uint64_t bd, uint32_t 
     for (int h = 0; h < R + 2; ++h) {
       const int lo = h - 2 > 0 ? h - 2 : 0;
       const int hi = h < R - 1 ? h : R - 1;
-      const uint64_t a = adk + static_cast<uint32_t>(h * 2 * kHaloPx);
+      const uint64_t a = adk + static_cast<uint32_t>(h * 2 * kHaloW);
 #pragma unroll
       for (int c = lo; c <= hi; c += G) {
         const int e = c + G - 1 < hi ? c + G - 1 : hi;
-        if (kx == 0 && h <= R - 1 && e == h) {
-          if (first) {
-            if (e > c)
-              mma_f16_ss(dbase + c * N, a, bdk + (2 - h + c) * N, idn[e - c], 1u);
-            mma_f16_ss(dbase + h * N, a, bdk + 2 * N, idn[1], 0u);
-            continue;
-          }
-        }
-        mma_f16_ss(dbase + c * N, a, bdk + (2 - h + c) * N, idn[e - c + 1], 1u);
+        umma(dbase + c * N, a, bdk + (2 - h + c) * N, idn[e - c + 1]);
       }
     }
   }
@@ -114,12 +134,12 @@ __device__ __forceinline__ void issue_kblock(uint64_t ad, uint64_t bd, uint32_t 
 template <int G>
 __device__ __forceinline__ void issue_kblock_r(int R, uint64_t ad, uint64_t bd, uint32_t dbase,
                                                uint32_t N, uint32_t kx_b16, uint32_t id1,
-                                               uint32_t id2, uint32_t id3, bool first) {
+                                               uint32_t id2, uint32_t id3) {
   switch (R) {
-    case 1: issue_kblock<1, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3, first); break;
-    case 2: issue_kblock<2, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3, first); break;
-    case 4: issue_kblock<4, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3, first); break;
-    default: issue_kblock<8, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3, first); break;
+    case 1: issue_kblock<1, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
+    case 2: issue_kblock<2, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
+    case 4: issue_kblock<4, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
+    default: issue_kblock<8, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
   }
 }
 
@@ -129,9 +149,8 @@ __device__ __forceinline__ void issue_kblock_r(int R, uint64_t ad, uint64_t bd, 
 // low-res row hl feeds output rows 2hl-3 .. 2hl of the tile (parity classes
 // (1,+1), (0,0), (1,0), (0,-1) in (row parity, row offset)), whose summed
 // weights are stacked along N in that order; the column offset dx runs over
-// two values selected by px (A shifted by d + px pixels).  In K block 0, d 0
-// the rows first reached at hl (2hl-1 and 2hl) are overwritten.
-template <int R, int G, bool FIRST>
+// two values selected by px (A shifted by d + px pixels).
+template <int R, int G>
 __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
                                          int px, int pxb, uint32_t id1, uint32_t id2,
                                          uint32_t id3, uint32_t id4) {
@@ -144,22 +163,12 @@ __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbas
       const int lo = 2 * hl - 3 > 0 ? 2 * hl - 3 : 0;
       const int hi = 2 * hl < R - 1 ? 2 * hl : R - 1;
       const uint64_t a = adk + static_cast<uint32_t>(hl * 2 * kHaloPx);
-      const int newlo = (FIRST && d == 0) ? (2 * hl - 1 > lo ? 2 * hl - 1 : lo) : hi + 1;
 #pragma unroll
       for (int c = lo; c <= hi; c += G) {
         const int e = c + G - 1 < hi ? c + G - 1 : hi;
-        const int ea = e < newlo - 1 ? e : newlo - 1;
-        if (c <= ea) {
-          const int n = ea - c + 1;
-          mma_f16_ss(dbase + c * N, a, bdk + static_cast<uint32_t>(c - 2 * hl + 3) * N,
-                     n == 1 ? id1 : n == 2 ? id2 : n == 3 ? id3 : id4, 1u);
-        }
-        const int c2 = c > newlo ? c : newlo;
-        if (c2 <= e) {
-          const int n = e - c2 + 1;
-          mma_f16_ss(dbase + c2 * N, a, bdk + static_cast<uint32_t>(c2 - 2 * hl + 3) * N,
-                     n == 1 ? id1 : n == 2 ? id2 : n == 3 ? id3 : id4, 0u);
-        }
+        const int n = e - c + 1;
+        umma(dbase + c * N, a, bdk + static_cast<uint32_t>(c - 2 * hl + 3) * N,
+             n == 1 ? id1 : n == 2 ? id2 : n == 3 ? id3 : id4);
       }
     }
   }
@@ -181,14 +190,14 @@ __device__ __forceinline__ void issue_skip(uint64_t ad, uint64_t bd, uint32_t db
     for (int c = lo; c <= hi; c += G) {
       const int e = c + G - 1 < hi ? c + G - 1 : hi;
       const int n = e - c + 1;
-      mma_f16_ss(dbase + c * N, a, bd + static_cast<uint32_t>(2 - h + c) * N,
-                 n == 1 ? id1 : n == 2 ? id2 : id3, 1u);
+      umma(dbase + c * N, a, bd + static_cast<uint32_t>(2 - h + c) * N,
+           n == 1 ? id1 : n == 2 ? id2 : id3);
     }
   }
 }
 
 template <int R, int G4, int G3>
-__device__ __forceinline__ void issue_subpixel_r(bool up, bool first, uint64_t ad, uint64_t bd,
+__device__ __forceinline__ void issue_subpixel_r(bool up, uint64_t ad, uint64_t bd,
                                                  uint32_t dbase, uint32_t N, int px, int pxb,
                                                  uint32_t id1, uint32_t id2, uint32_t id3,
                                                  uint32_t id4) {
@@ -196,21 +205,20 @@ __device__ __forceinline__ void issue_subpixel_r(bool up, bool first, uint64_t a
     // bd: first kx slice; pxb (reused): 16-byte units to the second slice, 0 if none
     issue_skip<R, G3>(ad, bd, dbase, N, id1, id2, id3);
     if (pxb) issue_skip<R, G3>(ad + 1, bd + static_cast<uint32_t>(pxb), dbase, N, id1, id2, id3);
-  } else if (first)
-    issue_up<R, G4, true>(ad, bd, dbase, N, px, pxb, id1, id2, id3, id4);
-  else
-    issue_up<R, G4, false>(ad, bd, dbase, N, px, pxb, id1, id2, id3, id4);
+  } else {
+    issue_up<R, G4>(ad, bd, dbase, N, px, pxb, id1, id2, id3, id4);
+  }
 }
 
 template <int G4, int G3>
 __device__ __forceinline__ void issue_subpixel_item(int R, bool up, uint64_t ad, uint64_t bd,
                                                     uint32_t dbase, uint32_t N, int px, int pxb,
                                                     uint32_t id1, uint32_t id2, uint32_t id3,
-                                                    uint32_t id4, bool first) {
+                                                    uint32_t id4) {
   switch (R) {
-    case 2: issue_subpixel_r<2, G4, G3>(up, first, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
-    case 4: issue_subpixel_r<4, G4, G3>(up, first, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
-    default: issue_subpixel_r<8, G4, G3>(up, first, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
+    case 2: issue_subpixel_r<2, G4, G3>(up, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
+    case 4: issue_subpixel_r<4, G4, G3>(up, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
+    default: issue_subpixel_r<8, G4, G3>(up, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
   }
 }
 
@@ -345,15 +353,17 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
           const bool low = p.upsample0 && kb < KB0;
           mbar_arrive_expect_tx(&full[s], (low ? p.st_tx : p.a_tx) + (p.resident ? 0u : p.b_tx));
           if (kb < KB0) {
+            // boxes start kGroupPx pixels left of the tile (a multiple of 8,
+            // so 128-byte-row maps address it in 8-pixel units)
             if (low)
               tma_load_4d(ST + static_cast<size_t>(s) * p.st_stage, &map0, &full[s], 0,
-                          (x0 >> 1) - 1, 2 * kb, (y0 >> 1) - 1);
+                          ((x0 >> 1) - kGroupPx) >> p.xs0, 2 * kb, (y0 >> 1) - 1);
             else
-              tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map0, &full[s], 0, x0 - 1,
-                          2 * kb, y0 - 1);
+              tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map0, &full[s], 0,
+                          (x0 - kGroupPx) >> p.xs0, 2 * kb, y0 - 1);
           } else {
-            tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map1, &full[s], 0, x0 - 1,
-                        2 * (kb - KB0), y0 - 1);
+            tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map1, &full[s], 0,
+                        (x0 - kGroupPx) >> p.xs1, 2 * (kb - KB0), y0 - 1);
           }
           if (!p.resident)
             bulk_load(B + static_cast<size_t>(s) * p.b_stage,
@@ -368,7 +378,10 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the loop (descriptor arithmetic stays warp-uniform);
+    // one elected lane issues each MMA and commit.  Waits are taken by every
+    // lane and their outcome agreed on, so the warp never diverges.
+    {
       const int g = min(3, 256 / N);
       const int g4 = min(4, 256 / N);
       const uint32_t id1 = idesc_f16_f32(kTileM, N);
@@ -379,16 +392,22 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
       const uint32_t wbase = smem_u32(p.resident ? Wres : B);
       const uint64_t b_up0 = smem_desc_noswizzle(wbase, 4u * N * kChunkBytes, 128);
       const uint64_t b_sk0 = smem_desc_noswizzle(wbase, 3u * N * kChunkBytes, 128);
-      const uint64_t a_desc0 = smem_desc_noswizzle(smem_u32(A), kHaloPx * kChunkBytes, 128);
+      // plain / expansion halo rows are kHaloW pixels, x0 - 1 at kHaloOff
+      const uint64_t a_desc0 =
+          smem_desc_noswizzle(smem_u32(A), kHaloW * kChunkBytes, 128) + kHaloOff;
       const uint64_t b_desc0 =
           smem_desc_noswizzle(smem_u32(p.resident ? Wres : B), 3u * N * kChunkBytes, 128);
       const uint32_t kx_b16 = 6u * N;  // one kx block of B = 2 x 3N rows x 16 B
       const uint32_t set_cols = static_cast<uint32_t>(R * N);
-      bool ok = !p.resident || mbar_wait_bounded(wbar, 0, p.status, kErrTimeoutMma);
+      bool ok = __all_sync(0xffffffffu,
+                           !p.resident || mbar_wait_bounded(wbar, 0, p.status, kErrTimeoutMma));
       uint32_t it = 0, tcount = 0;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tcount) {
         const uint32_t buf = tcount & 1u;
-        if (!mbar_wait_bounded(&tempty[buf], ((tcount >> 1) & 1u) ^ 1u, p.status, kErrTimeoutMma)) {
+        // use k of a set needs phase k of tempty: the epilogue's initial
+        // bias fill (k = 0), then its drain of use k - 1
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tempty[buf], (tcount >> 1) & 1u, p.status,
+                                                        kErrTimeoutMma))) {
           ok = false;
           break;
         }
@@ -399,8 +418,9 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
         for (int kb = 0; kb < items; ++kb, ++it) {
           const uint32_t s = it % S;
           const uint32_t ph = (it / S) & 1u;
-          ok = mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutMma);
-          if (ok && KIND == kTcExpand) ok = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
+          bool w = mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutMma);
+          if (KIND == kTcExpand && w) w = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
+          ok = __all_sync(0xffffffffu, w);
           if (!ok) break;
           tc_fence_after();
           if (SP) {
@@ -424,24 +444,24 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
             }
             const uint64_t ad = a_up0 + soff;
             const uint64_t bd = (up ? b_up0 : b_sk0) + (woff >> 4);
-            if (g4 == 4) issue_subpixel_item<4, 3>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4, kb == 0);
-            else if (g4 == 2) issue_subpixel_item<2, 2>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4, kb == 0);
-            else issue_subpixel_item<1, 1>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4, kb == 0);
-            mma_commit(&empty[s]);
+            if (g4 == 4) issue_subpixel_item<4, 3>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4);
+            else if (g4 == 2) issue_subpixel_item<2, 2>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4);
+            else issue_subpixel_item<1, 1>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4);
+            if (elect_one()) mma_commit(&empty[s]);
             continue;
           }
           const uint64_t ad = a_desc0 + ((s * p.a_stage) >> 4);
           const uint64_t bd = b_desc0 + ((static_cast<uint32_t>(p.resident ? kb : s) * p.b_stage) >> 4);
-          if (g == 3) issue_kblock_r<3>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, kb == 0);
-          else if (g == 2) issue_kblock_r<2>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, kb == 0);
-          else issue_kblock_r<1>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, kb == 0);
-          mma_commit(&empty[s]);
+          if (g == 3) issue_kblock_r<3>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3);
+          else if (g == 2) issue_kblock_r<2>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3);
+          else issue_kblock_r<1>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3);
+          if (elect_one()) mma_commit(&empty[s]);
         }
         if (!ok) break;
-        mma_commit(&tfull[buf]);
+        if (elect_one()) mma_commit(&tfull[buf]);
       }
       // TMEM is freed only after every MMA issued above has completed.
-      mma_commit(done);
+      if (elect_one()) mma_commit(done);
       mbar_wait_bounded(done, 0, p.status, kErrTimeoutMma);
     }
     __syncwarp();
@@ -455,7 +475,7 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       int x0, y0;
       tile_origin(p, tile, &x0, &y0);
-      const int ly0 = (y0 >> 1) - 1, lx0 = (x0 >> 1) - 1;
+      const int ly0 = (y0 >> 1) - 1, lx0 = (x0 >> 1) - kGroupPx;
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const uint32_t s = it % S;
         const uint32_t ph = (it / S) & 1u;
@@ -468,6 +488,7 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
         if (kb < KB0) {
           const uint4* src = reinterpret_cast<const uint4*>(ST + static_cast<size_t>(s) * p.st_stage);
           uint4* dst = reinterpret_cast<uint4*>(A + static_cast<size_t>(s) * p.a_stage);
+          // only the kHaloPx pixels the MMAs read (x0 - 1 .. x0 + 128)
           for (int i = et; i < total; i += 128) {
             const int px = i % kHaloPx;
             const int rc = i / kHaloPx;
@@ -476,9 +497,9 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (iy >= 0 && iy < p.H && ix >= 0 && ix < p.W) {
               const int sr = (iy >> 1) - ly0, sc = (ix >> 1) - lx0;
-              v = src[(sr * 2 + j) * kLowPx + sc];
+              v = src[(sr * 2 + j) * kLowW + sc];
             }
-            dst[i] = v;
+            dst[rc * kHaloW + kHaloOff + px] = v;
           }
           fence_proxy_async_smem();
         }
@@ -499,6 +520,18 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
     const int nc = N / 16;
     const int C8 = N / 8;
     const uint32_t set_cols = static_cast<uint32_t>(R * N);
+    // The accumulators start from the bias: both sets are filled before the
+    // first tile (rows sub, sub + 2, ... of this lane quarter), and every
+    // accumulator is refilled right after it has been read.
+    for (int b = 0; b < 2; ++b)
+      for (int r = sub; r < R; r += 2)
+        for (int c = 0; c < nc; ++c)
+          tmem_fill_bias(tmem + lane_off + b * set_cols + static_cast<uint32_t>(r * N + c * 16),
+                         bias_s + c * 16);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&tempty[0]);
+    mbar_arrive(&tempty[1]);
     uint32_t tcount = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
       const uint32_t buf = tcount & 1u;
@@ -510,35 +543,36 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
       const int x = SP ? x0 + 2 * m + px : x0 + m;
       const uint32_t tl = tmem + lane_off + buf * set_cols;
 
-      if (p.mode == kEpiRelu) {
+      // decoders (expansion, sub-pixel) always take the ReLU epilogue
+      if (KIND != kTcPlain || p.mode == kEpiRelu) {
         __half* out = static_cast<__half*>(p.out);
         for (int c0 = 0; c0 < nc; c0 += 2) {
           const bool two = c0 + 1 < nc;
-          float bv[32];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            bv[k] = bias_s[c0 * 16 + k];
-            bv[16 + k] = two ? bias_s[c0 * 16 + 16 + k] : 0.0f;
-          }
           for (int r = sub; r < R; r += 2) {
             const int y = y0 + r;
             uint32_t v[2][16];
-            tmem_ld16_nowait(tl + static_cast<uint32_t>(r * N + c0 * 16), v[0]);
-            if (two) tmem_ld16_nowait(tl + static_cast<uint32_t>(r * N + c0 * 16 + 16), v[1]);
+            const uint32_t t0 = tl + static_cast<uint32_t>(r * N + c0 * 16);
+            tmem_ld16_nowait(t0, v[0]);
+            if (two) tmem_ld16_nowait(t0 + 16, v[1]);
             tmem_wait_ld();
-            if (x < p.W && y < p.H) {
-              __half* row = out + (static_cast<size_t>(y) * C8 * p.W + x) * 8;
+            tmem_fill_bias(t0, bias_s + c0 * 16);
+            if (two) tmem_fill_bias(t0 + 16, bias_s + c0 * 16 + 16);
+            // columns [W, pitch) are row padding: stored as zeros
+            if (x < p.pitch && y < p.H) {
+              const bool pad = x >= p.W;
+              __half* row = out + (static_cast<size_t>(y) * C8 * p.pitch + x) * 8;
 #pragma unroll
               for (int b = 0; b < 2; ++b) {
                 if (b == 1 && !two) break;
                 uint32_t h[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                  h[k] = pack_half2(fmaxf(__uint_as_float(v[b][2 * k]) + bv[16 * b + 2 * k], 0.0f),
-                                    fmaxf(__uint_as_float(v[b][2 * k + 1]) + bv[16 * b + 2 * k + 1], 0.0f));
+                  h[k] = pad ? 0u
+                             : pack_half2(fmaxf(__uint_as_float(v[b][2 * k]), 0.0f),
+                                          fmaxf(__uint_as_float(v[b][2 * k + 1]), 0.0f));
                 const size_t c8 = 2 * (c0 + b);
-                *reinterpret_cast<uint4*>(row + c8 * p.W * 8) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(row + (c8 + 1) * p.W * 8) = make_uint4(h[4], h[5], h[6], h[7]);
+                *reinterpret_cast<uint4*>(row + c8 * p.pitch * 8) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(row + (c8 + 1) * p.pitch * 8) = make_uint4(h[4], h[5], h[6], h[7]);
               }
             }
           }
@@ -548,41 +582,43 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
         const int Wp = (p.W + 1) >> 1, Hp = (p.H + 1) >> 1;
         const int xp = x >> 1;
         for (int c = 0; c < nc; ++c) {
-          float bv[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) bv[k] = bias_s[c * 16 + k];
           for (int i = sub; i < R / 2; i += 2) {
             const int ya = y0 + 2 * i;
             const bool va = x < p.W && ya < p.H;
             const bool vb = x < p.W && ya + 1 < p.H;
             const int yp = ya >> 1;
             uint32_t v[2][16];
-            tmem_ld16_nowait(tl + static_cast<uint32_t>((2 * i) * N + c * 16), v[0]);
-            tmem_ld16_nowait(tl + static_cast<uint32_t>((2 * i + 1) * N + c * 16), v[1]);
+            const uint32_t t0 = tl + static_cast<uint32_t>((2 * i) * N + c * 16);
+            tmem_ld16_nowait(t0, v[0]);
+            tmem_ld16_nowait(t0 + static_cast<uint32_t>(N), v[1]);
             tmem_wait_ld();
+            tmem_fill_bias(t0, bias_s + c * 16);
+            tmem_fill_bias(t0 + static_cast<uint32_t>(N), bias_s + c * 16);
             float mx[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              const float a = va ? fmaxf(__uint_as_float(v[0][k]) + bv[k], 0.0f) : -INFINITY;
-              const float bb = vb ? fmaxf(__uint_as_float(v[1][k]) + bv[k], 0.0f) : -INFINITY;
-              float t = fmaxf(a, bb);
+              const float a = va ? fmaxf(__uint_as_float(v[0][k]), 0.0f) : -INFINITY;
+              const float b2 = vb ? fmaxf(__uint_as_float(v[1][k]), 0.0f) : -INFINITY;
+              float t = fmaxf(a, b2);
               t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 1));
               mx[k] = t;
             }
-            if (((lane & 1) == 0) && xp < Wp && yp < Hp) {
+            // pooled columns [Wp, pitch) are row padding: stored as zeros
+            if (((lane & 1) == 0) && xp < p.pitch && yp < Hp) {
+              const bool pad = xp >= Wp;
               uint32_t h[8];
 #pragma unroll
-              for (int k = 0; k < 8; ++k) h[k] = pack_half2(mx[2 * k], mx[2 * k + 1]);
-              const size_t base0 = ((static_cast<size_t>(yp) * C8 + 2 * c) * Wp + xp) * 8;
-              const size_t base1 = base0 + static_cast<size_t>(Wp) * 8;
+              for (int k = 0; k < 8; ++k) h[k] = pad ? 0u : pack_half2(mx[2 * k], mx[2 * k + 1]);
+              const size_t base0 = ((static_cast<size_t>(yp) * C8 + 2 * c) * p.pitch + xp) * 8;
+              const size_t base1 = base0 + static_cast<size_t>(p.pitch) * 8;
               *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
               *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
               if (p.out_split) {
-                // plane xp & 1, index xp >> 1 (Wp even whenever the copy exists)
+                // plane xp & 1, index xp >> 1 (the pitch is even)
                 __half* o2 = static_cast<__half*>(p.out_split);
                 const size_t s0 =
-                    ((((static_cast<size_t>(yp) * C8 + 2 * c) * 2 + (xp & 1)) * (Wp >> 1)) + (xp >> 1)) * 8;
-                const size_t s1 = s0 + static_cast<size_t>(Wp) * 8;
+                    ((((static_cast<size_t>(yp) * C8 + 2 * c) * 2 + (xp & 1)) * (p.pitch >> 1)) + (xp >> 1)) * 8;
+                const size_t s1 = s0 + static_cast<size_t>(p.pitch) * 8;
                 *reinterpret_cast<uint4*>(o2 + s0) = make_uint4(h[0], h[1], h[2], h[3]);
                 *reinterpret_cast<uint4*>(o2 + s1) = make_uint4(h[4], h[5], h[6], h[7]);
               }
@@ -591,7 +627,6 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
         }
       } else {
         float4* out = static_cast<float4*>(p.out);
-        const float b0 = bias_s[0], b1 = bias_s[1], b2 = bias_s[2], b3 = bias_s[3];
         for (int r0 = sub; r0 < R; r0 += 8) {
           uint32_t v[4][16];
 #pragma unroll
@@ -599,15 +634,19 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
             if (r0 + 2 * b < R) tmem_ld16_nowait(tl + static_cast<uint32_t>((r0 + 2 * b) * N), v[b]);
           tmem_wait_ld();
 #pragma unroll
+          for (int b = 0; b < 4; ++b)
+            if (r0 + 2 * b < R) tmem_fill_bias(tl + static_cast<uint32_t>((r0 + 2 * b) * N), bias_s);
+#pragma unroll
           for (int b = 0; b < 4; ++b) {
             const int y = y0 + r0 + 2 * b;
             if (r0 + 2 * b < R && x < p.W && y < p.H)
               out[static_cast<size_t>(y) * p.W + x] =
-                  make_float4(__uint_as_float(v[b][0]) + b0, __uint_as_float(v[b][1]) + b1,
-                              __uint_as_float(v[b][2]) + b2, __uint_as_float(v[b][3]) + b3);
+                  make_float4(__uint_as_float(v[b][0]), __uint_as_float(v[b][1]),
+                              __uint_as_float(v[b][2]), __uint_as_float(v[b][3]));
           }
         }
       }
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
     }

@@ -13,6 +13,14 @@ namespace oidnx {
 constexpr int kTileM = 128;
 constexpr int kHaloPx = kTileM + 2;        // input pixels of one halo row
 constexpr int kLowPx = kTileM / 2 + 2;     // low-resolution pixels for one M tile
+// Plain and expansion kernels stage each halo row 8-pixel aligned: the box
+// starts 8 pixels left of the tile, so that a TMA row can be 8 pixels x 16
+// bytes (128 B) wide instead of one 16-byte pixel; the first pixel the MMA
+// reads (x0 - 1) sits at index kHaloOff.
+constexpr int kGroupPx = 8;                      // pixels per 128-byte TMA row
+constexpr int kHaloW = kTileM + 2 * kGroupPx;    // 144 staged pixels per halo row
+constexpr int kLowW = kTileM / 2 + 2 * kGroupPx; // 80 staged low-resolution pixels
+constexpr int kHaloOff = kGroupPx - 1;           // 7
 constexpr int kChunkBytes = 16;            // one 16-byte channel block
 constexpr int kTcEpilogueWarps = 8;        // two per TMEM lane quarter
 constexpr int kTcThreads = 320;            // 10 warps: TMA, MMA, 8 x epilogue
@@ -49,8 +57,12 @@ struct TcConvParams {
   uint32_t b_tx2;
   uint32_t wres_bytes;
   // pool epilogue: optional second copy of the output, column-parity split
-  // [Ho][N/8][2][Wo/2][8] (read by the sub-pixel decoder as its skip source)
+  // [Ho][N/8][2][pitch/2][8] (read by the sub-pixel decoder as its skip source)
   void* out_split;
+  int pitch;               // fp16 output row pitch in pixels (>= output width);
+                           // columns [width, pitch) are written as zeros
+  int xs0, xs1;            // log2 pixels per x unit of map0 / map1: 3 for
+                           // 128-byte rows (pitch % 8 == 0), 0 for 16-byte rows
 };
 
 enum TcKind : int {
@@ -118,9 +130,10 @@ struct PackParams {
   int hdr;
   float scale;             // effective inputScale (HDR)
   int fp16;                // storage precision
-  void* out;               // [th][chunks][tw][lanes]
+  void* out;               // [th][chunks][pitch][lanes]; columns >= tw are zeros
+  int pitch;               // row pitch in pixels (fp16: tw rounded up to 8; fp32: tw)
   int chunks;              // 16-byte chunks per pixel
-  void* out_split;         // optional parity-split copy [th][chunks][2][tw/2][lanes]
+  void* out_split;         // optional parity-split copy [th][chunks][2][pitch/2][lanes]
 };
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 
@@ -139,9 +152,17 @@ struct UnpackParams {
 };
 cudaError_t launch_unpack(const UnpackParams& p, cudaStream_t stream);
 
-// Column-parity split copy of an fp16 activation: [h][chunks][w][8] ->
-// [h][chunks][2][w/2][8] (w even).
-cudaError_t launch_split_copy(const void* src, void* dst, int w, int h, int chunks,
-                              cudaStream_t stream);
+// Failure-detection probe: a wait that nothing completes, bounded by limit_ns.
+cudaError_t launch_wait_probe(int* status, unsigned long long limit_ns, cudaStream_t stream);
+
+// Column-parity split copy of an fp16 activation: [h][chunks][src_pitch][8]
+// -> [h][chunks][2][dst_pitch/2][8] (dst_pitch even); columns >= w are zeros.
+cudaError_t launch_split_copy(const void* src, int src_pitch, void* dst, int dst_pitch, int w,
+                              int h, int chunks, cudaStream_t stream);
+
+// Re-pitch an activation: rows of w 16-byte elements at src_pitch into rows
+// at dst_pitch >= w, columns [w, dst_pitch) written as zeros.
+cudaError_t launch_pitch_copy(const void* src, int src_pitch, void* dst, int dst_pitch, int w,
+                              int rows, cudaStream_t stream);
 
 }  // namespace oidnx

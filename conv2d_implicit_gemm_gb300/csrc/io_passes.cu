@@ -65,7 +65,28 @@ __global__ void pack_kernel(const PackParams p) {
   griddep_launch_dependents();
   const int tx = blockIdx.x * blockDim.x + threadIdx.x;
   const int ty = blockIdx.y;
-  if (tx >= p.tw) return;
+  if (tx >= p.pitch) return;
+  const size_t pixel = static_cast<size_t>(ty) * p.chunks * p.pitch + tx;
+  if (tx >= p.tw) {
+    // row padding: zeros, so that 8-pixel TMA rows read zero past the tile
+    if (FP16) {
+      uint4* out = static_cast<uint4*>(p.out);
+      out[pixel] = make_uint4(0u, 0u, 0u, 0u);
+      out[pixel + p.pitch] = make_uint4(0u, 0u, 0u, 0u);
+      if (p.out_split) {
+        uint4* o2 = static_cast<uint4*>(p.out_split);
+        const size_t half = static_cast<size_t>(p.pitch) >> 1;
+        const size_t s0 = (static_cast<size_t>(ty) * p.chunks * 2 + (tx & 1)) * half + (tx >> 1);
+        o2[s0] = make_uint4(0u, 0u, 0u, 0u);
+        o2[s0 + 2 * half] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else {
+      float4* out = static_cast<float4*>(p.out);
+      for (int j = 0; j < p.chunks; ++j)
+        out[pixel + static_cast<size_t>(j) * p.pitch] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
   const int ix = min(max(p.tx + tx, 0), p.width - 1);
   const int iy = min(max(p.ty + ty, 0), p.height - 1);
   constexpr int kCh = 3 * SOURCES;
@@ -92,7 +113,6 @@ __global__ void pack_kernel(const PackParams p) {
     ch[7 % kCh] = __fadd_rn(__fmul_rn(sanitize(n.y, -1.0f, 1.0f), 0.5f), 0.5f);
     ch[8 % kCh] = __fadd_rn(__fmul_rn(sanitize(n.z, -1.0f, 1.0f), 0.5f), 0.5f);
   }
-  const size_t pixel = static_cast<size_t>(ty) * p.chunks * p.tw + tx;
   if (FP16) {
     // 16 lanes = 2 chunks of 8 halves; lanes past 3*SOURCES are zero
     uint32_t w[8];
@@ -111,11 +131,11 @@ __global__ void pack_kernel(const PackParams p) {
     }
     uint4* out = static_cast<uint4*>(p.out);
     out[pixel] = make_uint4(w[0], w[1], w[2], w[3]);
-    out[pixel + p.tw] = make_uint4(w[4], w[5], w[6], w[7]);
+    out[pixel + p.pitch] = make_uint4(w[4], w[5], w[6], w[7]);
     if (p.out_split) {
-      // column-parity split copy: plane tx & 1, index tx >> 1 (tw even)
+      // column-parity split copy: plane tx & 1, index tx >> 1 (pitch even)
       uint4* o2 = static_cast<uint4*>(p.out_split);
-      const size_t half = static_cast<size_t>(p.tw) >> 1;
+      const size_t half = static_cast<size_t>(p.pitch) >> 1;
       const size_t s0 = (static_cast<size_t>(ty) * p.chunks * 2 + (tx & 1)) * half + (tx >> 1);
       o2[s0] = make_uint4(w[0], w[1], w[2], w[3]);
       o2[s0 + 2 * half] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -128,7 +148,7 @@ __global__ void pack_kernel(const PackParams p) {
     float4* out = static_cast<float4*>(p.out);
 #pragma unroll
     for (int j = 0; j < (kCh + 3) / 4; ++j)
-      out[pixel + static_cast<size_t>(j) * p.tw] =
+      out[pixel + static_cast<size_t>(j) * p.pitch] =
           make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
   }
 }
@@ -154,28 +174,70 @@ __global__ void unpack_kernel(const UnpackParams p) {
   p.out[static_cast<size_t>(y + p.oy) * p.out_stride + x + p.ox] = make_float4(r, g, b, a);
 }
 
-__global__ void split_copy_kernel(const uint4* src, uint4* dst, int w, int h, int chunks) {
+__global__ void split_copy_kernel(const uint4* src, int src_pitch, uint4* dst, int dst_pitch,
+                                  int w, int rows) {
   griddep_wait();
   griddep_launch_dependents();
   const int x = blockIdx.x * blockDim.x + threadIdx.x;
-  const int row = blockIdx.y;  // y * chunks + chunk
-  if (x >= w) return;
-  const size_t half = static_cast<size_t>(w) >> 1;
-  dst[(static_cast<size_t>(row) * 2 + (x & 1)) * half + (x >> 1)] = src[static_cast<size_t>(row) * w + x];
+  if (x >= dst_pitch) return;
+  const size_t half = static_cast<size_t>(dst_pitch) >> 1;
+  for (int row = blockIdx.y; row < rows; row += gridDim.y) {  // row = y * chunks + chunk
+    const uint4 v = x < w ? src[static_cast<size_t>(row) * src_pitch + x] : make_uint4(0u, 0u, 0u, 0u);
+    dst[(static_cast<size_t>(row) * 2 + (x & 1)) * half + (x >> 1)] = v;
+  }
+}
+
+__global__ void pitch_copy_kernel(const uint4* src, int src_pitch, uint4* dst, int dst_pitch,
+                                  int w, int rows) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= dst_pitch) return;
+  for (int row = blockIdx.y; row < rows; row += gridDim.y) {
+    const uint4 v = x < w ? src[static_cast<size_t>(row) * src_pitch + x] : make_uint4(0u, 0u, 0u, 0u);
+    dst[static_cast<size_t>(row) * dst_pitch + x] = v;
+  }
+}
+
+// Failure-detection probe: one thread waits on an mbarrier that nothing
+// completes, with the given limit; the bounded wait must give up, record
+// kErrTimeoutProbe in the status word and return.
+__global__ void wait_probe_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, status, kErrTimeoutProbe, limit_ns);
+  __syncthreads();
 }
 
 }  // namespace
 
-cudaError_t launch_split_copy(const void* src, void* dst, int w, int h, int chunks,
-                              cudaStream_t stream) {
-  dim3 grid((w + 127) / 128, h * chunks);
+cudaError_t launch_wait_probe(int* status, unsigned long long limit_ns, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_copy(const void* src, int src_pitch, void* dst, int dst_pitch, int w,
+                              int h, int chunks, cudaStream_t stream) {
+  const int rows = h * chunks;
+  dim3 grid((dst_pitch + 127) / 128, rows < 65535 ? rows : 65535);
   return launch_pdl(split_copy_kernel, grid, dim3(128), 0, stream, static_cast<const uint4*>(src),
-                    static_cast<uint4*>(dst), w, h, chunks);
+                    src_pitch, static_cast<uint4*>(dst), dst_pitch, w, rows);
+}
+
+cudaError_t launch_pitch_copy(const void* src, int src_pitch, void* dst, int dst_pitch, int w,
+                              int rows, cudaStream_t stream) {
+  dim3 grid((dst_pitch + 127) / 128, rows < 65535 ? rows : 65535);
+  return launch_pdl(pitch_copy_kernel, grid, dim3(128), 0, stream, static_cast<const uint4*>(src),
+                    src_pitch, static_cast<uint4*>(dst), dst_pitch, w, rows);
 }
 
 template <int S, bool F16, bool HDR>
 cudaError_t launch_pack_t(const PackParams& p, cudaStream_t stream) {
-  dim3 grid((p.tw + 127) / 128, p.th);
+  dim3 grid((p.pitch + 127) / 128, p.th);
   return launch_pdl(pack_kernel<S, F16, HDR>, grid, dim3(128), 0, stream, p);
 }
 

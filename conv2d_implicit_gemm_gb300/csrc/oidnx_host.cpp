@@ -474,35 +474,56 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// fp16 activation [H][C8][W][8] as a 4-D tensor {8 lanes, W, C8, H}; box
-// {8, box_w, 2, box_h}; zero fill outside.
-oidnx_status encode_act_map(CUtensorMap* map, const void* base, int W, int H, int C8, int box_w,
-                            int box_h, int x_stride = 1) {
+// fp16 activation [H][C8][pitch][8] (columns [W, pitch) zero) as a 4-D
+// tensor.  When the pitch is a multiple of 8 pixels the innermost dimension
+// is one 8-pixel group (64 halves = 128 B) and x counts groups (*xs = 3);
+// otherwise it is one pixel (16 B, *xs = 0).  The box is box_w pixels (a
+// multiple of 8 for the 8-pixel form) x 2 channel chunks x box_h rows.
+oidnx_status encode_act_map(CUtensorMap* map, const void* base, int W, int pitch, int H, int C8,
+                            int box_w, int box_h, bool allow_groups, int* xs) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  cuuint64_t dims[4] = {8, static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(C8),
-                        static_cast<cuuint64_t>(H)};
-  cuuint64_t strides[3] = {16, static_cast<cuuint64_t>(W) * 16,
-                           static_cast<cuuint64_t>(W) * 16 * C8};
-  cuuint32_t box[4] = {8, static_cast<cuuint32_t>(box_w), 2, static_cast<cuuint32_t>(box_h)};
-  cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(x_stride), 1, 1};
+  const bool groups = allow_groups && pitch % kGroupPx == 0 && box_w % kGroupPx == 0;
+  const cuuint64_t row = static_cast<cuuint64_t>(pitch) * 16;
+  cuuint64_t dims[4], strides[3] = {0, row, row * C8};
+  cuuint32_t box[4];
+  if (groups) {
+    dims[0] = 8 * kGroupPx;
+    dims[1] = static_cast<cuuint64_t>(pitch / kGroupPx);
+    strides[0] = 16 * kGroupPx;
+    box[0] = 8 * kGroupPx;
+    box[1] = static_cast<cuuint32_t>(box_w / kGroupPx);
+  } else {
+    dims[0] = 8;
+    dims[1] = static_cast<cuuint64_t>(W);
+    strides[0] = 16;
+    box[0] = 8;
+    box[1] = static_cast<cuuint32_t>(box_w);
+  }
+  dims[2] = static_cast<cuuint64_t>(C8);
+  dims[3] = static_cast<cuuint64_t>(H);
+  box[2] = 2;
+  box[3] = static_cast<cuuint32_t>(box_h);
+  cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
-    return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %dx%dx%d", int(r), W, H,
-                C8);
+    return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %dx%dx%d (pitch %d)",
+                int(r), W, H, C8, pitch);
+  if (xs) *xs = groups ? 3 : 0;
   return ok();
 }
 
-// fp16 column-parity split activation [H][C8][2][W/2][8] as a 5-D tensor
+// fp16 column-parity split activation [H][C8][2][pitch/2][8] as a 5-D tensor
 // {8 lanes, W/2, 2 planes, C8, H}; box {8, box_w, 1, 2, box_h}.
-oidnx_status encode_split_map(CUtensorMap* map, const void* base, int W, int H, int C8, int box_w,
-                              int box_h) {
+oidnx_status encode_split_map(CUtensorMap* map, const void* base, int W, int pitch, int H, int C8,
+                              int box_w, int box_h) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  const cuuint64_t half = static_cast<cuuint64_t>(W / 2);
-  cuuint64_t dims[5] = {8, half, 2, static_cast<cuuint64_t>(C8), static_cast<cuuint64_t>(H)};
+  const cuuint64_t half = static_cast<cuuint64_t>(pitch / 2);
+  cuuint64_t dims[5] = {8, static_cast<cuuint64_t>(W / 2), 2, static_cast<cuuint64_t>(C8),
+                        static_cast<cuuint64_t>(H)};
   cuuint64_t strides[4] = {16, half * 16, half * 32, half * 32 * C8};
   cuuint32_t box[5] = {8, static_cast<cuuint32_t>(box_w), 1, 2, static_cast<cuuint32_t>(box_h)};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
@@ -531,9 +552,13 @@ struct DeviceLayer {
   size_t weight_bytes = 0;
 };
 
+// Extent of an activation; pitch = row stride in pixels (fp16 values of the
+// network: w rounded up to 8, padding columns zero; otherwise w).
 struct Extent {
-  int w, h;
+  int w, h, pitch;
 };
+
+int fp16_pitch(int w) { return (w + kGroupPx - 1) / kGroupPx * kGroupPx; }
 
 struct LayerLaunch {
   int layer;
@@ -663,10 +688,16 @@ oidnx_status make_device_layer(const ConvTensors& T, int c0, int c1, int precisi
 
 // Bytes of one stored activation: fp16 rounds channels up to 16 lanes, fp32
 // to 4; the network output is [h][w][4] floats.
-size_t act_bytes(int precision, int w, int h, int c, bool final_out) {
-  if (final_out) return static_cast<size_t>(w) * h * 16;
-  if (precision == OIDNX_PRECISION_FP16) return static_cast<size_t>(w) * h * round_up(c, 16) * 2;
-  return static_cast<size_t>(w) * h * round_up(c, 4) * 4;
+size_t act_bytes(int precision, Extent e, int c, bool final_out) {
+  if (final_out) return static_cast<size_t>(e.w) * e.h * 16;
+  if (precision == OIDNX_PRECISION_FP16) return static_cast<size_t>(e.pitch) * e.h * round_up(c, 16) * 2;
+  return static_cast<size_t>(e.w) * e.h * round_up(c, 4) * 4;
+}
+
+// Extent of a stored value of conv extent e.
+Extent value_extent(int precision, Extent e, bool final_out) {
+  const bool padded = precision == OIDNX_PRECISION_FP16 && !final_out;
+  return Extent{e.w, e.h, padded ? fp16_pitch(e.w) : e.w};
 }
 
 int act_chunks(int precision, int c) {
@@ -712,8 +743,8 @@ oidnx_status bound_ctas_per_sm(size_t* smem, uint32_t tmem_cols, int* blocks) {
 // one column parity; the upsampled source is read as a low-resolution halo
 // box, the skip source (src1) from its column-parity split copy.
 oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Extent ext0,
-                                      const void* src1, int W, int H, void* out, int* status,
-                                      TcConvLaunch* T) {
+                                      const void* src1, Extent ext1, int W, int H, void* out,
+                                      int out_pitch, int* status, TcConvLaunch* T) {
   const int N = L.N;
   int R = 8;
   while (R > 2 && R * N > 256) R /= 2;
@@ -728,6 +759,7 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   p.weights = static_cast<const __half*>(L.w16_sub);
   p.bias = L.bias;
   p.out = out;
+  p.pitch = out_pitch;
   p.status = status;
   p.W = W;
   p.H = H;
@@ -772,8 +804,9 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, static_cast<long>(num_sms()) * blocks)), 1, 1);
   const int c8_0 = round_up(L.c0, 16) / 8;
   const int c8_1 = round_up(L.c1, 16) / 8;
-  OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.h, c8_0, kHaloPx, R / 2 + 2));
-  OIDNX_TRY(encode_split_map(&T->map1, src1, W, H, c8_1, kHaloPx, R + 2));
+  OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.pitch, ext0.h, c8_0, kHaloPx, R / 2 + 2,
+                           false, nullptr));
+  OIDNX_TRY(encode_split_map(&T->map1, src1, W, ext1.pitch, H, c8_1, kHaloPx, R + 2));
   return ok();
 }
 
@@ -784,11 +817,14 @@ bool use_subpixel(int precision, int W, int H, Extent ext0) {
          ext0.h * 2 == H;
 }
 
+// src0/src1: sources with their extents (pitch included); (W, H): conv
+// extent; out: destination with row pitch out_pitch (fp16 values).
 oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, Extent ext0,
-                             const void* src1, int W, int H, void* out, int* status,
-                             TcConvLaunch* T, bool subpixel = false, void* out_split = nullptr) {
+                             const void* src1, Extent ext1, int W, int H, void* out,
+                             int out_pitch, int* status, TcConvLaunch* T, bool subpixel = false,
+                             void* out_split = nullptr) {
   if (kind == kDecoder && subpixel && L.w16_sub)
-    return build_tc_launch_subpixel(L, src0, ext0, src1, W, H, out, status, T);
+    return build_tc_launch_subpixel(L, src0, ext0, src1, ext1, W, H, out, out_pitch, status, T);
   const bool up = kind == kDecoder;
   T->kind = up ? kTcExpand : kTcPlain;
   const int N = L.N;
@@ -807,6 +843,7 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   p.weights = static_cast<const __half*>(L.w16);
   p.bias = L.bias;
   p.out = out;
+  p.pitch = out_pitch;
   p.status = status;
   p.W = W;
   p.H = H;
@@ -820,9 +857,9 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   p.tiles_x = tiles_x;
   p.tiles_y = (H + R - 1) / R;
   p.tmem_cols = tmem_cols;
-  p.a_tx = static_cast<uint32_t>((R + 2) * 2 * kHaloPx * kChunkBytes);
+  p.a_tx = static_cast<uint32_t>((R + 2) * 2 * kHaloW * kChunkBytes);
   p.b_tx = static_cast<uint32_t>(9 * 2 * N * kChunkBytes);
-  p.st_tx = up ? static_cast<uint32_t>((R / 2 + 2) * 2 * kLowPx * kChunkBytes) : 0u;
+  p.st_tx = up ? static_cast<uint32_t>((R / 2 + 2) * 2 * kLowW * kChunkBytes) : 0u;
   p.a_stage = static_cast<uint32_t>(round_up_sz(p.a_tx, 1024));
   p.b_stage = static_cast<uint32_t>(round_up_sz(p.b_tx, 1024));
   p.st_stage = static_cast<uint32_t>(round_up_sz(p.st_tx, 1024));
@@ -868,15 +905,15 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, static_cast<long>(num_sms()) * blocks)), 1, 1);
 
   const int c8_0 = round_up(L.c0, 16) / 8;
-  if (up)
-    OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.h, c8_0, kLowPx, R / 2 + 2));
-  else
-    OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.h, c8_0, kHaloPx, R + 2));
+  OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.pitch, ext0.h, c8_0,
+                           up ? kLowW : kHaloW, up ? R / 2 + 2 : R + 2, true, &p.xs0));
   if (L.KB1 > 0) {
     const int c8_1 = round_up(L.c1, 16) / 8;
-    OIDNX_TRY(encode_act_map(&T->map1, src1, W, H, c8_1, kHaloPx, R + 2));
+    OIDNX_TRY(encode_act_map(&T->map1, src1, ext1.w, ext1.pitch, ext1.h, c8_1, kHaloW, R + 2, true,
+                             &p.xs1));
   } else {
     T->map1 = T->map0;
+    p.xs1 = p.xs0;
   }
   return ok();
 }
@@ -926,15 +963,18 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
   std::unique_ptr<Plan> P(new Plan());
   P->w = w;
   P->h = h;
-  P->lvl[0] = {w, h};
-  for (int l = 1; l < 5; ++l) P->lvl[l] = {(P->lvl[l - 1].w + 1) / 2, (P->lvl[l - 1].h + 1) / 2};
+  P->lvl[0] = {w, h, w};
+  for (int l = 1; l < 5; ++l) {
+    const int lw = (P->lvl[l - 1].w + 1) / 2;
+    P->lvl[l] = {lw, (P->lvl[l - 1].h + 1) / 2, lw};
+  }
   // value shapes
-  P->value_ext[V_IN] = P->lvl[0];
+  P->value_ext[V_IN] = value_extent(f->precision, P->lvl[0], false);
   P->value_ch[V_IN] = f->in_channels;
   for (int l = 0; l < kLayers; ++l) {
     const LayerDef& d = kDefs[l];
     const int lvl = d.kind == kPool ? d.level + 1 : d.level;
-    P->value_ext[d.dst] = P->lvl[lvl];
+    P->value_ext[d.dst] = value_extent(f->precision, P->lvl[lvl], d.dst == V_OUT);
     P->value_ch[d.dst] = f->layers[l].cout;
   }
   // last use of each value
@@ -964,8 +1004,7 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
     if (!f->keep_acts)
       for (Slot& s : slots)
         if (s.active >= 0 && last_use[s.active] < index) s.active = -1;
-    const size_t need = act_bytes(f->precision, P->value_ext[v].w, P->value_ext[v].h,
-                                  P->value_ch[v], v == V_OUT);
+    const size_t need = act_bytes(f->precision, P->value_ext[v], P->value_ch[v], v == V_OUT);
     int best = -1;
     for (size_t i = 0; i < slots.size(); ++i)
       if (slots[i].active < 0 && slots[i].cap >= need &&
@@ -1006,6 +1045,7 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
     LL.layer = l;
     const Extent conv = P->lvl[d.level];
     const void* s1 = d.src1 >= 0 ? P->ptr(d.src1) : nullptr;
+    Extent e1 = d.src1 >= 0 ? P->value_ext[d.src1] : Extent{0, 0, 0};
     bool subpixel = false;
     void* out_split = nullptr;
     for (int i = 0; i < 4; ++i) {
@@ -1013,13 +1053,15 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
       if (kSplits[i].consumer == l) {
         subpixel = true;
         s1 = P->ptr(kSplits[i].split);
+        e1 = P->value_ext[kSplits[i].split];
       }
       if (kSplits[i].producer == l) out_split = P->ptr(kSplits[i].split);
     }
     if (f->precision == OIDNX_PRECISION_FP16) {
       LL.tc = true;
-      OIDNX_TRY(build_tc_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, conv.w,
-                                conv.h, P->ptr(d.dst), f->status, &LL.tcl, subpixel, out_split));
+      OIDNX_TRY(build_tc_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, e1, conv.w,
+                                conv.h, P->ptr(d.dst), P->value_ext[d.dst].pitch, f->status,
+                                &LL.tcl, subpixel, out_split));
     } else {
       LL.tc = false;
       build_simt_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, conv.w, conv.h,
@@ -1153,6 +1195,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
       pp.out = P->ptr(V_IN);
       pp.out_split = P->split_on[0] ? P->ptr(V_INS) : nullptr;
       pp.chunks = act_chunks(f->precision, f->in_channels);
+      pp.pitch = P->value_ext[V_IN].pitch;
       (void)cudaGetLastError();
       cudaError_t e = launch_pack(pp, s);
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
@@ -1273,15 +1316,19 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     return fail(OIDNX_ERR_INVALID_ARGUMENT,
                 "network_execute_noalloc: pointers must be 16-byte aligned");
   Extent lvl[5];
-  lvl[0] = {w, h};
-  for (int l = 1; l < 5; ++l) lvl[l] = {(lvl[l - 1].w + 1) / 2, (lvl[l - 1].h + 1) / 2};
+  lvl[0] = {w, h, w};
+  for (int l = 1; l < 5; ++l) {
+    const int lw = (lvl[l - 1].w + 1) / 2;
+    lvl[l] = {lw, (lvl[l - 1].h + 1) / 2, lw};
+  }
   Extent ext[V_COUNT];
   int ch[V_COUNT] = {};
-  ext[V_IN] = lvl[0];
+  ext[V_IN] = lvl[0];  // the caller's buffer, rows of w pixels
   ch[V_IN] = f->in_channels;
   for (int l = 0; l < kLayers; ++l) {
     const LayerDef& d = kDefs[l];
-    ext[d.dst] = lvl[d.kind == kPool ? d.level + 1 : d.level];
+    ext[d.dst] = value_extent(f->precision, lvl[d.kind == kPool ? d.level + 1 : d.level],
+                              d.dst == V_OUT);
     ch[d.dst] = f->layers[l].cout;
   }
   int last_use[V_COUNT];
@@ -1307,7 +1354,7 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
   auto place = [&](int v, int l) {
     for (int i = 0; i < nslots; ++i)
       if (slots[i].active >= 0 && last_use[slots[i].active] < l) slots[i].active = -1;
-    const size_t need = round_up_sz(act_bytes(f->precision, ext[v].w, ext[v].h, ch[v], false), 1024);
+    const size_t need = round_up_sz(act_bytes(f->precision, ext[v], ch[v], false), 1024);
     int best = -1;
     for (int i = 0; i < nslots; ++i)
       if (slots[i].active < 0 && slots[i].cap >= need && (best < 0 || slots[i].cap < slots[best].cap))
@@ -1338,7 +1385,8 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     return static_cast<uint8_t*>(arena) + off[v];
   };
   if (split_on[0]) {
-    cudaError_t e = launch_split_copy(in, ptr(V_INS), w, h, act_chunks(f->precision, f->in_channels), s);
+    cudaError_t e = launch_split_copy(in, w, ptr(V_INS), ext[V_INS].pitch, w, h,
+                                      act_chunks(f->precision, f->in_channels), s);
     if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "split copy: %s", cudaGetErrorString(e));
   }
   for (int l = 0; l < kLayers; ++l) {
@@ -1349,6 +1397,7 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     LL.layer = l;
     const Extent conv = lvl[d.level];
     const void* s1 = d.src1 >= 0 ? ptr(d.src1) : nullptr;
+    Extent e1 = d.src1 >= 0 ? ext[d.src1] : Extent{0, 0, 0};
     bool subpixel = false;
     void* out_split = nullptr;
     for (int i = 0; i < 4; ++i) {
@@ -1356,13 +1405,15 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
       if (kSplits[i].consumer == l) {
         subpixel = true;
         s1 = ptr(kSplits[i].split);
+        e1 = ext[kSplits[i].split];
       }
       if (kSplits[i].producer == l) out_split = ptr(kSplits[i].split);
     }
     if (f->precision == OIDNX_PRECISION_FP16) {
       LL.tc = true;
-      OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, conv.w, conv.h,
-                                ptr(d.dst), f->status, &LL.tcl, subpixel, out_split));
+      OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, e1, conv.w, conv.h,
+                                ptr(d.dst), ext[d.dst].pitch, f->status, &LL.tcl, subpixel,
+                                out_split));
     } else {
       LL.tc = false;
       build_simt_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, conv.w, conv.h, ptr(d.dst),
@@ -1630,11 +1681,18 @@ oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w
   const bool prof = f->profile_next || f->profile_always;
   f->profile_next = false;
   if (prof) OIDNX_TRY(prof_begin(f, kLayers));
-  OIDNX_CUDA(cudaMemcpyAsync(P->ptr(V_IN), packed_in, P->value_bytes[V_IN],
-                             cudaMemcpyDeviceToDevice, s));
+  const Extent ein = P->value_ext[V_IN];
+  const int in_chunks = act_chunks(f->precision, f->in_channels);
+  if (ein.pitch == w) {
+    OIDNX_CUDA(cudaMemcpyAsync(P->ptr(V_IN), packed_in, P->value_bytes[V_IN],
+                               cudaMemcpyDeviceToDevice, s));
+  } else {
+    cudaError_t e = launch_pitch_copy(packed_in, w, P->ptr(V_IN), ein.pitch, w, h * in_chunks, s);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input copy: %s", cudaGetErrorString(e));
+  }
   if (P->split_on[0]) {
-    cudaError_t e = launch_split_copy(P->ptr(V_IN), P->ptr(V_INS), w, h,
-                                      act_chunks(f->precision, f->in_channels), s);
+    cudaError_t e = launch_split_copy(P->ptr(V_IN), ein.pitch, P->ptr(V_INS),
+                                      P->value_ext[V_INS].pitch, w, h, in_chunks, s);
     if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "split copy: %s", cudaGetErrorString(e));
   }
   OIDNX_TRY(prof_mark(f, prof, -2, s));
@@ -1655,6 +1713,16 @@ oidnx_status oidnx_filter_sync_status(oidnx_filter* f) {
     OIDNX_CUDA(cudaMemset(f->status, 0, sizeof(int)));
     return fail(OIDNX_ERR_TIMEOUT, "a device-side wait gave up (status bits 0x%x)", word);
   }
+  return ok();
+}
+
+oidnx_status oidnx_debug_wait_probe(oidnx_filter* f, unsigned int limit_us, void* stream) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  if (limit_us == 0 || limit_us > 1000000)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "wait probe limit must be 1 us .. 1 s");
+  cudaError_t e = launch_wait_probe(f->status, 1000ull * limit_us, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "wait probe: %s", cudaGetErrorString(e));
   return ok();
 }
 
@@ -1761,7 +1829,7 @@ oidnx_status oidnx_debug_read_activation(oidnx_filter* f, int layer, void* host_
   for (int y = 0; y < e.h; ++y)
     for (int x = 0; x < e.w; ++x)
       for (int c = 0; c < C; ++c) {
-        const size_t idx = ((static_cast<size_t>(y) * chunks + c / lanes) * e.w + x) * lanes + c % lanes;
+        const size_t idx = ((static_cast<size_t>(y) * chunks + c / lanes) * e.pitch + x) * lanes + c % lanes;
         float val;
         if (lanes == 8) {
           uint16_t b;
@@ -1836,11 +1904,12 @@ oidnx_status oidnx_conv_execute(oidnx_conv* c, const void* in, void* out, int w,
   LL.layer = 0;
   if (c->precision == OIDNX_PRECISION_FP16) {
     LL.tc = true;
-    OIDNX_TRY(build_tc_launch(c->L, kPlain, in, Extent{w, h}, nullptr, w, h, out, c->status,
-                              &LL.tcl));
+    // caller's buffers: rows of w pixels (128-byte TMA rows when w % 8 == 0)
+    OIDNX_TRY(build_tc_launch(c->L, kPlain, in, Extent{w, h, w}, nullptr, Extent{0, 0, 0}, w, h,
+                              out, w, c->status, &LL.tcl));
   } else {
     LL.tc = false;
-    build_simt_launch(c->L, kPlain, in, Extent{w, h}, nullptr, w, h, out, &LL.sp);
+    build_simt_launch(c->L, kPlain, in, Extent{w, h, w}, nullptr, w, h, out, &LL.sp);
   }
   return run_launch(LL, s);
 }

@@ -15,6 +15,7 @@ enum : int {
   kErrTimeoutMma = 2,
   kErrTimeoutEpilogue = 4,
   kErrTimeoutDrain = 8,
+  kErrTimeoutProbe = 16,
 };
 
 // A bounded wait gives up after this many nanoseconds of wall time.
@@ -66,14 +67,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for the phase with `parity` to complete; give up after the limit,
 // record `code` in the status word and return false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status,
-                                                  int code) {
+                                                  int code, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0; it < kWaitLimitIters; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63) == 63) {
       __nanosleep(64);
-      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+      if (globaltimer_ns() - t0 > limit_ns) break;
     }
   }
   if (status) atomicOr(status, code);
@@ -190,6 +191,18 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// True in exactly one lane of the (fully converged) warp: the same lane on
+// every call, so that MMAs and the commits tracking them come from one thread.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\t"
+      "elect.sync rx|px, 0xffffffff;\n\t"
+      "@px mov.s32 %0, 1;\n\t}"
+      : "+r"(pred));
+  return pred != 0;
+}
+
 // Arrive on `bar` once all previously issued tcgen05.mma of this thread end.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -229,6 +242,22 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[1
 
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns from registers (the same pattern
+// layout as tmem_ld16); complete with tmem_wait_st().
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {

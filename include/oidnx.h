@@ -174,6 +174,15 @@ oidnx_status oidnx_network_execute_noalloc(oidnx_filter* f, const void* packed_i
  * undefined).  Errors: CUDA.  */
 oidnx_status oidnx_filter_sync_status(oidnx_filter* f);
 
+/* Failure-detection probe: launch, on `stream`, one thread that waits on a
+ * device barrier nothing will complete, bounded by limit_us (1 .. 1e6).  The
+ * wait gives up after the limit, records a timeout bit in the filter's device
+ * error word and returns, leaving the context usable; the next
+ * oidnx_filter_sync_status reports OIDNX_ERR_TIMEOUT.  This exercises the
+ * same bounded wait every kernel of the library uses.  Errors:
+ * INVALID_ARGUMENT, CUDA.  */
+oidnx_status oidnx_debug_wait_probe(oidnx_filter* f, unsigned int limit_us, void* stream);
+
 /* Per-kernel timing of the next execute (or network_execute) only, like
  * "nativeUNet.ts" profileNextExecution.  */
 oidnx_status oidnx_profile_next(oidnx_filter* f);

@@ -2,6 +2,8 @@
 (profiled) run, the host-buffer path equals the device path, the LRU shape
 cache evicts safely, the profile and resource reports are well formed."""
 
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -105,3 +107,34 @@ def test_execute_requires_commit_and_release_is_final(weights):
     assert e.value.status == ox.ERR_UNSUPPORTED
     ox.oidnx_filter_release(f)
     torch.cuda.synchronize()
+
+
+def test_bounded_device_wait_reports_timeout_and_context_survives(weights):
+    """A device wait that nothing completes gives up after its limit, sets the
+    filter's error word (reported once as ERR_TIMEOUT) and leaves the context
+    usable: a network execution afterwards still matches the one before."""
+    f = ox.oidnx_filter_create(ox.write_weight_blob(weights), ox.PRECISION_FP16)
+    try:
+        w, h = 40, 24
+        x = round_storage(synth.uniform_activations(h, w, 9, seed=5, low=0, high=1), "fp16")
+        src = to_dev(_layout.to_internal(x, "fp16"))
+        out0, out1 = empty_dev(w * h * 16), empty_dev(w * h * 16)
+        ox.oidnx_network_execute(f, src.data_ptr(), w, h, out0.data_ptr(), stream())
+        ox.oidnx_filter_sync_status(f)
+        with pytest.raises(ox.OidnxError) as e:
+            ox.oidnx_debug_wait_probe(f, 0)
+        assert e.value.status == ox.ERR_INVALID_ARGUMENT
+        t0 = time.perf_counter()
+        ox.oidnx_debug_wait_probe(f, 20000, stream())      # 20 ms limit
+        with pytest.raises(ox.OidnxError) as e:
+            ox.oidnx_filter_sync_status(f)
+        elapsed = time.perf_counter() - t0
+        assert e.value.status == ox.ERR_TIMEOUT
+        assert "0x10" in str(e.value)
+        assert 0.015 <= elapsed < 5.0
+        ox.oidnx_filter_sync_status(f)                      # the word was cleared
+        ox.oidnx_network_execute(f, src.data_ptr(), w, h, out1.data_ptr(), stream())
+        ox.oidnx_filter_sync_status(f)
+        assert torch.equal(out0, out1)
+    finally:
+        ox.oidnx_filter_release(f)
