@@ -90,6 +90,14 @@ __device__ __forceinline__ void tmem_fill_bias(uint32_t taddr, const float* bias
   tmem_st16(taddr, r);
 }
 
+// Advance a pipeline position (stage s of S, phase parity ph) by one item.
+__device__ __forceinline__ void next_stage(uint32_t& s, uint32_t& ph, uint32_t S) {
+  if (++s == S) {
+    s = 0;
+    ph ^= 1u;
+  }
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -162,7 +170,7 @@ __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbas
     for (int hl = 0; hl < R / 2 + 2; ++hl) {
       const int lo = 2 * hl - 3 > 0 ? 2 * hl - 3 : 0;
       const int hi = 2 * hl < R - 1 ? 2 * hl : R - 1;
-      const uint64_t a = adk + static_cast<uint32_t>(hl * 2 * kHaloPx);
+      const uint64_t a = adk + static_cast<uint32_t>(hl * 2 * kHaloW);
 #pragma unroll
       for (int c = lo; c <= hi; c += G) {
         const int e = c + G - 1 < hi ? c + G - 1 : hi;
@@ -185,7 +193,7 @@ __device__ __forceinline__ void issue_skip(uint64_t ad, uint64_t bd, uint32_t db
   for (int h = 0; h < R + 2; ++h) {
     const int lo = h - 2 > 0 ? h - 2 : 0;
     const int hi = h < R - 1 ? h : R - 1;
-    const uint64_t a = ad + static_cast<uint32_t>(h * 2 * kHaloPx);
+    const uint64_t a = ad + static_cast<uint32_t>(h * 2 * kHaloW);
 #pragma unroll
     for (int c = lo; c <= hi; c += G) {
       const int e = c + G - 1 < hi ? c + G - 1 : hi;
@@ -302,14 +310,12 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
       // Weights and bias are constants; the activations come from the
       // previous kernel in the stream.
       griddep_wait();
-      uint32_t it = 0;
+      uint32_t it = 0, s = 0, ph = 0;  // item count, its stage and phase
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         int x0, y0, px;
         tile_origin_k<KIND>(p, tile, &x0, &y0, &px);
-        for (int kb = 0; kb < items; ++kb, ++it) {
-          const uint32_t s = it % S;
-          const uint32_t ph = (it / S) & 1u;
+        for (int kb = 0; kb < items; ++kb, ++it, next_stage(s, ph, S)) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kErrTimeoutProducer)) {
             ok = false;
             break;
@@ -319,8 +325,9 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
             if (kb < KB0) {
               const uint32_t half = p.b_tx / 2;  // one column parity of the block
               mbar_arrive_expect_tx(&full[s], p.a_tx + (p.resident ? 0u : half));
+              // low-resolution box from kGroupPx left of the block's first pixel
               tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map0, &full[s], 0,
-                          (x0 >> 1) - 1, 2 * kb, (y0 >> 1) - 1);
+                          ((x0 >> 1) - kGroupPx) >> p.xs0, 2 * kb, (y0 >> 1) - 1);
               if (!p.resident)
                 bulk_load(B + static_cast<size_t>(s) * p.b_stage,
                           wsrc + static_cast<size_t>(kb) * p.b_tx + static_cast<size_t>(px) * half,
@@ -328,10 +335,11 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
             } else {
               // skip source, column-parity split: the outer plane (parity
               // px ^ 1, serving kx = 0 and kx = 2) or the centre plane
-              // (parity px, kx = 1) of one 16-channel block
+              // (parity px, kx = 1) of one 16-channel block, from kGroupPx
+              // entries left of the block's first entry
               const int j = (kb - KB0) >> 1, part = (kb - KB0) & 1;
               const int plane = part ? px : (px ^ 1);
-              const int i0 = (x0 >> 1) - (part == 0 && px == 0 ? 1 : 0);
+              const int i0 = ((x0 >> 1) - kGroupPx) >> p.xs1;
               const uint32_t wb = part ? p.b_tx2 : 2u * p.b_tx2;
               mbar_arrive_expect_tx(&full[s], p.st_tx + (p.resident ? 0u : wb));
               tma_load_5d(A + static_cast<size_t>(s) * p.a_stage, &map1, &full[s], 0, i0, plane,
@@ -388,7 +396,9 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
       const uint32_t id2 = idesc_f16_f32(kTileM, min(2 * N, 256));
       const uint32_t id3 = idesc_f16_f32(kTileM, min(3 * N, 256));
       const uint32_t id4 = idesc_f16_f32(kTileM, min(4 * N, 256));
-      const uint64_t a_up0 = smem_desc_noswizzle(smem_u32(A), kHaloPx * kChunkBytes, 128);
+      // sub-pixel boxes: rows of kHaloW entries starting kGroupPx left of the
+      // block (low-resolution x0/2 - 1 at kHaloOff)
+      const uint64_t a_up0 = smem_desc_noswizzle(smem_u32(A), kHaloW * kChunkBytes, 128);
       const uint32_t wbase = smem_u32(p.resident ? Wres : B);
       const uint64_t b_up0 = smem_desc_noswizzle(wbase, 4u * N * kChunkBytes, 128);
       const uint64_t b_sk0 = smem_desc_noswizzle(wbase, 3u * N * kChunkBytes, 128);
@@ -401,7 +411,7 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
       const uint32_t set_cols = static_cast<uint32_t>(R * N);
       bool ok = __all_sync(0xffffffffu,
                            !p.resident || mbar_wait_bounded(wbar, 0, p.status, kErrTimeoutMma));
-      uint32_t it = 0, tcount = 0;
+      uint32_t it = 0, s = 0, ph = 0, tcount = 0;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tcount) {
         const uint32_t buf = tcount & 1u;
         // use k of a set needs phase k of tempty: the epilogue's initial
@@ -415,9 +425,7 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
         const uint32_t d_base = tmem + buf * set_cols;
         int tx0, ty0, tpx;
         tile_origin_k<KIND>(p, tile, &tx0, &ty0, &tpx);
-        for (int kb = 0; kb < items; ++kb, ++it) {
-          const uint32_t s = it % S;
-          const uint32_t ph = (it / S) & 1u;
+        for (int kb = 0; kb < items; ++kb, ++it, next_stage(s, ph, S)) {
           bool w = mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutMma);
           if (KIND == kTcExpand && w) w = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
           ok = __all_sync(0xffffffffu, w);
@@ -442,7 +450,10 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
               // adjacent when streamed); centre plane: kx = 1 only
               pxb = part ? 0 : static_cast<int>((p.resident ? 2u * p.b_tx2 : p.b_tx2) >> 4);
             }
-            const uint64_t ad = a_up0 + soff;
+            // upsampled: x0/2 - 1 at kHaloOff; skip: the centre plane's first
+            // entry at kGroupPx, the outer plane's x0/2 + px - 1 at kHaloOff + px
+            const int aoff = up ? kHaloOff : ((kb - KB0) & 1 ? kGroupPx : kHaloOff + tpx);
+            const uint64_t ad = a_up0 + soff + static_cast<uint32_t>(aoff);
             const uint64_t bd = (up ? b_up0 : b_sk0) + (woff >> 4);
             if (g4 == 4) issue_subpixel_item<4, 3>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4);
             else if (g4 == 2) issue_subpixel_item<2, 2>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4);
@@ -470,15 +481,13 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
     // ------------------------------------------------------------ upsampled halo
     const int et = threadIdx.x - 32 * (2 + kTcEpilogueWarps);  // 0..127
     const int total = (R + 2) * 2 * kHaloPx;
-    uint32_t it = 0;
+    uint32_t it = 0, s = 0, ph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       int x0, y0;
       tile_origin(p, tile, &x0, &y0);
       const int ly0 = (y0 >> 1) - 1, lx0 = (x0 >> 1) - kGroupPx;
-      for (int kb = 0; kb < KB; ++kb, ++it) {
-        const uint32_t s = it % S;
-        const uint32_t ph = (it / S) & 1u;
+      for (int kb = 0; kb < KB; ++kb, ++it, next_stage(s, ph, S)) {
         // Waiting on every stage keeps this warp group at most one use of a
         // stage ahead of the MMA issuer, so the xdone phases stay paired.
         if (!mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutEpilogue)) {
@@ -604,21 +613,23 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
               mx[k] = t;
             }
             // pooled columns [Wp, pitch) are row padding: stored as zeros
-            if (((lane & 1) == 0) && xp < p.pitch && yp < Hp) {
+            if (((lane & 1) == 0) && yp < Hp) {
               const bool pad = xp >= Wp;
               uint32_t h[8];
 #pragma unroll
               for (int k = 0; k < 8; ++k) h[k] = pad ? 0u : pack_half2(mx[2 * k], mx[2 * k + 1]);
-              const size_t base0 = ((static_cast<size_t>(yp) * C8 + 2 * c) * p.pitch + xp) * 8;
-              const size_t base1 = base0 + static_cast<size_t>(p.pitch) * 8;
-              *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
-              *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
-              if (p.out_split) {
-                // plane xp & 1, index xp >> 1 (the pitch is even)
+              if (xp < p.pitch) {
+                const size_t base0 = ((static_cast<size_t>(yp) * C8 + 2 * c) * p.pitch + xp) * 8;
+                const size_t base1 = base0 + static_cast<size_t>(p.pitch) * 8;
+                *reinterpret_cast<uint4*>(out + base0) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(out + base1) = make_uint4(h[4], h[5], h[6], h[7]);
+              }
+              if (p.out_split && xp < p.split_pitch) {
+                // plane xp & 1, index xp >> 1 (the split pitch is even)
                 __half* o2 = static_cast<__half*>(p.out_split);
                 const size_t s0 =
-                    ((((static_cast<size_t>(yp) * C8 + 2 * c) * 2 + (xp & 1)) * (p.pitch >> 1)) + (xp >> 1)) * 8;
-                const size_t s1 = s0 + static_cast<size_t>(p.pitch) * 8;
+                    ((((static_cast<size_t>(yp) * C8 + 2 * c) * 2 + (xp & 1)) * (p.split_pitch >> 1)) + (xp >> 1)) * 8;
+                const size_t s1 = s0 + static_cast<size_t>(p.split_pitch) * 8;
                 *reinterpret_cast<uint4*>(o2 + s0) = make_uint4(h[0], h[1], h[2], h[3]);
                 *reinterpret_cast<uint4*>(o2 + s1) = make_uint4(h[4], h[5], h[6], h[7]);
               }

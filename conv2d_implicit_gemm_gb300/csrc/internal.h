@@ -57,8 +57,10 @@ struct TcConvParams {
   uint32_t b_tx2;
   uint32_t wres_bytes;
   // pool epilogue: optional second copy of the output, column-parity split
-  // [Ho][N/8][2][pitch/2][8] (read by the sub-pixel decoder as its skip source)
+  // [Ho][N/8][2][split_pitch/2][8] (read by the sub-pixel decoder as its skip
+  // source); entries past the output width are written as zeros
   void* out_split;
+  int split_pitch;
   int pitch;               // fp16 output row pitch in pixels (>= output width);
                            // columns [width, pitch) are written as zeros
   int xs0, xs1;            // log2 pixels per x unit of map0 / map1: 3 for
@@ -133,7 +135,8 @@ struct PackParams {
   void* out;               // [th][chunks][pitch][lanes]; columns >= tw are zeros
   int pitch;               // row pitch in pixels (fp16: tw rounded up to 8; fp32: tw)
   int chunks;              // 16-byte chunks per pixel
-  void* out_split;         // optional parity-split copy [th][chunks][2][pitch/2][lanes]
+  void* out_split;         // optional parity-split copy [th][chunks][2][split_pitch/2][lanes]
+  int split_pitch;         // its pitch (a multiple of 16), columns >= tw zero
 };
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 

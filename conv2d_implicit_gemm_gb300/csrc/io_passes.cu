@@ -65,17 +65,19 @@ __global__ void pack_kernel(const PackParams p) {
   griddep_launch_dependents();
   const int tx = blockIdx.x * blockDim.x + threadIdx.x;
   const int ty = blockIdx.y;
-  if (tx >= p.pitch) return;
+  if (tx >= (p.out_split && p.split_pitch > p.pitch ? p.split_pitch : p.pitch)) return;
   const size_t pixel = static_cast<size_t>(ty) * p.chunks * p.pitch + tx;
   if (tx >= p.tw) {
     // row padding: zeros, so that 8-pixel TMA rows read zero past the tile
     if (FP16) {
       uint4* out = static_cast<uint4*>(p.out);
-      out[pixel] = make_uint4(0u, 0u, 0u, 0u);
-      out[pixel + p.pitch] = make_uint4(0u, 0u, 0u, 0u);
-      if (p.out_split) {
+      if (tx < p.pitch) {
+        out[pixel] = make_uint4(0u, 0u, 0u, 0u);
+        out[pixel + p.pitch] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (p.out_split && tx < p.split_pitch) {
         uint4* o2 = static_cast<uint4*>(p.out_split);
-        const size_t half = static_cast<size_t>(p.pitch) >> 1;
+        const size_t half = static_cast<size_t>(p.split_pitch) >> 1;
         const size_t s0 = (static_cast<size_t>(ty) * p.chunks * 2 + (tx & 1)) * half + (tx >> 1);
         o2[s0] = make_uint4(0u, 0u, 0u, 0u);
         o2[s0 + 2 * half] = make_uint4(0u, 0u, 0u, 0u);
@@ -133,9 +135,9 @@ __global__ void pack_kernel(const PackParams p) {
     out[pixel] = make_uint4(w[0], w[1], w[2], w[3]);
     out[pixel + p.pitch] = make_uint4(w[4], w[5], w[6], w[7]);
     if (p.out_split) {
-      // column-parity split copy: plane tx & 1, index tx >> 1 (pitch even)
+      // column-parity split copy: plane tx & 1, index tx >> 1
       uint4* o2 = static_cast<uint4*>(p.out_split);
-      const size_t half = static_cast<size_t>(p.pitch) >> 1;
+      const size_t half = static_cast<size_t>(p.split_pitch) >> 1;
       const size_t s0 = (static_cast<size_t>(ty) * p.chunks * 2 + (tx & 1)) * half + (tx >> 1);
       o2[s0] = make_uint4(w[0], w[1], w[2], w[3]);
       o2[s0 + 2 * half] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -237,7 +239,8 @@ cudaError_t launch_pitch_copy(const void* src, int src_pitch, void* dst, int dst
 
 template <int S, bool F16, bool HDR>
 cudaError_t launch_pack_t(const PackParams& p, cudaStream_t stream) {
-  dim3 grid((p.pitch + 127) / 128, p.th);
+  const int span = p.out_split && p.split_pitch > p.pitch ? p.split_pitch : p.pitch;
+  dim3 grid((span + 127) / 128, p.th);
   return launch_pdl(pack_kernel<S, F16, HDR>, grid, dim3(128), 0, stream, p);
 }
 

@@ -13,7 +13,7 @@
 // every intermediate activation lives in the array below.
 //
 // The array is a file-scope __device__ variable of kNoAllocScratchBytes
-// (40 MiB).  Every GPU that loads this library holds that much memory until
+// (48 MiB).  Every GPU that loads this library holds that much memory until
 // the process exits.  It is enough for fp16 inputs up to 384 x 384 pixels
 // and fp32 inputs up to 256 x 256; larger inputs are rejected with
 // OIDNX_ERR_INVALID_ARGUMENT and a message giving the bytes needed.
@@ -30,7 +30,7 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(40) << 20;
+constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;
 constexpr int kMaxDevices = 64;
 
 // Device-side scratch shared by every call on a device.  In host code this

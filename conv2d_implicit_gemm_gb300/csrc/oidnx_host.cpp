@@ -515,23 +515,46 @@ oidnx_status encode_act_map(CUtensorMap* map, const void* base, int W, int pitch
   return ok();
 }
 
-// fp16 column-parity split activation [H][C8][2][pitch/2][8] as a 5-D tensor
-// {8 lanes, W/2, 2 planes, C8, H}; box {8, box_w, 1, 2, box_h}.
+// fp16 column-parity split activation [H][C8][2][pitch/2][8] (entries
+// [W/2, pitch/2) of each plane zero) as a 5-D tensor {lanes, x, plane, C8, H}.
+// With pitch % 16 == 0 the innermost dimension is 8 entries (128 B) and x
+// counts 8-entry groups (*xs = 3), else one entry (16 B, *xs = 0); the box
+// is box_w entries (a multiple of 8 for the first form) x 1 plane x 2 chunks
+// x box_h rows.
 oidnx_status encode_split_map(CUtensorMap* map, const void* base, int W, int pitch, int H, int C8,
-                              int box_w, int box_h) {
+                              int box_w, int box_h, int* xs) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   const cuuint64_t half = static_cast<cuuint64_t>(pitch / 2);
-  cuuint64_t dims[5] = {8, static_cast<cuuint64_t>(W / 2), 2, static_cast<cuuint64_t>(C8),
-                        static_cast<cuuint64_t>(H)};
-  cuuint64_t strides[4] = {16, half * 16, half * 32, half * 32 * C8};
-  cuuint32_t box[5] = {8, static_cast<cuuint32_t>(box_w), 1, 2, static_cast<cuuint32_t>(box_h)};
+  const bool groups = half % kGroupPx == 0 && box_w % kGroupPx == 0;
+  cuuint64_t dims[5], strides[4] = {0, half * 16, half * 32, half * 32 * C8};
+  cuuint32_t box[5];
+  if (groups) {
+    dims[0] = 8 * kGroupPx;
+    dims[1] = half / kGroupPx;
+    strides[0] = 16 * kGroupPx;
+    box[0] = 8 * kGroupPx;
+    box[1] = static_cast<cuuint32_t>(box_w / kGroupPx);
+  } else {
+    dims[0] = 8;
+    dims[1] = static_cast<cuuint64_t>(W / 2);
+    strides[0] = 16;
+    box[0] = 8;
+    box[1] = static_cast<cuuint32_t>(box_w);
+  }
+  dims[2] = 2;
+  dims[3] = static_cast<cuuint64_t>(C8);
+  dims[4] = static_cast<cuuint64_t>(H);
+  box[2] = 1;
+  box[3] = 2;
+  box[4] = static_cast<cuuint32_t>(box_h);
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled (split) failed (%d)", int(r));
+  if (xs) *xs = groups ? 3 : 0;
   return ok();
 }
 
@@ -559,6 +582,10 @@ struct Extent {
 };
 
 int fp16_pitch(int w) { return (w + kGroupPx - 1) / kGroupPx * kGroupPx; }
+
+// Pitch of a column-parity split copy: 16-pixel multiple, so that each
+// parity plane (pitch / 2 entries) is a whole number of 8-entry TMA rows.
+int split_pitch(int w) { return (w + 2 * kGroupPx - 1) / (2 * kGroupPx) * (2 * kGroupPx); }
 
 struct LayerLaunch {
   int layer;
@@ -605,7 +632,7 @@ struct oidnx_filter {
   int* status = nullptr;  // device error word
   // parameters
   int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
-      overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 0;
+      overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 1;
   float input_scale = 1.0f;
   void* img[4] = {};
   size_t img_stride[4] = {};
@@ -772,8 +799,8 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   p.tiles_x = tiles_x;
   p.tiles_y = (H + R - 1) / R;
   p.tmem_cols = tmem_cols;
-  p.a_tx = static_cast<uint32_t>((R / 2 + 2) * 2 * kHaloPx * kChunkBytes);   // low-res box
-  p.st_tx = static_cast<uint32_t>((R + 2) * 2 * kHaloPx * kChunkBytes);      // skip plane box
+  p.a_tx = static_cast<uint32_t>((R / 2 + 2) * 2 * kHaloW * kChunkBytes);    // low-res box
+  p.st_tx = static_cast<uint32_t>((R + 2) * 2 * kHaloW * kChunkBytes);       // skip plane box
   p.b_tx = static_cast<uint32_t>(L.sub_ub);                                  // 512 N
   p.b_tx2 = static_cast<uint32_t>(6 * N * kChunkBytes);                      // 96 N
   p.a_stage = static_cast<uint32_t>(round_up_sz(std::max(p.a_tx, p.st_tx), 1024));
@@ -804,9 +831,9 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, static_cast<long>(num_sms()) * blocks)), 1, 1);
   const int c8_0 = round_up(L.c0, 16) / 8;
   const int c8_1 = round_up(L.c1, 16) / 8;
-  OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.pitch, ext0.h, c8_0, kHaloPx, R / 2 + 2,
-                           false, nullptr));
-  OIDNX_TRY(encode_split_map(&T->map1, src1, W, ext1.pitch, H, c8_1, kHaloPx, R + 2));
+  OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.pitch, ext0.h, c8_0, kHaloW, R / 2 + 2,
+                           true, &p.xs0));
+  OIDNX_TRY(encode_split_map(&T->map1, src1, W, ext1.pitch, H, c8_1, kHaloW, R + 2, &p.xs1));
   return ok();
 }
 
@@ -822,7 +849,7 @@ bool use_subpixel(int precision, int W, int H, Extent ext0) {
 oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, Extent ext0,
                              const void* src1, Extent ext1, int W, int H, void* out,
                              int out_pitch, int* status, TcConvLaunch* T, bool subpixel = false,
-                             void* out_split = nullptr) {
+                             void* out_split = nullptr, int out_split_pitch = 0) {
   if (kind == kDecoder && subpixel && L.w16_sub)
     return build_tc_launch_subpixel(L, src0, ext0, src1, ext1, W, H, out, out_pitch, status, T);
   const bool up = kind == kDecoder;
@@ -854,6 +881,7 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   p.mode = kind == kPool ? kEpiReluPool : (kind == kFinal ? kEpiFinal : kEpiRelu);
   p.upsample0 = up ? 1 : 0;
   p.out_split = kind == kPool ? out_split : nullptr;
+  p.split_pitch = out_split_pitch;
   p.tiles_x = tiles_x;
   p.tiles_y = (H + R - 1) / R;
   p.tmem_cols = tmem_cols;
@@ -991,6 +1019,7 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
     P->split_on[i] = f->subpixel && use_subpixel(f->precision, P->lvl[d.level].w,
                                                  P->lvl[d.level].h, P->value_ext[d.src0]);
     P->value_ext[sc.split] = P->value_ext[sc.base];
+    P->value_ext[sc.split].pitch = split_pitch(P->value_ext[sc.base].w);
     P->value_ch[sc.split] = P->value_ch[sc.base];
     last_use[sc.split] = sc.consumer;
   }
@@ -1048,6 +1077,7 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
     Extent e1 = d.src1 >= 0 ? P->value_ext[d.src1] : Extent{0, 0, 0};
     bool subpixel = false;
     void* out_split = nullptr;
+    int out_split_pitch = 0;
     for (int i = 0; i < 4; ++i) {
       if (!P->split_on[i]) continue;
       if (kSplits[i].consumer == l) {
@@ -1055,13 +1085,16 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
         s1 = P->ptr(kSplits[i].split);
         e1 = P->value_ext[kSplits[i].split];
       }
-      if (kSplits[i].producer == l) out_split = P->ptr(kSplits[i].split);
+      if (kSplits[i].producer == l) {
+        out_split = P->ptr(kSplits[i].split);
+        out_split_pitch = P->value_ext[kSplits[i].split].pitch;
+      }
     }
     if (f->precision == OIDNX_PRECISION_FP16) {
       LL.tc = true;
       OIDNX_TRY(build_tc_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, e1, conv.w,
                                 conv.h, P->ptr(d.dst), P->value_ext[d.dst].pitch, f->status,
-                                &LL.tcl, subpixel, out_split));
+                                &LL.tcl, subpixel, out_split, out_split_pitch));
     } else {
       LL.tc = false;
       build_simt_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, conv.w, conv.h,
@@ -1194,6 +1227,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
       pp.fp16 = f->precision == OIDNX_PRECISION_FP16;
       pp.out = P->ptr(V_IN);
       pp.out_split = P->split_on[0] ? P->ptr(V_INS) : nullptr;
+      pp.split_pitch = P->split_on[0] ? P->value_ext[V_INS].pitch : 0;
       pp.chunks = act_chunks(f->precision, f->in_channels);
       pp.pitch = P->value_ext[V_IN].pitch;
       (void)cudaGetLastError();
@@ -1344,6 +1378,7 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     split_on[i] = f->subpixel && use_subpixel(f->precision, lvl[d.level].w, lvl[d.level].h,
                                               ext[d.src0]);
     ext[sc.split] = ext[sc.base];
+    ext[sc.split].pitch = split_pitch(ext[sc.base].w);
     ch[sc.split] = ch[sc.base];
     last_use[sc.split] = sc.consumer;
   }
@@ -1400,6 +1435,7 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     Extent e1 = d.src1 >= 0 ? ext[d.src1] : Extent{0, 0, 0};
     bool subpixel = false;
     void* out_split = nullptr;
+    int out_split_pitch = 0;
     for (int i = 0; i < 4; ++i) {
       if (!split_on[i]) continue;
       if (kSplits[i].consumer == l) {
@@ -1407,13 +1443,16 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
         s1 = ptr(kSplits[i].split);
         e1 = ext[kSplits[i].split];
       }
-      if (kSplits[i].producer == l) out_split = ptr(kSplits[i].split);
+      if (kSplits[i].producer == l) {
+        out_split = ptr(kSplits[i].split);
+        out_split_pitch = ext[kSplits[i].split].pitch;
+      }
     }
     if (f->precision == OIDNX_PRECISION_FP16) {
       LL.tc = true;
       OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, e1, conv.w, conv.h,
                                 ptr(d.dst), ext[d.dst].pitch, f->status, &LL.tcl, subpixel,
-                                out_split));
+                                out_split, out_split_pitch));
     } else {
       LL.tc = false;
       build_simt_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, conv.w, conv.h, ptr(d.dst),

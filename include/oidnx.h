@@ -96,8 +96,8 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *                        upsampled part as parity-class 2x2 taps on the
  *                        low-resolution source (fewer MMAs; weights of one
  *                        class are summed, then rounded to fp16), reading
- *                        parity-split copies of the skip sources; 0 (default)
- *                        builds the upsampled halo in shared memory
+ *                        parity-split copies of the skip sources (default);
+ *                        0 builds the upsampled halo in shared memory
  *   "profile"            1 = record per-kernel events on every execute
  * Errors: INVALID_ARGUMENT for unknown names or out-of-range values.  */
 oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value);
@@ -149,11 +149,11 @@ oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w
  * library.
  *   - Allocates nothing: no cudaMalloc/cudaFree, no plan is created or
  *     cached.  The intermediate activations live in one library-owned
- *     device array of 40 MiB (41943040 bytes), present on every GPU that
+ *     device array of 48 MiB (50331648 bytes), present on every GPU that
  *     loads the library until the process exits.
  *   - Limit: the input must fit that array: fp16 up to 384 x 384 pixels,
  *     fp32 up to 256 x 256 (other shapes: whatever the liveness plan of
- *     the activations fits in 40 MiB).  Larger inputs fail with
+ *     the activations fits in 48 MiB).  Larger inputs fail with
  *     INVALID_ARGUMENT and a message stating the bytes needed.
  *   - packed_in / out: as for oidnx_network_execute (the kernels read the
  *     input and write the output in place, without copies).

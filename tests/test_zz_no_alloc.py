@@ -64,3 +64,20 @@ def test_noalloc_rejects_inputs_beyond_the_array():
     finally:
         ox.oidnx_filter_release(f)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("precision,side", [("fp16", 384), ("fp32", 256)])
+def test_noalloc_accepts_the_documented_maximum(precision, side):
+    """The largest square input the header promises (the fp16 one with the
+    sub-pixel decoders' parity-split copies) runs and writes every output."""
+    prec = ox.PRECISION_FP16 if precision == "fp16" else ox.PRECISION_FP32
+    f = ox.oidnx_filter_create(ox.write_weight_blob(synth.unet_weights(9, bias_scale=0.05)), prec)
+    try:
+        src = _packed(side, side, 3, precision)
+        got = empty_dev(side * side * 16)
+        got.fill_(0xFF)
+        ox.oidnx_network_execute_noalloc(f, src.data_ptr(), side, side, got.data_ptr(), stream())
+        ox.oidnx_filter_sync_status(f)
+        assert np.isfinite(to_host(got, np.float32, (side, side, 4))).all()
+    finally:
+        ox.oidnx_filter_release(f)
