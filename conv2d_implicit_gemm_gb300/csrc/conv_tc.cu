@@ -295,10 +295,20 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
       if (p.KB1 > 0) prefetch_tmap(&map1);
       if (p.resident) {
         if (SP) {
+          // This CTA's tiles all have column parity blockIdx.x & 1 (even
+          // grid): only that parity's half of each upsampled block stays
+          // resident, followed by the skip blocks.
+          const uint8_t* w = reinterpret_cast<const uint8_t*>(p.weights);
+          const uint32_t half = p.b_tx / 2;
+          const uint32_t cpx = blockIdx.x & 1u;
           mbar_arrive_expect_tx(wbar, p.wres_bytes);
-          for (uint32_t off = 0; off < p.wres_bytes; off += 65536u)
-            bulk_load(Wres + off, reinterpret_cast<const uint8_t*>(p.weights) + off,
-                      min(65536u, p.wres_bytes - off), wbar);
+          for (int kb = 0; kb < KB0; ++kb)
+            bulk_load(Wres + static_cast<size_t>(kb) * half,
+                      w + static_cast<size_t>(kb) * p.b_tx + cpx * half, half, wbar);
+          const uint32_t skip = p.wres_bytes - static_cast<uint32_t>(KB0) * half;
+          for (uint32_t off = 0; off < skip; off += 65536u)
+            bulk_load(Wres + static_cast<size_t>(KB0) * half + off,
+                      w + static_cast<size_t>(KB0) * p.b_tx + off, min(65536u, skip - off), wbar);
         } else {
           mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(KB) * p.b_tx);
           for (int kb = 0; kb < KB; ++kb)
@@ -437,13 +447,14 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
             uint32_t woff;
             int pxb;
             if (up) {
-              woff = p.resident ? static_cast<uint32_t>(kb) * p.b_tx : s * p.b_stage;
-              // streamed stages hold only this tile's parity half of an upsampled block
-              pxb = p.resident ? tpx : 0;
+              // resident weights and streamed stages both hold only this
+              // tile's parity half of an upsampled block
+              woff = p.resident ? static_cast<uint32_t>(kb) * (p.b_tx / 2) : s * p.b_stage;
+              pxb = 0;
             } else {
               const int j = (kb - KB0) >> 1, part = (kb - KB0) & 1;
               if (p.resident)
-                woff = static_cast<uint32_t>(KB0) * p.b_tx + static_cast<uint32_t>(3 * j + part) * p.b_tx2;
+                woff = static_cast<uint32_t>(KB0) * (p.b_tx / 2) + static_cast<uint32_t>(3 * j + part) * p.b_tx2;
               else
                 woff = s * p.b_stage;
               // outer plane: kx = 0 then kx = 2 (two slices apart when resident,

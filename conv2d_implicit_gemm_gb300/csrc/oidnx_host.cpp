@@ -809,12 +809,15 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   const int items = L.KB0 + 2 * L.KB1;
   const size_t max_smem = 227 * 1024;
   const size_t fixed = 1024 + static_cast<size_t>((N + 31) / 32) * 32 * 4 + 256;
-  const size_t wbytes = round_up_sz(L.sub_bytes, 1024);
+  // resident: one column parity's half of every upsampled block + the skip blocks
+  const size_t wres = static_cast<size_t>(L.KB0) * (L.sub_ub / 2) +
+                      (L.sub_bytes - static_cast<size_t>(L.KB0) * L.sub_ub);
+  const size_t wbytes = round_up_sz(wres, 1024);
   const int min_stages = std::max(2, std::min(items, 3));
   size_t smem;
   if (fixed + wbytes + min_stages * static_cast<size_t>(p.a_stage) <= max_smem) {
     p.resident = 1;
-    p.wres_bytes = static_cast<uint32_t>(L.sub_bytes);  // bytes loaded; the layout rounds up to 1 KB
+    p.wres_bytes = static_cast<uint32_t>(wres);  // bytes loaded; the layout rounds up to 1 KB
     p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed - wbytes) / p.a_stage));
     smem = fixed + wbytes + p.S * static_cast<size_t>(p.a_stage);
   } else {
@@ -828,7 +831,10 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   OIDNX_TRY(bound_ctas_per_sm(&smem, tmem_cols, &blocks));
   T->smem = smem;
   const long tiles = static_cast<long>(p.tiles_x) * p.tiles_y;
-  T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, static_cast<long>(num_sms()) * blocks)), 1, 1);
+  long grid = std::min<long>(tiles, static_cast<long>(num_sms()) * blocks);
+  // an even grid keeps each CTA on one column parity (tiles alternate parity)
+  if (grid > 1 && grid % 2) --grid;
+  T->grid = dim3(static_cast<unsigned>(grid), 1, 1);
   const int c8_0 = round_up(L.c0, 16) / 8;
   const int c8_1 = round_up(L.c1, 16) / 8;
   OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.pitch, ext0.h, c8_0, kHaloW, R / 2 + 2,
