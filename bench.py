@@ -256,6 +256,7 @@ def run_ours(args):
             ox.oidnx_filter_execute(f, sptr)
             prof = ox.oidnx_get_profile(f)   # waits for this step's events
             prof_steps.append(prof["totalMs"])
+            launches_per_step = sum(l["launches"] for l in prof["layers"])
             for l in prof["layers"]:
                 layer_ms[l["id"]] = layer_ms.get(l["id"], 0.0) + l["ms"]
                 layer_flop[l["id"]] = l["flop"]
@@ -328,7 +329,7 @@ def run_ours(args):
             "layers": layers,
             "e2e": {"value": e2e_value, "unit": "MP/s", "h2d_bytes_per_step": 3 * px * 16,
                     "d2h_bytes_per_step": px * 16, "ms_per_step": e2e_mean},
-            "gpu_launches": steps * tiles * 18,
+            "gpu_launches": steps * launches_per_step,
             "profiled_ms_per_step": float(np.mean(prof_steps)),
             "layers_note": "per-kernel times from the profiled steps (event after every kernel)",
             "clocks": clocks.summary(),
