@@ -31,16 +31,20 @@ __device__ __forceinline__ float sanitize(float v, float lo, float hi) {
 constexpr double kLn2 = 0.69314718055994530942;
 
 // F(s) = log2(1 + s), s in [0, FLT_MAX], correctly rounded to fp16.
-// The float estimate y (log1pf is within 1 ulp, so y is within 3 ulp of
-// F(s)) decides the code unless y(1 -+ 2^-20) round differently.  Then the
+// The float estimate y is within 2^-22 (relative) of F(s): log1pf is within
+// 1 ulp (2^-23), the rounded constant log2(e) and the product add 2^-24
+// each.  y decides the code unless y(1 -+ 1.5 * 2^-22) round differently
+// (the bracket also covers the rounding of those two products).  Then the
 // rounding boundary b between the two candidate codes (exact in float) is
 // compared through the monotone inverse instead: F(s) >= b <=> s >= 2^b - 1,
 // with 2^b - 1 from exp2f/expm1f (a few ulp).  Only when s lies within
-// 2^-18 (relative) of that value is F evaluated in double precision.
+// 2^-18 (relative) of that value is F evaluated in double precision.  The
+// bracket is kept tight because FP64 is slow on this GPU and one lane on
+// the double path holds up its whole warp.
 __device__ __forceinline__ __half hdr_forward_f16(float s) {
   const float y = log1pf(s) * 1.44269504088896341f;
-  const __half lo = __float2half_rn(y * (1.0f - 0x1p-20f));
-  const __half hi = __float2half_rn(y * (1.0f + 0x1p-20f));
+  const __half lo = __float2half_rn(y * (1.0f - 0x1.8p-22f));
+  const __half hi = __float2half_rn(y * (1.0f + 0x1.8p-22f));
   if (__half_as_ushort(lo) == __half_as_ushort(hi)) return lo;
   const float b = 0.5f * (__half2float(lo) + __half2float(hi));
   const float c = b < 1.0f ? expm1f(b * 0.693147180559945309f) : exp2f(b) - 1.0f;
