@@ -440,7 +440,9 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
           if (KIND == kTcExpand && w) w = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
           ok = __all_sync(0xffffffffu, w);
           if (!ok) break;
-          tc_fence_after();
+          // (no tcgen05 fence: the stage barrier orders the TMA / expansion
+          // writes before these MMA reads; the accumulator release below is
+          // the one that orders TMEM accesses of other threads)
           if (SP) {
             const bool up = kb < KB0;
             const uint32_t soff = (s * p.a_stage) >> 4;
