@@ -160,8 +160,8 @@ __device__ __forceinline__ void issue_kblock_r(int R, uint64_t ad, uint64_t bd, 
 // two values selected by px (A shifted by d + px pixels).
 template <int R, int G>
 __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
-                                         int px, int pxb, uint32_t id1, uint32_t id2,
-                                         uint32_t id3, uint32_t id4) {
+                                         int px, int pxb, uint32_t row16, uint32_t id1,
+                                         uint32_t id2, uint32_t id3, uint32_t id4) {
 #pragma unroll
   for (int d = 0; d < 2; ++d) {
     const uint64_t adk = ad + static_cast<uint32_t>(d + px);
@@ -170,7 +170,7 @@ __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbas
     for (int hl = 0; hl < R / 2 + 2; ++hl) {
       const int lo = 2 * hl - 3 > 0 ? 2 * hl - 3 : 0;
       const int hi = 2 * hl < R - 1 ? 2 * hl : R - 1;
-      const uint64_t a = adk + static_cast<uint32_t>(hl * 2 * kHaloW);
+      const uint64_t a = adk + static_cast<uint32_t>(hl) * row16;
 #pragma unroll
       for (int c = lo; c <= hi; c += G) {
         const int e = c + G - 1 < hi ? c + G - 1 : hi;
@@ -188,12 +188,12 @@ __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbas
 // as in issue_kblock.
 template <int R, int G>
 __device__ __forceinline__ void issue_skip(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
-                                           uint32_t id1, uint32_t id2, uint32_t id3) {
+                                           uint32_t row16, uint32_t id1, uint32_t id2, uint32_t id3) {
 #pragma unroll
   for (int h = 0; h < R + 2; ++h) {
     const int lo = h - 2 > 0 ? h - 2 : 0;
     const int hi = h < R - 1 ? h : R - 1;
-    const uint64_t a = ad + static_cast<uint32_t>(h * 2 * kHaloW);
+    const uint64_t a = ad + static_cast<uint32_t>(h) * row16;
 #pragma unroll
     for (int c = lo; c <= hi; c += G) {
       const int e = c + G - 1 < hi ? c + G - 1 : hi;
@@ -207,26 +207,26 @@ __device__ __forceinline__ void issue_skip(uint64_t ad, uint64_t bd, uint32_t db
 template <int R, int G4, int G3>
 __device__ __forceinline__ void issue_subpixel_r(bool up, uint64_t ad, uint64_t bd,
                                                  uint32_t dbase, uint32_t N, int px, int pxb,
-                                                 uint32_t id1, uint32_t id2, uint32_t id3,
-                                                 uint32_t id4) {
+                                                 uint32_t row16, uint32_t id1, uint32_t id2,
+                                                 uint32_t id3, uint32_t id4) {
   if (!up) {
     // bd: first kx slice; pxb (reused): 16-byte units to the second slice, 0 if none
-    issue_skip<R, G3>(ad, bd, dbase, N, id1, id2, id3);
-    if (pxb) issue_skip<R, G3>(ad + 1, bd + static_cast<uint32_t>(pxb), dbase, N, id1, id2, id3);
+    issue_skip<R, G3>(ad, bd, dbase, N, row16, id1, id2, id3);
+    if (pxb) issue_skip<R, G3>(ad + 1, bd + static_cast<uint32_t>(pxb), dbase, N, row16, id1, id2, id3);
   } else {
-    issue_up<R, G4>(ad, bd, dbase, N, px, pxb, id1, id2, id3, id4);
+    issue_up<R, G4>(ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4);
   }
 }
 
 template <int G4, int G3>
 __device__ __forceinline__ void issue_subpixel_item(int R, bool up, uint64_t ad, uint64_t bd,
                                                     uint32_t dbase, uint32_t N, int px, int pxb,
-                                                    uint32_t id1, uint32_t id2, uint32_t id3,
-                                                    uint32_t id4) {
+                                                    uint32_t row16, uint32_t id1, uint32_t id2,
+                                                    uint32_t id3, uint32_t id4) {
   switch (R) {
-    case 2: issue_subpixel_r<2, G4, G3>(up, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
-    case 4: issue_subpixel_r<4, G4, G3>(up, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
-    default: issue_subpixel_r<8, G4, G3>(up, ad, bd, dbase, N, px, pxb, id1, id2, id3, id4); break;
+    case 2: issue_subpixel_r<2, G4, G3>(up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4); break;
+    case 4: issue_subpixel_r<4, G4, G3>(up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4); break;
+    default: issue_subpixel_r<8, G4, G3>(up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4); break;
   }
 }
 
@@ -246,7 +246,10 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
   constexpr bool SP = KIND == kTcSubpixel;
   // pipeline items per tile: K blocks, or (sub-pixel) upsampled K blocks plus
   // one item per (skip K block, kx)
-  const int items = SP ? KB0 + 2 * p.KB1 : KB;
+  // sub-pixel: items are groups of up_pair upsampled K blocks (one TMA box
+  // of 2 * up_pair chunks), then one item per (skip K block, plane)
+  const int n_up = SP ? (KB0 + p.up_pair - 1) / p.up_pair : KB0;
+  const int items = SP ? n_up + 2 * p.KB1 : KB;
   // shared memory: [resident weights][A stages][B stages][staging][bias][barriers]
   uint8_t* Wres = smem;
   uint8_t* A = Wres + (p.resident ? ((p.wres_bytes + 1023u) & ~1023u) : 0u);
@@ -332,12 +335,14 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
           }
           if (SP) {
             const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(p.weights);
-            if (kb < KB0) {
+            if (kb < n_up) {
               const uint32_t half = p.b_tx / 2;  // one column parity of the block
               mbar_arrive_expect_tx(&full[s], p.a_tx + (p.resident ? 0u : half));
-              // low-resolution box from kGroupPx left of the block's first pixel
+              // low-resolution box from kGroupPx left of the block's first
+              // pixel (up_pair K blocks; a box reaching past the last chunk
+              // reads zeros there, and no MMA uses them)
               tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map0, &full[s], 0,
-                          ((x0 >> 1) - kGroupPx) >> p.xs0, 2 * kb, (y0 >> 1) - 1);
+                          ((x0 >> 1) - kGroupPx) >> p.xs0, 2 * p.up_pair * kb, (y0 >> 1) - 1);
               if (!p.resident)
                 bulk_load(B + static_cast<size_t>(s) * p.b_stage,
                           wsrc + static_cast<size_t>(kb) * p.b_tx + static_cast<size_t>(px) * half,
@@ -347,7 +352,7 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
               // px ^ 1, serving kx = 0 and kx = 2) or the centre plane
               // (parity px, kx = 1) of one 16-channel block, from kGroupPx
               // entries left of the block's first entry
-              const int j = (kb - KB0) >> 1, part = (kb - KB0) & 1;
+              const int j = (kb - n_up) >> 1, part = (kb - n_up) & 1;
               const int plane = part ? px : (px ^ 1);
               const int i0 = ((x0 >> 1) - kGroupPx) >> p.xs1;
               const uint32_t wb = part ? p.b_tx2 : 2u * p.b_tx2;
@@ -444,17 +449,33 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
           // writes before these MMA reads; the accumulator release below is
           // the one that orders TMEM accesses of other threads)
           if (SP) {
-            const bool up = kb < KB0;
+            const bool up = kb < n_up;
             const uint32_t soff = (s * p.a_stage) >> 4;
             uint32_t woff;
             int pxb;
             if (up) {
               // resident weights and streamed stages both hold only this
               // tile's parity half of an upsampled block
-              woff = p.resident ? static_cast<uint32_t>(kb) * (p.b_tx / 2) : s * p.b_stage;
-              pxb = 0;
+              const uint32_t half = p.b_tx / 2;
+              const int kb0 = kb * p.up_pair;
+              woff = p.resident ? static_cast<uint32_t>(kb0) * half : s * p.b_stage;
+              // one item covers up_pair K blocks: their chunks sit 2 * kHaloW
+              // entries apart in each box row, their weights one half apart
+              const uint64_t ad = a_up0 + soff + static_cast<uint32_t>(kHaloOff);
+              const uint64_t bd = b_up0 + (woff >> 4);
+              const uint32_t row16 = static_cast<uint32_t>(2 * p.up_pair * kHaloW);
+              const int nkb = min(p.up_pair, KB0 - kb0);
+              for (int jj = 0; jj < nkb; ++jj) {
+                const uint64_t adj = ad + static_cast<uint32_t>(jj * 2 * kHaloW);
+                const uint64_t bdj = bd + static_cast<uint32_t>(jj) * (half >> 4);
+                if (g4 == 4) issue_subpixel_item<4, 3>(R, true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
+                else if (g4 == 2) issue_subpixel_item<2, 2>(R, true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
+                else issue_subpixel_item<1, 1>(R, true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
+              }
+              if (elect_one()) mma_commit(&empty[s]);
+              continue;
             } else {
-              const int j = (kb - KB0) >> 1, part = (kb - KB0) & 1;
+              const int j = (kb - n_up) >> 1, part = (kb - n_up) & 1;
               if (p.resident)
                 woff = static_cast<uint32_t>(KB0) * (p.b_tx / 2) + static_cast<uint32_t>(3 * j + part) * p.b_tx2;
               else
@@ -465,12 +486,13 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
             }
             // upsampled: x0/2 - 1 at kHaloOff; skip: the centre plane's first
             // entry at kGroupPx, the outer plane's x0/2 + px - 1 at kHaloOff + px
-            const int aoff = up ? kHaloOff : ((kb - KB0) & 1 ? kGroupPx : kHaloOff + tpx);
+            const int aoff = (kb - n_up) & 1 ? kGroupPx : kHaloOff + tpx;
             const uint64_t ad = a_up0 + soff + static_cast<uint32_t>(aoff);
-            const uint64_t bd = (up ? b_up0 : b_sk0) + (woff >> 4);
-            if (g4 == 4) issue_subpixel_item<4, 3>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4);
-            else if (g4 == 2) issue_subpixel_item<2, 2>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4);
-            else issue_subpixel_item<1, 1>(R, up, ad, bd, d_base, N, tpx, pxb, id1, id2, id3, id4);
+            const uint64_t bd = b_sk0 + (woff >> 4);
+            const uint32_t row16 = static_cast<uint32_t>(2 * kHaloW);
+            if (g4 == 4) issue_subpixel_item<4, 3>(R, false, ad, bd, d_base, N, tpx, pxb, row16, id1, id2, id3, id4);
+            else if (g4 == 2) issue_subpixel_item<2, 2>(R, false, ad, bd, d_base, N, tpx, pxb, row16, id1, id2, id3, id4);
+            else issue_subpixel_item<1, 1>(R, false, ad, bd, d_base, N, tpx, pxb, row16, id1, id2, id3, id4);
             if (elect_one()) mma_commit(&empty[s]);
             continue;
           }

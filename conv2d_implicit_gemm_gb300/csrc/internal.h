@@ -63,6 +63,7 @@ struct TcConvParams {
   int split_pitch;
   int pitch;               // fp16 output row pitch in pixels (>= output width);
                            // columns [width, pitch) are written as zeros
+  int up_pair;             // sub-pixel: upsampled K blocks per pipeline item (1 or 2)
   int xs0, xs1;            // log2 pixels per x unit of map0 / map1: 3 for
                            // 128-byte rows (pitch % 8 == 0), 0 for 16-byte rows
 };

@@ -480,7 +480,7 @@ EncodeTiledFn get_encode_fn() {
 // otherwise it is one pixel (16 B, *xs = 0).  The box is box_w pixels (a
 // multiple of 8 for the 8-pixel form) x 2 channel chunks x box_h rows.
 oidnx_status encode_act_map(CUtensorMap* map, const void* base, int W, int pitch, int H, int C8,
-                            int box_w, int box_h, bool allow_groups, int* xs) {
+                            int box_w, int box_h, bool allow_groups, int* xs, int box_c = 2) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   const bool groups = allow_groups && pitch % kGroupPx == 0 && box_w % kGroupPx == 0;
@@ -502,7 +502,7 @@ oidnx_status encode_act_map(CUtensorMap* map, const void* base, int W, int pitch
   }
   dims[2] = static_cast<cuuint64_t>(C8);
   dims[3] = static_cast<cuuint64_t>(H);
-  box[2] = 2;
+  box[2] = static_cast<cuuint32_t>(box_c);
   box[3] = static_cast<cuuint32_t>(box_h);
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides,
@@ -799,6 +799,7 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   p.tiles_x = tiles_x;
   p.tiles_y = (H + R - 1) / R;
   p.tmem_cols = tmem_cols;
+  p.up_pair = 1;
   p.a_tx = static_cast<uint32_t>((R / 2 + 2) * 2 * kHaloW * kChunkBytes);    // low-res box
   p.st_tx = static_cast<uint32_t>((R + 2) * 2 * kHaloW * kChunkBytes);       // skip plane box
   p.b_tx = static_cast<uint32_t>(L.sub_ub);                                  // 512 N
@@ -815,6 +816,15 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   const size_t wbytes = round_up_sz(wres, 1024);
   const int min_stages = std::max(2, std::min(items, 3));
   size_t smem;
+  // resident weights: pairs of upsampled K blocks per item (one wait and one
+  // commit per pair) when at least three stages of the wider box still fit
+  const uint32_t a_tx_pair = static_cast<uint32_t>((R / 2 + 2) * 4 * kHaloW * kChunkBytes);
+  const uint32_t a_stage_pair = static_cast<uint32_t>(round_up_sz(std::max(a_tx_pair, p.st_tx), 1024));
+  if (L.KB0 >= 2 && fixed + wbytes + 3 * static_cast<size_t>(a_stage_pair) <= max_smem) {
+    p.up_pair = 2;
+    p.a_tx = a_tx_pair;
+    p.a_stage = a_stage_pair;
+  }
   if (fixed + wbytes + min_stages * static_cast<size_t>(p.a_stage) <= max_smem) {
     p.resident = 1;
     p.wres_bytes = static_cast<uint32_t>(wres);  // bytes loaded; the layout rounds up to 1 KB
@@ -838,7 +848,7 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   const int c8_0 = round_up(L.c0, 16) / 8;
   const int c8_1 = round_up(L.c1, 16) / 8;
   OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.pitch, ext0.h, c8_0, kHaloW, R / 2 + 2,
-                           true, &p.xs0));
+                           true, &p.xs0, 2 * p.up_pair));
   OIDNX_TRY(encode_split_map(&T->map1, src1, W, ext1.pitch, H, c8_1, kHaloW, R + 2, &p.xs1));
   return ok();
 }
