@@ -831,6 +831,13 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
     p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed - wbytes) / p.a_stage));
     smem = fixed + wbytes + p.S * static_cast<size_t>(p.a_stage);
   } else {
+    // streamed weights: each stage holds one upsampled K block's weights,
+    // so an item is one K block
+    if (p.up_pair != 1) {
+      p.up_pair = 1;
+      p.a_tx = static_cast<uint32_t>((R / 2 + 2) * 2 * kHaloW * kChunkBytes);
+      p.a_stage = static_cast<uint32_t>(round_up_sz(std::max(p.a_tx, p.st_tx), 1024));
+    }
     p.resident = 0;
     const size_t stage = static_cast<size_t>(p.a_stage) + p.b_stage;
     p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed) / stage));
