@@ -111,12 +111,19 @@ __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_
   if (elect_one()) mma_f16_ss(d, a, b, idesc, 1u);
 }
 
+// fp16 (kind::f16) or tf32 (kind::tf32) MMA by the elected lane.
+template <bool TF>
+__device__ __forceinline__ void umma_k(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+  if (!TF) umma(d, a, b, idesc);
+  else if (elect_one()) mma_tf32_ss(d, a, b, idesc);
+}
+
 // All MMAs of one K block for a tile of R rows, fully unrolled so that the
 // issuing warp spends a handful of instructions per MMA (its instruction
 // stream, not the tensor core, is otherwise the bottleneck).  Halo row h
 // updates output rows lo..hi = max(0,h-2)..min(R-1,h) with the ky-stacked B
 // block; rows are grouped G at a time (N = rows x Cout <= 256).
-template <int R, int G>
+template <int R, int G, bool TF>
 __device__ __forceinline__ void issue_kblock(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
                                              uint32_t kx_b16, uint32_t id1, uint32_t id2,
                                              uint32_t id3) {
@@ -133,21 +140,44 @@ __device__ __forceinline__ void issue_kblock(uint64_t ad, uint64_t bd, uint32_t 
 #pragma unroll
       for (int c = lo; c <= hi; c += G) {
         const int e = c + G - 1 < hi ? c + G - 1 : hi;
-        umma(dbase + c * N, a, bdk + (2 - h + c) * N, idn[e - c + 1]);
+        umma_k<TF>(dbase + c * N, a, bdk + (2 - h + c) * N, idn[e - c + 1]);
       }
     }
   }
 }
 
-template <int G>
+template <int G, bool TF>
+__device__ __forceinline__ void issue_kblock_r1(int R, uint64_t ad, uint64_t bd, uint32_t dbase,
+                                                uint32_t N, uint32_t kx_b16, uint32_t id1,
+                                                uint32_t id2, uint32_t id3) {
+  switch (R) {
+    case 1: issue_kblock<1, G, TF>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
+    case 2: issue_kblock<2, G, TF>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
+    case 4: issue_kblock<4, G, TF>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
+    default: issue_kblock<8, G, TF>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
+  }
+}
+
+// One K block.  fp32 storage (TF): each product A * B as three tf32 MMAs,
+// A*B_hi + A*B_lo + A_lo*B_hi, issued as three passes over the K block.  The
+// stage holds A_hi (A rounded to the nearest tf32 value) and, alo16 units
+// further, A_lo = A - A_hi; the weights hold B_hi and, blo16 units further,
+// B_lo.  The omitted A_lo*B_lo term and the tf32 precision of the lo parts
+// leave a relative error near 2^-21 per product.
+template <int G, bool TF>
 __device__ __forceinline__ void issue_kblock_r(int R, uint64_t ad, uint64_t bd, uint32_t dbase,
                                                uint32_t N, uint32_t kx_b16, uint32_t id1,
-                                               uint32_t id2, uint32_t id3) {
-  switch (R) {
-    case 1: issue_kblock<1, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
-    case 2: issue_kblock<2, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
-    case 4: issue_kblock<4, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
-    default: issue_kblock<8, G>(ad, bd, dbase, N, kx_b16, id1, id2, id3); break;
+                                               uint32_t id2, uint32_t id3, uint32_t alo16,
+                                               uint32_t blo16) {
+  if (!TF) {
+    issue_kblock_r1<G, TF>(R, ad, bd, dbase, N, kx_b16, id1, id2, id3);
+    return;
+  }
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const uint64_t a = ad + (pass == 2 ? alo16 : 0u);
+    const uint64_t b = bd + (pass == 1 ? blo16 : 0u);
+    issue_kblock_r1<G, TF>(R, a, b, dbase, N, kx_b16, id1, id2, id3);
   }
 }
 
@@ -232,8 +262,13 @@ __device__ __forceinline__ void issue_subpixel_item(int R, bool up, uint64_t ad,
 
 }  // namespace
 
+// 3xTF32 kinds (fp32 storage) and kinds with the four helper warps
+template <int KIND> __host__ __device__ constexpr bool kind_tf32() { return KIND == kTcPlain32 || KIND == kTcExpand32; }
+template <int KIND> __host__ __device__ constexpr bool kind_expand() { return KIND == kTcExpand || KIND == kTcExpand32; }
+template <int KIND> __host__ __device__ constexpr bool kind_helpers() { return kind_tf32<KIND>() || kind_expand<KIND>(); }
+
 template <int KIND>
-__global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThreads, 1)
+__global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTcThreads, 1)
     conv3x3_tc_kernel(const __grid_constant__ CUtensorMap map0,
                       const __grid_constant__ CUtensorMap map1, const TcConvParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -244,16 +279,21 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
   const int KB = p.KB0 + p.KB1;
   const int num_tiles = p.tiles_x * p.tiles_y;
   constexpr bool SP = KIND == kTcSubpixel;
+  constexpr bool TF = kind_tf32<KIND>();
+  constexpr bool EXP = kind_expand<KIND>();
+  constexpr bool HELP = kind_helpers<KIND>();
   // pipeline items per tile: K blocks, or (sub-pixel) upsampled K blocks plus
   // one item per (skip K block, kx)
   // sub-pixel: items are groups of up_pair upsampled K blocks (one TMA box
   // of 2 * up_pair chunks), then one item per (skip K block, plane)
   const int n_up = SP ? (KB0 + p.up_pair - 1) / p.up_pair : KB0;
   const int items = SP ? n_up + 2 * p.KB1 : KB;
-  // shared memory: [resident weights][A stages][B stages][staging][bias][barriers]
+  // shared memory: [resident weights][A stages][A_lo stages (tf32)][B stages]
+  // [staging][bias][barriers]
   uint8_t* Wres = smem;
   uint8_t* A = Wres + (p.resident ? ((p.wres_bytes + 1023u) & ~1023u) : 0u);
-  uint8_t* B = A + static_cast<size_t>(S) * p.a_stage;
+  uint8_t* ALO = A + static_cast<size_t>(S) * p.a_stage;
+  uint8_t* B = ALO + (TF ? static_cast<size_t>(S) * p.a_stage : 0u);
   uint8_t* ST = B + (p.resident ? 0 : static_cast<size_t>(S) * p.b_stage);
   float* bias_s = reinterpret_cast<float*>(ST + static_cast<size_t>(S) * p.st_stage);
   uint64_t* full = reinterpret_cast<uint64_t*>(bias_s + ((N + 31) / 32) * 32);
@@ -407,10 +447,16 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
     {
       const int g = min(3, 256 / N);
       const int g4 = min(4, 256 / N);
-      const uint32_t id1 = idesc_f16_f32(kTileM, N);
-      const uint32_t id2 = idesc_f16_f32(kTileM, min(2 * N, 256));
-      const uint32_t id3 = idesc_f16_f32(kTileM, min(3 * N, 256));
+      const uint32_t id1 = TF ? idesc_tf32_f32(kTileM, N) : idesc_f16_f32(kTileM, N);
+      const uint32_t id2 = TF ? idesc_tf32_f32(kTileM, min(2 * N, 256))
+                              : idesc_f16_f32(kTileM, min(2 * N, 256));
+      const uint32_t id3 = TF ? idesc_tf32_f32(kTileM, min(3 * N, 256))
+                              : idesc_f16_f32(kTileM, min(3 * N, 256));
       const uint32_t id4 = idesc_f16_f32(kTileM, min(4 * N, 256));
+      // tf32: the A_lo stages follow the A stages; each K block's B_lo
+      // follows its B_hi (half of the block)
+      const uint32_t alo16 = TF ? (static_cast<uint32_t>(S) * p.a_stage) >> 4 : 0u;
+      const uint32_t blo16 = TF ? (p.b_tx / 2) >> 4 : 0u;
       // sub-pixel boxes: rows of kHaloW entries starting kGroupPx left of the
       // block (low-resolution x0/2 - 1 at kHaloOff)
       const uint64_t a_up0 = smem_desc_noswizzle(smem_u32(A), kHaloW * kChunkBytes, 128);
@@ -442,7 +488,7 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
         tile_origin_k<KIND>(p, tile, &tx0, &ty0, &tpx);
         for (int kb = 0; kb < items; ++kb, ++it, next_stage(s, ph, S)) {
           bool w = mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutMma);
-          if (KIND == kTcExpand && w) w = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
+          if (HELP && w) w = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
           ok = __all_sync(0xffffffffu, w);
           if (!ok) break;
           // (no tcgen05 fence: the stage barrier orders the TMA / expansion
@@ -498,9 +544,9 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
           }
           const uint64_t ad = a_desc0 + ((s * p.a_stage) >> 4);
           const uint64_t bd = b_desc0 + ((static_cast<uint32_t>(p.resident ? kb : s) * p.b_stage) >> 4);
-          if (g == 3) issue_kblock_r<3>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3);
-          else if (g == 2) issue_kblock_r<2>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3);
-          else issue_kblock_r<1>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3);
+          if (g == 3) issue_kblock_r<3, TF>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, alo16, blo16);
+          else if (g == 2) issue_kblock_r<2, TF>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, alo16, blo16);
+          else issue_kblock_r<1, TF>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, alo16, blo16);
           if (elect_one()) mma_commit(&empty[s]);
         }
         if (!ok) break;
@@ -512,8 +558,13 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
     }
     __syncwarp();
   } else if (warp >= 2 + kTcEpilogueWarps) {
-    // (only launched with these warps for KIND == kTcExpand)
-    // ------------------------------------------------------------ upsampled halo
+    // (only launched with these warps for the expansion and tf32 kinds)
+    // ------------------------------------------------------------ helpers
+    // Expansion kinds: build the upsampled halo of each upsampled K block
+    // from its low-resolution staging box.  tf32 kinds: split every stage's
+    // A into A_hi (rounded to tf32, in place) and A_lo = A - A_hi (the A_lo
+    // stage).  Only the kHaloPx pixels the MMAs read (x0 - 1
+    // .. x0 + 128) of each row are touched.
     const int et = threadIdx.x - 32 * (2 + kTcEpilogueWarps);  // 0..127
     const int total = (R + 2) * 2 * kHaloPx;
     uint32_t it = 0, s = 0, ph = 0;
@@ -529,21 +580,38 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
           ok = false;
           break;
         }
-        if (kb < KB0) {
+        uint4* dst = reinterpret_cast<uint4*>(A + static_cast<size_t>(s) * p.a_stage);
+        uint4* lo = reinterpret_cast<uint4*>(ALO + static_cast<size_t>(s) * p.a_stage);
+        const bool expand = EXP && kb < KB0;
+        if (expand || TF) {
           const uint4* src = reinterpret_cast<const uint4*>(ST + static_cast<size_t>(s) * p.st_stage);
-          uint4* dst = reinterpret_cast<uint4*>(A + static_cast<size_t>(s) * p.a_stage);
-          // only the kHaloPx pixels the MMAs read (x0 - 1 .. x0 + 128)
           for (int i = et; i < total; i += 128) {
             const int px = i % kHaloPx;
             const int rc = i / kHaloPx;
-            const int j = rc & 1, rr = rc >> 1;
-            const int iy = y0 - 1 + rr, ix = x0 - 1 + px;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (iy >= 0 && iy < p.H && ix >= 0 && ix < p.W) {
-              const int sr = (iy >> 1) - ly0, sc = (ix >> 1) - lx0;
-              v = src[(sr * 2 + j) * kLowW + sc];
+            const int at = rc * kHaloW + kHaloOff + px;
+            uint4 v;
+            if (expand) {
+              const int j = rc & 1, rr = rc >> 1;
+              const int iy = y0 - 1 + rr, ix = x0 - 1 + px;
+              v = make_uint4(0u, 0u, 0u, 0u);
+              if (iy >= 0 && iy < p.H && ix >= 0 && ix < p.W) {
+                const int sr = (iy >> 1) - ly0, sc = (ix >> 1) - lx0;
+                v = src[(sr * 2 + j) * kLowW + sc];
+              }
+            } else {
+              v = dst[at];
             }
-            dst[rc * kHaloW + kHaloOff + px] = v;
+            if (TF) {
+              // hi: rounded to the nearest tf32 value, so |lo| <= 2^-11 |A|
+              const uint4 h = make_uint4((v.x + 0x1000u) & 0xFFFFE000u, (v.y + 0x1000u) & 0xFFFFE000u,
+                                         (v.z + 0x1000u) & 0xFFFFE000u, (v.w + 0x1000u) & 0xFFFFE000u);
+              lo[at] = make_uint4(__float_as_uint(__uint_as_float(v.x) - __uint_as_float(h.x)),
+                                  __float_as_uint(__uint_as_float(v.y) - __uint_as_float(h.y)),
+                                  __float_as_uint(__uint_as_float(v.z) - __uint_as_float(h.z)),
+                                  __float_as_uint(__uint_as_float(v.w) - __uint_as_float(h.w)));
+              v = h;
+            }
+            dst[at] = v;
           }
           fence_proxy_async_smem();
         }
@@ -588,7 +656,7 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
       const uint32_t tl = tmem + lane_off + buf * set_cols;
 
       // decoders (expansion, sub-pixel) always take the ReLU epilogue
-      if (KIND != kTcPlain || p.mode == kEpiRelu) {
+      if (EXP || SP || p.mode == kEpiRelu) {
         __half* out = static_cast<__half*>(p.out);
         for (int c0 = 0; c0 < nc; c0 += 2) {
           const bool two = c0 + 1 < nc;
@@ -602,7 +670,26 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
             tmem_fill_bias(t0, bias_s + c0 * 16);
             if (two) tmem_fill_bias(t0 + 16, bias_s + c0 * 16 + 16);
             // columns [W, pitch) are row padding: stored as zeros
-            if (x < p.pitch && y < p.H) {
+            if (TF && x < p.pitch && y < p.H) {
+              const bool pad = x >= p.W;
+              float* row = static_cast<float*>(p.out) + (static_cast<size_t>(y) * p.out_c4 * p.pitch + x) * 4;
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                if (b == 1 && !two) break;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+                  if (!pad)
+                    f = make_float4(fmaxf(__uint_as_float(v[b][4 * q4]), 0.0f),
+                                    fmaxf(__uint_as_float(v[b][4 * q4 + 1]), 0.0f),
+                                    fmaxf(__uint_as_float(v[b][4 * q4 + 2]), 0.0f),
+                                    fmaxf(__uint_as_float(v[b][4 * q4 + 3]), 0.0f));
+                  const int c4 = 4 * (c0 + b) + q4;
+                  if (c4 < p.out_c4)
+                    *reinterpret_cast<float4*>(row + static_cast<size_t>(c4) * p.pitch * 4) = f;
+                }
+              }
+            } else if (!TF && x < p.pitch && y < p.H) {
               const bool pad = x >= p.W;
               __half* row = out + (static_cast<size_t>(y) * C8 * p.pitch + x) * 8;
 #pragma unroll
@@ -648,7 +735,17 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
               mx[k] = t;
             }
             // pooled columns [Wp, pitch) are row padding: stored as zeros
-            if (((lane & 1) == 0) && yp < Hp) {
+            if (TF && ((lane & 1) == 0) && yp < Hp && xp < p.pitch) {
+              const bool pad = xp >= Wp;
+              float* base = static_cast<float*>(p.out) + (static_cast<size_t>(yp) * p.out_c4 * p.pitch + xp) * 4;
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 f = pad ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                     : make_float4(mx[4 * q4], mx[4 * q4 + 1], mx[4 * q4 + 2], mx[4 * q4 + 3]);
+                if (4 * c + q4 < p.out_c4)
+                  *reinterpret_cast<float4*>(base + (4 * c + q4) * static_cast<size_t>(p.pitch) * 4) = f;
+              }
+            } else if (!TF && ((lane & 1) == 0) && yp < Hp) {
               const bool pad = xp >= Wp;
               uint32_t h[8];
 #pragma unroll
@@ -674,10 +771,10 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
       } else {
         float4* out = static_cast<float4*>(p.out);
         for (int r0 = sub; r0 < R; r0 += 8) {
-          uint32_t v[4][16];
+          uint32_t v[4][4];  // the 3 output channels and the zero lane
 #pragma unroll
           for (int b = 0; b < 4; ++b)
-            if (r0 + 2 * b < R) tmem_ld16_nowait(tl + static_cast<uint32_t>((r0 + 2 * b) * N), v[b]);
+            if (r0 + 2 * b < R) tmem_ld4_nowait(tl + static_cast<uint32_t>((r0 + 2 * b) * N), v[b]);
           tmem_wait_ld();
 #pragma unroll
           for (int b = 0; b < 4; ++b)
@@ -707,6 +804,12 @@ __global__ void __launch_bounds__(KIND == kTcExpand ? kTcThreadsDecoder : kTcThr
 }
 
 cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
+  if (L.kind == kTcPlain32)
+    return launch_pdl(conv3x3_tc_kernel<kTcPlain32>, L.grid, dim3(kTcThreadsDecoder), L.smem,
+                      stream, L.map0, L.map1, L.p);
+  if (L.kind == kTcExpand32)
+    return launch_pdl(conv3x3_tc_kernel<kTcExpand32>, L.grid, dim3(kTcThreadsDecoder), L.smem,
+                      stream, L.map0, L.map1, L.p);
   if (L.kind == kTcExpand)
     return launch_pdl(conv3x3_tc_kernel<kTcExpand>, L.grid, dim3(kTcThreadsDecoder), L.smem,
                       stream, L.map0, L.map1, L.p);
@@ -723,6 +826,12 @@ cudaError_t conv_tc_set_smem_limit(size_t bytes) {
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcSubpixel>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcPlain32>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcExpand32>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(conv3x3_tc_kernel<kTcPlain>,

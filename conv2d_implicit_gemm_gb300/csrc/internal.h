@@ -24,7 +24,7 @@ constexpr int kHaloOff = kGroupPx - 1;           // 7
 constexpr int kChunkBytes = 16;            // one 16-byte channel block
 constexpr int kTcEpilogueWarps = 8;        // two per TMEM lane quarter
 constexpr int kTcThreads = 320;            // 10 warps: TMA, MMA, 8 x epilogue
-constexpr int kTcThreadsDecoder = 448;     // + 4 warps building the upsampled halo
+constexpr int kTcThreadsDecoder = 448;     // + 4 helper warps (upsampled halo, tf32 split)
 
 enum EpilogueMode : int {
   kEpiRelu = 0,      // bias + ReLU, fp16 store
@@ -34,7 +34,8 @@ enum EpilogueMode : int {
 
 // Parameters of one tensor-core conv launch (one layer).
 struct TcConvParams {
-  const __half* weights;   // packed B operand, [kb][tap][2][N][8] halves
+  const __half* weights;   // packed B operand, [kb][tap][2][N][8] halves (fp32 kinds:
+                           // [kb][hi, lo][tap][2][N][4] floats)
   const float* bias;       // [N] (zero padded)
   void* out;               // fp16 [Ho][N/8][Wo][8] or f32 [H][W][4]
   int* status;             // device error word
@@ -64,6 +65,8 @@ struct TcConvParams {
   int pitch;               // fp16 output row pitch in pixels (>= output width);
                            // columns [width, pitch) are written as zeros
   int up_pair;             // sub-pixel: upsampled K blocks per pipeline item (1 or 2)
+  int out_c4;              // fp32 storage: 4-channel chunks of the output value
+                           // (Cout rounded up to 4; may be fewer than N / 4)
   int xs0, xs1;            // log2 pixels per x unit of map0 / map1: 3 for
                            // 128-byte rows (pitch % 8 == 0), 0 for 16-byte rows
 };
@@ -72,6 +75,8 @@ enum TcKind : int {
   kTcPlain = 0,     // plain conv (also pool / final epilogues)
   kTcExpand = 1,    // decoder, upsampled halo built in shared memory
   kTcSubpixel = 2,  // decoder, upsampled part as parity-class 2x2 taps
+  kTcPlain32 = 3,   // fp32 storage, 3xTF32 products: plain conv
+  kTcExpand32 = 4,  // fp32 storage, 3xTF32 products: decoder with expansion
 };
 
 struct TcConvLaunch {
@@ -106,22 +111,6 @@ cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream);
 cudaError_t conv_tc_set_smem_limit(size_t bytes);
 cudaError_t conv_tc_occupancy(size_t smem, int* blocks_per_sm);
 
-// Parameters of one fp32 CUDA-core conv launch (one layer).
-struct SimtConvParams {
-  const float* src0;       // [H0][C40][W0][4]
-  const float* src1;       // [H][C41][W][4] or null
-  const float* weights;    // [groups][9][K4*4][8]
-  const float* bias;       // [groups*8]
-  float* out;              // [Ho][Cout4][Wo][4] or [H][W][4] (final)
-  int W, H;                // conv extent
-  int W0, H0;              // source 0 extent
-  int C40, C41;            // 4-lane chunks per source
-  int cout4;               // output chunks
-  int groups;              // output groups of 8 lanes
-  int mode;                // EpilogueMode
-  int upsample0;
-};
-cudaError_t launch_conv_simt(const SimtConvParams& p, cudaStream_t stream);
 
 // Input pass of one tile.
 struct PackParams {

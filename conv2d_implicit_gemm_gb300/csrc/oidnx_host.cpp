@@ -291,6 +291,44 @@ std::vector<uint16_t> pack_weights_tc(const ConvTensors& L, int c0, int c1, int*
   return out;
 }
 
+// fp32 storage: the B operand for 3xTF32 products.  K blocks of 8 channels
+// (two 16-byte chunks of 4 lanes) over each source padded to 4 lanes; per
+// block [hi, lo][kx][j][pos][N][4] floats with pos = 2 - ky, where hi is the
+// weight rounded to the nearest tf32 value and lo = w - hi (exact).
+std::vector<float> pack_weights_tf32(const ConvTensors& L, int c0, int c1, int* KB0, int* KB1,
+                                     int* N) {
+  const int q0 = round_up(c0, 4) / 4, q1 = c1 > 0 ? round_up(c1, 4) / 4 : 0;  // chunks
+  *KB0 = (q0 + 1) / 2;
+  *KB1 = (q1 + 1) / 2;
+  *N = round_up(L.cout, 16);
+  const int KB = *KB0 + *KB1;
+  std::vector<float> out(static_cast<size_t>(KB) * 2 * 9 * 2 * (*N) * 4, 0.0f);
+  for (int kb = 0; kb < KB; ++kb)
+    for (int kx = 0; kx < 3; ++kx)
+      for (int j = 0; j < 2; ++j)
+        for (int pos = 0; pos < 3; ++pos)
+          for (int n = 0; n < L.cout; ++n)
+            for (int l = 0; l < 4; ++l) {
+              const bool first = kb < *KB0;
+              const int ci = ((first ? kb : kb - *KB0) * 2 + j) * 4 + l;  // within the source
+              if (ci >= (first ? c0 : c1)) continue;
+              const int ch = first ? ci : c0 + ci;
+              const int ky = 2 - pos;
+              const float w = L.w[(static_cast<size_t>(n) * L.cin + ch) * 9 + ky * 3 + kx];
+              uint32_t bits;
+              std::memcpy(&bits, &w, 4);
+              bits = (bits + 0x1000u) & 0xFFFFE000u;  // nearest tf32 value
+              float hi;
+              std::memcpy(&hi, &bits, 4);
+              for (int part = 0; part < 2; ++part) {
+                const size_t idx =
+                    ((((((static_cast<size_t>(kb) * 2 + part) * 3 + kx) * 2 + j) * 3 + pos) * (*N) + n) * 4) + l;
+                out[idx] = part == 0 ? hi : w - hi;
+              }
+            }
+  return out;
+}
+
 // Sub-pixel decoder B operand.  Upsampled K blocks (source 0): per block
 // [px][d][j][pos][N][8] where, for output column parity px, d selects the
 // low-resolution column offset dx = d - 1 + px and pos the (row parity py,
@@ -356,32 +394,6 @@ std::vector<uint16_t> pack_weights_subpixel(const ConvTensors& L, int c0, int c1
   return out;
 }
 
-// fp32 CUDA-core weights: [group of 8 outputs][tap][K lane][8 outputs], K lanes
-// enumerate the concatenated sources each padded to a multiple of 4.
-std::vector<float> pack_weights_simt(const ConvTensors& L, int c0, int c1, int* C40, int* C41,
-                                     int* groups) {
-  const int p0 = round_up(c0, 4), p1 = c1 > 0 ? round_up(c1, 4) : 0;
-  *C40 = p0 / 4;
-  *C41 = p1 / 4;
-  *groups = (L.cout + 7) / 8;
-  const int K = p0 + p1;
-  std::vector<float> out(static_cast<size_t>(*groups) * 9 * K * 8, 0.0f);
-  for (int g = 0; g < *groups; ++g)
-    for (int t = 0; t < 9; ++t)
-      for (int v = 0; v < K; ++v) {
-        int ch = -1;
-        if (v < p0) ch = v < c0 ? v : -1;
-        else ch = (v - p0) < c1 ? c0 + (v - p0) : -1;
-        if (ch < 0) continue;
-        for (int o = 0; o < 8; ++o) {
-          const int n = g * 8 + o;
-          if (n >= L.cout) continue;
-          out[((static_cast<size_t>(g) * 9 + t) * K + v) * 8 + o] =
-              L.w[(static_cast<size_t>(n) * L.cin + ch) * 9 + t];
-        }
-      }
-  return out;
-}
 
 // ---------------------------------------------------------------- tiles
 struct AxisTile {
@@ -564,14 +576,12 @@ oidnx_status encode_split_map(CUtensorMap* map, const void* base, int W, int pit
 struct DeviceLayer {
   int cout = 0, cin = 0, c0 = 0, c1 = 0;
   // fp16 path
-  void* w16 = nullptr;  // packed B operand
+  void* wtc = nullptr;  // packed tensor-core B operand (fp16, or tf32 hi/lo for fp32)
+  bool tf32 = false;    // fp32 storage: 3xTF32 products
   int KB0 = 0, KB1 = 0, N = 0;
   void* w16_sub = nullptr;  // sub-pixel decoder B operand (decoders only)
   size_t sub_bytes = 0, sub_ub = 0;
-  // fp32 path
-  float* w32 = nullptr;
-  int C40 = 0, C41 = 0, groups = 0;
-  float* bias = nullptr;  // [max(N, groups*8)]
+  float* bias = nullptr;  // [N]
   size_t weight_bytes = 0;
 };
 
@@ -589,9 +599,7 @@ int split_pitch(int w) { return (w + 2 * kGroupPx - 1) / (2 * kGroupPx) * (2 * k
 
 struct LayerLaunch {
   int layer;
-  bool tc;
   TcConvLaunch tcl;
-  SimtConvParams sp;
   double flop;   // logical conv FLOPs
   double bytes;  // algorithmic bytes: inputs read once, output written once
 };
@@ -675,11 +683,9 @@ oidnx_status upload(const void* host, size_t bytes, void** dev) {
 void free_layer(DeviceLayer& L) {
   cudaFree(L.w16_sub);
   L.w16_sub = nullptr;
-  cudaFree(L.w16);
-  cudaFree(L.w32);
+  cudaFree(L.wtc);
   cudaFree(L.bias);
-  L.w16 = nullptr;
-  L.w32 = nullptr;
+  L.wtc = nullptr;
   L.bias = nullptr;
 }
 
@@ -692,7 +698,7 @@ oidnx_status make_device_layer(const ConvTensors& T, int c0, int c1, int precisi
   if (precision == OIDNX_PRECISION_FP16) {
     std::vector<uint16_t> w = pack_weights_tc(T, c0, c1, &L->KB0, &L->KB1, &L->N);
     if (L->N > 256) return fail(OIDNX_ERR_UNSUPPORTED, "more than 256 output channels");
-    OIDNX_TRY(upload(w.data(), w.size() * 2, &L->w16));
+    OIDNX_TRY(upload(w.data(), w.size() * 2, &L->wtc));
     if (c1 > 0) {
       std::vector<uint16_t> ws = pack_weights_subpixel(T, c0, c1, L->N, &L->sub_ub);
       L->sub_bytes = ws.size() * 2;
@@ -703,9 +709,11 @@ oidnx_status make_device_layer(const ConvTensors& T, int c0, int c1, int precisi
     OIDNX_TRY(upload(b.data(), b.size() * 4, reinterpret_cast<void**>(&L->bias)));
     L->weight_bytes = w.size() * 2 + b.size() * 4 + L->sub_bytes;
   } else {
-    std::vector<float> w = pack_weights_simt(T, c0, c1, &L->C40, &L->C41, &L->groups);
-    OIDNX_TRY(upload(w.data(), w.size() * 4, reinterpret_cast<void**>(&L->w32)));
-    std::vector<float> b(L->groups * 8, 0.0f);
+    std::vector<float> w = pack_weights_tf32(T, c0, c1, &L->KB0, &L->KB1, &L->N);
+    if (L->N > 256) return fail(OIDNX_ERR_UNSUPPORTED, "more than 256 output channels");
+    OIDNX_TRY(upload(w.data(), w.size() * 4, &L->wtc));
+    L->tf32 = true;
+    std::vector<float> b(L->N, 0.0f);
     std::copy(T.b.begin(), T.b.end(), b.begin());
     OIDNX_TRY(upload(b.data(), b.size() * 4, reinterpret_cast<void**>(&L->bias)));
     L->weight_bytes = w.size() * 4 + b.size() * 4;
@@ -868,7 +876,8 @@ bool use_subpixel(int precision, int W, int H, Extent ext0) {
 }
 
 // src0/src1: sources with their extents (pitch included); (W, H): conv
-// extent; out: destination with row pitch out_pitch (fp16 values).
+// extent; out: destination with row pitch out_pitch.  fp16 layers, or fp32
+// layers (L.tf32) whose products are formed as three tf32 MMAs.
 oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, Extent ext0,
                              const void* src1, Extent ext1, int W, int H, void* out,
                              int out_pitch, int* status, TcConvLaunch* T, bool subpixel = false,
@@ -876,7 +885,7 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   if (kind == kDecoder && subpixel && L.w16_sub)
     return build_tc_launch_subpixel(L, src0, ext0, src1, ext1, W, H, out, out_pitch, status, T);
   const bool up = kind == kDecoder;
-  T->kind = up ? kTcExpand : kTcPlain;
+  T->kind = up ? (L.tf32 ? kTcExpand32 : kTcExpand) : (L.tf32 ? kTcPlain32 : kTcPlain);
   const int N = L.N;
   const int minR = (kind == kPool || kind == kDecoder) ? 2 : 1;
   // Two accumulator sets of R x N fp32 columns must fit the 512 TMEM columns.
@@ -890,7 +899,7 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
 
   TcConvParams& p = T->p;
   std::memset(&p, 0, sizeof(p));
-  p.weights = static_cast<const __half*>(L.w16);
+  p.weights = static_cast<const __half*>(L.wtc);
   p.bias = L.bias;
   p.out = out;
   p.pitch = out_pitch;
@@ -903,13 +912,15 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   p.R = R;
   p.mode = kind == kPool ? kEpiReluPool : (kind == kFinal ? kEpiFinal : kEpiRelu);
   p.upsample0 = up ? 1 : 0;
+  p.out_c4 = round_up(L.cout, 4) / 4;
   p.out_split = kind == kPool ? out_split : nullptr;
   p.split_pitch = out_split_pitch;
   p.tiles_x = tiles_x;
   p.tiles_y = (H + R - 1) / R;
   p.tmem_cols = tmem_cols;
   p.a_tx = static_cast<uint32_t>((R + 2) * 2 * kHaloW * kChunkBytes);
-  p.b_tx = static_cast<uint32_t>(9 * 2 * N * kChunkBytes);
+  // a K block of B: 9 taps x 2 chunks x N rows of 16 bytes (tf32: hi, then lo)
+  p.b_tx = static_cast<uint32_t>((L.tf32 ? 2 : 1) * 9 * 2 * N * kChunkBytes);
   p.st_tx = up ? static_cast<uint32_t>((R / 2 + 2) * 2 * kLowW * kChunkBytes) : 0u;
   p.a_stage = static_cast<uint32_t>(round_up_sz(p.a_tx, 1024));
   p.b_stage = static_cast<uint32_t>(round_up_sz(p.b_tx, 1024));
@@ -919,7 +930,8 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   // alignment slack + bias + barriers
   const size_t fixed = 1024 + static_cast<size_t>((N + 31) / 32) * 32 * 4 + 256;
   const size_t wbytes = static_cast<size_t>(KB) * p.b_stage;
-  const size_t a_st = static_cast<size_t>(p.a_stage) + p.st_stage;
+  // per stage: A (and for tf32 its A_lo split), low-resolution staging
+  const size_t a_st = static_cast<size_t>(p.a_stage) * (L.tf32 ? 2 : 1) + p.st_stage;
   const int min_stages = std::min(KB, 3) < 2 ? 2 : std::min(KB, 3);
   size_t smem;
   if (fixed + wbytes + min_stages * a_st <= max_smem) {
@@ -955,11 +967,13 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   const long tiles = static_cast<long>(p.tiles_x) * p.tiles_y;
   T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, static_cast<long>(num_sms()) * blocks)), 1, 1);
 
-  const int c8_0 = round_up(L.c0, 16) / 8;
+  // 16-byte chunks per pixel of each source: 8 halves, or 4 floats
+  auto chunks = [&](int c) { return L.tf32 ? round_up(c, 4) / 4 : round_up(c, 16) / 8; };
+  const int c8_0 = chunks(L.c0);
   OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.pitch, ext0.h, c8_0,
                            up ? kLowW : kHaloW, up ? R / 2 + 2 : R + 2, true, &p.xs0));
   if (L.KB1 > 0) {
-    const int c8_1 = round_up(L.c1, 16) / 8;
+    const int c8_1 = chunks(L.c1);
     OIDNX_TRY(encode_act_map(&T->map1, src1, ext1.w, ext1.pitch, ext1.h, c8_1, kHaloW, R + 2, true,
                              &p.xs1));
   } else {
@@ -969,29 +983,9 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   return ok();
 }
 
-void build_simt_launch(const DeviceLayer& L, int kind, const void* src0, Extent ext0,
-                       const void* src1, int W, int H, void* out, SimtConvParams* p) {
-  std::memset(p, 0, sizeof(*p));
-  p->src0 = static_cast<const float*>(src0);
-  p->src1 = static_cast<const float*>(src1);
-  p->weights = L.w32;
-  p->bias = L.bias;
-  p->out = static_cast<float*>(out);
-  p->W = W;
-  p->H = H;
-  p->W0 = ext0.w;
-  p->H0 = ext0.h;
-  p->C40 = L.C40;
-  p->C41 = L.C41;
-  p->cout4 = (L.cout + 3) / 4;
-  p->groups = L.groups;
-  p->mode = kind == kPool ? kEpiReluPool : (kind == kFinal ? kEpiFinal : kEpiRelu);
-  p->upsample0 = kind == kDecoder ? 1 : 0;
-}
-
 oidnx_status run_launch(const LayerLaunch& L, cudaStream_t s) {
   (void)cudaGetLastError();  // drop a stale, non-sticky error of an earlier call
-  cudaError_t e = L.tc ? launch_conv_tc(L.tcl, s) : launch_conv_simt(L.sp, s);
+  cudaError_t e = launch_conv_tc(L.tcl, s);
   if (e != cudaSuccess)
     return fail(OIDNX_ERR_CUDA, "%s launch: %s", kLayerNames[L.layer], cudaGetErrorString(e));
   return ok();
@@ -1113,16 +1107,9 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
         out_split_pitch = P->value_ext[kSplits[i].split].pitch;
       }
     }
-    if (f->precision == OIDNX_PRECISION_FP16) {
-      LL.tc = true;
-      OIDNX_TRY(build_tc_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, e1, conv.w,
-                                conv.h, P->ptr(d.dst), P->value_ext[d.dst].pitch, f->status,
-                                &LL.tcl, subpixel, out_split, out_split_pitch));
-    } else {
-      LL.tc = false;
-      build_simt_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, conv.w, conv.h,
-                        P->ptr(d.dst), &LL.sp);
-    }
+    OIDNX_TRY(build_tc_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, e1, conv.w,
+                              conv.h, P->ptr(d.dst), P->value_ext[d.dst].pitch, f->status,
+                              &LL.tcl, subpixel, out_split, out_split_pitch));
     const double px = static_cast<double>(conv.w) * conv.h;
     LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
     const int bpe = f->precision == OIDNX_PRECISION_FP16 ? 2 : 4;
@@ -1471,16 +1458,9 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
         out_split_pitch = ext[kSplits[i].split].pitch;
       }
     }
-    if (f->precision == OIDNX_PRECISION_FP16) {
-      LL.tc = true;
-      OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, e1, conv.w, conv.h,
-                                ptr(d.dst), ext[d.dst].pitch, f->status, &LL.tcl, subpixel,
-                                out_split, out_split_pitch));
-    } else {
-      LL.tc = false;
-      build_simt_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, conv.w, conv.h, ptr(d.dst),
-                        &LL.sp);
-    }
+    OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, e1, conv.w, conv.h,
+                              ptr(d.dst), ext[d.dst].pitch, f->status, &LL.tcl, subpixel,
+                              out_split, out_split_pitch));
     OIDNX_TRY(run_launch(LL, s));
   }
   return ok();
@@ -1964,15 +1944,9 @@ oidnx_status oidnx_conv_execute(oidnx_conv* c, const void* in, void* out, int w,
   LayerLaunch LL;
   std::memset(&LL, 0, sizeof(LL));
   LL.layer = 0;
-  if (c->precision == OIDNX_PRECISION_FP16) {
-    LL.tc = true;
-    // caller's buffers: rows of w pixels (128-byte TMA rows when w % 8 == 0)
-    OIDNX_TRY(build_tc_launch(c->L, kPlain, in, Extent{w, h, w}, nullptr, Extent{0, 0, 0}, w, h,
-                              out, w, c->status, &LL.tcl));
-  } else {
-    LL.tc = false;
-    build_simt_launch(c->L, kPlain, in, Extent{w, h, w}, nullptr, w, h, out, &LL.sp);
-  }
+  // caller's buffers: rows of w pixels (128-byte TMA rows when w % 8 == 0)
+  OIDNX_TRY(build_tc_launch(c->L, kPlain, in, Extent{w, h, w}, nullptr, Extent{0, 0, 0}, w, h,
+                            out, w, c->status, &LL.tcl));
   return run_launch(LL, s);
 }
 

@@ -180,6 +180,18 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
          | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
 }
 
+// Instruction descriptor for kind::tf32 with tf32 A/B (32-bit containers of
+// which the MMA uses sign, exponent and 10 mantissa bits), fp32 D, both
+// K-major.  One MMA covers K = 8.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int m, int n) {
+  return (1u << 4)                                  // D format: f32
+         | (2u << 7)                                // A format: tf32
+         | (2u << 10)                               // B format: tf32
+         | (0u << 15) | (0u << 16)                  // A, B K-major
+         | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
@@ -201,6 +213,17 @@ __device__ __forceinline__ bool elect_one() {
       "@px mov.s32 %0, 1;\n\t}"
       : "+r"(pred));
   return pred != 0;
+}
+
+// D[tmem] += A[smem] * B[smem]^T with tf32 operands.
+__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(1u)
+      : "memory");
 }
 
 // Arrive on `bar` once all previously issued tcgen05.mma of this thread end.
@@ -238,6 +261,14 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[1
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
+}
+
+// 32 lanes x 4 consecutive 32-bit columns, no wait.
+__device__ __forceinline__ void tmem_ld4_nowait(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

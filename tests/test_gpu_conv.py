@@ -1,4 +1,4 @@
-"""Single conv layer on the GPU (tcgen05 fp16 path and fp32 CUDA-core path)
+"""Single conv layer on the GPU (tcgen05 fp16 path and the 3xTF32 fp32 path)
 against the oracle, element by element, through the C ABI."""
 
 import numpy as np

@@ -53,8 +53,13 @@ def test_config_128x128_fp32_full_image():
     ref = unet.denoise(imgs, weights, hdr=True, precision="fp32")
     ref_net = unet.forward(passes.pack_tile(imgs, (0, 0, w, h), True, 1.0, "fp32"),
                            weights, "fp32")
+    # the stated fp32 bound applies to the network (per layer, and here to its
+    # output); the output pass F^-1(y) = 2^y - 1 scales relative errors by its
+    # condition number y ln2 / (1 - 2^-y), so the image gets that factor
     assert rel_l2(net, ref_net) <= 1e-4
-    assert rel_l2(out[..., :3], ref[..., :3]) <= 1e-4
+    y = np.clip(ref_net.astype(np.float64), 1e-6, None)
+    kappa = float((y * np.log(2.0) / (1.0 - 2.0 ** -y)).max())
+    assert rel_l2(out[..., :3], ref[..., :3]) <= 1e-4 * kappa
     assert np.array_equal(out[..., 3].view(np.uint32), imgs[0][..., 3].view(np.uint32))
 
 

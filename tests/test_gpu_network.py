@@ -98,3 +98,30 @@ def test_network_one_pixel_and_tiny_inputs():
         _, final = _run_network(weights, x, "fp16")
         ref = unet.forward(x, weights, "fp16")
         assert np.abs(final[..., :3] - ref).max() <= 2e-2
+
+
+@pytest.mark.parametrize("precision", ["fp16", "fp32"])
+@pytest.mark.parametrize("in_channels", [3, 6])
+def test_colour_only_and_colour_albedo_models_match_oracle(precision, in_channels):
+    """The 3- and 6-channel model variants (colour; colour + albedo): the
+    input block and dec_conv1a's skip have fewer lanes.  Every stored
+    activation is checked in isolation, the output end to end."""
+    weights = synth.unet_weights(in_channels, bias_scale=0.05)
+    w, h = 130, 36
+    x = round_storage(synth.uniform_activations(h, w, in_channels, seed=in_channels, low=0, high=1),
+                      precision)
+    acts_flat, final = _run_network(weights, x, precision, subpixel=1 if precision == "fp16" else 0)
+    ref = unet.forward(x, weights, precision, keep=True)
+    acts = []
+    for k, name in enumerate(VALUE_NAMES):
+        shape = ref[name].shape if k < 16 else ref["dec_conv0"].shape
+        acts.append(acts_flat[k].reshape(shape))
+    tol = 1e-2 if precision == "fp16" else 1e-4
+    for k in range(1, 17):
+        err = rel_l2(acts[k], _isolated(k, acts, weights, precision))
+        assert err <= tol, (VALUE_NAMES[k], err)
+    out = ref["dec_conv0"]
+    if precision == "fp16":
+        assert np.abs(final[..., :3] - out).max() <= 2e-2
+    else:
+        assert rel_l2(final[..., :3], out) <= 1e-4
