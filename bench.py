@@ -29,6 +29,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "U-Net denoise megapixels/s at 1080p fp16 on 1 GB300; conv TFLOP/s vs FP16 peak"
+# --precision fp32: the same workload with fp32 storage (3xTF32 products)
+METRIC_FP32 = "U-Net denoise megapixels/s at 1080p fp32 (3xTF32) on 1 GB300; conv TFLOP/s vs TF32 peak / 3"
 WIDTH, HEIGHT = 1920, 1080
 WORKLOAD = "OIDN-shaped U-Net denoise, 1920x1080 HDR colour+albedo+normal (9 ch), fp16, single tile"
 CPU_CROP = 768          # oracle sample: a 768x768 crop denoised as one tile
@@ -120,7 +122,7 @@ def _cpu_threads():
     return os.cpu_count()
 
 
-def cpu_oracle_sample(steps=1):
+def cpu_oracle_sample(steps=1, precision="fp16"):
     """Oracle denoise of a CPU_CROP x CPU_CROP crop of the bench inputs."""
     import synth
     from oracle import unet
@@ -129,13 +131,13 @@ def cpu_oracle_sample(steps=1):
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        unet.denoise(imgs, weights, hdr=True, input_scale=1.0, precision="fp16")
+        unet.denoise(imgs, weights, hdr=True, input_scale=1.0, precision=precision)
         times.append(time.perf_counter() - t0)
     px = CPU_CROP * CPU_CROP
     return {"value": px / 1e6 / float(np.mean(times)), "unit": "MP/s", "cores": _cpu_threads(),
             "kind": "oracle",
             "sample": f"oracle (numpy float64) denoise of one {CPU_CROP}x{CPU_CROP} crop of the "
-                      f"1920x1080 inputs as one tile, fp16 storage; {steps} run(s)",
+                      f"1920x1080 inputs as one tile, {precision} storage; {steps} run(s)",
             "seconds": float(np.mean(times))}
 
 
@@ -170,9 +172,10 @@ def run_reference(args):
         return
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state; warm-up steps do no work
-    cpu = cpu_oracle_sample(args.steps)
+    cpu = cpu_oracle_sample(args.steps, args.precision)
     line = {
-        "impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "MP/s",
+        "impl": "reference", "metric": METRIC_FP32 if args.precision == "fp32" else METRIC,
+        "value": cpu["value"], "unit": "MP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": cpu["seconds"] * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -201,7 +204,9 @@ def run_ours(args):
 
     imgs = synth.denoise_inputs(WIDTH, HEIGHT, 3, hdr=True)
     weights = synth.unet_weights(9)
-    f = ox.oidnx_filter_create(ox.write_weight_blob(weights), ox.PRECISION_FP16)
+    fp32 = args.precision == "fp32"
+    f = ox.oidnx_filter_create(ox.write_weight_blob(weights),
+                               ox.PRECISION_FP32 if fp32 else ox.PRECISION_FP16)
     d_imgs = [torch.from_numpy(im).cuda() for im in imgs]
     d_out = torch.zeros((HEIGHT, WIDTH, 4), dtype=torch.float32, device="cuda")
     for i, t in enumerate(d_imgs):
@@ -293,6 +298,9 @@ def run_ours(args):
     conv_flop = sum(layer_flop[k] for k in conv_ids)
     peaks = _peaks()
     tensor_peak = peaks["bf16_tflops_sustained"]   # fp16 dense rate = bf16 dense rate
+    if fp32:
+        # tf32 dense rate = bf16 rate x nominal 1.1 / 2.25; three tf32 MMAs per product
+        tensor_peak *= (1.1 / 2.25) / 3.0
     top = max(conv_ids, key=lambda k: avg[k])
     top_flop, top_bytes = layer_flop[top], layer_bytes[top]
     ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -303,24 +311,28 @@ def run_ours(args):
         roof = {"kernel": top, "bound": "hbm", "achieved": top_bytes / (avg[top] * 1e-3) / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = TRAFFIC.get(top)
+    roof["traffic"] = None if fp32 else TRAFFIC.get(top)
     roof["traffic_unit"] = "bytes per launch (ncu dram read + write)"
-    roof["peak_source"] = peaks["source"] + (" sustained bf16 (dense fp16 = bf16 rate)"
-                                             if roof["bound"] == "tensor" else " HBM copy")
+    roof["peak_source"] = peaks["source"] + (
+        (" sustained bf16 x tf32/bf16 nominal ratio (1.1/2.25) / 3 (three tf32 MMAs per product)"
+         if fp32 else " sustained bf16 (dense fp16 = bf16 rate)")
+        if roof["bound"] == "tensor" else " HBM copy")
     roof["launch_ms"] = avg[top] / tiles
     layers = {k: {"ms": round(avg[k], 5),
                   "tflops": round(layer_flop[k] / (avg[k] * 1e-3) / 1e12, 2) if layer_flop[k] else None,
                   "gbs": round(layer_bytes[k] / (avg[k] * 1e-3) / 1e9, 1)} for k in avg}
 
     if rank == 0:
-        cpu = cpu_oracle_sample(1) if world == 1 else None
+        cpu = cpu_oracle_sample(1, args.precision) if world == 1 else None
         line = {
-            "metric": METRIC, "value": value, "unit": "MP/s", "n_gpus": world,
+            "metric": METRIC_FP32 if fp32 else METRIC, "value": value, "unit": "MP/s", "n_gpus": world,
             "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "width": WIDTH, "height": HEIGHT, "tiles": tiles,
-                       "precision": "fp16 storage, fp32 accumulate", "hdr": True,
+            "dtype": "f32" if fp32 else "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD.replace("fp16", "fp32") if fp32 else WORKLOAD,
+                       "width": WIDTH, "height": HEIGHT, "tiles": tiles,
+                       "precision": ("fp32 storage, 3xTF32 products, fp32 accumulate" if fp32
+                                     else "fp16 storage, fp32 accumulate"), "hdr": True,
                        "transfer": "log", "l2": "flushed (256 MiB write) before every step",
                        "parallelism": f"replicas x{world}"},
             "conv_tflops": conv_flop / (conv_ms * 1e-3) / 1e12,
@@ -356,6 +368,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--precision", choices=["fp16", "fp32"], default="fp16",
+                    help="activation storage (fp32: 3xTF32 products); the headline is fp16")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
