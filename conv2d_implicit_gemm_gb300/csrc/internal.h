@@ -127,8 +127,16 @@ struct PackParams {
   int chunks;              // 16-byte chunks per pixel
   void* out_split;         // optional parity-split copy [th][chunks][2][split_pitch/2][lanes]
   int split_pitch;         // its pitch (a multiple of 16), columns >= tw zero
+  const float4* log2_tab;  // fp32 HDR: kLog2TabSize entries from fill_log2_table
 };
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
+
+// Reduction table of the fp32 log transfer: entry j covers mantissas
+// m in [1 + j/512, 1 + (j+1)/512) and holds {r_j, -log2(r_j) as a float
+// pair (hi, lo), 0}; r_j (a multiple of 2^-10, r_0 = 1) is close enough to
+// 1/m that m * r_j - 1 is exact in float.
+constexpr int kLog2TabSize = 512;
+void fill_log2_table(float (*tab)[4]);
 
 // Output pass of one tile.
 struct UnpackParams {

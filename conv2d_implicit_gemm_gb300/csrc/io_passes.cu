@@ -11,8 +11,10 @@
 // The input pass stores F correctly rounded to the storage precision (see
 // hdr_forward_f16: float estimate, exact decision near rounding boundaries
 // through the inverse, double precision only when that decision is too
-// close to call; fp32 storage evaluates F in double precision).
+// close to call; hdr_forward_f32: a float-float evaluation of F that decides
+// the fp32 rounding unless it is too close to call, then double precision).
 #include <cfloat>
+#include <cmath>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -53,8 +55,80 @@ __device__ __forceinline__ __half hdr_forward_f16(float s) {
   return __double2half(log1p(static_cast<double>(s)) / kLn2);
 }
 
-// F(s) rounded to fp32 from a double-precision evaluation.
-__device__ __forceinline__ float hdr_forward_f32(float s) {
+// Error-free transformations on floats (Knuth's two-sum; the product
+// remainder via one fused multiply-add).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ float pow2_neg(int k) {  // 2^-k, 0 <= k <= 126
+  return __int_as_float((127 - k) << 23);
+}
+
+// F(s) = log2(1 + s), s in [0, FLT_MAX], correctly rounded to fp32.
+//  1. 1 + s = uh + ul exactly (fast two-sum), uh = m 2^e with m in [1, 2);
+//     ml = ul 2^-e exactly, so 1 + s = 2^e (m + ml).
+//  2. A table entry r ~ 1/m (indexed by the top 9 mantissa bits) gives
+//     w = (m + ml) r - 1 as a float pair: z = m r - 1 is exact (r is a
+//     multiple of 2^-10 and |z| < 2^-9), ml r is split by an FMA.
+//  3. ln(1 + w) by its Taylor series, |w| < 2^-9: w - w^2/2 kept exactly as
+//     a pair, the terms from w^3/3 up to w^6/6 in float, plus the first-order
+//     terms in the low part of w.
+//  4. F = e + (-log2 r) + ln(1 + w) log2(e), summed as float pairs.
+// The pair y + yl is within 2^-40.3 |F| of F for s < 2^-9 (the float error
+// of the w^3/3 term dominates there) and within 2^-42.9 |F| otherwise.  If
+// y + yl -+ tol (tol = 2^-38 resp. 2^-41 of |y|) round to the same float,
+// that float is the correctly rounded F; else, and for 0 < s < 2^-60 where
+// the result may be subnormal, F is evaluated in double precision.
+__device__ __forceinline__ float hdr_forward_f32(float s, const float4* __restrict__ tab) {
+  if (s < 0x1p-60f) {
+    if (s == 0.0f) return 0.0f;
+    return __double2float_rn(log1p(static_cast<double>(s)) / kLn2);
+  }
+  const float a = fmaxf(s, 1.0f), b = fminf(s, 1.0f);
+  const float uh = __fadd_rn(a, b);
+  const float ul = __fsub_rn(b, __fsub_rn(uh, a));
+  const uint32_t bits = __float_as_uint(uh);
+  const int e = static_cast<int>(bits >> 23) - 127;
+  const float m = __uint_as_float((bits & 0x7FFFFFu) | 0x3F800000u);
+  const float ml = __fmul_rn(__fmul_rn(ul, pow2_neg(e >> 1)), pow2_neg(e - (e >> 1)));
+  const int j = static_cast<int>((bits >> 14) & 0x1FFu);
+  const float4 t = __ldg(tab + j);  // {r, -log2 r hi, lo, 0}
+  const float z = __fmaf_rn(m, t.x, -1.0f);
+  const float q = __fmul_rn(ml, t.x);
+  const float ql = __fmaf_rn(ml, t.x, -q);
+  float wh, wl;
+  two_sum(z, q, wh, wl);
+  wl = __fadd_rn(wl, ql);
+  // ln(1 + w) = Lh + Ll
+  const float p = __fmul_rn(wh, wh);
+  const float pl = __fmaf_rn(wh, wh, -p);
+  float poly = __fmaf_rn(wh, -1.0f / 6.0f, 0.2f);
+  poly = __fmaf_rn(wh, poly, -0.25f);
+  poly = __fmaf_rn(wh, poly, 1.0f / 3.0f);
+  const float tail = __fmul_rn(__fmul_rn(wh, p), poly);
+  float Lh, Ll;
+  two_sum(wh, -0.5f * p, Lh, Ll);
+  // first-order terms of wl: wl (1 - w), and -pl/2 from w^2/2
+  const float corr = __fsub_rn(__fmaf_rn(-0.5f, pl, wl), __fmul_rn(__fmul_rn(wh, wl), 1.0f - wh));
+  Ll = __fadd_rn(Ll, __fadd_rn(tail, corr));
+  // times log2(e) = Ch + Cl
+  constexpr float Ch = 0x1.715476p+0f;
+  constexpr float Cl = 0x1.4ae0cp-26f;
+  const float Ph = __fmul_rn(Lh, Ch);
+  const float Pl = __fadd_rn(__fmaf_rn(Lh, Ch, -Ph), __fadd_rn(__fmul_rn(Lh, Cl), __fmul_rn(Ll, Ch)));
+  float s1h, s1l, s2h, s2l;
+  two_sum(static_cast<float>(e), t.y, s1h, s1l);
+  two_sum(s1h, Ph, s2h, s2l);
+  const float lo = __fadd_rn(__fadd_rn(s1l, s2l), __fadd_rn(t.z, Pl));
+  const float y = __fadd_rn(s2h, lo);
+  const float yl = __fsub_rn(lo, __fsub_rn(y, s2h));
+  const float tol = y * ((e == 0 && j == 0) ? 0x1p-38f : 0x1p-41f);
+  const float y0 = __fadd_rn(y, __fsub_rn(yl, tol));
+  const float y1 = __fadd_rn(y, __fadd_rn(yl, tol));
+  if (y0 == y1) return y0;
   return __double2float_rn(log1p(static_cast<double>(s)) / kLn2);
 }
 
@@ -150,7 +224,7 @@ __global__ void pack_kernel(const PackParams p) {
     float v[12];
 #pragma unroll
     for (int k = 0; k < 12; ++k)
-      v[k] = k < kCh ? ((HDR && k < 3) ? hdr_forward_f32(ch[k]) : ch[k]) : 0.0f;
+      v[k] = k < kCh ? ((HDR && k < 3) ? hdr_forward_f32(ch[k], p.log2_tab) : ch[k]) : 0.0f;
     float4* out = static_cast<float4*>(p.out);
 #pragma unroll
     for (int j = 0; j < (kCh + 3) / 4; ++j)
@@ -255,9 +329,26 @@ cudaError_t launch_pack_s(const PackParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream) {
+  if (!p.fp16 && p.hdr && !p.log2_tab) return cudaErrorInvalidValue;
   if (p.sources == 1) return launch_pack_s<1>(p, stream);
   if (p.sources == 2) return launch_pack_s<2>(p, stream);
   return launch_pack_s<3>(p, stream);
+}
+
+void fill_log2_table(float (*tab)[4]) {
+  for (int j = 0; j < kLog2TabSize; ++j) {
+    // r_j = 1 / (centre of the interval), rounded to a multiple of 2^-10;
+    // then |m r_j - 1| < 2^-9 over the interval, and m r_j - 1 (a multiple
+    // of 2^-33) fits in a float's 24 bits.  r_0 = 1 keeps F free of
+    // cancellation for small s.
+    const double r = j == 0 ? 1.0 : std::nearbyint(1024.0 / (1.0 + (j + 0.5) / kLog2TabSize)) / 1024.0;
+    const double g = -std::log2(r);
+    const float gh = static_cast<float>(g);
+    tab[j][0] = static_cast<float>(r);
+    tab[j][1] = gh;
+    tab[j][2] = static_cast<float>(g - static_cast<double>(gh));
+    tab[j][3] = 0.0f;
+  }
 }
 
 cudaError_t launch_unpack(const UnpackParams& p, cudaStream_t stream) {

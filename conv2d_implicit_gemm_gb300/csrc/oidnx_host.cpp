@@ -638,6 +638,7 @@ struct oidnx_filter {
   DeviceLayer layers[kLayers];
   size_t weight_bytes = 0;
   int* status = nullptr;  // device error word
+  void* log2_tab = nullptr;  // fp32 log-transfer table (kLog2TabSize float4)
   // parameters
   int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
       overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 1;
@@ -1240,6 +1241,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
       pp.split_pitch = P->split_on[0] ? P->value_ext[V_INS].pitch : 0;
       pp.chunks = act_chunks(f->precision, f->in_channels);
       pp.pitch = P->value_ext[V_IN].pitch;
+      pp.log2_tab = static_cast<const float4*>(f->log2_tab);
       (void)cudaGetLastError();
       cudaError_t e = launch_pack(pp, s);
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
@@ -1533,10 +1535,16 @@ oidnx_status oidnx_filter_create(const void* blob, size_t bytes, int precision,
     if (e == cudaSuccess) e = cudaMemset(f->status, 0, 256);
     if (e != cudaSuccess) st = fail(OIDNX_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
   }
+  if (st == OIDNX_OK && f->precision == OIDNX_PRECISION_FP32) {
+    float tab[kLog2TabSize][4];
+    fill_log2_table(tab);
+    st = upload(tab, sizeof(tab), &f->log2_tab);
+  }
   if (st != OIDNX_OK) {
     std::string msg = g_last_error;
     for (DeviceLayer& L : f->layers) free_layer(L);
     cudaFree(f->status);
+    cudaFree(f->log2_tab);
     g_last_error = msg;
     return st;
   }
@@ -1899,6 +1907,7 @@ void oidnx_filter_release(oidnx_filter* f) {
   for (cudaEvent_t e : f->prof.ev) cudaEventDestroy(e);
   if (f->capture_stream) cudaStreamDestroy(f->capture_stream);
   cudaFree(f->status);
+  cudaFree(f->log2_tab);
   delete f;
 }
 

@@ -23,6 +23,59 @@ def _images(w, h, sources, hdr, nan_fraction):
     return imgs
 
 
+
+def _near_fp32_midpoints(n, rel, seed):
+    """Colour values whose log2(1 + x) lies within rel (relative) of a
+    rounding boundary between two fp32 codes: the hardest inputs for any
+    evaluation that is not exact."""
+    rng = np.random.default_rng(seed)
+    x = np.concatenate([(10.0 ** rng.uniform(-18, 38, n)),
+                        rng.uniform(0.0, 2.0 ** -9, n),
+                        rng.uniform(0.0, 8.0, n)]).astype(np.float32)
+    x = x[x > 0]
+    f = np.log1p(x.astype(np.float64)) / np.log(2.0)
+    y = f.astype(np.float32)
+    other = np.nextafter(y, np.where(f > y, np.float32(np.inf), np.float32(0)))
+    mid = (y.astype(np.float64) + other.astype(np.float64)) / 2
+    return x[np.abs(f - mid) < rel * f]
+
+
+def test_pack_hdr_transfer_fp32_is_correctly_rounded_everywhere():
+    # fp32 input pass: every stored value must equal the correctly rounded
+    # fp32 of log2(1 + x), over a dense sweep from subnormal colour to
+    # FLT_MAX, the small-value range, the edges of the evaluation's ranges
+    # and values whose F lies within 2^-36 of a rounding boundary
+    f32max = np.finfo(np.float32).max
+    edges = np.array([0.0, 2.0 ** -149, 2.0 ** -61, 2.0 ** -60, 2.0 ** -24, 2.0 ** -23,
+                      2.0 ** -9, 2.0 ** -8, 0.5, 1.0, 2.0, 2.0 ** 24, 2.0 ** 24 + 2,
+                      2.0 ** 25 + 4, 2.0 ** 126, 2.0 ** 127, f32max], np.float32)
+    edges = np.concatenate([edges, np.nextafter(edges, np.float32(0)),
+                            np.nextafter(edges, np.float32(np.inf))])
+    edges = edges[np.isfinite(edges)]
+    hard = _near_fp32_midpoints(1 << 20, 2.0 ** -36, 7)
+    assert hard.size > 100
+    vals = np.concatenate([np.logspace(-44, 38.5, 90000).astype(np.float32),
+                           np.random.default_rng(3).uniform(0, 2.0 ** -8, 20000).astype(np.float32),
+                           edges, hard])
+    w = 512
+    h = -(-vals.size // (3 * w * 16)) * 16   # a whole number of 16-row blocks: one tile
+    flat = np.ones(w * h * 3, np.float32)
+    flat[:vals.size] = vals
+    color = np.ones((h, w, 4), np.float32)
+    color[..., :3] = flat.reshape(h, w, 3)
+    imgs = [color, synth.albedo(w, h), synth.normal(w, h)]
+    d = Denoiser(synth.unet_weights(9), ox.PRECISION_FP32, imgs, True, keep=True)
+    try:
+        d.run()
+        packed = d.activation(0, h, w, 9)
+    finally:
+        d.close()
+    ref = passes.pack_tile(imgs, (0, 0, w, h), True, 1.0, "fp32")
+    got = packed[..., :3].astype(np.float32)
+    bad = np.flatnonzero(got.view(np.uint32) != ref[..., :3].astype(np.float32).view(np.uint32))
+    assert bad.size == 0, (bad.size, flat[bad[:5]], got.reshape(-1)[bad[:5]],
+                           ref[..., :3].reshape(-1)[bad[:5]])
+
 @pytest.mark.parametrize("precision", ["fp16", "fp32"])
 @pytest.mark.parametrize("sources", [1, 2, 3])
 @pytest.mark.parametrize("hdr", [True, False])
