@@ -79,6 +79,55 @@ enum TcKind : int {
   kTcExpand32 = 4,  // fp32 storage, 3xTF32 products: decoder with expansion
 };
 
+// Two same-padded 3x3 convs fused in one kernel (fp16 storage): conv 1
+// (Cin -> 32, bias + ReLU, fp16-rounded) streams its output rows through
+// tensor memory into shared memory, where conv 2 reads them; the 32-channel
+// map between the two never reaches global memory.
+enum PairMode : int {
+  kPairFinal = 0,  // conv 2: 32 -> 3 final conv, fp32 [H][W][4] output
+  kPairPool = 1,   // conv 2: 32 -> 32, bias + ReLU + 2x2 max-pool, fp16 output
+};
+
+constexpr int kPairSlots = 8;      // TMEM row accumulators per conv (ring)
+constexpr int kPairBatch = 3;      // source rows whose MMAs are issued interleaved
+constexpr int kPairMid = 2 * kPairBatch;  // conv-1 output rows held in shared memory
+constexpr int kPairSpan = kTileM - 2;  // output pixels per strip at most
+
+struct PairConvParams {
+  const __half* w1;        // conv 1 B operand, [kb][kx][2][3 x 32][8] halves
+  const __half* w2;        // conv 2 B operand: final [kb][2][3 x 16][8] (kx folded:
+                           // row 16 * (2 - ky) + 4 * kx + co), pool as w1
+  const float* bias1;      // [32]
+  const float* bias2;      // final: [16] = {b0, b1, b2, 0, ...}; pool: [32]
+  void* out;               // final: f32 [H][W][4]; pool: fp16 [Hp][4][pitch][8]
+  void* out_split;         // pool: optional column-parity split copy, or null
+  int* status;
+  int W, H;                // conv extent (both convs)
+  int KB1;                 // 16-channel K blocks of conv 1's input
+  int C8;                  // 16-byte chunks per input pixel (2 * KB1)
+  int strips, sw;          // column strips of sw output pixels (sw even, <= kPairSpan)
+  int row_unit;            // 1 (final) or 2 (pool: rows in pairs)
+  int units;               // strips * ceil(H / row_unit)
+  int pitch, split_pitch;  // pool output pitches (pooled pixels)
+  int S;                   // input row stages
+  uint32_t stage_tx;       // one input row: kHaloW pixels x C8 chunks x 16 B
+  uint32_t stage_bytes;    // its shared-memory stride (a multiple of 1024)
+  uint32_t w1_bytes, w2_bytes;
+  int xs;                  // log2 pixels per x unit of the input map
+};
+
+struct PairConvLaunch {
+  CUtensorMap map;         // conv 1 input: boxes of one row, kHaloW pixels, C8 chunks
+  PairConvParams p;
+  int mode;                // PairMode
+  dim3 grid;
+  size_t smem;
+};
+
+cudaError_t launch_conv_pair(const PairConvLaunch& L, cudaStream_t stream);
+cudaError_t conv_pair_set_smem_limit(size_t bytes);
+cudaError_t conv_pair_occupancy(int mode, size_t smem, int* blocks_per_sm);
+
 struct TcConvLaunch {
   CUtensorMap map0;        // source 0 (full-res halo box, or low-res box)
   CUtensorMap map1;        // source 1 (full-res halo box, or stride-2 box); unused if KB1 == 0

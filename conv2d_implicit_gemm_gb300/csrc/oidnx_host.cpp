@@ -291,6 +291,28 @@ std::vector<uint16_t> pack_weights_tc(const ConvTensors& L, int c0, int c1, int*
   return out;
 }
 
+// The final 32 -> 3 conv's B operand for the fused pair kernel, kx folded
+// into N: per K block [j][pos][16][8] halves, row pos * 16 + 4 * kx + co
+// (pos = 2 - ky); rows 4 kx + 3 and 12..15 are zero.
+std::vector<uint16_t> pack_weights_folded(const ConvTensors& L) {
+  const int KB = round_up(L.cin, 16) / 16;
+  std::vector<uint16_t> out(static_cast<size_t>(KB) * 2 * 48 * 8, 0);
+  for (int kb = 0; kb < KB; ++kb)
+    for (int j = 0; j < 2; ++j)
+      for (int pos = 0; pos < 3; ++pos)
+        for (int kx = 0; kx < 3; ++kx)
+          for (int co = 0; co < L.cout; ++co)
+            for (int l = 0; l < 8; ++l) {
+              const int ch = kb * 16 + j * 8 + l;
+              if (ch >= L.cin) continue;
+              const int ky = 2 - pos;
+              const float w = L.w[(static_cast<size_t>(co) * L.cin + ch) * 9 + ky * 3 + kx];
+              const size_t row = static_cast<size_t>(pos) * 16 + 4 * kx + co;
+              out[((static_cast<size_t>(kb) * 2 + j) * 48 + row) * 8 + l] = to_half_bits(w);
+            }
+  return out;
+}
+
 // fp32 storage: the B operand for 3xTF32 products.  K blocks of 8 channels
 // (two 16-byte chunks of 4 lanes) over each source padded to 4 lanes; per
 // block [hi, lo][kx][j][pos][N][4] floats with pos = 2 - ky, where hi is the
@@ -581,6 +603,8 @@ struct DeviceLayer {
   int KB0 = 0, KB1 = 0, N = 0;
   void* w16_sub = nullptr;  // sub-pixel decoder B operand (decoders only)
   size_t sub_bytes = 0, sub_ub = 0;
+  void* wfold = nullptr;    // fused final conv: B operand with kx folded into N
+  size_t fold_bytes = 0;
   float* bias = nullptr;  // [N]
   size_t weight_bytes = 0;
 };
@@ -598,8 +622,11 @@ int fp16_pitch(int w) { return (w + kGroupPx - 1) / kGroupPx * kGroupPx; }
 int split_pitch(int w) { return (w + 2 * kGroupPx - 1) / (2 * kGroupPx) * (2 * kGroupPx); }
 
 struct LayerLaunch {
-  int layer;
+  int layer;               // first layer of the launch
+  int pair;                // 1: layers `layer` and `layer + 1` fused (pcl)
+  const char* name;
   TcConvLaunch tcl;
+  PairConvLaunch pcl;
   double flop;   // logical conv FLOPs
   double bytes;  // algorithmic bytes: inputs read once, output written once
 };
@@ -615,6 +642,7 @@ struct Plan {
   size_t arena_bytes = 0;
   std::vector<LayerLaunch> launches;
   bool split_on[4] = {};  // kSplits[i] in use (its decoder runs in sub-pixel mode)
+  bool fused[2] = {};     // kPairs[i] runs as one fused kernel
   uint64_t last_used = 0;
   cudaEvent_t done = nullptr;  // recorded after each use
   bool used = false;
@@ -641,7 +669,8 @@ struct oidnx_filter {
   void* log2_tab = nullptr;  // fp32 log-transfer table (kLog2TabSize float4)
   // parameters
   int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
-      overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 1;
+      overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 1,
+      fuse = 0;
   float input_scale = 1.0f;
   void* img[4] = {};
   size_t img_stride[4] = {};
@@ -684,6 +713,8 @@ oidnx_status upload(const void* host, size_t bytes, void** dev) {
 void free_layer(DeviceLayer& L) {
   cudaFree(L.w16_sub);
   L.w16_sub = nullptr;
+  cudaFree(L.wfold);
+  L.wfold = nullptr;
   cudaFree(L.wtc);
   cudaFree(L.bias);
   L.wtc = nullptr;
@@ -705,10 +736,15 @@ oidnx_status make_device_layer(const ConvTensors& T, int c0, int c1, int precisi
       L->sub_bytes = ws.size() * 2;
       OIDNX_TRY(upload(ws.data(), L->sub_bytes, &L->w16_sub));
     }
+    if (T.cout == 3 && T.cin == 32 && c1 == 0) {
+      std::vector<uint16_t> wf = pack_weights_folded(T);
+      L->fold_bytes = wf.size() * 2;
+      OIDNX_TRY(upload(wf.data(), L->fold_bytes, &L->wfold));
+    }
     std::vector<float> b(L->N, 0.0f);
     std::copy(T.b.begin(), T.b.end(), b.begin());
     OIDNX_TRY(upload(b.data(), b.size() * 4, reinterpret_cast<void**>(&L->bias)));
-    L->weight_bytes = w.size() * 2 + b.size() * 4 + L->sub_bytes;
+    L->weight_bytes = w.size() * 2 + b.size() * 4 + L->sub_bytes + L->fold_bytes;
   } else {
     std::vector<float> w = pack_weights_tf32(T, c0, c1, &L->KB0, &L->KB1, &L->N);
     if (L->N > 256) return fail(OIDNX_ERR_UNSUPPORTED, "more than 256 output channels");
@@ -984,8 +1020,105 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   return ok();
 }
 
+// Layer pairs that run as one fused kernel when the filter allows it (fp16
+// storage, "fuseLayers"): the first layer's output is never stored.
+struct PairDef {
+  int first, mode;
+  const char* name;
+};
+const PairDef kPairs[2] = {{0, kPairPool, "enc_conv0+enc_conv1"},
+                           {14, kPairFinal, "dec_conv1b+dec_conv0"}};
+
+bool pair_fusable(const oidnx_filter* f, const PairDef& d) {
+  if (!f->fuse || f->precision != OIDNX_PRECISION_FP16) return false;
+  const DeviceLayer& a = f->layers[d.first];
+  const DeviceLayer& b = f->layers[d.first + 1];
+  if (a.c1 != 0 || a.cout != 32 || a.KB0 < 1 || a.KB0 > 4 || b.c0 != 32 || b.c1 != 0) return false;
+  return d.mode == kPairFinal ? b.cout == 3 && b.wfold != nullptr : b.cout == 32;
+}
+
+// Launch of a fused pair over a W x H conv extent: conv 1 reads `src`
+// (fp16, one source), conv 2 writes `out` (final: f32 [H][W][4]; pool:
+// fp16 pooled with pitch out_pitch, plus the optional split copy).
+oidnx_status build_pair_launch(const DeviceLayer& A, const DeviceLayer& B, int mode,
+                               const void* src, Extent ext, int W, int H, void* out,
+                               int out_pitch, void* out_split, int out_split_pitch, int* status,
+                               PairConvLaunch* T) {
+  T->mode = mode;
+  PairConvParams& p = T->p;
+  std::memset(&p, 0, sizeof(p));
+  p.w1 = static_cast<const __half*>(A.wtc);
+  p.w2 = static_cast<const __half*>(mode == kPairFinal ? B.wfold : B.wtc);
+  p.bias1 = A.bias;
+  p.bias2 = B.bias;
+  p.out = out;
+  p.out_split = out_split;
+  p.status = status;
+  p.W = W;
+  p.H = H;
+  p.KB1 = A.KB0;
+  p.C8 = 2 * A.KB0;
+  p.row_unit = mode == kPairPool ? 2 : 1;
+  p.pitch = out_pitch;
+  p.split_pitch = out_split ? out_split_pitch : 0;
+  // Strips of sw output columns (even, at most kPairSpan); the last strip's
+  // lanes reach kPairSpan columns past its start, which must cover every
+  // column to be written (pooled: the zero padding of both pitched copies).
+  const int need = mode == kPairPool ? 2 * std::max(p.pitch, p.split_pitch) : W;
+  for (int n = std::max(1, (W + kPairSpan - 1) / kPairSpan);; ++n) {
+    const int sw = round_up((W + n - 1) / n, 2);
+    if (sw <= kPairSpan && (n - 1) * sw + kPairSpan >= need) {
+      p.strips = n;
+      p.sw = sw;
+      break;
+    }
+  }
+  p.units = p.strips * ((H + p.row_unit - 1) / p.row_unit);
+  // one stage: the kPairBatch input rows of one batch
+  p.stage_tx = static_cast<uint32_t>(kPairBatch * kHaloW * p.C8 * kChunkBytes);
+  p.stage_bytes = static_cast<uint32_t>(round_up_sz(p.stage_tx, 1024));
+  p.w1_bytes = static_cast<uint32_t>(A.KB0 * 9 * 2 * 32 * kChunkBytes);
+  p.w2_bytes = static_cast<uint32_t>(mode == kPairFinal ? B.fold_bytes : 2 * 9 * 2 * 32 * kChunkBytes);
+  const size_t mid_row = static_cast<size_t>(4) * (mode == kPairFinal ? kTileM : kTileM + 8) * kChunkBytes;
+  const size_t xb = mode == kPairFinal ? static_cast<size_t>(4) * kTileM * 16 : 0;
+  // alignment slack, weights, conv-1 rows, exchange, bias, 17 barriers + 2
+  // per stage, the TMEM address
+  const size_t fixed = 1024 + p.w1_bytes + round_up_sz(p.w2_bytes, 1024) + kPairMid * mid_row + xb +
+                       64 * 4 + 17 * 8 + 16;
+  const size_t max_smem = 227 * 1024;
+  // the MMA issuer holds one batch of input rows while the next one loads
+  if (fixed + 2 * (16 + static_cast<size_t>(p.stage_bytes)) > max_smem)
+    return fail(OIDNX_ERR_UNSUPPORTED, "fused conv does not fit shared memory");
+  p.S = static_cast<int>(std::min<size_t>(4, (max_smem - fixed) / (16 + p.stage_bytes)));
+  size_t smem = fixed + 16 * static_cast<size_t>(p.S) + static_cast<size_t>(p.S) * p.stage_bytes;
+  static bool limit_set = false;
+  if (!limit_set) {
+    cudaError_t e = conv_pair_set_smem_limit(max_smem);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
+    limit_set = true;
+  }
+  // one CTA per SM: it allocates all 512 TMEM columns
+  for (;;) {
+    int blocks = 0;
+    cudaError_t e = conv_pair_occupancy(mode, smem, &blocks);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "occupancy: %s", cudaGetErrorString(e));
+    if (blocks <= 1) break;
+    smem += 4096;
+    if (smem > max_smem) return fail(OIDNX_ERR_UNSUPPORTED, "cannot bound CTAs per SM");
+  }
+  T->smem = smem;
+  T->grid = dim3(static_cast<unsigned>(std::min(p.units, num_sms())), 1, 1);
+  return encode_act_map(&T->map, src, ext.w, ext.pitch, ext.h, p.C8, kHaloW, kPairBatch, true, &p.xs,
+                        p.C8);
+}
+
 oidnx_status run_launch(const LayerLaunch& L, cudaStream_t s) {
   (void)cudaGetLastError();  // drop a stale, non-sticky error of an earlier call
+  if (L.pair) {
+    cudaError_t e = launch_conv_pair(L.pcl, s);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "%s launch: %s", L.name, cudaGetErrorString(e));
+    return ok();
+  }
   cudaError_t e = launch_conv_tc(L.tcl, s);
   if (e != cudaSuccess)
     return fail(OIDNX_ERR_CUDA, "%s launch: %s", kLayerNames[L.layer], cudaGetErrorString(e));
@@ -1066,12 +1199,22 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
     P->value_off[v] = slots[best].off;
     P->value_bytes[v] = need;
   };
+  // a fused pair's intermediate map is never stored
+  bool stored[kLayers];
+  for (int l = 0; l < kLayers; ++l) stored[l] = true;
+  for (int i = 0; i < 2; ++i) {
+    P->fused[i] = pair_fusable(f, kPairs[i]);
+    if (P->fused[i]) stored[kPairs[i].first] = false;
+  }
   allocate(V_IN, -1);
   if (P->split_on[0]) allocate(V_INS, -1);
   for (int l = 0; l < kLayers; ++l) {
-    allocate(kDefs[l].dst, l);
+    // a fused pair reads the first layer's inputs while it writes the second
+    // layer's outputs: place those as if the first layer wrote them
+    const int at = l > 0 && !stored[l - 1] ? l - 1 : l;
+    if (stored[l]) allocate(kDefs[l].dst, at);
     for (int i = 0; i < 4; ++i)
-      if (P->split_on[i] && kSplits[i].producer == l) allocate(kSplits[i].split, l);
+      if (P->split_on[i] && kSplits[i].producer == l) allocate(kSplits[i].split, at);
   }
   P->arena_bytes = total;
   cudaError_t e = cudaMalloc(&P->arena, total);
@@ -1084,13 +1227,44 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
   e = cudaEventCreateWithFlags(&P->done, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "event: %s", cudaGetErrorString(e));
 
+  const int bpe = f->precision == OIDNX_PRECISION_FP16 ? 2 : 4;
+  auto value_bytes = [&](int v) {
+    return static_cast<double>(P->value_ext[v].w) * P->value_ext[v].h * P->value_ch[v] * bpe;
+  };
   for (int l = 0; l < kLayers; ++l) {
     const LayerDef& d = kDefs[l];
     const DeviceLayer& L = f->layers[l];
     LayerLaunch LL;
     std::memset(&LL, 0, sizeof(LL));
     LL.layer = l;
+    LL.name = kLayerNames[l];
     const Extent conv = P->lvl[d.level];
+    const int pi = l == kPairs[0].first ? 0 : (l == kPairs[1].first ? 1 : -1);
+    if (pi >= 0 && P->fused[pi]) {
+      const LayerDef& d2 = kDefs[l + 1];
+      const DeviceLayer& L2 = f->layers[l + 1];
+      void* out_split = nullptr;
+      int out_split_pitch = 0;
+      for (int i = 0; i < 4; ++i)
+        if (P->split_on[i] && kSplits[i].producer == l + 1) {
+          out_split = P->ptr(kSplits[i].split);
+          out_split_pitch = P->value_ext[kSplits[i].split].pitch;
+        }
+      LL.pair = 1;
+      LL.name = kPairs[pi].name;
+      OIDNX_TRY(build_pair_launch(L, L2, kPairs[pi].mode, P->ptr(d.src0), P->value_ext[d.src0],
+                                  conv.w, conv.h, P->ptr(d2.dst), P->value_ext[d2.dst].pitch,
+                                  out_split, out_split_pitch, f->status, &LL.pcl));
+      const double px = static_cast<double>(conv.w) * conv.h;
+      LL.flop = 2.0 * 9.0 * (L.cin * L.cout + L2.cin * L2.cout) * px;
+      const Extent oe = P->value_ext[d2.dst];
+      LL.bytes = value_bytes(d.src0) +
+                 (d2.kind == kFinal ? static_cast<double>(oe.w) * oe.h * 16 : value_bytes(d2.dst)) +
+                 static_cast<double>(L.weight_bytes + L2.weight_bytes);
+      P->launches.push_back(LL);
+      ++l;
+      continue;
+    }
     const void* s1 = d.src1 >= 0 ? P->ptr(d.src1) : nullptr;
     Extent e1 = d.src1 >= 0 ? P->value_ext[d.src1] : Extent{0, 0, 0};
     bool subpixel = false;
@@ -1113,7 +1287,6 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
                               &LL.tcl, subpixel, out_split, out_split_pitch));
     const double px = static_cast<double>(conv.w) * conv.h;
     LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
-    const int bpe = f->precision == OIDNX_PRECISION_FP16 ? 2 : 4;
     double in_bytes = static_cast<double>(P->value_ext[d.src0].w) * P->value_ext[d.src0].h *
                       P->value_ch[d.src0] * bpe;
     if (d.src1 >= 0)
@@ -1414,12 +1587,21 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     slots[best].active = v;
     off[v] = slots[best].off;
   };
+  bool fused[2];
+  bool stored[kLayers];
+  for (int l = 0; l < kLayers; ++l) stored[l] = true;
+  for (int i = 0; i < 2; ++i) {
+    fused[i] = pair_fusable(f, kPairs[i]);
+    if (fused[i]) stored[kPairs[i].first] = false;
+  }
   if (split_on[0]) place(V_INS, -1);
   for (int l = 0; l < kLayers; ++l) {
     const int v = kDefs[l].dst;
-    if (v != V_OUT) place(v, l);  // V_OUT is written straight into the caller's output
+    const int at = l > 0 && !stored[l - 1] ? l - 1 : l;  // see create_plan
+    // V_OUT is written straight into the caller's output
+    if (v != V_OUT && stored[l]) place(v, at);
     for (int i = 0; i < 4; ++i)
-      if (split_on[i] && kSplits[i].producer == l) place(kSplits[i].split, l);
+      if (split_on[i] && kSplits[i].producer == l) place(kSplits[i].split, at);
   }
   if (total > cap)
     return fail(OIDNX_ERR_INVALID_ARGUMENT,
@@ -1442,7 +1624,27 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
     LayerLaunch LL;
     std::memset(&LL, 0, sizeof(LL));
     LL.layer = l;
+    LL.name = kLayerNames[l];
     const Extent conv = lvl[d.level];
+    const int pi = l == kPairs[0].first ? 0 : (l == kPairs[1].first ? 1 : -1);
+    if (pi >= 0 && fused[pi]) {
+      const LayerDef& d2 = kDefs[l + 1];
+      void* out_split = nullptr;
+      int out_split_pitch = 0;
+      for (int i = 0; i < 4; ++i)
+        if (split_on[i] && kSplits[i].producer == l + 1) {
+          out_split = ptr(kSplits[i].split);
+          out_split_pitch = ext[kSplits[i].split].pitch;
+        }
+      LL.pair = 1;
+      LL.name = kPairs[pi].name;
+      OIDNX_TRY(build_pair_launch(L, f->layers[l + 1], kPairs[pi].mode, ptr(d.src0), ext[d.src0],
+                                  conv.w, conv.h, ptr(d2.dst), ext[d2.dst].pitch, out_split,
+                                  out_split_pitch, f->status, &LL.pcl));
+      OIDNX_TRY(run_launch(LL, s));
+      ++l;
+      continue;
+    }
     const void* s1 = d.src1 >= 0 ? ptr(d.src1) : nullptr;
     Extent e1 = d.src1 >= 0 ? ext[d.src1] : Extent{0, 0, 0};
     bool subpixel = false;
@@ -1592,8 +1794,9 @@ oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value) 
   } else if (n == "shapeCacheSize") {
     if (value < 1) return fail(OIDNX_ERR_INVALID_ARGUMENT, "shapeCacheSize must be >= 1");
     f->shape_cache = value;
-  } else if (n == "keepActivations" || n == "subpixelDecoder") {
-    (n == "keepActivations" ? f->keep_acts : f->subpixel) = value ? 1 : 0;
+  } else if (n == "keepActivations" || n == "subpixelDecoder" || n == "fuseLayers") {
+    (n == "keepActivations" ? f->keep_acts : n == "subpixelDecoder" ? f->subpixel : f->fuse) =
+        value ? 1 : 0;
     for (auto& p : f->plans) f->retired.push_back(std::move(p));
     f->plans.clear();
     f->current = nullptr;
@@ -1622,6 +1825,7 @@ oidnx_status oidnx_filter_get_int(oidnx_filter* f, const char* name, int* value)
   else if (n == "shapeCacheSize") *value = f->shape_cache;
   else if (n == "keepActivations") *value = f->keep_acts;
   else if (n == "subpixelDecoder") *value = f->subpixel;
+  else if (n == "fuseLayers") *value = f->fuse;
   else if (n == "profile") *value = f->profile_always;
   else if (n == "inputChannels") *value = f->in_channels;
   else if (n == "precision") *value = f->precision;
@@ -1818,9 +2022,8 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
   const int bpe = f->precision == OIDNX_PRECISION_FP16 ? 2 : 4;
   const double tile_px = plan ? static_cast<double>(plan->w) * plan->h : 0;
   add("input-pack", 1, 0, tile_px * (16.0 * sources + f->in_channels * bpe));
-  for (int l = 0; l < kLayers; ++l)
-    add(kLayerNames[l], l + 2, plan ? plan->launches[l].flop : 0,
-        plan ? plan->launches[l].bytes : 0);
+  if (plan)
+    for (const LayerLaunch& L : plan->launches) add(L.name, L.layer + 2, L.flop, L.bytes);
   double out_px = 0;
   for (const AxisTile& y : f->ty)
     for (const AxisTile& x : f->tx) out_px += static_cast<double>(x.out_size) * y.out_size;
@@ -1858,6 +2061,10 @@ oidnx_status oidnx_debug_read_activation(oidnx_filter* f, int layer, void* host_
   if (!P) return fail(OIDNX_ERR_INVALID_ARGUMENT, "no network run to read from");
   if (layer < 0 || layer > kLayers) return fail(OIDNX_ERR_INVALID_ARGUMENT, "bad layer %d", layer);
   const int v = layer == 0 ? V_IN : kDefs[layer - 1].dst;
+  if (P->value_bytes[v] == 0)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT,
+                "the output of layer %d is not stored (fused into the next layer's kernel; "
+                "set keepActivations)", layer - 1);
   const Extent e = P->value_ext[v];
   const int C = v == V_OUT ? 3 : P->value_ch[v];
   const size_t need = static_cast<size_t>(e.w) * e.h * C * 4;

@@ -296,4 +296,23 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Refill 16 accumulator columns (32 lanes) with the bias values bias16[0..15]
+// (16-byte aligned shared memory).
+__device__ __forceinline__ void tmem_fill_bias(uint32_t taddr, const float* bias16) {
+  uint32_t r[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 b = reinterpret_cast<const float4*>(bias16)[k];
+    r[4 * k] = __float_as_uint(b.x);
+    r[4 * k + 1] = __float_as_uint(b.y);
+    r[4 * k + 2] = __float_as_uint(b.z);
+    r[4 * k + 3] = __float_as_uint(b.w);
+  }
+  tmem_st16(taddr, r);
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 }  // namespace oidnx

@@ -98,6 +98,12 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *                        class are summed, then rounded to fp16), reading
  *                        parity-split copies of the skip sources (default);
  *                        0 builds the upsampled halo in shared memory
+ *   "fuseLayers"         1 = with fp16 storage, enc_conv0+enc_conv1 and
+ *                        dec_conv1b+dec_conv0 each run as one kernel that
+ *                        never stores the first conv's output; default 0:
+ *                        on GB300 the separate kernels are faster (the MMAs
+ *                        of these layers are bound by shared-memory operand
+ *                        reads, which fusion does not reduce)
  *   "profile"            1 = record per-kernel events on every execute
  * Errors: INVALID_ARGUMENT for unknown names or out-of-range values.  */
 oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value);
@@ -204,8 +210,11 @@ oidnx_status oidnx_get_resource_info(oidnx_filter* f, char* json, size_t cap);
  * host memory as float32 [h_l][w_l][C_l] with logical channels.
  * layer: 0 = packed network input, 1..16 = outputs of enc_conv0 ..
  * dec_conv0 in network order (enc_conv1..enc_conv4 store their pooled
- * outputs).  Valid for every layer only with "keepActivations" = 1; the
- * required size is returned in *bytes_needed.  Synchronises.
+ * outputs).  Valid for every layer only with "keepActivations" = 1 and
+ * "fuseLayers" = 0 (the output of a layer fused with the next one is never
+ * stored: its read fails with INVALID_ARGUMENT); the required size is
+ * returned in *bytes_needed.
+ * Synchronises.
  * Errors: INVALID_ARGUMENT, CUDA.  */
 oidnx_status oidnx_debug_read_activation(oidnx_filter* f, int layer, void* host_dst,
                                          size_t cap, size_t* bytes_needed);

@@ -45,18 +45,22 @@ def _isolated(k, acts, weights, precision):
     return y
 
 
-def _run_network(weights, packed_logical, precision, subpixel=0):
+def _run_network(weights, packed_logical, precision, subpixel=0, fuse=0):
+    # fuse=1: the fused pairs' intermediate maps (activations 1 and 15) are
+    # never stored and come back as None
     h, w, c = packed_logical.shape
     prec = ox.PRECISION_FP16 if precision == "fp16" else ox.PRECISION_FP32
     f = ox.oidnx_filter_create(ox.write_weight_blob(weights), prec)
     try:
         ox.oidnx_filter_set_int(f, "keepActivations", 1)
         ox.oidnx_filter_set_int(f, "subpixelDecoder", subpixel)
+        ox.oidnx_filter_set_int(f, "fuseLayers", fuse)
         src = to_dev(_layout.to_internal(packed_logical, precision))
         out = empty_dev(w * h * 16)
         ox.oidnx_network_execute(f, src.data_ptr(), w, h, out.data_ptr(), stream())
         ox.oidnx_filter_sync_status(f)
-        acts = [ox.oidnx_debug_read_activation(f, k) for k in range(17)]
+        skip = (1, 15) if fuse and precision == "fp16" else ()
+        acts = [None if k in skip else ox.oidnx_debug_read_activation(f, k) for k in range(17)]
         final = to_host(out, np.float32, (h, w, 4)).copy()
     finally:
         ox.oidnx_filter_release(f)
