@@ -284,12 +284,28 @@ def run_ours(args):
         t0 = time.perf_counter()
         ox._check(ox._lib.oidnx_filter_execute_host(f, *host_ptr, host_out.data_ptr(), sptr))
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    # a stream of K frames through the enqueue-only host call: every step
+    # still uploads its inputs and downloads its output, but one frame's
+    # copies overlap another frame's denoise (two device staging sets); the
+    # wall clock runs from the first enqueue to the last output in host
+    # memory (device working set per step > L2, no flush in between)
+    outs = [torch.empty((HEIGHT, WIDTH, 4), dtype=torch.float32).pin_memory() for _ in range(2)]
+    for k in range(3):
+        ox._check(ox._lib.oidnx_filter_execute_host_async(f, *host_ptr, outs[k & 1].data_ptr(), sptr))
+    ox._check(ox._lib.oidnx_filter_wait_host(f))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        ox._check(ox._lib.oidnx_filter_execute_host_async(f, *host_ptr, outs[k & 1].data_ptr(), sptr))
+    ox._check(ox._lib.oidnx_filter_wait_host(f))
+    stream_ms = (time.perf_counter() - t0) * 1e3 / args.steps
     ox.oidnx_filter_release(f)
 
     px = WIDTH * HEIGHT
-    mean_ms, e2e_mean = max_over_ranks([mean_ms, float(np.mean(e2e_ms))])
+    mean_ms, e2e_mean, stream_ms = max_over_ranks([mean_ms, float(np.mean(e2e_ms)), stream_ms])
     value, _ = aggregate([mean_ms] * world, [px] * world)
-    e2e_value, _ = aggregate([e2e_mean] * world, [px] * world)
+    e2e_value, _ = aggregate([stream_ms] * world, [px] * world)
+    e2e_sync_value, _ = aggregate([e2e_mean] * world, [px] * world)
 
     steps = args.steps
     avg = {k: v / steps for k, v in layer_ms.items()}
@@ -339,8 +355,12 @@ def run_ours(args):
             "conv_frac_of_peak": conv_flop / (conv_ms * 1e-3) / 1e12 / tensor_peak,
             "roofline": roof,
             "layers": layers,
+            "e2e_sync": {"value": e2e_sync_value, "unit": "MP/s", "ms_per_step": e2e_mean,
+                         "mode": "one blocking host-buffer call per step (L2 flushed before each)"},
             "e2e": {"value": e2e_value, "unit": "MP/s", "h2d_bytes_per_step": 3 * px * 16,
-                    "d2h_bytes_per_step": px * 16, "ms_per_step": e2e_mean},
+                    "d2h_bytes_per_step": px * 16, "ms_per_step": stream_ms,
+                    "mode": "frame stream through the enqueue-only host-buffer call (uploads and "
+                            "downloads overlap other frames' denoise), K steps then one wait"},
             "gpu_launches": steps * launches_per_step,
             "profiled_ms_per_step": float(np.mean(prof_steps)),
             "layers_note": "per-kernel times from the profiled steps (event after every kernel)",

@@ -66,6 +66,8 @@ _sig("oidnx_filter_set_float", _st, _vp, ctypes.c_char_p, ctypes.c_float)
 _sig("oidnx_filter_commit", _st, _vp)
 _sig("oidnx_filter_execute", _st, _vp, _vp)
 _sig("oidnx_filter_execute_host", _st, _vp, _vp, _vp, _vp, _vp, _vp)
+_sig("oidnx_filter_execute_host_async", _st, _vp, _vp, _vp, _vp, _vp, _vp)
+_sig("oidnx_filter_wait_host", _st, _vp)
 _sig("oidnx_network_execute", _st, _vp, _vp, _i, _i, _vp, _vp)
 _sig("oidnx_network_execute_noalloc", _st, _vp, _vp, _i, _i, _vp, _vp)
 _sig("oidnx_filter_sync_status", _st, _vp)
@@ -154,6 +156,17 @@ def oidnx_filter_execute(f, stream=0):
 def oidnx_filter_execute_host(f, color, albedo, normal, output, stream=0):
     _check(_lib.oidnx_filter_execute_host(f, _host_ptr(color), _host_ptr(albedo),
                                           _host_ptr(normal), _host_ptr(output), stream))
+
+
+def oidnx_filter_execute_host_async(f, color, albedo, normal, output, stream=0):
+    """Enqueue only: the arrays must stay alive and unchanged, and `output`
+    unread, until oidnx_filter_wait_host(f) returns."""
+    _check(_lib.oidnx_filter_execute_host_async(f, _host_ptr(color), _host_ptr(albedo),
+                                                _host_ptr(normal), _host_ptr(output), stream))
+
+
+def oidnx_filter_wait_host(f):
+    _check(_lib.oidnx_filter_wait_host(f))
 
 
 def oidnx_network_execute(f, packed_in, w, h, out, stream=0):

@@ -681,20 +681,38 @@ struct oidnx_filter {
   std::list<std::unique_ptr<Plan>> plans;    // LRU cache
   std::list<std::unique_ptr<Plan>> retired;  // evicted, maybe still in flight
   uint64_t clock = 0;
-  // graph of the committed denoise
-  cudaGraphExec_t graph = nullptr;
-  bool graph_profiled = false;
-  void* graph_img[4] = {};
+  // graphs of the committed denoise, one per image set (the host path
+  // alternates two device staging sets), least recently used replaced
+  struct GraphEntry {
+    cudaGraphExec_t exec = nullptr;
+    bool profiled = false;
+    void* img[4] = {};
+    uint64_t used = 0;
+  } graphs[2];
+  uint64_t graph_clock = 0;
   cudaStream_t capture_stream = nullptr;
   // profiling
   bool profile_next = false;
   Profile prof;
-  // host-path staging images
-  void* host_img[4] = {};
+  // host path: two device staging sets (colour, albedo, normal, output), an
+  // upload and a download stream, and per set the events that order them
+  // with the denoise: inputs uploaded, denoise done, output downloaded
+  void* host_img[2][4] = {};
   size_t host_img_bytes = 0;
+  cudaStream_t host_in = nullptr, host_out = nullptr;
+  cudaEvent_t ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+  bool host_used[2] = {};
+  int host_next = 0;
   // last network run (for debug reads)
   Plan* last_plan = nullptr;
 };
+
+static void drop_graphs(oidnx_filter* f) {
+  for (auto& g : f->graphs) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    g = oidnx_filter::GraphEntry();
+  }
+}
 
 struct oidnx_conv {
   DeviceLayer L;
@@ -1332,10 +1350,7 @@ oidnx_status get_plan(oidnx_filter* f, int w, int h, Plan** out) {
     if (oldest == f->plans.end()) break;
     if (f->current == oldest->get()) {
       f->current = nullptr;
-      if (f->graph) {
-        cudaGraphExecDestroy(f->graph);
-        f->graph = nullptr;
-      }
+      drop_graphs(f);
     }
     if (f->last_plan == oldest->get()) f->last_plan = nullptr;
     f->retired.push_back(std::move(*oldest));
@@ -1461,10 +1476,7 @@ bool filter_alive(oidnx_filter* f, oidnx_status* st) {
 
 void invalidate(oidnx_filter* f) {
   f->committed = false;
-  if (f->graph) {
-    cudaGraphExecDestroy(f->graph);
-    f->graph = nullptr;
-  }
+  drop_graphs(f);
 }
 
 oidnx_status execute_images(oidnx_filter* f, void* const img[4], const size_t stride[4],
@@ -1477,12 +1489,17 @@ oidnx_status execute_images(oidnx_filter* f, void* const img[4], const size_t st
     OIDNX_TRY(prof_begin(f, denoise_launches(f)));
     OIDNX_TRY(enqueue_denoise(f, img, stride, true, s));
   } else {
-    bool same = f->graph && f->graph_profiled == prof;
-    for (int i = 0; i < 4 && same; ++i) same = f->graph_img[i] == img[i];
-    if (!same) {
-      if (f->graph) {
-        cudaGraphExecDestroy(f->graph);
-        f->graph = nullptr;
+    oidnx_filter::GraphEntry* ge = nullptr;
+    for (auto& g : f->graphs) {
+      bool same = g.exec && g.profiled == prof;
+      for (int i = 0; i < 4 && same; ++i) same = g.img[i] == img[i];
+      if (same) ge = &g;
+    }
+    if (!ge) {
+      ge = f->graphs[0].used <= f->graphs[1].used ? &f->graphs[0] : &f->graphs[1];
+      if (ge->exec) {
+        cudaGraphExecDestroy(ge->exec);
+        *ge = oidnx_filter::GraphEntry();
       }
       if (!f->capture_stream)
         OIDNX_CUDA(cudaStreamCreateWithFlags(&f->capture_stream, cudaStreamNonBlocking));
@@ -1496,13 +1513,14 @@ oidnx_status execute_images(oidnx_filter* f, void* const img[4], const size_t st
         return st;
       }
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
-      e = cudaGraphInstantiate(&f->graph, g, 0);
+      e = cudaGraphInstantiate(&ge->exec, g, 0);
       cudaGraphDestroy(g);
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
-      f->graph_profiled = prof;
-      for (int i = 0; i < 4; ++i) f->graph_img[i] = img[i];
+      ge->profiled = prof;
+      for (int i = 0; i < 4; ++i) ge->img[i] = img[i];
     }
-    OIDNX_CUDA(cudaGraphLaunch(f->graph, s));
+    ge->used = ++f->graph_clock;
+    OIDNX_CUDA(cudaGraphLaunch(ge->exec, s));
   }
   OIDNX_CUDA(cudaEventRecord(f->current->done, s));
   f->last_plan = f->current;
@@ -1888,8 +1906,9 @@ oidnx_status oidnx_filter_execute(oidnx_filter* f, void* stream) {
   return execute_images(f, img, stride, static_cast<cudaStream_t>(stream));
 }
 
-oidnx_status oidnx_filter_execute_host(oidnx_filter* f, const float* color, const float* albedo,
-                                       const float* normal, float* output, void* stream) {
+oidnx_status oidnx_filter_execute_host_async(oidnx_filter* f, const float* color,
+                                             const float* albedo, const float* normal,
+                                             float* output, void* stream) {
   oidnx_status st;
   if (!filter_alive(f, &st)) return st;
   if (!f->committed) return fail(OIDNX_ERR_NOT_COMMITTED, "execute before a successful commit");
@@ -1898,24 +1917,65 @@ oidnx_status oidnx_filter_execute_host(oidnx_filter* f, const float* color, cons
     return fail(OIDNX_ERR_INVALID_ARGUMENT, "missing host image");
   const size_t bytes = static_cast<size_t>(f->width) * f->height * 16;
   if (f->host_img_bytes != bytes) {
-    for (int i = 0; i < 4; ++i) {
-      cudaFree(f->host_img[i]);
-      f->host_img[i] = nullptr;
-    }
+    // the staging sets are resized only with nothing in flight
+    if (f->host_out) OIDNX_CUDA(cudaStreamSynchronize(f->host_out));
+    for (int b = 0; b < 2; ++b)
+      for (int i = 0; i < 4; ++i) {
+        cudaFree(f->host_img[b][i]);
+        f->host_img[b][i] = nullptr;
+      }
     f->host_img_bytes = 0;
-    for (int i = 0; i < 4; ++i) OIDNX_CUDA(cudaMalloc(&f->host_img[i], bytes));
+    f->host_used[0] = f->host_used[1] = false;
+    for (int b = 0; b < 2; ++b)
+      for (int i = 0; i < 4; ++i) OIDNX_CUDA(cudaMalloc(&f->host_img[b][i], bytes));
     f->host_img_bytes = bytes;
   }
+  if (!f->host_in) {
+    OIDNX_CUDA(cudaStreamCreateWithFlags(&f->host_in, cudaStreamNonBlocking));
+    OIDNX_CUDA(cudaStreamCreateWithFlags(&f->host_out, cudaStreamNonBlocking));
+    for (int b = 0; b < 2; ++b) {
+      OIDNX_CUDA(cudaEventCreateWithFlags(&f->ev_in[b], cudaEventDisableTiming));
+      OIDNX_CUDA(cudaEventCreateWithFlags(&f->ev_comp[b], cudaEventDisableTiming));
+      OIDNX_CUDA(cudaEventCreateWithFlags(&f->ev_out[b], cudaEventDisableTiming));
+    }
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int b = f->host_next;
+  f->host_next ^= 1;
+  void** img = f->host_img[b];
+  // upload: the set's inputs were last read by the denoise two calls ago
+  if (f->host_used[b]) OIDNX_CUDA(cudaStreamWaitEvent(f->host_in, f->ev_comp[b], 0));
   const float* src[3] = {color, albedo, normal};
   for (int i = 0; i < sources; ++i)
-    OIDNX_CUDA(cudaMemcpyAsync(f->host_img[i], src[i], bytes, cudaMemcpyHostToDevice, s));
+    OIDNX_CUDA(cudaMemcpyAsync(img[i], src[i], bytes, cudaMemcpyHostToDevice, f->host_in));
+  OIDNX_CUDA(cudaEventRecord(f->ev_in[b], f->host_in));
+  // denoise on the caller's stream once the inputs are in and the set's
+  // output buffer has been downloaded
+  OIDNX_CUDA(cudaStreamWaitEvent(s, f->ev_in[b], 0));
+  if (f->host_used[b]) OIDNX_CUDA(cudaStreamWaitEvent(s, f->ev_out[b], 0));
   size_t stride[4];
   for (int i = 0; i < 4; ++i) stride[i] = static_cast<size_t>(f->width) * 16;
-  OIDNX_TRY(execute_images(f, f->host_img, stride, s));
-  OIDNX_CUDA(cudaMemcpyAsync(output, f->host_img[3], bytes, cudaMemcpyDeviceToHost, s));
-  OIDNX_CUDA(cudaStreamSynchronize(s));
+  OIDNX_TRY(execute_images(f, img, stride, s));
+  OIDNX_CUDA(cudaEventRecord(f->ev_comp[b], s));
+  // download
+  OIDNX_CUDA(cudaStreamWaitEvent(f->host_out, f->ev_comp[b], 0));
+  OIDNX_CUDA(cudaMemcpyAsync(output, img[3], bytes, cudaMemcpyDeviceToHost, f->host_out));
+  OIDNX_CUDA(cudaEventRecord(f->ev_out[b], f->host_out));
+  f->host_used[b] = true;
   return ok();
+}
+
+oidnx_status oidnx_filter_wait_host(oidnx_filter* f) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  if (f->host_out) OIDNX_CUDA(cudaStreamSynchronize(f->host_out));
+  return ok();
+}
+
+oidnx_status oidnx_filter_execute_host(oidnx_filter* f, const float* color, const float* albedo,
+                                       const float* normal, float* output, void* stream) {
+  OIDNX_TRY(oidnx_filter_execute_host_async(f, color, albedo, normal, output, stream));
+  return oidnx_filter_wait_host(f);
 }
 
 oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w, int h,
@@ -1928,9 +1988,6 @@ oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w
     return fail(OIDNX_ERR_INVALID_ARGUMENT, "network_execute: pointers must be 16-byte aligned");
   Plan* P = nullptr;
   OIDNX_TRY(get_plan(f, w, h, &P));
-  if (f->current != P && f->graph) {
-    // the denoise graph stays valid: it refers to its own plan
-  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool prof = f->profile_next || f->profile_always;
   f->profile_next = false;
@@ -2045,8 +2102,10 @@ oidnx_status oidnx_get_resource_info(oidnx_filter* f, char* json, size_t cap) {
   snprintf(buf, sizeof(buf),
            "{\"weightBytes\":%zu,\"arenaBytes\":%zu,\"plans\":%zu,\"retiredPlans\":%zu,"
            "\"graphs\":%d,\"hostImageBytes\":%zu,\"precision\":\"%s\",\"inputChannels\":%d}",
-           f->weight_bytes, arena, f->plans.size(), f->retired.size(), f->graph ? 1 : 0,
-           f->host_img_bytes * 4, f->precision == OIDNX_PRECISION_FP16 ? "fp16" : "fp32",
+           f->weight_bytes, arena, f->plans.size(), f->retired.size(),
+           (f->graphs[0].exec ? 1 : 0) + (f->graphs[1].exec ? 1 : 0),
+           f->host_img_bytes * 4 * ((f->host_img[0][0] ? 1 : 0) + (f->host_img[1][0] ? 1 : 0)),
+           f->precision == OIDNX_PRECISION_FP16 ? "fp16" : "fp32",
            f->in_channels);
   if (strlen(buf) + 1 > cap) return fail(OIDNX_ERR_INVALID_ARGUMENT, "buffer too small");
   std::memcpy(json, buf, strlen(buf) + 1);
@@ -2104,13 +2163,20 @@ void oidnx_filter_release(oidnx_filter* f) {
   if (!f || f->released) return;
   f->released = true;
   cudaDeviceSynchronize();
-  if (f->graph) cudaGraphExecDestroy(f->graph);
+  drop_graphs(f);
   for (auto& p : f->plans) destroy_plan(p.get());
   for (auto& p : f->retired) destroy_plan(p.get());
   f->plans.clear();
   f->retired.clear();
   for (DeviceLayer& L : f->layers) free_layer(L);
-  for (int i = 0; i < 4; ++i) cudaFree(f->host_img[i]);
+  for (int b = 0; b < 2; ++b) {
+    for (int i = 0; i < 4; ++i) cudaFree(f->host_img[b][i]);
+    if (f->ev_in[b]) cudaEventDestroy(f->ev_in[b]);
+    if (f->ev_comp[b]) cudaEventDestroy(f->ev_comp[b]);
+    if (f->ev_out[b]) cudaEventDestroy(f->ev_out[b]);
+  }
+  if (f->host_in) cudaStreamDestroy(f->host_in);
+  if (f->host_out) cudaStreamDestroy(f->host_out);
   for (cudaEvent_t e : f->prof.ev) cudaEventDestroy(e);
   if (f->capture_stream) cudaStreamDestroy(f->capture_stream);
   cudaFree(f->status);

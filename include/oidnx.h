@@ -128,14 +128,30 @@ oidnx_status oidnx_filter_commit(oidnx_filter* f);
 oidnx_status oidnx_filter_execute(oidnx_filter* f, void* stream);
 
 /* Same denoise with HOST images (float4 RGBA, width*16 bytes per row):
- * copies the inputs to filter-owned device buffers, executes, and copies
- * the output back, all on `stream`; returns after the stream has finished.
+ * copies the inputs to filter-owned device buffers, executes on `stream`,
+ * and copies the output back; returns once the output is in `output`.
  * Inputs not used by the model (albedo/normal for 3-channel models) may be
  * NULL.  The device images bound by set_image are not touched.
  * Errors: as execute, plus INVALID_ARGUMENT, OUT_OF_MEMORY.  */
 oidnx_status oidnx_filter_execute_host(oidnx_filter* f, const float* color,
                                        const float* albedo, const float* normal,
                                        float* output, void* stream);
+
+/* The same, returning once the work is enqueued, for frame streams.  The
+ * inputs are uploaded on an internal stream into one of two filter-owned
+ * device staging sets, the denoise runs on `stream`, and the output is
+ * downloaded on a second internal stream.  Consecutive calls alternate the
+ * sets, so that one call's upload and another's download overlap a
+ * denoise.  The caller keeps the input buffers unchanged and does not read
+ * `output` until oidnx_filter_wait_host has returned; pinned host memory
+ * gives the full link bandwidth.  Errors: as oidnx_filter_execute_host.  */
+oidnx_status oidnx_filter_execute_host_async(oidnx_filter* f, const float* color,
+                                             const float* albedo, const float* normal,
+                                             float* output, void* stream);
+
+/* Block until every download enqueued by the host-buffer calls of `f` has
+ * finished.  Errors: RELEASED, CUDA.  */
+oidnx_status oidnx_filter_wait_host(oidnx_filter* f);
 
 /* The network alone (conv layers enc_conv0 .. dec_conv0) on one packed input
  * ("nativeUNet.ts", execute / executePacked):

@@ -46,7 +46,8 @@ def test_graph_replay_equals_eager_and_host_path(weights):
     assert all(l["launches"] == 10 for l in prof["layers"])
     assert all(l["ms"] > 0 for l in prof["layers"])
     assert prof["totalMs"] >= sum(l["ms"] for l in prof["layers"]) * 0.99
-    assert info["graphs"] == 1 and info["plans"] >= 1 and info["weightBytes"] > 0
+    # one graph for the bound device images, one for the host path's staging set
+    assert info["graphs"] == 2 and info["plans"] >= 1 and info["weightBytes"] > 0
 
 
 def test_profile_every_execution_through_the_graph(weights):
@@ -138,3 +139,33 @@ def test_bounded_device_wait_reports_timeout_and_context_survives(weights):
         assert torch.equal(out0, out1)
     finally:
         ox.oidnx_filter_release(f)
+
+
+def test_host_async_frame_stream_equals_sync_calls(weights):
+    # five frames in flight through the two staging sets: every output equals
+    # the synchronous host call's, bit for bit, whatever the overlap
+    w, h = 200, 120
+    frames = []
+    for k in range(5):
+        imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+        frames.append([np.ascontiguousarray(im * np.float32(1.0 + 0.25 * k)) for im in imgs])
+        frames[-1][0][..., 3] = np.float32(k)   # distinct alpha per frame
+    d = Denoiser(weights, ox.PRECISION_FP16, frames[0], True)
+    try:
+        sync = []
+        for fr in frames:
+            out = np.zeros((h, w, 4), np.float32)
+            ox.oidnx_filter_execute_host(d.f, fr[0], fr[1], fr[2], out, stream())
+            sync.append(out)
+        outs = [np.full((h, w, 4), np.nan, np.float32) for _ in frames]
+        for fr, out in zip(frames, outs):
+            ox.oidnx_filter_execute_host_async(d.f, fr[0], fr[1], fr[2], out, stream())
+        ox.oidnx_filter_wait_host(d.f)
+        info = ox.oidnx_get_resource_info(d.f)
+    finally:
+        d.close()
+    for k in range(len(frames)):
+        assert np.array_equal(outs[k].view(np.uint32), sync[k].view(np.uint32)), k
+        assert (outs[k][..., 3] == k).all()
+    assert not np.array_equal(sync[0], sync[1])
+    assert info["graphs"] == 2 and info["hostImageBytes"] == 2 * 4 * w * h * 16
