@@ -128,6 +128,44 @@ cudaError_t launch_conv_pair(const PairConvLaunch& L, cudaStream_t stream);
 cudaError_t conv_pair_set_smem_limit(size_t bytes);
 cudaError_t conv_pair_occupancy(int mode, size_t smem, int* blocks_per_sm);
 
+// The final conv (32 -> 3, bias, no ReLU; fp16 operands) with the three kx
+// taps folded into N: tiles of kFinalRows rows x kFinalSpan output pixels.
+// Optionally the output pass runs in its epilogue (denoise path), writing
+// the output image directly.
+constexpr int kFinalRows = 8;
+constexpr int kFinalSpan = kTileM - 2;
+
+struct FinalConvParams {
+  const __half* w;         // folded B operand: [kb][2][3 x 16][8], row 16 (2 - ky) + 4 kx + co
+  const float* bias;       // [16]: b0, b1, b2, zeros
+  float4* net;             // [H][W] network output (lane 3 zero), or null
+  int* status;
+  int W, H;                // conv extent
+  int tiles_x, tiles_y;    // tiles of kFinalRows rows x kFinalSpan pixels
+  int S;                   // stages (one per K block)
+  uint32_t stage_tx, stage_bytes;
+  int xs;                  // log2 pixels per x unit of the input map
+  // output pass (when fused): the tile's output rectangle, as UnpackParams
+  const float4* color;
+  size_t color_stride;
+  float4* out;
+  size_t out_stride;
+  int in_x, in_y, ox, oy, ow, oh;
+  int hdr;
+  float scale;
+};
+
+struct FinalConvLaunch {
+  CUtensorMap map;         // input: boxes of kFinalRows + 2 rows x kHaloW pixels x 2 chunks
+  FinalConvParams p;
+  int outpass;             // epilogue also runs the output pass
+  dim3 grid;
+  size_t smem;
+};
+
+cudaError_t launch_conv_final(const FinalConvLaunch& L, cudaStream_t stream);
+cudaError_t conv_final_set_smem_limit(size_t bytes);
+
 struct TcConvLaunch {
   CUtensorMap map0;        // source 0 (full-res halo box, or low-res box)
   CUtensorMap map1;        // source 1 (full-res halo box, or stride-2 box); unused if KB1 == 0

@@ -17,18 +17,12 @@
 #include <cmath>
 
 #include "internal.h"
+#include "passes.cuh"
 #include "ptx.cuh"
 
 namespace oidnx {
 
 namespace {
-
-__device__ __forceinline__ float sanitize(float v, float lo, float hi) {
-  if (isnan(v)) v = 0.0f;
-  if (v < lo) v = lo;
-  else if (v > hi) v = hi;
-  return v;
-}
 
 constexpr double kLn2 = 0.69314718055994530942;
 
@@ -130,11 +124,6 @@ __device__ __forceinline__ float hdr_forward_f32(float s, const float4* __restri
   const float y1 = __fadd_rn(y, __fadd_rn(yl, tol));
   if (y0 == y1) return y0;
   return __double2float_rn(log1p(static_cast<double>(s)) / kLn2);
-}
-
-// F^-1(d) = 2^d - 1 for d >= 0: expm1 where cancellation would hurt.
-__device__ __forceinline__ float hdr_inverse(float d) {
-  return d < 1.0f ? expm1f(d * 0.693147180559945309f) : exp2f(d) - 1.0f;
 }
 
 template <int SOURCES, bool FP16, bool HDR>
@@ -241,17 +230,8 @@ __global__ void unpack_kernel(const UnpackParams p) {
   if (x >= p.ow) return;
   const float4 net = p.net[static_cast<size_t>(y + p.in_y) * p.tw + x + p.in_x];
   const float4 col = p.color[static_cast<size_t>(y + p.oy) * p.color_stride + x + p.ox];
-  const float hi = p.hdr ? FLT_MAX : 1.0f;
-  float r = sanitize(net.x, 0.0f, hi);
-  float g = sanitize(net.y, 0.0f, hi);
-  float b = sanitize(net.z, 0.0f, hi);
-  if (p.hdr) {
-    r = __fdiv_rn(hdr_inverse(r), p.scale);
-    g = __fdiv_rn(hdr_inverse(g), p.scale);
-    b = __fdiv_rn(hdr_inverse(b), p.scale);
-  }
-  const float a = __int_as_float(__float_as_int(col.w));
-  p.out[static_cast<size_t>(y + p.oy) * p.out_stride + x + p.ox] = make_float4(r, g, b, a);
+  p.out[static_cast<size_t>(y + p.oy) * p.out_stride + x + p.ox] =
+      output_pixel(net.x, net.y, net.z, col, p.hdr, p.scale);
 }
 
 __global__ void split_copy_kernel(const uint4* src, int src_pitch, uint4* dst, int dst_pitch,

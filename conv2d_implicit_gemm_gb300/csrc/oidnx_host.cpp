@@ -624,9 +624,11 @@ int split_pitch(int w) { return (w + 2 * kGroupPx - 1) / (2 * kGroupPx) * (2 * k
 struct LayerLaunch {
   int layer;               // first layer of the launch
   int pair;                // 1: layers `layer` and `layer + 1` fused (pcl)
+  int final;               // 1: the final conv with kx folded (fcl)
   const char* name;
   TcConvLaunch tcl;
   PairConvLaunch pcl;
+  FinalConvLaunch fcl;
   double flop;   // logical conv FLOPs
   double bytes;  // algorithmic bytes: inputs read once, output written once
 };
@@ -670,7 +672,7 @@ struct oidnx_filter {
   // parameters
   int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
       overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 1,
-      fuse = 0;
+      fuse = 0, fuse_output = 1;
   float input_scale = 1.0f;
   void* img[4] = {};
   size_t img_stride[4] = {};
@@ -1130,8 +1132,55 @@ oidnx_status build_pair_launch(const DeviceLayer& A, const DeviceLayer& B, int m
                         p.C8);
 }
 
+// The final conv with kx folded (fp16, 32 -> 3): tiles of kFinalRows rows x
+// kFinalSpan pixels over the W x H extent, writing the network output to
+// `net` (may be null when the output pass runs in the epilogue).
+bool final_foldable(const DeviceLayer& L) {
+  return !L.tf32 && L.wfold && L.cin == 32 && L.cout == 3 && L.c1 == 0;
+}
+
+oidnx_status build_final_launch(const DeviceLayer& L, const void* src, Extent ext, int W, int H,
+                                void* net, int* status, FinalConvLaunch* T) {
+  T->outpass = 0;
+  FinalConvParams& p = T->p;
+  std::memset(&p, 0, sizeof(p));
+  p.w = static_cast<const __half*>(L.wfold);
+  p.bias = L.bias;
+  p.net = static_cast<float4*>(net);
+  p.status = status;
+  p.W = W;
+  p.H = H;
+  p.tiles_x = (W + kFinalSpan - 1) / kFinalSpan;
+  p.tiles_y = (H + kFinalRows - 1) / kFinalRows;
+  p.stage_tx = static_cast<uint32_t>((kFinalRows + 2) * 2 * kHaloW * kChunkBytes);
+  p.stage_bytes = static_cast<uint32_t>(round_up_sz(p.stage_tx, 1024));
+  // alignment slack, weights, exchange buffers, bias, barriers (10 + 2 per stage)
+  // alignment slack, weights, boundary exchange (4 sub x 2 x 4 quarters x
+  // 2 rows x 3 float4), bias, barriers (14 + 2 per stage)
+  const size_t fixed = 1024 + 2 * 2 * 3 * 16 * kChunkBytes + 4 * 2 * 4 * 2 * 3 * 16 + 16 * 4 + 14 * 8 + 16;
+  const size_t max_smem = 227 * 1024;
+  p.S = static_cast<int>(std::min<size_t>(4, (max_smem - fixed) / (16 + p.stage_bytes)));
+  if (p.S < 2) return fail(OIDNX_ERR_UNSUPPORTED, "final conv stages do not fit");
+  T->smem = fixed + static_cast<size_t>(p.S) * (16 + p.stage_bytes);
+  static bool limit_set = false;
+  if (!limit_set) {
+    cudaError_t e = conv_final_set_smem_limit(max_smem);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
+    limit_set = true;
+  }
+  const long tiles = static_cast<long>(p.tiles_x) * p.tiles_y;
+  T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, num_sms())), 1, 1);
+  return encode_act_map(&T->map, src, ext.w, ext.pitch, ext.h, act_chunks(OIDNX_PRECISION_FP16, L.cin),
+                        kHaloW, kFinalRows + 2, true, &p.xs);
+}
+
 oidnx_status run_launch(const LayerLaunch& L, cudaStream_t s) {
   (void)cudaGetLastError();  // drop a stale, non-sticky error of an earlier call
+  if (L.final) {
+    cudaError_t e = launch_conv_final(L.fcl, s);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "%s launch: %s", L.name, cudaGetErrorString(e));
+    return ok();
+  }
   if (L.pair) {
     cudaError_t e = launch_conv_pair(L.pcl, s);
     if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "%s launch: %s", L.name, cudaGetErrorString(e));
@@ -1283,6 +1332,17 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
       ++l;
       continue;
     }
+    if (d.kind == kFinal && final_foldable(L)) {
+      LL.final = 1;
+      OIDNX_TRY(build_final_launch(L, P->ptr(d.src0), P->value_ext[d.src0], conv.w, conv.h,
+                                   P->ptr(d.dst), f->status, &LL.fcl));
+      const double px = static_cast<double>(conv.w) * conv.h;
+      LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
+      LL.bytes = value_bytes(d.src0) + static_cast<double>(P->value_ext[d.dst].w) * P->value_ext[d.dst].h * 16 +
+                 static_cast<double>(L.weight_bytes);
+      P->launches.push_back(LL);
+      continue;
+    }
     const void* s1 = d.src1 >= 0 ? P->ptr(d.src1) : nullptr;
     Extent e1 = d.src1 >= 0 ? P->value_ext[d.src1] : Extent{0, 0, 0};
     bool subpixel = false;
@@ -1399,6 +1459,12 @@ oidnx_status enqueue_network(oidnx_filter* f, Plan* P, bool prof, cudaStream_t s
   return ok();
 }
 
+// The output pass runs in the final conv's epilogue (kx-folded final conv,
+// "fuseOutput" on).
+bool output_fused(const oidnx_filter* f, const Plan* P) {
+  return P && f->fuse_output && !P->launches.empty() && P->launches.back().final;
+}
+
 // All tiles: input pass -> network -> output pass, on stream s.
 oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t stride[4],
                              bool prof, cudaStream_t s) {
@@ -1434,6 +1500,33 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
       cudaError_t e = launch_pack(pp, s);
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
       OIDNX_TRY(prof_mark(f, prof, -1, s));
+      if (output_fused(f, P)) {
+        // the final conv's epilogue runs the output pass for this tile
+        for (size_t i = 0; i + 1 < P->launches.size(); ++i) {
+          OIDNX_TRY(run_launch(P->launches[i], s));
+          OIDNX_TRY(prof_mark(f, prof, P->launches[i].layer, s));
+        }
+        LayerLaunch L = P->launches.back();
+        L.fcl.outpass = 1;
+        L.name = "dec_conv0+output";
+        FinalConvParams& fp = L.fcl.p;
+        fp.net = f->keep_acts ? static_cast<float4*>(P->ptr(V_OUT)) : nullptr;
+        fp.color = static_cast<const float4*>(img[0]);
+        fp.color_stride = stride[0] / 16;
+        fp.out = static_cast<float4*>(img[3]);
+        fp.out_stride = stride[3] / 16;
+        fp.in_x = tx.out_start - tx.in_start;
+        fp.in_y = ty.out_start - ty.in_start;
+        fp.ox = tx.out_start;
+        fp.oy = ty.out_start;
+        fp.ow = tx.out_size;
+        fp.oh = ty.out_size;
+        fp.hdr = f->hdr;
+        fp.scale = scale;
+        OIDNX_TRY(run_launch(L, s));
+        OIDNX_TRY(prof_mark(f, prof, L.layer, s));
+        continue;
+      }
       OIDNX_TRY(enqueue_network(f, P, prof, s));
       UnpackParams up;
       std::memset(&up, 0, sizeof(up));
@@ -1459,7 +1552,11 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
 }
 
 size_t denoise_launches(const oidnx_filter* f) {
-  return f->tx.size() * f->ty.size() * (kLayers + 2);
+  // input pass, the plan's conv launches, output pass (folded into the final
+  // conv when fused)
+  const Plan* P = f->current;
+  const size_t convs = P ? P->launches.size() : kLayers;
+  return f->tx.size() * f->ty.size() * (convs + (output_fused(f, P) ? 1 : 2));
 }
 
 bool filter_alive(oidnx_filter* f, oidnx_status* st) {
@@ -1663,6 +1760,13 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
       ++l;
       continue;
     }
+    if (d.kind == kFinal && final_foldable(L)) {
+      LL.final = 1;
+      OIDNX_TRY(build_final_launch(L, ptr(d.src0), ext[d.src0], conv.w, conv.h, ptr(d.dst), f->status,
+                                   &LL.fcl));
+      OIDNX_TRY(run_launch(LL, s));
+      continue;
+    }
     const void* s1 = d.src1 >= 0 ? ptr(d.src1) : nullptr;
     Extent e1 = d.src1 >= 0 ? ext[d.src1] : Extent{0, 0, 0};
     bool subpixel = false;
@@ -1812,6 +1916,8 @@ oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value) 
   } else if (n == "shapeCacheSize") {
     if (value < 1) return fail(OIDNX_ERR_INVALID_ARGUMENT, "shapeCacheSize must be >= 1");
     f->shape_cache = value;
+  } else if (n == "fuseOutput") {
+    f->fuse_output = value ? 1 : 0;  // the graph is re-recorded on commit
   } else if (n == "keepActivations" || n == "subpixelDecoder" || n == "fuseLayers") {
     (n == "keepActivations" ? f->keep_acts : n == "subpixelDecoder" ? f->subpixel : f->fuse) =
         value ? 1 : 0;
@@ -1844,6 +1950,7 @@ oidnx_status oidnx_filter_get_int(oidnx_filter* f, const char* name, int* value)
   else if (n == "keepActivations") *value = f->keep_acts;
   else if (n == "subpixelDecoder") *value = f->subpixel;
   else if (n == "fuseLayers") *value = f->fuse;
+  else if (n == "fuseOutput") *value = f->fuse_output;
   else if (n == "profile") *value = f->profile_always;
   else if (n == "inputChannels") *value = f->in_channels;
   else if (n == "precision") *value = f->precision;
@@ -2079,13 +2186,20 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
   const int bpe = f->precision == OIDNX_PRECISION_FP16 ? 2 : 4;
   const double tile_px = plan ? static_cast<double>(plan->w) * plan->h : 0;
   add("input-pack", 1, 0, tile_px * (16.0 * sources + f->in_channels * bpe));
-  if (plan)
-    for (const LayerLaunch& L : plan->launches) add(L.name, L.layer + 2, L.flop, L.bytes);
   double out_px = 0;
   for (const AxisTile& y : f->ty)
     for (const AxisTile& x : f->tx) out_px += static_cast<double>(x.out_size) * y.out_size;
   const int tiles = static_cast<int>(std::max<size_t>(1, f->tx.size() * f->ty.size()));
-  add("output", kLayers + 2, 0, out_px / tiles * 48.0);
+  const double out_bytes = out_px / tiles * 48.0;  // per tile: net + colour read, image written
+  if (plan)
+    for (const LayerLaunch& L : plan->launches) {
+      const bool fused_out = &L == &plan->launches.back() && output_fused(f, plan);
+      // with the output pass fused the network output is not stored: the
+      // kernel reads the colour and writes the image instead
+      add(fused_out ? "dec_conv0+output" : L.name, L.layer + 2, L.flop,
+          fused_out ? L.bytes - tile_px * 16 + out_bytes - out_px / tiles * 16 : L.bytes);
+    }
+  add("output", kLayers + 2, 0, out_bytes);
   s += "]}";
   if (s.size() + 1 > cap) return fail(OIDNX_ERR_INVALID_ARGUMENT, "profile buffer too small");
   std::memcpy(json, s.c_str(), s.size() + 1);

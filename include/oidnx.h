@@ -104,6 +104,9 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *                        on GB300 the separate kernels are faster (the MMAs
  *                        of these layers are bound by shared-memory operand
  *                        reads, which fusion does not reduce)
+ *   "fuseOutput"         1 = with fp16 storage, the output pass runs in the
+ *                        final conv's epilogue (the network output is then
+ *                        not stored unless "keepActivations" is 1); default 1
  *   "profile"            1 = record per-kernel events on every execute
  * Errors: INVALID_ARGUMENT for unknown names or out-of-range values.  */
 oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value);

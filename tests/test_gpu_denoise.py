@@ -67,7 +67,9 @@ def test_config_1080p_fp16_single_tile():
     w, h = 1920, 1080
     imgs = synth.denoise_inputs(w, h, 3, hdr=True)
     weights = synth.unet_weights(9)
-    d = Denoiser(weights, ox.PRECISION_FP16, imgs, True)
+    # keep=True: the network output is read back (with the output pass in
+    # the final conv's epilogue it is not stored otherwise)
+    d = Denoiser(weights, ox.PRECISION_FP16, imgs, True, keep=True)
     try:
         out = d.run()
         assert ox.oidnx_filter_get_int(d.f, "tiles") == 1
@@ -93,7 +95,7 @@ def test_config_4k_fp16_tiled_equals_single_tile():
         assert ox.oidnx_filter_get_int(d.f, "tiles") == 15
     finally:
         d.close()
-    d = Denoiser(weights, ox.PRECISION_FP16, imgs, True, max_tile_size=0)
+    d = Denoiser(weights, ox.PRECISION_FP16, imgs, True, max_tile_size=0, keep=True)
     try:
         whole = d.run()
         net = d.activation(16, 2160, 3840, 3)   # 2160 is already 16-aligned
@@ -128,7 +130,7 @@ def test_subpixel_decoder_denoise_matches_oracle():
     weights = synth.unet_weights(9, bias_scale=0.05)
     outs = []
     for mode in (0, 1):
-        d = Denoiser(weights, ox.PRECISION_FP16, imgs, True)
+        d = Denoiser(weights, ox.PRECISION_FP16, imgs, True, keep=True)
         try:
             ox.oidnx_filter_set_int(d.f, "subpixelDecoder", mode)
             ox.oidnx_filter_commit(d.f)
@@ -140,3 +142,26 @@ def test_subpixel_decoder_denoise_matches_oracle():
     diff = np.abs(sanitize(net, 0, FLT_MAX).astype(np.float64) - sanitize(ref, 0, FLT_MAX))
     assert diff.max() <= 2e-2
     assert rel_l2(outs[1][..., :3], outs[0][..., :3]) <= 2e-2
+
+
+@pytest.mark.parametrize("hdr", [True, False])
+def test_output_pass_in_final_conv_equals_separate_pass(hdr):
+    """The output pass run in the final conv's epilogue gives the bits of the
+    separate output pass kernel, over a tile grid with ragged edges (so the
+    output rectangles are offset inside their tiles)."""
+    w, h = 700, 430
+    imgs = synth.denoise_inputs(w, h, 3, hdr=hdr, nan_fraction=0.02)
+    weights = synth.unet_weights(9, bias_scale=0.05)
+    outs = []
+    for fuse in (1, 0):
+        d = Denoiser(weights, ox.PRECISION_FP16, imgs, hdr, input_scale=0.7 if hdr else 1.0,
+                     max_tile_size=256, overlap=96)
+        try:
+            ox.oidnx_filter_set_int(d.f, "fuseOutput", fuse)
+            ox.oidnx_filter_commit(d.f)
+            assert ox.oidnx_filter_get_int(d.f, "tiles") > 4
+            outs.append(d.run())
+        finally:
+            d.close()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert np.array_equal(outs[0][..., 3].view(np.uint32), imgs[0][..., 3].view(np.uint32))
