@@ -40,15 +40,25 @@
 //    one block per pipeline stage is streamed with the A halo.
 //  * Warp roles: warp 0 issues TMA, warp 1 allocates TMEM and issues the
 //    MMAs from one thread, warps 2-9 run the epilogue (bias, ReLU, pool,
-//    fp16/fp32 stores), warps 10-13 (decoders only) build the upsampled halo
-//    in shared memory from a low-resolution TMA box, since nearest
-//    upsampling is not an affine TMA box.
+//    fp16/fp32 stores), warps 10-13 (expansion decoders and fp32 kinds)
+//    build the upsampled halo in shared memory from a low-resolution TMA
+//    box, since nearest upsampling is not an affine TMA box, and split fp32
+//    operands into their tf32 parts.
 //  * Every wait is bounded: on timeout the kernel records a bit in the
 //    status word, lets its in-flight copies land, frees TMEM and returns.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace oidnx {
+
+// 3xTF32 kinds (fp32 storage), expansion and sub-pixel decoder kinds, and the
+// kinds with the four helper warps
+template <int KIND> __host__ __device__ constexpr bool kind_tf32() {
+  return KIND == kTcPlain32 || KIND == kTcExpand32 || KIND == kTcSubpixel32;
+}
+template <int KIND> __host__ __device__ constexpr bool kind_expand() { return KIND == kTcExpand || KIND == kTcExpand32; }
+template <int KIND> __host__ __device__ constexpr bool kind_subpixel() { return KIND == kTcSubpixel || KIND == kTcSubpixel32; }
+template <int KIND> __host__ __device__ constexpr bool kind_helpers() { return kind_tf32<KIND>() || kind_expand<KIND>(); }
 
 namespace {
 
@@ -66,7 +76,7 @@ __device__ __forceinline__ void tile_origin_k(const TcConvParams& p, int tile, i
   const int ty = tile / p.tiles_x;
   const int tx = tile - ty * p.tiles_x;
   *y0 = ty * p.R;
-  if (KIND == kTcSubpixel) {
+  if (kind_subpixel<KIND>()) {
     *x0 = (tx >> 1) * (2 * kTileM);
     *px = tx & 1;
   } else {
@@ -169,7 +179,7 @@ __device__ __forceinline__ void issue_kblock_r(int R, uint64_t ad, uint64_t bd, 
 // (1,+1), (0,0), (1,0), (0,-1) in (row parity, row offset)), whose summed
 // weights are stacked along N in that order; the column offset dx runs over
 // two values selected by px (A shifted by d + px pixels).
-template <int R, int G>
+template <int R, int G, bool TF>
 __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
                                          int px, int pxb, uint32_t row16, uint32_t id1,
                                          uint32_t id2, uint32_t id3, uint32_t id4) {
@@ -186,8 +196,8 @@ __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbas
       for (int c = lo; c <= hi; c += G) {
         const int e = c + G - 1 < hi ? c + G - 1 : hi;
         const int n = e - c + 1;
-        umma(dbase + c * N, a, bdk + static_cast<uint32_t>(c - 2 * hl + 3) * N,
-             n == 1 ? id1 : n == 2 ? id2 : n == 3 ? id3 : id4);
+        umma_k<TF>(dbase + c * N, a, bdk + static_cast<uint32_t>(c - 2 * hl + 3) * N,
+                   n == 1 ? id1 : n == 2 ? id2 : n == 3 ? id3 : id4);
       }
     }
   }
@@ -197,7 +207,7 @@ __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbas
 // plane of the skip source holds the skip pixels xb + px + kx - 1 + 2m (A
 // shifted by one element for kx = 2 in the outer plane); ky stacked along N
 // as in issue_kblock.
-template <int R, int G>
+template <int R, int G, bool TF>
 __device__ __forceinline__ void issue_skip(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
                                            uint32_t row16, uint32_t id1, uint32_t id2, uint32_t id3) {
 #pragma unroll
@@ -209,44 +219,64 @@ __device__ __forceinline__ void issue_skip(uint64_t ad, uint64_t bd, uint32_t db
     for (int c = lo; c <= hi; c += G) {
       const int e = c + G - 1 < hi ? c + G - 1 : hi;
       const int n = e - c + 1;
-      umma(dbase + c * N, a, bd + static_cast<uint32_t>(2 - h + c) * N,
-           n == 1 ? id1 : n == 2 ? id2 : id3);
+      umma_k<TF>(dbase + c * N, a, bd + static_cast<uint32_t>(2 - h + c) * N,
+                 n == 1 ? id1 : n == 2 ? id2 : id3);
     }
   }
 }
 
-template <int R, int G4, int G3>
+template <int R, int G4, int G3, bool TF>
 __device__ __forceinline__ void issue_subpixel_r(bool up, uint64_t ad, uint64_t bd,
                                                  uint32_t dbase, uint32_t N, int px, int pxb,
                                                  uint32_t row16, uint32_t id1, uint32_t id2,
                                                  uint32_t id3, uint32_t id4) {
   if (!up) {
     // bd: first kx slice; pxb (reused): 16-byte units to the second slice, 0 if none
-    issue_skip<R, G3>(ad, bd, dbase, N, row16, id1, id2, id3);
-    if (pxb) issue_skip<R, G3>(ad + 1, bd + static_cast<uint32_t>(pxb), dbase, N, row16, id1, id2, id3);
+    issue_skip<R, G3, TF>(ad, bd, dbase, N, row16, id1, id2, id3);
+    if (pxb) issue_skip<R, G3, TF>(ad + 1, bd + static_cast<uint32_t>(pxb), dbase, N, row16, id1, id2, id3);
   } else {
-    issue_up<R, G4>(ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4);
+    issue_up<R, G4, TF>(ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4);
   }
 }
 
-template <int G4, int G3>
+template <int G4, int G3, bool TF>
 __device__ __forceinline__ void issue_subpixel_item(int R, bool up, uint64_t ad, uint64_t bd,
                                                     uint32_t dbase, uint32_t N, int px, int pxb,
                                                     uint32_t row16, uint32_t id1, uint32_t id2,
                                                     uint32_t id3, uint32_t id4) {
   switch (R) {
-    case 2: issue_subpixel_r<2, G4, G3>(up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4); break;
-    case 4: issue_subpixel_r<4, G4, G3>(up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4); break;
-    default: issue_subpixel_r<8, G4, G3>(up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4); break;
+    case 2: issue_subpixel_r<2, G4, G3, TF>(up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4); break;
+    case 4: issue_subpixel_r<4, G4, G3, TF>(up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4); break;
+    default: issue_subpixel_r<8, G4, G3, TF>(up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4); break;
   }
 }
 
-}  // namespace
+// One sub-pixel item with the row grouping G4 = min(4, 256 / N) (upsampled
+// part; the skip part groups min(3, G4) rows).
+template <bool TF>
+__device__ __forceinline__ void issue_subpixel_g(int g4, int R, bool up, uint64_t ad, uint64_t bd,
+                                                 uint32_t dbase, uint32_t N, int px, int pxb,
+                                                 uint32_t row16, uint32_t id1, uint32_t id2,
+                                                 uint32_t id3, uint32_t id4) {
+  if (g4 == 4) issue_subpixel_item<4, 3, TF>(R, up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4);
+  else if (g4 == 2) issue_subpixel_item<2, 2, TF>(R, up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4);
+  else issue_subpixel_item<1, 1, TF>(R, up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4);
+}
 
-// 3xTF32 kinds (fp32 storage) and kinds with the four helper warps
-template <int KIND> __host__ __device__ constexpr bool kind_tf32() { return KIND == kTcPlain32 || KIND == kTcExpand32; }
-template <int KIND> __host__ __device__ constexpr bool kind_expand() { return KIND == kTcExpand || KIND == kTcExpand32; }
-template <int KIND> __host__ __device__ constexpr bool kind_helpers() { return kind_tf32<KIND>() || kind_expand<KIND>(); }
+// tf32 split of 16 staged bytes: hi = each float rounded to the nearest tf32
+// value (in place), lo = the remainder, exact, with |lo| <= 2^-11 |v|.
+__device__ __forceinline__ void split_tf32(uint4* hi, uint4* lo) {
+  const uint4 v = *hi;
+  const uint4 h = make_uint4((v.x + 0x1000u) & 0xFFFFE000u, (v.y + 0x1000u) & 0xFFFFE000u,
+                             (v.z + 0x1000u) & 0xFFFFE000u, (v.w + 0x1000u) & 0xFFFFE000u);
+  *lo = make_uint4(__float_as_uint(__uint_as_float(v.x) - __uint_as_float(h.x)),
+                   __float_as_uint(__uint_as_float(v.y) - __uint_as_float(h.y)),
+                   __float_as_uint(__uint_as_float(v.z) - __uint_as_float(h.z)),
+                   __float_as_uint(__uint_as_float(v.w) - __uint_as_float(h.w)));
+  *hi = h;
+}
+
+}  // namespace
 
 template <int KIND>
 __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTcThreads, 1)
@@ -259,7 +289,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
   const int S = p.S, R = p.R, N = p.N, KB0 = p.KB0;
   const int KB = p.KB0 + p.KB1;
   const int num_tiles = p.tiles_x * p.tiles_y;
-  constexpr bool SP = KIND == kTcSubpixel;
+  constexpr bool SP = kind_subpixel<KIND>();
   constexpr bool TF = kind_tf32<KIND>();
   constexpr bool EXP = kind_expand<KIND>();
   constexpr bool HELP = kind_helpers<KIND>();
@@ -433,11 +463,17 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
                               : idesc_f16_f32(kTileM, min(2 * N, 256));
       const uint32_t id3 = TF ? idesc_tf32_f32(kTileM, min(3 * N, 256))
                               : idesc_f16_f32(kTileM, min(3 * N, 256));
-      const uint32_t id4 = idesc_f16_f32(kTileM, min(4 * N, 256));
+      const uint32_t id4 = TF ? idesc_tf32_f32(kTileM, min(4 * N, 256))
+                              : idesc_f16_f32(kTileM, min(4 * N, 256));
       // tf32: the A_lo stages follow the A stages; each K block's B_lo
-      // follows its B_hi (half of the block)
+      // follows its B_hi (half of the block).  Sub-pixel: B_lo follows B_hi
+      // within each column parity's half of an upsampled block and within
+      // each kx slice of a skip block.
       const uint32_t alo16 = TF ? (static_cast<uint32_t>(S) * p.a_stage) >> 4 : 0u;
       const uint32_t blo16 = TF ? (p.b_tx / 2) >> 4 : 0u;
+      const uint32_t blo_up16 = TF ? (p.b_tx / 4) >> 4 : 0u;
+      const uint32_t blo_sk16 = TF ? (p.b_tx2 / 2) >> 4 : 0u;
+      constexpr int kPasses = TF ? 3 : 1;
       // sub-pixel boxes: rows of kHaloW entries starting kGroupPx left of the
       // block (low-resolution x0/2 - 1 at kHaloOff)
       const uint64_t a_up0 = smem_desc_noswizzle(smem_u32(A), kHaloW * kChunkBytes, 128);
@@ -492,12 +528,16 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
               const uint64_t bd = b_up0 + (woff >> 4);
               const uint32_t row16 = static_cast<uint32_t>(2 * p.up_pair * kHaloW);
               const int nkb = min(p.up_pair, KB0 - kb0);
-              for (int jj = 0; jj < nkb; ++jj) {
-                const uint64_t adj = ad + static_cast<uint32_t>(jj * 2 * kHaloW);
-                const uint64_t bdj = bd + static_cast<uint32_t>(jj) * (half >> 4);
-                if (g4 == 4) issue_subpixel_item<4, 3>(R, true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
-                else if (g4 == 2) issue_subpixel_item<2, 2>(R, true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
-                else issue_subpixel_item<1, 1>(R, true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
+              // tf32: passes A_hi B_hi, A_hi B_lo, A_lo B_hi
+#pragma unroll 1
+              for (int pass = 0; pass < kPasses; ++pass) {
+                const uint64_t ap = ad + (pass == 2 ? alo16 : 0u);
+                const uint64_t bp = bd + (pass == 1 ? blo_up16 : 0u);
+                for (int jj = 0; jj < nkb; ++jj) {
+                  const uint64_t adj = ap + static_cast<uint32_t>(jj * 2 * kHaloW);
+                  const uint64_t bdj = bp + static_cast<uint32_t>(jj) * (half >> 4);
+                  issue_subpixel_g<TF>(g4, R, true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
+                }
               }
               if (elect_one()) mma_commit(&empty[s]);
               continue;
@@ -517,9 +557,11 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
             const uint64_t ad = a_up0 + soff + static_cast<uint32_t>(aoff);
             const uint64_t bd = b_sk0 + (woff >> 4);
             const uint32_t row16 = static_cast<uint32_t>(2 * kHaloW);
-            if (g4 == 4) issue_subpixel_item<4, 3>(R, false, ad, bd, d_base, N, tpx, pxb, row16, id1, id2, id3, id4);
-            else if (g4 == 2) issue_subpixel_item<2, 2>(R, false, ad, bd, d_base, N, tpx, pxb, row16, id1, id2, id3, id4);
-            else issue_subpixel_item<1, 1>(R, false, ad, bd, d_base, N, tpx, pxb, row16, id1, id2, id3, id4);
+#pragma unroll 1
+            for (int pass = 0; pass < kPasses; ++pass)
+              issue_subpixel_g<TF>(g4, R, false, ad + (pass == 2 ? alo16 : 0u),
+                                   bd + (pass == 1 ? blo_sk16 : 0u), d_base, N, tpx, pxb, row16, id1,
+                                   id2, id3, id4);
             if (elect_one()) mma_commit(&empty[s]);
             continue;
           }
@@ -550,7 +592,23 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
     const int total = (R + 2) * 2 * kHaloPx;
     uint32_t it = 0, s = 0, ph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    // sub-pixel (tf32 only): every staged box is split whole, the upsampled
+    // items' low-resolution box or the skip items' plane box
+    for (int tile = blockIdx.x; SP && tile < num_tiles && ok; tile += gridDim.x) {
+      for (int kb = 0; kb < items; ++kb, ++it, next_stage(s, ph, S)) {
+        if (!mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutEpilogue)) {
+          ok = false;
+          break;
+        }
+        uint4* hi = reinterpret_cast<uint4*>(A + static_cast<size_t>(s) * p.a_stage);
+        uint4* lo = reinterpret_cast<uint4*>(ALO + static_cast<size_t>(s) * p.a_stage);
+        const int n16 = static_cast<int>((kb < n_up ? p.a_tx : p.st_tx) >> 4);
+        for (int i = et; i < n16; i += 128) split_tf32(hi + i, lo + i);
+        fence_proxy_async_smem();
+        mbar_arrive(&xdone[s]);
+      }
+    }
+    for (int tile = blockIdx.x; !SP && tile < num_tiles && ok; tile += gridDim.x) {
       int x0, y0;
       tile_origin(p, tile, &x0, &y0);
       const int ly0 = (y0 >> 1) - 1, lx0 = (x0 >> 1) - kGroupPx;
@@ -716,15 +774,22 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
               mx[k] = t;
             }
             // pooled columns [Wp, pitch) are row padding: stored as zeros
-            if (TF && ((lane & 1) == 0) && yp < Hp && xp < p.pitch) {
+            if (TF && ((lane & 1) == 0) && yp < Hp) {
               const bool pad = xp >= Wp;
               float* base = static_cast<float*>(p.out) + (static_cast<size_t>(yp) * p.out_c4 * p.pitch + xp) * 4;
+              // split copy: plane xp & 1, index xp >> 1 (the split pitch is even)
+              float* base2 = p.out_split == nullptr ? nullptr
+                             : static_cast<float*>(p.out_split) +
+                                   ((static_cast<size_t>(yp) * p.out_c4 * 2 + (xp & 1)) * (p.split_pitch >> 1) + (xp >> 1)) * 4;
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) {
                 const float4 f = pad ? make_float4(0.f, 0.f, 0.f, 0.f)
                                      : make_float4(mx[4 * q4], mx[4 * q4 + 1], mx[4 * q4 + 2], mx[4 * q4 + 3]);
-                if (4 * c + q4 < p.out_c4)
-                  *reinterpret_cast<float4*>(base + (4 * c + q4) * static_cast<size_t>(p.pitch) * 4) = f;
+                const int c4 = 4 * c + q4;
+                if (c4 < p.out_c4 && xp < p.pitch)
+                  *reinterpret_cast<float4*>(base + c4 * static_cast<size_t>(p.pitch) * 4) = f;
+                if (c4 < p.out_c4 && p.out_split && xp < p.split_pitch)
+                  *reinterpret_cast<float4*>(base2 + c4 * static_cast<size_t>(p.split_pitch) * 4) = f;
               }
             } else if (!TF && ((lane & 1) == 0) && yp < Hp) {
               const bool pad = xp >= Wp;
@@ -797,6 +862,9 @@ cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
   if (L.kind == kTcSubpixel)
     return launch_pdl(conv3x3_tc_kernel<kTcSubpixel>, L.grid, dim3(kTcThreads), L.smem, stream,
                       L.map0, L.map1, L.p);
+  if (L.kind == kTcSubpixel32)
+    return launch_pdl(conv3x3_tc_kernel<kTcSubpixel32>, L.grid, dim3(kTcThreadsDecoder), L.smem,
+                      stream, L.map0, L.map1, L.p);
   return launch_pdl(conv3x3_tc_kernel<kTcPlain>, L.grid, dim3(kTcThreads), L.smem, stream, L.map0,
                     L.map1, L.p);
 }
@@ -813,6 +881,9 @@ cudaError_t conv_tc_set_smem_limit(size_t bytes) {
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcExpand32>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcSubpixel32>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(conv3x3_tc_kernel<kTcPlain>,

@@ -53,13 +53,15 @@ struct TcConvParams {
   uint32_t b_stage;        // bytes per B block (1024-aligned)
   uint32_t st_stage;       // bytes per low-res staging stage (0 if none)
   uint32_t a_tx, b_tx, st_tx;  // transaction bytes per stage
-  // sub-pixel decoder: b_tx = upsampled B block (512 N), b_tx2 = skip B kx
-  // slice (96 N), st_tx = strided skip box; wres_bytes = resident weights
+  // sub-pixel decoder: b_tx = upsampled B block (512 N; tf32 1024 N), b_tx2 =
+  // skip B kx slice (96 N; tf32 192 N), st_tx = strided skip box; wres_bytes =
+  // resident weights
   uint32_t b_tx2;
   uint32_t wres_bytes;
   // pool epilogue: optional second copy of the output, column-parity split
-  // [Ho][N/8][2][split_pitch/2][8] (read by the sub-pixel decoder as its skip
-  // source); entries past the output width are written as zeros
+  // [Ho][N/8][2][split_pitch/2][8] (fp32: [Ho][out_c4][2][split_pitch/2][4])
+  // read by the sub-pixel decoder as its skip source; entries past the output
+  // width are written as zeros
   void* out_split;
   int split_pitch;
   int pitch;               // fp16 output row pitch in pixels (>= output width);
@@ -77,6 +79,7 @@ enum TcKind : int {
   kTcSubpixel = 2,  // decoder, upsampled part as parity-class 2x2 taps
   kTcPlain32 = 3,   // fp32 storage, 3xTF32 products: plain conv
   kTcExpand32 = 4,  // fp32 storage, 3xTF32 products: decoder with expansion
+  kTcSubpixel32 = 5,  // fp32 storage, 3xTF32 products: sub-pixel decoder
 };
 
 // Two same-padded 3x3 convs fused in one kernel (fp16 storage): conv 1

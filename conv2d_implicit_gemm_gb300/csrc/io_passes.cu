@@ -151,8 +151,13 @@ __global__ void pack_kernel(const PackParams p) {
       }
     } else {
       float4* out = static_cast<float4*>(p.out);
-      for (int j = 0; j < p.chunks; ++j)
-        out[pixel + static_cast<size_t>(j) * p.pitch] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const size_t half = static_cast<size_t>(p.split_pitch) >> 1;
+      for (int j = 0; j < p.chunks; ++j) {
+        if (tx < p.pitch) out[pixel + static_cast<size_t>(j) * p.pitch] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.out_split && tx < p.split_pitch)
+          static_cast<float4*>(p.out_split)[((static_cast<size_t>(ty) * p.chunks + j) * 2 + (tx & 1)) * half +
+                                            (tx >> 1)] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     return;
   }
@@ -215,10 +220,16 @@ __global__ void pack_kernel(const PackParams p) {
     for (int k = 0; k < 12; ++k)
       v[k] = k < kCh ? ((HDR && k < 3) ? hdr_forward_f32(ch[k], p.log2_tab) : ch[k]) : 0.0f;
     float4* out = static_cast<float4*>(p.out);
+    const size_t half = static_cast<size_t>(p.split_pitch) >> 1;
 #pragma unroll
-    for (int j = 0; j < (kCh + 3) / 4; ++j)
-      out[pixel + static_cast<size_t>(j) * p.pitch] =
-          make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    for (int j = 0; j < (kCh + 3) / 4; ++j) {
+      const float4 f = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      out[pixel + static_cast<size_t>(j) * p.pitch] = f;
+      // column-parity split copy: plane tx & 1, index tx >> 1
+      if (p.out_split)
+        static_cast<float4*>(p.out_split)[((static_cast<size_t>(ty) * p.chunks + j) * 2 + (tx & 1)) * half +
+                                          (tx >> 1)] = f;
+    }
   }
 }
 

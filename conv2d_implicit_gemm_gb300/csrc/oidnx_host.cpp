@@ -86,7 +86,7 @@ enum Kind { kPlain, kPool, kDecoder, kFinal };
 enum Val {
   V_IN, V_E0, V_P1, V_P2, V_P3, V_P4, V_E5A, V_E5B, V_D4A, V_D4B,
   V_D3A, V_D3B, V_D2A, V_D2B, V_D1A, V_D1B, V_OUT,
-  // column-parity split copies of the decoders' skip sources (fp16 only)
+  // column-parity split copies of the decoders' skip sources
   V_INS, V_P1S, V_P2S, V_P3S, V_COUNT
 };
 
@@ -313,6 +313,16 @@ std::vector<uint16_t> pack_weights_folded(const ConvTensors& L) {
   return out;
 }
 
+// tf32 split of an fp32 weight: hi = w rounded to the nearest tf32 value,
+// lo = w - hi (exact).
+void split_tf32(float w, float* hi, float* lo) {
+  uint32_t bits;
+  std::memcpy(&bits, &w, 4);
+  bits = (bits + 0x1000u) & 0xFFFFE000u;
+  std::memcpy(hi, &bits, 4);
+  *lo = w - *hi;
+}
+
 // fp32 storage: the B operand for 3xTF32 products.  K blocks of 8 channels
 // (two 16-byte chunks of 4 lanes) over each source padded to 4 lanes; per
 // block [hi, lo][kx][j][pos][N][4] floats with pos = 2 - ky, where hi is the
@@ -337,15 +347,12 @@ std::vector<float> pack_weights_tf32(const ConvTensors& L, int c0, int c1, int* 
               const int ch = first ? ci : c0 + ci;
               const int ky = 2 - pos;
               const float w = L.w[(static_cast<size_t>(n) * L.cin + ch) * 9 + ky * 3 + kx];
-              uint32_t bits;
-              std::memcpy(&bits, &w, 4);
-              bits = (bits + 0x1000u) & 0xFFFFE000u;  // nearest tf32 value
-              float hi;
-              std::memcpy(&hi, &bits, 4);
+              float hl[2];
+              split_tf32(w, &hl[0], &hl[1]);
               for (int part = 0; part < 2; ++part) {
                 const size_t idx =
                     ((((((static_cast<size_t>(kb) * 2 + part) * 3 + kx) * 2 + j) * 3 + pos) * (*N) + n) * 4) + l;
-                out[idx] = part == 0 ? hi : w - hi;
+                out[idx] = hl[part];
               }
             }
   return out;
@@ -359,20 +366,29 @@ std::vector<float> pack_weights_tf32(const ConvTensors& L, int c0, int c1, int* 
 // (ky in Ky(py,dy), kx in Kx(px,dx)), rounded once more to fp16.  Skip K
 // blocks follow in the plain layout.  Returns bytes of the upsampled part per
 // K block in *ub.
+// Taps of a 3x3 kernel row (or column) that fall on low-resolution offset
+// `off` for output parity `parity` under nearest 2x upsampling: the output at
+// 2i + parity reads the upsampled source at 2i + parity + k - 1, i.e. the
+// low-resolution pixel i + floor((parity + k - 1) / 2).
+int subpixel_taps(int parity, int off, int* t) {
+  if (parity == 0) {
+    if (off == -1) { t[0] = 0; return 1; }
+    t[0] = 1; t[1] = 2; return 2;       // off 0
+  }
+  if (off == 0) { t[0] = 0; t[1] = 1; return 2; }
+  t[0] = 2; return 1;                    // off +1
+}
+
+// (row parity, row offset) of the four row classes stacked along N
+const int kPosPy[4] = {1, 0, 1, 0}, kPosDy[4] = {1, 0, 0, -1};
+
 std::vector<uint16_t> pack_weights_subpixel(const ConvTensors& L, int c0, int c1, int N,
                                             size_t* ub) {
   const int p0 = round_up(c0, 16), p1 = round_up(c1, 16);
   const int KB0 = p0 / 16, KB1 = p1 / 16;
-  // taps of the 3x3 kernel (row or column) that fall on low-res offset d for parity p
-  auto taps = [](int parity, int off, int* t) -> int {
-    if (parity == 0) {
-      if (off == -1) { t[0] = 0; return 1; }
-      t[0] = 1; t[1] = 2; return 2;       // off 0
-    }
-    if (off == 0) { t[0] = 0; t[1] = 1; return 2; }
-    t[0] = 2; return 1;                    // off +1
-  };
-  const int pos_py[4] = {1, 0, 1, 0}, pos_dy[4] = {1, 0, 0, -1};
+  auto taps = subpixel_taps;
+  const int* pos_py = kPosPy;
+  const int* pos_dy = kPosDy;
   const size_t up_halves = static_cast<size_t>(2) * 2 * 2 * 4 * N * 8;   // per K block
   const size_t sk_halves = static_cast<size_t>(3) * 2 * 3 * N * 8;
   *ub = up_halves * 2;
@@ -412,6 +428,63 @@ std::vector<uint16_t> pack_weights_subpixel(const ConvTensors& L, int c0, int c1
               const size_t idx = KB0 * up_halves +
                                  ((((static_cast<size_t>(kb) * 3 + kx) * 2 + j) * 3 + pos) * N + n) * 8 + l;
               out[idx] = to_half_bits(w);
+            }
+  return out;
+}
+
+
+// Sub-pixel decoder B operand for fp32 storage (3xTF32 products): the same
+// per-class sums, taken in double over the fp32 weights and rounded once to
+// fp32, then split into tf32 hi and lo parts.  K blocks of 8 channels (two
+// 4-lane chunks j).  Upsampled blocks: [px][hi, lo][d][j][pos][N][4] floats
+// (1024 N bytes, so each column parity's half holds its hi and lo parts);
+// skip blocks, per kx slice: [hi, lo][j][pos][N][4] floats (192 N bytes),
+// pos = 2 - ky.  Returns bytes of the upsampled part per K block in *ub.
+std::vector<float> pack_weights_subpixel_tf32(const ConvTensors& L, int c0, int c1, int N,
+                                              size_t* ub) {
+  const int KB0 = (round_up(c0, 4) / 4 + 1) / 2, KB1 = (round_up(c1, 4) / 4 + 1) / 2;
+  const size_t up_f = static_cast<size_t>(2) * 2 * 2 * 2 * 4 * N * 4;  // floats per block
+  const size_t sl_f = static_cast<size_t>(2) * 2 * 3 * N * 4;          // floats per kx slice
+  *ub = up_f * 4;
+  std::vector<float> out(KB0 * up_f + static_cast<size_t>(KB1) * 3 * sl_f, 0.0f);
+  for (int kb = 0; kb < KB0; ++kb)
+    for (int px = 0; px < 2; ++px)
+      for (int d = 0; d < 2; ++d)
+        for (int j = 0; j < 2; ++j)
+          for (int pos = 0; pos < 4; ++pos) {
+            int kys[2], kxs[2];
+            const int nky = subpixel_taps(kPosPy[pos], kPosDy[pos], kys);
+            const int nkx = subpixel_taps(px, d - 1 + px, kxs);
+            for (int n = 0; n < L.cout; ++n)
+              for (int l = 0; l < 4; ++l) {
+                const int ch = kb * 8 + j * 4 + l;
+                if (ch >= c0) continue;
+                double sum = 0.0;
+                for (int a = 0; a < nky; ++a)
+                  for (int b = 0; b < nkx; ++b)
+                    sum += L.w[(static_cast<size_t>(n) * L.cin + ch) * 9 + kys[a] * 3 + kxs[b]];
+                float hl[2];
+                split_tf32(static_cast<float>(sum), &hl[0], &hl[1]);
+                for (int part = 0; part < 2; ++part)
+                  out[kb * up_f +
+                      ((((((static_cast<size_t>(px) * 2 + part) * 2 + d) * 2 + j) * 4 + pos) * N + n) * 4) + l] =
+                      hl[part];
+              }
+          }
+  for (int kb = 0; kb < KB1; ++kb)
+    for (int kx = 0; kx < 3; ++kx)
+      for (int j = 0; j < 2; ++j)
+        for (int pos = 0; pos < 3; ++pos)
+          for (int n = 0; n < L.cout; ++n)
+            for (int l = 0; l < 4; ++l) {
+              const int v = kb * 8 + j * 4 + l;
+              if (v >= c1) continue;
+              const int ky = 2 - pos;
+              float hl[2];
+              split_tf32(L.w[(static_cast<size_t>(n) * L.cin + c0 + v) * 9 + ky * 3 + kx], &hl[0], &hl[1]);
+              for (int part = 0; part < 2; ++part)
+                out[KB0 * up_f + (static_cast<size_t>(kb) * 3 + kx) * sl_f +
+                    (((static_cast<size_t>(part) * 2 + j) * 3 + pos) * N + n) * 4 + l] = hl[part];
             }
   return out;
 }
@@ -601,7 +674,7 @@ struct DeviceLayer {
   void* wtc = nullptr;  // packed tensor-core B operand (fp16, or tf32 hi/lo for fp32)
   bool tf32 = false;    // fp32 storage: 3xTF32 products
   int KB0 = 0, KB1 = 0, N = 0;
-  void* w16_sub = nullptr;  // sub-pixel decoder B operand (decoders only)
+  void* wsub = nullptr;  // sub-pixel decoder B operand (decoders only)
   size_t sub_bytes = 0, sub_ub = 0;
   void* wfold = nullptr;    // fused final conv: B operand with kx folded into N
   size_t fold_bytes = 0;
@@ -731,8 +804,8 @@ oidnx_status upload(const void* host, size_t bytes, void** dev) {
 }
 
 void free_layer(DeviceLayer& L) {
-  cudaFree(L.w16_sub);
-  L.w16_sub = nullptr;
+  cudaFree(L.wsub);
+  L.wsub = nullptr;
   cudaFree(L.wfold);
   L.wfold = nullptr;
   cudaFree(L.wtc);
@@ -754,7 +827,7 @@ oidnx_status make_device_layer(const ConvTensors& T, int c0, int c1, int precisi
     if (c1 > 0) {
       std::vector<uint16_t> ws = pack_weights_subpixel(T, c0, c1, L->N, &L->sub_ub);
       L->sub_bytes = ws.size() * 2;
-      OIDNX_TRY(upload(ws.data(), L->sub_bytes, &L->w16_sub));
+      OIDNX_TRY(upload(ws.data(), L->sub_bytes, &L->wsub));
     }
     if (T.cout == 3 && T.cin == 32 && c1 == 0) {
       std::vector<uint16_t> wf = pack_weights_folded(T);
@@ -770,10 +843,15 @@ oidnx_status make_device_layer(const ConvTensors& T, int c0, int c1, int precisi
     if (L->N > 256) return fail(OIDNX_ERR_UNSUPPORTED, "more than 256 output channels");
     OIDNX_TRY(upload(w.data(), w.size() * 4, &L->wtc));
     L->tf32 = true;
+    if (c1 > 0) {
+      std::vector<float> ws = pack_weights_subpixel_tf32(T, c0, c1, L->N, &L->sub_ub);
+      L->sub_bytes = ws.size() * 4;
+      OIDNX_TRY(upload(ws.data(), L->sub_bytes, &L->wsub));
+    }
     std::vector<float> b(L->N, 0.0f);
     std::copy(T.b.begin(), T.b.end(), b.begin());
     OIDNX_TRY(upload(b.data(), b.size() * 4, reinterpret_cast<void**>(&L->bias)));
-    L->weight_bytes = w.size() * 4 + b.size() * 4;
+    L->weight_bytes = w.size() * 4 + b.size() * 4 + L->sub_bytes;
   }
   return ok();
 }
@@ -783,7 +861,7 @@ oidnx_status make_device_layer(const ConvTensors& T, int c0, int c1, int precisi
 size_t act_bytes(int precision, Extent e, int c, bool final_out) {
   if (final_out) return static_cast<size_t>(e.w) * e.h * 16;
   if (precision == OIDNX_PRECISION_FP16) return static_cast<size_t>(e.pitch) * e.h * round_up(c, 16) * 2;
-  return static_cast<size_t>(e.w) * e.h * round_up(c, 4) * 4;
+  return static_cast<size_t>(e.pitch) * e.h * round_up(c, 4) * 4;
 }
 
 // Extent of a stored value of conv extent e.
@@ -833,7 +911,9 @@ oidnx_status bound_ctas_per_sm(size_t* smem, uint32_t tmem_cols, int* blocks) {
 
 // Sub-pixel decoder launch (even W and H): tiles of R rows x 128 outputs of
 // one column parity; the upsampled source is read as a low-resolution halo
-// box, the skip source (src1) from its column-parity split copy.
+// box, the skip source (src1) from its column-parity split copy.  fp16
+// layers, or fp32 layers (L.tf32: 3xTF32 products, every A stage followed by
+// its A_lo stage).
 oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Extent ext0,
                                       const void* src1, Extent ext1, int W, int H, void* out,
                                       int out_pitch, int* status, TcConvLaunch* T) {
@@ -847,8 +927,8 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   while (tmem_cols < static_cast<uint32_t>(2 * R * N)) tmem_cols *= 2;
   TcConvParams& p = T->p;
   std::memset(&p, 0, sizeof(p));
-  T->kind = kTcSubpixel;
-  p.weights = static_cast<const __half*>(L.w16_sub);
+  T->kind = L.tf32 ? kTcSubpixel32 : kTcSubpixel;
+  p.weights = static_cast<const __half*>(L.wsub);
   p.bias = L.bias;
   p.out = out;
   p.pitch = out_pitch;
@@ -861,14 +941,15 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   p.R = R;
   p.mode = kEpiRelu;
   p.upsample0 = 1;
+  p.out_c4 = round_up(L.cout, 4) / 4;
   p.tiles_x = tiles_x;
   p.tiles_y = (H + R - 1) / R;
   p.tmem_cols = tmem_cols;
   p.up_pair = 1;
   p.a_tx = static_cast<uint32_t>((R / 2 + 2) * 2 * kHaloW * kChunkBytes);    // low-res box
   p.st_tx = static_cast<uint32_t>((R + 2) * 2 * kHaloW * kChunkBytes);       // skip plane box
-  p.b_tx = static_cast<uint32_t>(L.sub_ub);                                  // 512 N
-  p.b_tx2 = static_cast<uint32_t>(6 * N * kChunkBytes);                      // 96 N
+  p.b_tx = static_cast<uint32_t>(L.sub_ub);                                  // 512 N (tf32 1024 N)
+  p.b_tx2 = static_cast<uint32_t>((L.tf32 ? 12 : 6) * N * kChunkBytes);      // 96 N (tf32 192 N)
   p.a_stage = static_cast<uint32_t>(round_up_sz(std::max(p.a_tx, p.st_tx), 1024));
   p.b_stage = static_cast<uint32_t>(round_up_sz(std::max(p.b_tx / 2, 2 * p.b_tx2), 1024));
   p.st_stage = 0;
@@ -880,21 +961,22 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
                       (L.sub_bytes - static_cast<size_t>(L.KB0) * L.sub_ub);
   const size_t wbytes = round_up_sz(wres, 1024);
   const int min_stages = std::max(2, std::min(items, 3));
+  const size_t a_mul = L.tf32 ? 2 : 1;  // A (and A_lo) stages
   size_t smem;
   // resident weights: pairs of upsampled K blocks per item (one wait and one
   // commit per pair) when at least three stages of the wider box still fit
   const uint32_t a_tx_pair = static_cast<uint32_t>((R / 2 + 2) * 4 * kHaloW * kChunkBytes);
   const uint32_t a_stage_pair = static_cast<uint32_t>(round_up_sz(std::max(a_tx_pair, p.st_tx), 1024));
-  if (L.KB0 >= 2 && fixed + wbytes + 3 * static_cast<size_t>(a_stage_pair) <= max_smem) {
+  if (L.KB0 >= 2 && fixed + wbytes + 3 * a_mul * a_stage_pair <= max_smem) {
     p.up_pair = 2;
     p.a_tx = a_tx_pair;
     p.a_stage = a_stage_pair;
   }
-  if (fixed + wbytes + min_stages * static_cast<size_t>(p.a_stage) <= max_smem) {
+  if (fixed + wbytes + min_stages * a_mul * p.a_stage <= max_smem) {
     p.resident = 1;
     p.wres_bytes = static_cast<uint32_t>(wres);  // bytes loaded; the layout rounds up to 1 KB
-    p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed - wbytes) / p.a_stage));
-    smem = fixed + wbytes + p.S * static_cast<size_t>(p.a_stage);
+    p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed - wbytes) / (a_mul * p.a_stage)));
+    smem = fixed + wbytes + p.S * a_mul * p.a_stage;
   } else {
     // streamed weights: each stage holds one upsampled K block's weights,
     // so an item is one K block
@@ -904,7 +986,7 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
       p.a_stage = static_cast<uint32_t>(round_up_sz(std::max(p.a_tx, p.st_tx), 1024));
     }
     p.resident = 0;
-    const size_t stage = static_cast<size_t>(p.a_stage) + p.b_stage;
+    const size_t stage = a_mul * p.a_stage + p.b_stage;
     p.S = static_cast<int>(std::min<size_t>(8, (max_smem - fixed) / stage));
     if (p.S < 2) return fail(OIDNX_ERR_UNSUPPORTED, "conv stage does not fit shared memory");
     smem = fixed + p.S * stage;
@@ -917,8 +999,10 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   // an even grid keeps each CTA on one column parity (tiles alternate parity)
   if (grid > 1 && grid % 2) --grid;
   T->grid = dim3(static_cast<unsigned>(grid), 1, 1);
-  const int c8_0 = round_up(L.c0, 16) / 8;
-  const int c8_1 = round_up(L.c1, 16) / 8;
+  // 16-byte chunks per pixel of each source: 8 halves, or 4 floats
+  auto chunks = [&](int c) { return L.tf32 ? round_up(c, 4) / 4 : round_up(c, 16) / 8; };
+  const int c8_0 = chunks(L.c0);
+  const int c8_1 = chunks(L.c1);
   OIDNX_TRY(encode_act_map(&T->map0, src0, ext0.w, ext0.pitch, ext0.h, c8_0, kHaloW, R / 2 + 2,
                            true, &p.xs0, 2 * p.up_pair));
   OIDNX_TRY(encode_split_map(&T->map1, src1, W, ext1.pitch, H, c8_1, kHaloW, R + 2, &p.xs1));
@@ -927,9 +1011,8 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
 
 // Whether a decoder with conv extent (W, H) and low-resolution source ext0
 // runs in sub-pixel mode (then its skip source must be the split copy).
-bool use_subpixel(int precision, int W, int H, Extent ext0) {
-  return precision == OIDNX_PRECISION_FP16 && W % 2 == 0 && H % 2 == 0 && ext0.w * 2 == W &&
-         ext0.h * 2 == H;
+bool use_subpixel(int W, int H, Extent ext0) {
+  return W % 2 == 0 && H % 2 == 0 && ext0.w * 2 == W && ext0.h * 2 == H;
 }
 
 // src0/src1: sources with their extents (pitch included); (W, H): conv
@@ -939,7 +1022,7 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
                              const void* src1, Extent ext1, int W, int H, void* out,
                              int out_pitch, int* status, TcConvLaunch* T, bool subpixel = false,
                              void* out_split = nullptr, int out_split_pitch = 0) {
-  if (kind == kDecoder && subpixel && L.w16_sub)
+  if (kind == kDecoder && subpixel && L.wsub)
     return build_tc_launch_subpixel(L, src0, ext0, src1, ext1, W, H, out, out_pitch, status, T);
   const bool up = kind == kDecoder;
   T->kind = up ? (L.tf32 ? kTcExpand32 : kTcExpand) : (L.tf32 ? kTcPlain32 : kTcPlain);
@@ -1234,8 +1317,8 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
   for (int i = 0; i < 4; ++i) {
     const SplitCopy& sc = kSplits[i];
     const LayerDef& d = kDefs[sc.consumer];
-    P->split_on[i] = f->subpixel && use_subpixel(f->precision, P->lvl[d.level].w,
-                                                 P->lvl[d.level].h, P->value_ext[d.src0]);
+    P->split_on[i] = f->subpixel && use_subpixel(P->lvl[d.level].w, P->lvl[d.level].h,
+                                                 P->value_ext[d.src0]);
     P->value_ext[sc.split] = P->value_ext[sc.base];
     P->value_ext[sc.split].pitch = split_pitch(P->value_ext[sc.base].w);
     P->value_ch[sc.split] = P->value_ch[sc.base];
@@ -1675,8 +1758,7 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
   for (int i = 0; i < 4; ++i) {
     const SplitCopy& sc = kSplits[i];
     const LayerDef& d = kDefs[sc.consumer];
-    split_on[i] = f->subpixel && use_subpixel(f->precision, lvl[d.level].w, lvl[d.level].h,
-                                              ext[d.src0]);
+    split_on[i] = f->subpixel && use_subpixel(lvl[d.level].w, lvl[d.level].h, ext[d.src0]);
     ext[sc.split] = ext[sc.base];
     ext[sc.split].pitch = split_pitch(ext[sc.base].w);
     ch[sc.split] = ch[sc.base];

@@ -92,11 +92,13 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *   "overlap"            -1 = alignUp(receptive field / 2, 16) (default)
  *   "shapeCacheSize"     number of per-shape plans kept (LRU, default 2)
  *   "keepActivations"    1 = no activation-slot reuse (for debug reads)
- *   "subpixelDecoder"    1 = fp16 decoder convs with even extents compute the
+ *   "subpixelDecoder"    1 = decoder convs with even extents compute the
  *                        upsampled part as parity-class 2x2 taps on the
  *                        low-resolution source (fewer MMAs; weights of one
- *                        class are summed, then rounded to fp16), reading
- *                        parity-split copies of the skip sources (default);
+ *                        class are summed, then rounded to fp16, or for fp32
+ *                        storage summed in double and rounded to fp32),
+ *                        reading parity-split copies of the skip sources
+ *                        (default);
  *                        0 builds the upsampled halo in shared memory
  *   "fuseLayers"         1 = with fp16 storage, enc_conv0+enc_conv1 and
  *                        dec_conv1b+dec_conv0 each run as one kernel that

@@ -67,7 +67,7 @@ def _run_network(weights, packed_logical, precision, subpixel=0, fuse=0):
     return acts, final
 
 
-@pytest.mark.parametrize("precision,subpixel", [("fp16", 0), ("fp16", 1), ("fp32", 0)])
+@pytest.mark.parametrize("precision,subpixel", [("fp16", 0), ("fp16", 1), ("fp32", 0), ("fp32", 1)])
 @pytest.mark.parametrize("w,h", [(64, 48), (80, 34), (130, 20), (512, 64)])
 def test_network_layers_match_oracle(precision, subpixel, w, h):
     weights = synth.unet_weights(9, bias_scale=0.05)
@@ -104,9 +104,9 @@ def test_network_one_pixel_and_tiny_inputs():
         assert np.abs(final[..., :3] - ref).max() <= 2e-2
 
 
-@pytest.mark.parametrize("precision", ["fp16", "fp32"])
+@pytest.mark.parametrize("precision,subpixel", [("fp16", 1), ("fp32", 0), ("fp32", 1)])
 @pytest.mark.parametrize("in_channels", [3, 6])
-def test_colour_only_and_colour_albedo_models_match_oracle(precision, in_channels):
+def test_colour_only_and_colour_albedo_models_match_oracle(precision, subpixel, in_channels):
     """The 3- and 6-channel model variants (colour; colour + albedo): the
     input block and dec_conv1a's skip have fewer lanes.  Every stored
     activation is checked in isolation, the output end to end."""
@@ -114,7 +114,7 @@ def test_colour_only_and_colour_albedo_models_match_oracle(precision, in_channel
     w, h = 130, 36
     x = round_storage(synth.uniform_activations(h, w, in_channels, seed=in_channels, low=0, high=1),
                       precision)
-    acts_flat, final = _run_network(weights, x, precision, subpixel=1 if precision == "fp16" else 0)
+    acts_flat, final = _run_network(weights, x, precision, subpixel)
     ref = unet.forward(x, weights, precision, keep=True)
     acts = []
     for k, name in enumerate(VALUE_NAMES):
