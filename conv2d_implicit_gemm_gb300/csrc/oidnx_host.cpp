@@ -1285,6 +1285,27 @@ void destroy_plan(Plan* p) {
   p->arena = nullptr;
 }
 
+// Tensor-core FLOPs one launch issues (2 M N K summed over its MMAs; tile
+// rows and channels padded as the kernels run them): per tile, K blocks x
+// taps x R rows x N x 128 pixels x K x 2, with 4 taps on the upsampled
+// channels of a sub-pixel decoder, three passes for 3xTF32, and for the
+// folded final conv 3 R rows of N = 16 (three kx taps) per K block.  0 for
+// fused pairs.
+double mma_flop(const LayerLaunch& LL) {
+  if (LL.pair) return 0;
+  if (LL.final) {
+    const FinalConvParams& p = LL.fcl.p;
+    return static_cast<double>(p.tiles_x) * p.tiles_y * 2 * 3 * kFinalRows * 16 * 128.0 * 16 * 2;
+  }
+  const TcConvParams& p = LL.tcl.p;
+  const int kind = LL.tcl.kind;
+  const bool tf = kind == kTcPlain32 || kind == kTcExpand32 || kind == kTcSubpixel32;
+  const bool sp = kind == kTcSubpixel || kind == kTcSubpixel32;
+  const double per_tap = static_cast<double>(p.R) * p.N * 128.0 * (tf ? 8 : 16) * 2 * (tf ? 3 : 1);
+  const double taps = sp ? 4.0 * p.KB0 + 9.0 * p.KB1 : 9.0 * (p.KB0 + p.KB1);
+  return static_cast<double>(p.tiles_x) * p.tiles_y * taps * per_tap;
+}
+
 // Liveness-based activation plan for a w x h network input
 // ("nativeUNet.ts", _createExecution: a value's slot is free after its last
 // use; each new value takes the smallest free slot that fits, else a new one).
@@ -2256,11 +2277,13 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
   const Plan* plan = f->last_plan;
   std::string s = "{\"totalMs\":" + std::to_string(total) + ",\"layers\":[";
   bool first = true;
-  auto add = [&](const char* id, int idx, double flop, double bytes) {
+  auto add = [&](const char* id, int idx, double flop, double bytes, double mma = 0) {
     if (count[idx] == 0) return;
-    char buf[256];
-    snprintf(buf, sizeof(buf), "%s{\"id\":\"%s\",\"ms\":%.6f,\"launches\":%d,\"flop\":%.0f,\"bytes\":%.0f}",
-             first ? "" : ",", id, ms[idx], count[idx], flop * count[idx], bytes * count[idx]);
+    char buf[320];
+    snprintf(buf, sizeof(buf),
+             "%s{\"id\":\"%s\",\"ms\":%.6f,\"launches\":%d,\"flop\":%.0f,\"bytes\":%.0f,\"mmaFlop\":%.0f}",
+             first ? "" : ",", id, ms[idx], count[idx], flop * count[idx], bytes * count[idx],
+             mma * count[idx]);
     s += buf;
     first = false;
   };
@@ -2279,7 +2302,8 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
       // with the output pass fused the network output is not stored: the
       // kernel reads the colour and writes the image instead
       add(fused_out ? "dec_conv0+output" : L.name, L.layer + 2, L.flop,
-          fused_out ? L.bytes - tile_px * 16 + out_bytes - out_px / tiles * 16 : L.bytes);
+          fused_out ? L.bytes - tile_px * 16 + out_bytes - out_px / tiles * 16 : L.bytes,
+          mma_flop(L));
     }
   add("output", kLayers + 2, 0, out_bytes);
   s += "]}";

@@ -216,9 +216,12 @@ oidnx_status oidnx_profile_next(oidnx_filter* f);
 
 /* JSON of the last profiled execution:
  * {"totalMs":T,"layers":[{"id":"input-pack","ms":..,"flop":..,"bytes":..,
- *  "launches":..},...,{"id":"output",...}]} summed over tiles; flop and bytes
- * are the algorithmic counts (logical channels; each input activation read
- * once, each output written once).  Synchronises with the profiled work.
+ *  "launches":..,"mmaFlop":..},...,{"id":"output",...}]} summed over tiles;
+ * flop and bytes are the algorithmic counts (logical channels; each input
+ * activation read once, each output written once); mmaFlop is what the
+ * tensor cores execute (padded tiles and channels; 4 of the 9 taps on the
+ * upsampled channels of a sub-pixel decoder, three tf32 products per fp32
+ * product; 0 where not counted).  Synchronises with the profiled work.
  * Errors: INVALID_ARGUMENT (cap too small or nothing profiled), CUDA.  */
 oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap);
 

@@ -66,6 +66,33 @@ def test_profile_every_execution_through_the_graph(weights):
     assert len(prof["layers"]) == 17
 
 
+@pytest.mark.parametrize("precision", ["fp16", "fp32"])
+def test_profile_counts_executed_tensor_flops(weights, precision):
+    """mmaFlop against per-pixel counts at a 256 x 128 tile, which the conv
+    tiles cover exactly (no padded rows or columns): enc_conv1 (32 -> 32,
+    plain) executes its logical FLOPs; dec_conv1a (sub-pixel, 64 upsampled +
+    9 skip channels -> 64) executes 4 taps on the upsampled channels and 9 on
+    the skip lanes padded to one K block (16 fp16 lanes, 16 fp32 lanes as two
+    8-lane blocks), x3 for the three tf32 products of fp32 storage."""
+    w, h = 256, 128
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    prec = ox.PRECISION_FP16 if precision == "fp16" else ox.PRECISION_FP32
+    d = Denoiser(weights, prec, imgs, True)
+    try:
+        ox.oidnx_profile_next(d.f)
+        d.run()
+        prof = {l["id"]: l for l in ox.oidnx_get_profile(d.f)["layers"]}
+    finally:
+        d.close()
+    px = w * h
+    passes = 1 if precision == "fp16" else 3
+    assert prof["enc_conv1"]["flop"] == 2 * 9 * 32 * 32 * px
+    assert prof["enc_conv1"]["mmaFlop"] == passes * prof["enc_conv1"]["flop"]
+    assert prof["dec_conv1a"]["flop"] == 2 * 9 * 73 * 64 * px
+    assert prof["dec_conv1a"]["mmaFlop"] == passes * 2 * (4 * 64 + 9 * 16) * 64 * px
+    assert prof["input-pack"]["mmaFlop"] == 0
+
+
 def test_shape_cache_eviction_with_work_in_flight(weights):
     f = ox.oidnx_filter_create(ox.write_weight_blob(weights), ox.PRECISION_FP16)
     try:
