@@ -189,9 +189,12 @@ __global__ void __launch_bounds__(kFinalThreads, 1)
     const int et = threadIdx.x - 64;
     if (et < kNc) bias_s[et] = p.bias[et];
     named_barrier_sync(1, 32 * kEpiWarps);
+    // every accumulator row restarts from the same 16 values: kept in registers
+    uint32_t bz[16];
+    bias16_regs(bias_s, bz);
     for (int b = 0; b < 2; ++b)
       for (int r = sub; r < kR; r += kSubs)
-        tmem_fill_bias(tmem + lane_off + b * kSetCols + static_cast<uint32_t>(r * kNc), bias_s);
+        tmem_st16(tmem + lane_off + b * kSetCols + static_cast<uint32_t>(r * kNc), bz);
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&tempty[0]);
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kFinalThreads, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < kJ; ++j)
-        tmem_fill_bias(tmem + lane_off + buf * kSetCols + static_cast<uint32_t>((sub + kSubs * j) * kNc), bias_s);
+        tmem_st16(tmem + lane_off + buf * kSetCols + static_cast<uint32_t>((sub + kSubs * j) * kNc), bz);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&tempty[buf]);

@@ -699,6 +699,15 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
         __half* out = static_cast<__half*>(p.out);
         for (int c0 = 0; c0 < nc; c0 += 2) {
           const bool two = c0 + 1 < nc;
+          // the refill values of these 32 columns, read once for all rows
+          // (per row in the fp32 kinds, whose helper warps leave no
+          // registers to spare for them)
+          constexpr bool kHoist = !TF;
+          uint32_t bz[2][16];
+          if (kHoist) {
+            bias16_regs(bias_s + c0 * 16, bz[0]);
+            if (two) bias16_regs(bias_s + c0 * 16 + 16, bz[1]);
+          }
           for (int r = sub; r < R; r += 2) {
             const int y = y0 + r;
             uint32_t v[2][16];
@@ -706,8 +715,12 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
             tmem_ld16_nowait(t0, v[0]);
             if (two) tmem_ld16_nowait(t0 + 16, v[1]);
             tmem_wait_ld();
-            tmem_fill_bias(t0, bias_s + c0 * 16);
-            if (two) tmem_fill_bias(t0 + 16, bias_s + c0 * 16 + 16);
+            if (!kHoist) {
+              bias16_regs(bias_s + c0 * 16, bz[0]);
+              if (two) bias16_regs(bias_s + c0 * 16 + 16, bz[1]);
+            }
+            tmem_st16(t0, bz[0]);
+            if (two) tmem_st16(t0 + 16, bz[1]);
             // columns [W, pitch) are row padding: stored as zeros
             if (TF && x < p.pitch && y < p.H) {
               const bool pad = x >= p.W;
@@ -752,6 +765,8 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
         const int Wp = (p.W + 1) >> 1, Hp = (p.H + 1) >> 1;
         const int xp = x >> 1;
         for (int c = 0; c < nc; ++c) {
+          uint32_t bz[16];  // refill values of these 16 columns, read once
+          bias16_regs(bias_s + c * 16, bz);
           for (int i = sub; i < R / 2; i += 2) {
             const int ya = y0 + 2 * i;
             const bool va = x < p.W && ya < p.H;
@@ -762,8 +777,8 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
             tmem_ld16_nowait(t0, v[0]);
             tmem_ld16_nowait(t0 + static_cast<uint32_t>(N), v[1]);
             tmem_wait_ld();
-            tmem_fill_bias(t0, bias_s + c * 16);
-            tmem_fill_bias(t0 + static_cast<uint32_t>(N), bias_s + c * 16);
+            tmem_st16(t0, bz);
+            tmem_st16(t0 + static_cast<uint32_t>(N), bz);
             float mx[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {

@@ -298,8 +298,9 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 
 // Refill 16 accumulator columns (32 lanes) with the bias values bias16[0..15]
 // (16-byte aligned shared memory).
-__device__ __forceinline__ void tmem_fill_bias(uint32_t taddr, const float* bias16) {
-  uint32_t r[16];
+// 16 consecutive bias values (shared memory) as the registers of one
+// 16-column TMEM store.
+__device__ __forceinline__ void bias16_regs(const float* bias16, uint32_t r[16]) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const float4 b = reinterpret_cast<const float4*>(bias16)[k];
@@ -308,6 +309,11 @@ __device__ __forceinline__ void tmem_fill_bias(uint32_t taddr, const float* bias
     r[4 * k + 2] = __float_as_uint(b.z);
     r[4 * k + 3] = __float_as_uint(b.w);
   }
+}
+
+__device__ __forceinline__ void tmem_fill_bias(uint32_t taddr, const float* bias16) {
+  uint32_t r[16];
+  bias16_regs(bias16, r);
   tmem_st16(taddr, r);
 }
 
