@@ -20,6 +20,9 @@
 //  * The fused output pass reads the tile's input colour and writes the
 //    output image in place of the separate output pass kernel, which would
 //    re-read the network output from HBM.
+//  * fp32 storage (TF): K blocks of 8 channels, each product as three tf32
+//    MMAs (A B_hi + A B_lo + A_lo B_hi) as in the generic kernel; four helper
+//    warps split every staged box into A_hi (in place) and A_lo.
 #include "internal.h"
 #include "passes.cuh"
 #include "ptx.cuh"
@@ -29,7 +32,8 @@ namespace oidnx {
 namespace {
 
 constexpr int kEpiWarps = 16;       // four per TMEM lane quarter
-constexpr int kFinalThreads = 32 * (2 + kEpiWarps);  // TMA, MMA, epilogue
+// TMA, MMA, epilogue warps, and for tf32 four helper warps
+template <bool TF> constexpr int final_threads() { return 32 * (2 + kEpiWarps + (TF ? 4 : 0)); }
 constexpr int kSubs = kEpiWarps / 4;  // epilogue warps per lane quarter
 constexpr int kNc = 16;             // accumulator columns per output row (12 used)
 constexpr int kR = kFinalRows;
@@ -42,6 +46,7 @@ __device__ __forceinline__ void final_tile(const FinalConvParams& p, int tile, i
 
 // The MMAs of one K block: halo row h updates output rows
 // max(0, h - 2) .. min(kR - 1, h) (ky stacked), one MMA each.
+template <bool TF>
 __device__ __forceinline__ void final_kblock(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t id1,
                                              uint32_t id2, uint32_t id3) {
 #pragma unroll
@@ -49,30 +54,42 @@ __device__ __forceinline__ void final_kblock(uint64_t ad, uint64_t bd, uint32_t 
     const int lo = h - 2 > 0 ? h - 2 : 0;
     const int hi = h < kR - 1 ? h : kR - 1;
     const int n = hi - lo + 1;
-    if (elect_one())
-      mma_f16_ss(dbase + static_cast<uint32_t>(lo * kNc), ad + static_cast<uint32_t>(h * 2 * kHaloW),
-                 bd + static_cast<uint32_t>((2 - h + lo) * kNc), n == 1 ? id1 : (n == 2 ? id2 : id3), 1u);
+    const uint32_t d = dbase + static_cast<uint32_t>(lo * kNc);
+    const uint64_t a = ad + static_cast<uint32_t>(h * 2 * kHaloW);
+    const uint64_t b = bd + static_cast<uint32_t>((2 - h + lo) * kNc);
+    const uint32_t id = n == 1 ? id1 : (n == 2 ? id2 : id3);
+    if (elect_one()) {
+      if (TF) mma_tf32_ss(d, a, b, id);
+      else mma_f16_ss(d, a, b, id, 1u);
+    }
   }
 }
 
 }  // namespace
 
-template <bool OUT>
-__global__ void __launch_bounds__(kFinalThreads, 1)
+template <bool OUT, bool TF>
+__global__ void __launch_bounds__(final_threads<TF>(), 1)
     conv3x3_final_kernel(const __grid_constant__ CUtensorMap map, const FinalConvParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   const int S = p.S;
-  constexpr uint32_t kWBytes = 2u * 2u * 3u * kNc * kChunkBytes;  // two K blocks
-  // shared memory: [stages][weights][boundary [sub][2 buf][4 quarter][rows][3]][bias][barriers]
+  // 32 input channels: two K blocks of 16 (fp16) or four of 8 (tf32, each
+  // with its B_hi then its B_lo)
+  constexpr int kKB = TF ? 4 : 2;
+  constexpr uint32_t kWkbBytes = (TF ? 2u : 1u) * 2u * 3u * kNc * kChunkBytes;
+  constexpr uint32_t kWBytes = kKB * kWkbBytes;
+  // shared memory: [stages][A_lo stages (tf32)][weights][boundary [sub][2
+  // buf][4 quarter][rows][3]][bias][barriers]
   uint8_t* A = smem;
-  uint8_t* Wsm = A + static_cast<size_t>(S) * p.stage_bytes;
+  uint8_t* ALO = A + static_cast<size_t>(S) * p.stage_bytes;
+  uint8_t* Wsm = ALO + (TF ? static_cast<size_t>(S) * p.stage_bytes : 0u);
   float4* BND = reinterpret_cast<float4*>(Wsm + kWBytes);
   float* bias_s = reinterpret_cast<float*>(BND + kSubs * 2 * 4 * (kR / kSubs) * 3);
   uint64_t* full = reinterpret_cast<uint64_t*>(bias_s + kNc);
   uint64_t* empty = full + S;
-  uint64_t* tfull = empty + S;   // [2]
+  uint64_t* xdone = empty + S;   // [S] tf32: stage split by the helper warps
+  uint64_t* tfull = xdone + (TF ? S : 0);   // [2]
   uint64_t* tempty = tfull + 2;  // [2]
   uint64_t* xbar = tempty + 2;   // [sub][2 buf] boundary values written
   uint64_t* wbar = xbar + 2 * kSubs;
@@ -88,6 +105,7 @@ __global__ void __launch_bounds__(kFinalThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      if (TF) mbar_init(&xdone[s], 128);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -118,7 +136,7 @@ __global__ void __launch_bounds__(kFinalThreads, 1)
         int x0, y0;
         final_tile(p, tile, &x0, &y0);
         const int bx = (x0 - 1) & ~(kGroupPx - 1);
-        for (int kb = 0; kb < 2; ++kb, ++it) {
+        for (int kb = 0; kb < kKB; ++kb, ++it) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kErrTimeoutProducer)) {
             ok = false;
             break;
@@ -138,11 +156,14 @@ __global__ void __launch_bounds__(kFinalThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t id1 = idesc_f16_f32(kTileM, kNc), id2 = idesc_f16_f32(kTileM, 2 * kNc),
-                   id3 = idesc_f16_f32(kTileM, 3 * kNc);
+    const uint32_t id1 = TF ? idesc_tf32_f32(kTileM, kNc) : idesc_f16_f32(kTileM, kNc);
+    const uint32_t id2 = TF ? idesc_tf32_f32(kTileM, 2 * kNc) : idesc_f16_f32(kTileM, 2 * kNc);
+    const uint32_t id3 = TF ? idesc_tf32_f32(kTileM, 3 * kNc) : idesc_f16_f32(kTileM, 3 * kNc);
     const uint64_t a0 = smem_desc_noswizzle(smem_u32(A), kHaloW * kChunkBytes, 128);
     const uint64_t w0 = smem_desc_noswizzle(smem_u32(Wsm), 3u * kNc * kChunkBytes, 128);
-    constexpr uint32_t kWkb = (2u * 3u * kNc * kChunkBytes) >> 4;  // one K block, 16 B units
+    constexpr uint32_t kWkb = kWkbBytes >> 4;                       // one K block, 16 B units
+    constexpr uint32_t kBlo = (2u * 3u * kNc * kChunkBytes) >> 4;   // tf32: B_lo after B_hi
+    const uint32_t alo16 = TF ? (static_cast<uint32_t>(S) * p.stage_bytes) >> 4 : 0u;
     bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(wbar, 0, p.status, kErrTimeoutMma));
     uint32_t s = 0, ph = 0, tcount = 0;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tcount) {
@@ -157,11 +178,18 @@ __global__ void __launch_bounds__(kFinalThreads, 1)
       final_tile(p, tile, &x0, &y0);
       // A row i is input pixel x0 - 1 + i: o pixels past the box start
       const uint32_t o = static_cast<uint32_t>((x0 - 1) - ((x0 - 1) & ~(kGroupPx - 1)));
-      for (int kb = 0; kb < 2; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutMma));
+      for (int kb = 0; kb < kKB; ++kb) {
+        bool w = mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutMma);
+        if (TF && w) w = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
+        ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
-        final_kblock(a0 + ((s * p.stage_bytes) >> 4) + o, w0 + static_cast<uint32_t>(kb) * kWkb,
-                     tmem + buf * kSetCols, id1, id2, id3);
+        const uint64_t ad = a0 + ((s * p.stage_bytes) >> 4) + o;
+        const uint64_t bd = w0 + static_cast<uint32_t>(kb) * kWkb;
+        // tf32: passes A_hi B_hi, A_hi B_lo, A_lo B_hi
+#pragma unroll 1
+        for (int pass = 0; pass < (TF ? 3 : 1); ++pass)
+          final_kblock<TF>(ad + (pass == 2 ? alo16 : 0u), bd + (pass == 1 ? kBlo : 0u),
+                           tmem + buf * kSetCols, id1, id2, id3);
         if (elect_one()) mma_commit(&empty[s]);
         if (++s == static_cast<uint32_t>(S)) {
           s = 0;
@@ -174,6 +202,32 @@ __global__ void __launch_bounds__(kFinalThreads, 1)
     if (elect_one()) mma_commit(done);
     mbar_wait_bounded(done, 0, p.status, kErrTimeoutMma);
     __syncwarp();
+  } else if (TF && warp >= 2 + kEpiWarps) {
+    // ------------------------------------------------------------ tf32 split
+    // Every staged box, whole: A_hi in place, A_lo into the A_lo stage.
+    // Waiting on every stage keeps these warps at most one use of a stage
+    // ahead of the MMA warp, so the xdone phases stay paired.
+    const int et = threadIdx.x - 32 * (2 + kEpiWarps);  // 0..127
+    const int n16 = static_cast<int>(p.stage_tx >> 4);
+    uint32_t s = 0, ph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int kb = 0; kb < kKB; ++kb) {
+        if (!mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutEpilogue)) {
+          ok = false;
+          break;
+        }
+        uint4* hi = reinterpret_cast<uint4*>(A + static_cast<size_t>(s) * p.stage_bytes);
+        uint4* lo = reinterpret_cast<uint4*>(ALO + static_cast<size_t>(s) * p.stage_bytes);
+        for (int i = et; i < n16; i += 128) split_tf32(hi + i, lo + i);
+        fence_proxy_async_smem();
+        mbar_arrive(&xdone[s]);
+        if (++s == static_cast<uint32_t>(S)) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     // Warp w reads TMEM lane quarter w % 4 (pixel m of the 128-pixel row,
@@ -284,17 +338,32 @@ __global__ void __launch_bounds__(kFinalThreads, 1)
 }
 
 cudaError_t launch_conv_final(const FinalConvLaunch& L, cudaStream_t stream) {
+  if (L.tf32) {
+    const dim3 block(final_threads<true>());
+    if (L.outpass)
+      return launch_pdl(conv3x3_final_kernel<true, true>, L.grid, block, L.smem, stream, L.map, L.p);
+    return launch_pdl(conv3x3_final_kernel<false, true>, L.grid, block, L.smem, stream, L.map, L.p);
+  }
+  const dim3 block(final_threads<false>());
   if (L.outpass)
-    return launch_pdl(conv3x3_final_kernel<true>, L.grid, dim3(kFinalThreads), L.smem, stream, L.map, L.p);
-  return launch_pdl(conv3x3_final_kernel<false>, L.grid, dim3(kFinalThreads), L.smem, stream, L.map, L.p);
+    return launch_pdl(conv3x3_final_kernel<true, false>, L.grid, block, L.smem, stream, L.map, L.p);
+  return launch_pdl(conv3x3_final_kernel<false, false>, L.grid, block, L.smem, stream, L.map, L.p);
 }
 
 cudaError_t conv_final_set_smem_limit(size_t bytes) {
-  cudaError_t e = cudaFuncSetAttribute(conv3x3_final_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(conv3x3_final_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(bytes));
+  const int b = static_cast<int>(bytes);
+  cudaError_t e = cudaFuncSetAttribute(conv3x3_final_kernel<true, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(conv3x3_final_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(conv3x3_final_kernel<true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(conv3x3_final_kernel<false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  return e;
 }
 
 }  // namespace oidnx

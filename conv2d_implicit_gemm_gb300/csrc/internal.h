@@ -140,6 +140,7 @@ constexpr int kFinalSpan = kTileM - 2;
 
 struct FinalConvParams {
   const __half* w;         // folded B operand: [kb][2][3 x 16][8], row 16 (2 - ky) + 4 kx + co
+                           // (tf32: floats, [kb][hi, lo][2][3 x 16][4] over 8-channel blocks)
   const float* bias;       // [16]: b0, b1, b2, zeros
   float4* net;             // [H][W] network output (lane 3 zero), or null
   int* status;
@@ -162,6 +163,7 @@ struct FinalConvLaunch {
   CUtensorMap map;         // input: boxes of kFinalRows + 2 rows x kHaloW pixels x 2 chunks
   FinalConvParams p;
   int outpass;             // epilogue also runs the output pass
+  int tf32;                // fp32 storage: 3xTF32 products
   dim3 grid;
   size_t smem;
 };

@@ -490,6 +490,30 @@ std::vector<float> pack_weights_subpixel_tf32(const ConvTensors& L, int c0, int 
 }
 
 
+// The folded final-conv B operand for fp32 storage: per K block of 8
+// channels [hi, lo][j][pos][16][4] floats, row pos * 16 + 4 * kx + co
+// (pos = 2 - ky), each weight split into its tf32 hi and lo parts.
+std::vector<float> pack_weights_folded_tf32(const ConvTensors& L) {
+  const int KB = round_up(L.cin, 8) / 8;
+  std::vector<float> out(static_cast<size_t>(KB) * 2 * 2 * 48 * 4, 0.0f);
+  for (int kb = 0; kb < KB; ++kb)
+    for (int j = 0; j < 2; ++j)
+      for (int pos = 0; pos < 3; ++pos)
+        for (int kx = 0; kx < 3; ++kx)
+          for (int co = 0; co < L.cout; ++co)
+            for (int l = 0; l < 4; ++l) {
+              const int ch = kb * 8 + j * 4 + l;
+              if (ch >= L.cin) continue;
+              const int ky = 2 - pos;
+              float hl[2];
+              split_tf32(L.w[(static_cast<size_t>(co) * L.cin + ch) * 9 + ky * 3 + kx], &hl[0], &hl[1]);
+              const size_t row = static_cast<size_t>(pos) * 16 + 4 * kx + co;
+              for (int part = 0; part < 2; ++part)
+                out[(((static_cast<size_t>(kb) * 2 + part) * 2 + j) * 48 + row) * 4 + l] = hl[part];
+            }
+  return out;
+}
+
 // ---------------------------------------------------------------- tiles
 struct AxisTile {
   int in_start, in_size, out_start, out_size;
@@ -718,6 +742,9 @@ struct Plan {
   std::vector<LayerLaunch> launches;
   bool split_on[4] = {};  // kSplits[i] in use (its decoder runs in sub-pixel mode)
   bool fused[2] = {};     // kPairs[i] runs as one fused kernel
+  // the last execution stored the network output (not so when the output
+  // pass ran in the final conv's epilogue without keepActivations)
+  bool out_stored = true;
   uint64_t last_used = 0;
   cudaEvent_t done = nullptr;  // recorded after each use
   bool used = false;
@@ -848,10 +875,15 @@ oidnx_status make_device_layer(const ConvTensors& T, int c0, int c1, int precisi
       L->sub_bytes = ws.size() * 4;
       OIDNX_TRY(upload(ws.data(), L->sub_bytes, &L->wsub));
     }
+    if (T.cout == 3 && T.cin == 32 && c1 == 0) {
+      std::vector<float> wf = pack_weights_folded_tf32(T);
+      L->fold_bytes = wf.size() * 4;
+      OIDNX_TRY(upload(wf.data(), L->fold_bytes, &L->wfold));
+    }
     std::vector<float> b(L->N, 0.0f);
     std::copy(T.b.begin(), T.b.end(), b.begin());
     OIDNX_TRY(upload(b.data(), b.size() * 4, reinterpret_cast<void**>(&L->bias)));
-    L->weight_bytes = w.size() * 4 + b.size() * 4 + L->sub_bytes;
+    L->weight_bytes = w.size() * 4 + b.size() * 4 + L->sub_bytes + L->fold_bytes;
   }
   return ok();
 }
@@ -1219,12 +1251,13 @@ oidnx_status build_pair_launch(const DeviceLayer& A, const DeviceLayer& B, int m
 // kFinalSpan pixels over the W x H extent, writing the network output to
 // `net` (may be null when the output pass runs in the epilogue).
 bool final_foldable(const DeviceLayer& L) {
-  return !L.tf32 && L.wfold && L.cin == 32 && L.cout == 3 && L.c1 == 0;
+  return L.wfold && L.cin == 32 && L.cout == 3 && L.c1 == 0;
 }
 
 oidnx_status build_final_launch(const DeviceLayer& L, const void* src, Extent ext, int W, int H,
                                 void* net, int* status, FinalConvLaunch* T) {
   T->outpass = 0;
+  T->tf32 = L.tf32 ? 1 : 0;
   FinalConvParams& p = T->p;
   std::memset(&p, 0, sizeof(p));
   p.w = static_cast<const __half*>(L.wfold);
@@ -1237,14 +1270,17 @@ oidnx_status build_final_launch(const DeviceLayer& L, const void* src, Extent ex
   p.tiles_y = (H + kFinalRows - 1) / kFinalRows;
   p.stage_tx = static_cast<uint32_t>((kFinalRows + 2) * 2 * kHaloW * kChunkBytes);
   p.stage_bytes = static_cast<uint32_t>(round_up_sz(p.stage_tx, 1024));
-  // alignment slack, weights, exchange buffers, bias, barriers (10 + 2 per stage)
-  // alignment slack, weights, boundary exchange (4 sub x 2 x 4 quarters x
-  // 2 rows x 3 float4), bias, barriers (14 + 2 per stage)
-  const size_t fixed = 1024 + 2 * 2 * 3 * 16 * kChunkBytes + 4 * 2 * 4 * 2 * 3 * 16 + 16 * 4 + 14 * 8 + 16;
+  // alignment slack, weights (fp16: 2 K blocks; tf32: 4 K blocks, hi and
+  // lo), boundary exchange (4 sub x 2 x 4 quarters x 2 rows x 3 float4),
+  // bias, barriers (14 + 2 per stage, 3 for tf32)
+  const size_t wbytes = static_cast<size_t>(L.tf32 ? 4 * 2 : 2) * 2 * 3 * 16 * kChunkBytes;
+  const size_t fixed = 1024 + wbytes + 4 * 2 * 4 * 2 * 3 * 16 + 16 * 4 + 14 * 8 + 16;
+  // per stage: the halo box (tf32: and its A_lo split) and its barriers
+  const size_t per_stage = static_cast<size_t>(p.stage_bytes) * (L.tf32 ? 2 : 1) + 24;
   const size_t max_smem = 227 * 1024;
-  p.S = static_cast<int>(std::min<size_t>(4, (max_smem - fixed) / (16 + p.stage_bytes)));
+  p.S = static_cast<int>(std::min<size_t>(4, (max_smem - fixed) / per_stage));
   if (p.S < 2) return fail(OIDNX_ERR_UNSUPPORTED, "final conv stages do not fit");
-  T->smem = fixed + static_cast<size_t>(p.S) * (16 + p.stage_bytes);
+  T->smem = fixed + static_cast<size_t>(p.S) * per_stage;
   static bool limit_set = false;
   if (!limit_set) {
     cudaError_t e = conv_final_set_smem_limit(max_smem);
@@ -1253,8 +1289,9 @@ oidnx_status build_final_launch(const DeviceLayer& L, const void* src, Extent ex
   }
   const long tiles = static_cast<long>(p.tiles_x) * p.tiles_y;
   T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, num_sms())), 1, 1);
-  return encode_act_map(&T->map, src, ext.w, ext.pitch, ext.h, act_chunks(OIDNX_PRECISION_FP16, L.cin),
-                        kHaloW, kFinalRows + 2, true, &p.xs);
+  return encode_act_map(&T->map, src, ext.w, ext.pitch, ext.h,
+                        act_chunks(L.tf32 ? OIDNX_PRECISION_FP32 : OIDNX_PRECISION_FP16, L.cin), kHaloW,
+                        kFinalRows + 2, true, &p.xs);
 }
 
 oidnx_status run_launch(const LayerLaunch& L, cudaStream_t s) {
@@ -1293,9 +1330,10 @@ void destroy_plan(Plan* p) {
 // fused pairs.
 double mma_flop(const LayerLaunch& LL) {
   if (LL.pair) return 0;
-  if (LL.final) {
+  if (LL.final) {  // 32 input channels: 2 K blocks of 16, or 4 of 8 x 3 tf32 passes
     const FinalConvParams& p = LL.fcl.p;
-    return static_cast<double>(p.tiles_x) * p.tiles_y * 2 * 3 * kFinalRows * 16 * 128.0 * 16 * 2;
+    return static_cast<double>(p.tiles_x) * p.tiles_y * 3 * kFinalRows * 16 * 128.0 * 32 * 2 *
+           (LL.fcl.tf32 ? 3 : 1);
   }
   const TcConvParams& p = LL.tcl.p;
   const int kind = LL.tcl.kind;
@@ -1615,6 +1653,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
         L.name = "dec_conv0+output";
         FinalConvParams& fp = L.fcl.p;
         fp.net = f->keep_acts ? static_cast<float4*>(P->ptr(V_OUT)) : nullptr;
+        P->out_stored = f->keep_acts != 0;
         fp.color = static_cast<const float4*>(img[0]);
         fp.color_stride = stride[0] / 16;
         fp.out = static_cast<float4*>(img[3]);
@@ -1632,6 +1671,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
         continue;
       }
       OIDNX_TRY(enqueue_network(f, P, prof, s));
+      P->out_stored = true;
       UnpackParams up;
       std::memset(&up, 0, sizeof(up));
       up.net = static_cast<const float4*>(P->ptr(V_OUT));
@@ -2216,6 +2256,7 @@ oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w
                                       P->value_ext[V_INS].pitch, w, h, in_chunks, s);
     if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "split copy: %s", cudaGetErrorString(e));
   }
+  P->out_stored = true;
   OIDNX_TRY(prof_mark(f, prof, -2, s));
   OIDNX_TRY(enqueue_network(f, P, prof, s));
   OIDNX_CUDA(cudaMemcpyAsync(out, P->ptr(V_OUT), P->value_bytes[V_OUT], cudaMemcpyDeviceToDevice, s));
@@ -2340,6 +2381,10 @@ oidnx_status oidnx_debug_read_activation(oidnx_filter* f, int layer, void* host_
   if (!P) return fail(OIDNX_ERR_INVALID_ARGUMENT, "no network run to read from");
   if (layer < 0 || layer > kLayers) return fail(OIDNX_ERR_INVALID_ARGUMENT, "bad layer %d", layer);
   const int v = layer == 0 ? V_IN : kDefs[layer - 1].dst;
+  if (v == V_OUT && !P->out_stored)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT,
+                "the network output is not stored (the output pass ran in the final conv's "
+                "epilogue); set keepActivations");
   if (P->value_bytes[v] == 0)
     return fail(OIDNX_ERR_INVALID_ARGUMENT,
                 "the output of layer %d is not stored (fused into the next layer's kernel; "

@@ -317,6 +317,20 @@ __device__ __forceinline__ void tmem_fill_bias(uint32_t taddr, const float* bias
   tmem_st16(taddr, r);
 }
 
+// tf32 split of 16 staged bytes (four floats): hi = each float rounded to
+// the nearest tf32 value (in place), lo = the remainder, exact, with
+// |lo| <= 2^-11 |v|.
+__device__ __forceinline__ void split_tf32(uint4* hi, uint4* lo) {
+  const uint4 v = *hi;
+  const uint4 h = make_uint4((v.x + 0x1000u) & 0xFFFFE000u, (v.y + 0x1000u) & 0xFFFFE000u,
+                             (v.z + 0x1000u) & 0xFFFFE000u, (v.w + 0x1000u) & 0xFFFFE000u);
+  *lo = make_uint4(__float_as_uint(__uint_as_float(v.x) - __uint_as_float(h.x)),
+                   __float_as_uint(__uint_as_float(v.y) - __uint_as_float(h.y)),
+                   __float_as_uint(__uint_as_float(v.z) - __uint_as_float(h.z)),
+                   __float_as_uint(__uint_as_float(v.w) - __uint_as_float(h.w)));
+  *hi = h;
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

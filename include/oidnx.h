@@ -106,9 +106,9 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *                        on GB300 the separate kernels are faster (the MMAs
  *                        of these layers are bound by shared-memory operand
  *                        reads, which fusion does not reduce)
- *   "fuseOutput"         1 = with fp16 storage, the output pass runs in the
- *                        final conv's epilogue (the network output is then
- *                        not stored unless "keepActivations" is 1); default 1
+ *   "fuseOutput"         1 = the output pass runs in the final conv's
+ *                        epilogue (the network output is then not stored
+ *                        unless "keepActivations" is 1); default 1
  *   "profile"            1 = record per-kernel events on every execute
  * Errors: INVALID_ARGUMENT for unknown names or out-of-range values.  */
 oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value);
@@ -236,8 +236,9 @@ oidnx_status oidnx_get_resource_info(oidnx_filter* f, char* json, size_t cap);
  * dec_conv0 in network order (enc_conv1..enc_conv4 store their pooled
  * outputs).  Valid for every layer only with "keepActivations" = 1 and
  * "fuseLayers" = 0 (the output of a layer fused with the next one is never
- * stored: its read fails with INVALID_ARGUMENT); the required size is
- * returned in *bytes_needed.
+ * stored, nor is the network output of a denoise whose output pass ran in
+ * the final conv's epilogue without "keepActivations": such reads fail
+ * with INVALID_ARGUMENT); the required size is returned in *bytes_needed.
  * Synchronises.
  * Errors: INVALID_ARGUMENT, CUDA.  */
 oidnx_status oidnx_debug_read_activation(oidnx_filter* f, int layer, void* host_dst,

@@ -109,7 +109,7 @@ def test_config_4k_fp32_ldr_color_only_nan_inf():
     w, h = 3840, 2160
     imgs = synth.denoise_inputs(w, h, 1, hdr=False, nan_fraction=0.05)
     weights = synth.unet_weights(3)
-    d = Denoiser(weights, ox.PRECISION_FP32, imgs, False)
+    d = Denoiser(weights, ox.PRECISION_FP32, imgs, False, keep=True)
     try:
         out = d.run()
         net = d.activation(16, 2160, 3840, 3)
@@ -159,17 +159,19 @@ def test_subpixel_decoder_denoise_matches_oracle(precision):
             assert rel_l2(out[..., :3], ref_out[..., :3]) <= 1e-4 * kappa
 
 
+@pytest.mark.parametrize("precision", ["fp16", "fp32"])
 @pytest.mark.parametrize("hdr", [True, False])
-def test_output_pass_in_final_conv_equals_separate_pass(hdr):
+def test_output_pass_in_final_conv_equals_separate_pass(hdr, precision):
     """The output pass run in the final conv's epilogue gives the bits of the
     separate output pass kernel, over a tile grid with ragged edges (so the
     output rectangles are offset inside their tiles)."""
     w, h = 700, 430
     imgs = synth.denoise_inputs(w, h, 3, hdr=hdr, nan_fraction=0.02)
     weights = synth.unet_weights(9, bias_scale=0.05)
+    prec = ox.PRECISION_FP16 if precision == "fp16" else ox.PRECISION_FP32
     outs = []
     for fuse in (1, 0):
-        d = Denoiser(weights, ox.PRECISION_FP16, imgs, hdr, input_scale=0.7 if hdr else 1.0,
+        d = Denoiser(weights, prec, imgs, hdr, input_scale=0.7 if hdr else 1.0,
                      max_tile_size=256, overlap=96)
         try:
             ox.oidnx_filter_set_int(d.f, "fuseOutput", fuse)
