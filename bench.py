@@ -384,11 +384,11 @@ def run_ours(args):
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of this workload with the current kernels, see
-# profiles/conv3x3_tc_dec_conv1a_dec_conv1b_dec_conv0_1080p_fp16.md; emptied
-# whenever the kernels change after that capture (traffic reported null).
-TRAFFIC = {"dec_conv1a": 134.036224e6 + 208.302592e6,
-           "dec_conv1b": 267.568640e6 + 97.284608e6,
-           "dec_conv0": 133.781248e6 + 13.655040e6}
+# profiles/conv3x3_tc_dec_conv1a_dec_conv1b_1080p_fp16.md and
+# profiles/conv3x3_final_dec_conv0_output_1080p_fp16.md; emptied whenever the
+# kernels change after that capture (traffic reported null).
+TRAFFIC = {"dec_conv1a": 133.998080e6 + 207.760128e6,
+           "dec_conv1b": 267.561984e6 + 96.793600e6}
 
 
 def main():
