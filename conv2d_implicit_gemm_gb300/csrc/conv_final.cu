@@ -204,14 +204,18 @@ __global__ void __launch_bounds__(final_threads<TF>(), 1)
     __syncwarp();
   } else if (TF && warp >= 2 + kEpiWarps) {
     // ------------------------------------------------------------ tf32 split
-    // Every staged box, whole: A_hi in place, A_lo into the A_lo stage.
-    // Waiting on every stage keeps these warps at most one use of a stage
-    // ahead of the MMA warp, so the xdone phases stay paired.
+    // The 128 entries of every staged box row that the MMAs read (from the
+    // tile's offset o): A_hi in place, A_lo into the A_lo stage.  Waiting on
+    // every stage keeps these warps at most one use of a stage ahead of the
+    // MMA warp, so the xdone phases stay paired.
     const int et = threadIdx.x - 32 * (2 + kEpiWarps);  // 0..127
-    const int n16 = static_cast<int>(p.stage_tx >> 4);
+    constexpr int kRows = (kR + 2) * 2;                 // halo rows x 2 chunks
     uint32_t s = 0, ph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      int x0, y0;
+      final_tile(p, tile, &x0, &y0);
+      const int o = (x0 - 1) - ((x0 - 1) & ~(kGroupPx - 1));
       for (int kb = 0; kb < kKB; ++kb) {
         if (!mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutEpilogue)) {
           ok = false;
@@ -219,7 +223,10 @@ __global__ void __launch_bounds__(final_threads<TF>(), 1)
         }
         uint4* hi = reinterpret_cast<uint4*>(A + static_cast<size_t>(s) * p.stage_bytes);
         uint4* lo = reinterpret_cast<uint4*>(ALO + static_cast<size_t>(s) * p.stage_bytes);
-        for (int i = et; i < n16; i += 128) split_tf32(hi + i, lo + i);
+        for (int i = et; i < kRows * kTileM; i += 128) {
+          const int at = (i >> 7) * kHaloW + o + (i & (kTileM - 1));
+          split_tf32(hi + at, lo + at);
+        }
         fence_proxy_async_smem();
         mbar_arrive(&xdone[s]);
         if (++s == static_cast<uint32_t>(S)) {

@@ -580,7 +580,8 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
     uint32_t it = 0, s = 0, ph = 0;
     bool ok = true;
     // sub-pixel (tf32 only): every staged box is split whole, the upsampled
-    // items' low-resolution box or the skip items' plane box
+    // items' low-resolution box or the skip items' plane box.  (Splitting
+    // only the 130 entries per row the MMAs read was not faster.)
     for (int tile = blockIdx.x; SP && tile < num_tiles && ok; tile += gridDim.x) {
       for (int kb = 0; kb < items; ++kb, ++it, next_stage(s, ph, S)) {
         if (!mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutEpilogue)) {
