@@ -34,6 +34,8 @@ METRIC_FP32 = "U-Net denoise megapixels/s at 1080p fp32 (3xTF32) on 1 GB300; con
 WIDTH, HEIGHT = 1920, 1080
 WORKLOAD = "OIDN-shaped U-Net denoise, 1920x1080 HDR colour+albedo+normal (9 ch), fp16, single tile"
 CPU_CROP = 768          # oracle sample: a 768x768 crop denoised as one tile
+CPU_BASELINE_RUNS = 3   # cpu_baseline of our arm: three runs of that crop (~10 s)
+REF_BUDGET_S = 120.0    # reference arm: the whole run's oracle time
 FLUSH_BYTES = 256 << 20
 
 
@@ -122,23 +124,31 @@ def _cpu_threads():
     return os.cpu_count()
 
 
-def cpu_oracle_sample(steps=1, precision="fp16"):
-    """Oracle denoise of a CPU_CROP x CPU_CROP crop of the bench inputs."""
+def cpu_oracle_sample(steps=1, precision="fp16", crop=CPU_CROP):
+    """Oracle denoise of a crop x crop crop of the bench inputs, `steps` times."""
     import synth
     from oracle import unet
-    imgs = [im[:CPU_CROP, :CPU_CROP].copy() for im in synth.denoise_inputs(WIDTH, HEIGHT, 3, hdr=True)]
+    imgs = [im[:crop, :crop].copy() for im in synth.denoise_inputs(WIDTH, HEIGHT, 3, hdr=True)]
     weights = synth.unet_weights(9)
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
         unet.denoise(imgs, weights, hdr=True, input_scale=1.0, precision=precision)
         times.append(time.perf_counter() - t0)
-    px = CPU_CROP * CPU_CROP
+    px = crop * crop
     return {"value": px / 1e6 / float(np.mean(times)), "unit": "MP/s", "cores": _cpu_threads(),
             "kind": "oracle",
-            "sample": f"oracle (numpy float64) denoise of one {CPU_CROP}x{CPU_CROP} crop of the "
+            "sample": f"oracle (numpy float64) denoise of one {crop}x{crop} crop of the "
                       f"1920x1080 inputs as one tile, {precision} storage; {steps} run(s)",
-            "seconds": float(np.mean(times))}
+            "seconds": float(np.mean(times)), "crop": crop}
+
+
+def reference_crop(steps, precision, budget_s=REF_BUDGET_S):
+    """Crop side (multiple of 16, 64 .. CPU_CROP) for which `steps` oracle
+    runs take about budget_s on this host, from the rate of one 128 x 128 run."""
+    probe = cpu_oracle_sample(1, precision, crop=128)
+    px = probe["value"] * 1e6 * budget_s / max(steps, 1)
+    return int(max(64, min(CPU_CROP, int(np.sqrt(px)) // 16 * 16)))
 
 
 def _dist():
@@ -170,16 +180,17 @@ def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state; warm-up steps do no work
-    cpu = cpu_oracle_sample(args.steps, args.precision)
+    # warm-up: the oracle has no warm-up state; the calibration run that
+    # sizes each step's crop (K steps in about REF_BUDGET_S) stands in for it
+    crop = reference_crop(args.steps, args.precision)
+    cpu = cpu_oracle_sample(args.steps, args.precision, crop=crop)
     line = {
         "impl": "reference", "metric": METRIC_FP32 if args.precision == "fp32" else METRIC,
         "value": cpu["value"], "unit": "MP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": cpu["seconds"] * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": f"{CPU_CROP}x{CPU_CROP} crop per step",
+        "config": {"workload": WORKLOAD, "sample": f"{crop}x{crop} crop per step",
                    "l2": "n/a (CPU)"},
         "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
         "e2e": {"value": cpu["value"], "unit": "MP/s", "h2d_bytes_per_step": 0,
@@ -348,7 +359,7 @@ def run_ours(args):
                   "gbs": round(layer_bytes[k] / (avg[k] * 1e-3) / 1e9, 1)} for k in avg}
 
     if rank == 0:
-        cpu = cpu_oracle_sample(1, args.precision) if world == 1 else None
+        cpu = cpu_oracle_sample(CPU_BASELINE_RUNS, args.precision) if world == 1 else None
         line = {
             "metric": METRIC_FP32 if fp32 else METRIC, "value": value, "unit": "MP/s", "n_gpus": world,
             "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": mean_ms,
