@@ -131,8 +131,9 @@ cudaError_t launch_conv_pair(const PairConvLaunch& L, cudaStream_t stream);
 cudaError_t conv_pair_set_smem_limit(size_t bytes);
 cudaError_t conv_pair_occupancy(int mode, size_t smem, int* blocks_per_sm);
 
-// The final conv (32 -> 3, bias, no ReLU; fp16 operands) with the three kx
-// taps folded into N: tiles of kFinalRows rows x kFinalSpan output pixels.
+// The final conv (32 -> 3, bias, no ReLU; fp16 operands, or for fp32
+// storage 3xTF32 products) with the three kx taps folded into N: tiles of
+// kFinalRows rows x kFinalSpan output pixels.
 // Optionally the output pass runs in its epilogue (denoise path), writing
 // the output image directly.
 constexpr int kFinalRows = 8;

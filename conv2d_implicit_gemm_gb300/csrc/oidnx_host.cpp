@@ -694,8 +694,8 @@ oidnx_status encode_split_map(CUtensorMap* map, const void* base, int W, int pit
 // ======================================================================
 struct DeviceLayer {
   int cout = 0, cin = 0, c0 = 0, c1 = 0;
-  // fp16 path
-  void* wtc = nullptr;  // packed tensor-core B operand (fp16, or tf32 hi/lo for fp32)
+  // B operands, each fp16 or (fp32 storage) tf32 hi/lo
+  void* wtc = nullptr;  // packed tensor-core B operand of the generic kinds
   bool tf32 = false;    // fp32 storage: 3xTF32 products
   int KB0 = 0, KB1 = 0, N = 0;
   void* wsub = nullptr;  // sub-pixel decoder B operand (decoders only)
