@@ -33,6 +33,16 @@ METRIC = "U-Net denoise megapixels/s at 1080p fp16 on 1 GB300; conv TFLOP/s vs F
 METRIC_FP32 = "U-Net denoise megapixels/s at 1080p fp32 (3xTF32) on 1 GB300; conv TFLOP/s vs TF32 peak / 3"
 WIDTH, HEIGHT = 1920, 1080
 WORKLOAD = "OIDN-shaped U-Net denoise, 1920x1080 HDR colour+albedo+normal (9 ch), fp16, single tile"
+MAX_TILE, OVERLAP = 0, -1   # single tile (0 = whole image), default overlap
+# --workload 4k-tiled: the 3840x2160 tiled configuration (a parity-test
+# workload, timed on request; not the headline)
+WORKLOADS = {
+    "1080p": (1920, 1080, 0, -1, METRIC, WORKLOAD),
+    "4k-tiled": (3840, 2160, 1024, 96,
+                 "U-Net denoise megapixels/s at 3840x2160 (maxTileSize 1024, overlap 96) fp16 on 1 GB300",
+                 "OIDN-shaped U-Net denoise, 3840x2160 HDR colour+albedo+normal (9 ch), fp16, "
+                 "maxTileSize 1024, overlap 96 (15 tiles)"),
+}
 CPU_CROP = 768          # oracle sample: a 768x768 crop denoised as one tile
 CPU_BASELINE_RUNS = 3   # cpu_baseline of our arm: three runs of that crop (~10 s)
 REF_BUDGET_S = 120.0    # reference arm: the whole run's oracle time
@@ -124,6 +134,13 @@ def _cpu_threads():
     return os.cpu_count()
 
 
+def metric_name(fp32):
+    """The metric of the selected workload and precision."""
+    if not fp32:
+        return METRIC
+    return METRIC_FP32 if METRIC == WORKLOADS["1080p"][4] else METRIC.replace("fp16", "fp32 (3xTF32)")
+
+
 def cpu_oracle_sample(steps=1, precision="fp16", crop=CPU_CROP):
     """Oracle denoise of a crop x crop crop of the bench inputs, `steps` times."""
     import synth
@@ -185,7 +202,7 @@ def run_reference(args):
     crop = reference_crop(args.steps, args.precision)
     cpu = cpu_oracle_sample(args.steps, args.precision, crop=crop)
     line = {
-        "impl": "reference", "metric": METRIC_FP32 if args.precision == "fp32" else METRIC,
+        "impl": "reference", "metric": metric_name(args.precision == "fp32"),
         "value": cpu["value"], "unit": "MP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": cpu["seconds"] * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -225,6 +242,8 @@ def run_ours(args):
     ox.oidnx_filter_set_image(f, ox.IMAGE_OUTPUT, d_out.data_ptr(), 0)
     ox.oidnx_filter_set_int(f, "width", WIDTH)
     ox.oidnx_filter_set_int(f, "height", HEIGHT)
+    ox.oidnx_filter_set_int(f, "maxTileSize", MAX_TILE)
+    ox.oidnx_filter_set_int(f, "overlap", OVERLAP)
     ox.oidnx_filter_set_int(f, "hdr", 1)
     ox.oidnx_filter_set_int(f, "transfer", ox.TRANSFER_LOG)
     ox.oidnx_filter_set_float(f, "inputScale", 1.0)
@@ -347,7 +366,7 @@ def run_ours(args):
         executed = layer_mma[top] / (3.0 if fp32 else 1.0) / (avg[top] * 1e-3) / 1e12
         roof["executed"] = executed
         roof["executed_frac"] = executed / tensor_peak
-    roof["traffic"] = None if fp32 else TRAFFIC.get(top)
+    roof["traffic"] = None if fp32 or (WIDTH, HEIGHT, MAX_TILE) != (1920, 1080, 0) else TRAFFIC.get(top)
     roof["traffic_unit"] = "bytes per launch (ncu dram read + write)"
     roof["peak_source"] = peaks["source"] + (
         (" sustained bf16 x tf32/bf16 nominal ratio (1.1/2.25) / 3 (three tf32 MMAs per product)"
@@ -361,7 +380,7 @@ def run_ours(args):
     if rank == 0:
         cpu = cpu_oracle_sample(CPU_BASELINE_RUNS, args.precision) if world == 1 else None
         line = {
-            "metric": METRIC_FP32 if fp32 else METRIC, "value": value, "unit": "MP/s", "n_gpus": world,
+            "metric": metric_name(fp32), "value": value, "unit": "MP/s", "n_gpus": world,
             "steps": steps, "warmup": max(args.warmup, 3), "ms_per_step": mean_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if fp32 else "f16", "data": "synthetic",
@@ -410,7 +429,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--precision", choices=["fp16", "fp32"], default="fp16",
                     help="activation storage (fp32: 3xTF32 products); the headline is fp16")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="1080p",
+                    help="1080p single tile (the headline) or the 3840x2160 tiled configuration")
     args = ap.parse_args()
+    global WIDTH, HEIGHT, MAX_TILE, OVERLAP, METRIC, WORKLOAD
+    WIDTH, HEIGHT, MAX_TILE, OVERLAP, METRIC, WORKLOAD = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args)
     else:
