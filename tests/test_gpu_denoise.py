@@ -105,6 +105,28 @@ def test_config_4k_fp16_tiled_equals_single_tile():
     _crop_check(net, imgs, weights, "fp16", True, 1.0, (2144, 1008, 256, 256), 3840, 2160, 2e-2)
 
 
+def test_8k_single_tile_with_activations_over_4gib():
+    """8192 x 8192 as one tile: dec_conv1a's fp16 output alone is 8 GiB, so
+    the 64-bit offsets of every kernel are exercised.  The output image is
+    checked on an interior window and on the bottom-right corner window
+    (whose image-edge sides need no margin) against the oracle."""
+    w = h = 8192
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    weights = synth.unet_weights(9)
+    d = Denoiser(weights, ox.PRECISION_FP16, imgs, True, max_tile_size=0)
+    try:
+        out = d.run()
+        assert ox.oidnx_filter_get_int(d.f, "tiles") == 1
+    finally:
+        d.close()
+    assert np.isfinite(out[..., :3]).all()
+    for y0, x0, edge in [(4000, 4000, False), (h - 256, w - 256, True)]:
+        ref = unet.denoise([im[y0:y0 + 256, x0:x0 + 256] for im in imgs], weights, hdr=True)
+        end = 256 if edge else 256 - MARGIN
+        got = out[y0 + MARGIN:y0 + end, x0 + MARGIN:x0 + end, :3]
+        assert rel_l2(got, ref[MARGIN:end, MARGIN:end, :3]) <= 2e-2
+
+
 def test_config_4k_fp32_ldr_color_only_nan_inf():
     w, h = 3840, 2160
     imgs = synth.denoise_inputs(w, h, 1, hdr=False, nan_fraction=0.05)

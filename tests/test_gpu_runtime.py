@@ -138,6 +138,41 @@ def test_execute_requires_commit_and_release_is_final(weights):
     torch.cuda.synchronize()
 
 
+def test_oversized_single_tile_reports_out_of_memory_and_filter_stays_usable(weights):
+    """A 65536 x 65536 single tile needs an activation arena of over a
+    terabyte: commit (which plans and allocates, and launches nothing)
+    reports OUT_OF_MEMORY, and the same filter then commits and runs a small
+    image.  No buffer limit below device memory applies: sizes are 64-bit."""
+    f = ox.oidnx_filter_create(ox.write_weight_blob(weights), ox.PRECISION_FP16)
+    try:
+        img = empty_dev(64 * 64 * 16)
+        for i in range(4):
+            ox.oidnx_filter_set_image(f, i, img.data_ptr(), 0)
+        ox.oidnx_filter_set_int(f, "width", 65536)
+        ox.oidnx_filter_set_int(f, "height", 65536)
+        ox.oidnx_filter_set_int(f, "maxTileSize", 0)
+        with pytest.raises(ox.OidnxError) as e:
+            ox.oidnx_filter_commit(f)
+        assert e.value.status == ox.ERR_OUT_OF_MEMORY
+        assert "arena" in str(e.value)
+        imgs = synth.denoise_inputs(64, 64, 3, hdr=False)
+        dev = [to_dev(im) for im in imgs]
+        out = empty_dev(64 * 64 * 16)
+        for i, t in enumerate(dev):
+            ox.oidnx_filter_set_image(f, i, t.data_ptr(), 0)
+        ox.oidnx_filter_set_image(f, ox.IMAGE_OUTPUT, out.data_ptr(), 0)
+        ox.oidnx_filter_set_int(f, "width", 64)
+        ox.oidnx_filter_set_int(f, "height", 64)
+        ox.oidnx_filter_commit(f)
+        ox.oidnx_filter_execute(f, stream())
+        ox.oidnx_filter_sync_status(f)
+        got = to_host(out, np.float32, (64, 64, 4))
+        assert np.isfinite(got).all() and (got[..., :3] >= 0).all() and (got[..., :3] <= 1).all()
+    finally:
+        ox.oidnx_filter_release(f)
+    torch.cuda.synchronize()
+
+
 def test_bounded_device_wait_reports_timeout_and_context_survives(weights):
     """A device wait that nothing completes gives up after its limit, sets the
     filter's error word (reported once as ERR_TIMEOUT) and leaves the context
