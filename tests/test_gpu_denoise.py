@@ -105,6 +105,28 @@ def test_config_4k_fp16_tiled_equals_single_tile():
     _crop_check(net, imgs, weights, "fp16", True, 1.0, (2144, 1008, 256, 256), 3840, 2160, 2e-2)
 
 
+@pytest.mark.parametrize("precision", ["fp16", "fp32"])
+@pytest.mark.parametrize("w,h", [(1, 1), (1, 37), (37, 1), (17, 5)])
+def test_degenerate_image_shapes_match_oracle(w, h, precision):
+    """One-pixel, one-row and one-column images through the whole filter
+    path: the tile is padded to 16 x 16 with clamp-to-edge reads, and the
+    output pass writes only the image's pixels."""
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    weights = synth.unet_weights(9, bias_scale=0.05)
+    prec = ox.PRECISION_FP16 if precision == "fp16" else ox.PRECISION_FP32
+    d = Denoiser(weights, prec, imgs, True)
+    try:
+        out = d.run()
+    finally:
+        d.close()
+    ref = unet.denoise(imgs, weights, hdr=True, precision=precision)
+    assert np.array_equal(out[..., 3].view(np.uint32), imgs[0][..., 3].view(np.uint32))
+    if precision == "fp16":
+        assert rel_l2(out[..., :3], ref[..., :3]) <= 2e-2
+    else:
+        assert rel_l2(out[..., :3], ref[..., :3]) <= 3e-4   # 1e-4 on the network output x kappa
+
+
 def test_8k_single_tile_with_activations_over_4gib():
     """8192 x 8192 as one tile: dec_conv1a's fp16 output alone is 8 GiB, so
     the 64-bit offsets of every kernel are exercised.  The output image is

@@ -138,6 +138,33 @@ def test_execute_requires_commit_and_release_is_final(weights):
     torch.cuda.synchronize()
 
 
+def test_degenerate_dimensions_and_input_scale(weights):
+    """Non-positive image dimensions and a negative or non-finite inputScale
+    are rejected when set, leaving the committed filter as it was; an
+    inputScale of 0 stands for 1 (the pages' default): an HDR denoise with
+    inputScale 0 gives the bits of one with inputScale 1."""
+    w, h = 80, 48
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    outs = []
+    for scale in (1.0, 0.0):
+        d = Denoiser(weights, ox.PRECISION_FP16, imgs, True, input_scale=scale)
+        try:
+            outs.append(d.run())
+            for bad in (-1.0, float("nan"), float("inf")):
+                with pytest.raises(ox.OidnxError) as e:
+                    ox.oidnx_filter_set_float(d.f, "inputScale", bad)
+                assert e.value.status == ox.ERR_INVALID_ARGUMENT
+            for name, value in (("width", 0), ("height", -3)):
+                with pytest.raises(ox.OidnxError) as e:
+                    ox.oidnx_filter_set_int(d.f, name, value)
+                assert e.value.status == ox.ERR_INVALID_ARGUMENT
+            again = d.run()
+            assert np.array_equal(again.view(np.uint32), outs[-1].view(np.uint32))
+        finally:
+            d.close()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
 def test_oversized_single_tile_reports_out_of_memory_and_filter_stays_usable(weights):
     """A 65536 x 65536 single tile needs an activation arena of over a
     terabyte: commit (which plans and allocates, and launches nothing)
