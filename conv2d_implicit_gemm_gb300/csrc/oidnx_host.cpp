@@ -1344,101 +1344,106 @@ double mma_flop(const LayerLaunch& LL) {
   return static_cast<double>(p.tiles_x) * p.tiles_y * taps * per_tap;
 }
 
-// Liveness-based activation plan for a w x h network input
-// ("nativeUNet.ts", _createExecution: a value's slot is free after its last
-// use; each new value takes the smallest free slot that fits, else a new one).
-oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* out) {
-  std::unique_ptr<Plan> P(new Plan());
-  P->w = w;
-  P->h = h;
-  P->lvl[0] = {w, h, w};
+// Shapes, liveness and arena placement of the network's values for a w x h
+// input, shared by the plan cache and the allocation-free path.  Values are
+// placed by liveness best-fit ("nativeUNet.ts", _createExecution: a value's
+// slot is free after its last use; each new value takes the smallest free
+// slot that fits, else a new one).  io_external: the network input (rows of
+// w pixels) and output are the caller's buffers and are not placed; keep:
+// no slot reuse.  Fixed-size arrays only: no allocation.
+struct ValueLayout {
+  Extent lvl[5];
+  Extent ext[V_COUNT];
+  int ch[V_COUNT];
+  int last_use[V_COUNT];
+  bool split_on[4];       // kSplits[i] in use (its decoder runs in sub-pixel mode)
+  bool fused[2];          // kPairs[i] runs as one fused kernel
+  bool stored[kLayers];   // layer l's output is stored (not fused away)
+  size_t off[V_COUNT];    // arena offset of each placed value
+  size_t bytes[V_COUNT];  // its bytes; 0 if not placed
+  size_t total;           // arena bytes
+};
+
+void layout_values(const oidnx_filter* f, int w, int h, bool io_external, bool keep,
+                   ValueLayout* V) {
+  std::memset(V, 0, sizeof(*V));
+  V->lvl[0] = {w, h, w};
   for (int l = 1; l < 5; ++l) {
-    const int lw = (P->lvl[l - 1].w + 1) / 2;
-    P->lvl[l] = {lw, (P->lvl[l - 1].h + 1) / 2, lw};
+    const int lw = (V->lvl[l - 1].w + 1) / 2;
+    V->lvl[l] = {lw, (V->lvl[l - 1].h + 1) / 2, lw};
   }
-  // value shapes
-  P->value_ext[V_IN] = value_extent(f->precision, P->lvl[0], false);
-  P->value_ch[V_IN] = f->in_channels;
+  V->ext[V_IN] = io_external ? V->lvl[0] : value_extent(f->precision, V->lvl[0], false);
+  V->ch[V_IN] = f->in_channels;
   for (int l = 0; l < kLayers; ++l) {
     const LayerDef& d = kDefs[l];
-    const int lvl = d.kind == kPool ? d.level + 1 : d.level;
-    P->value_ext[d.dst] = value_extent(f->precision, P->lvl[lvl], d.dst == V_OUT);
-    P->value_ch[d.dst] = f->layers[l].cout;
+    V->ext[d.dst] = value_extent(f->precision, V->lvl[d.kind == kPool ? d.level + 1 : d.level],
+                                 d.dst == V_OUT);
+    V->ch[d.dst] = f->layers[l].cout;
   }
-  // last use of each value
-  int last_use[V_COUNT];
-  for (int v = 0; v < V_COUNT; ++v) last_use[v] = -1;
+  for (int v = 0; v < V_COUNT; ++v) V->last_use[v] = -1;
   for (int l = 0; l < kLayers; ++l) {
-    last_use[kDefs[l].src0] = l;
-    if (kDefs[l].src1 >= 0) last_use[kDefs[l].src1] = l;
+    V->last_use[kDefs[l].src0] = l;
+    if (kDefs[l].src1 >= 0) V->last_use[kDefs[l].src1] = l;
   }
-  last_use[V_OUT] = kLayers;
+  V->last_use[V_OUT] = kLayers;
   for (int i = 0; i < 4; ++i) {
     const SplitCopy& sc = kSplits[i];
     const LayerDef& d = kDefs[sc.consumer];
-    P->split_on[i] = f->subpixel && use_subpixel(P->lvl[d.level].w, P->lvl[d.level].h,
-                                                 P->value_ext[d.src0]);
-    P->value_ext[sc.split] = P->value_ext[sc.base];
-    P->value_ext[sc.split].pitch = split_pitch(P->value_ext[sc.base].w);
-    P->value_ch[sc.split] = P->value_ch[sc.base];
-    last_use[sc.split] = sc.consumer;
+    V->split_on[i] = f->subpixel && use_subpixel(V->lvl[d.level].w, V->lvl[d.level].h, V->ext[d.src0]);
+    V->ext[sc.split] = V->ext[sc.base];
+    V->ext[sc.split].pitch = split_pitch(V->ext[sc.base].w);
+    V->ch[sc.split] = V->ch[sc.base];
+    V->last_use[sc.split] = sc.consumer;
+  }
+  // a fused pair's intermediate map is never stored
+  for (int l = 0; l < kLayers; ++l) V->stored[l] = true;
+  for (int i = 0; i < 2; ++i) {
+    V->fused[i] = pair_fusable(f, kPairs[i]);
+    if (V->fused[i]) V->stored[kPairs[i].first] = false;
   }
   struct Slot {
     size_t cap, off;
     int active;
-  };
-  std::vector<Slot> slots;
-  size_t total = 0;
-  auto allocate = [&](int v, int index) {
-    if (!f->keep_acts)
-      for (Slot& s : slots)
-        if (s.active >= 0 && last_use[s.active] < index) s.active = -1;
-    const size_t need = act_bytes(f->precision, P->value_ext[v], P->value_ch[v], v == V_OUT);
+  } slots[V_COUNT];
+  int nslots = 0;
+  auto place = [&](int v, int index) {
+    if (!keep)
+      for (int i = 0; i < nslots; ++i)
+        if (slots[i].active >= 0 && V->last_use[slots[i].active] < index) slots[i].active = -1;
+    const size_t need = act_bytes(f->precision, V->ext[v], V->ch[v], v == V_OUT);
     int best = -1;
-    for (size_t i = 0; i < slots.size(); ++i)
-      if (slots[i].active < 0 && slots[i].cap >= need &&
-          (best < 0 || slots[i].cap < slots[best].cap))
-        best = static_cast<int>(i);
+    for (int i = 0; i < nslots; ++i)
+      if (slots[i].active < 0 && slots[i].cap >= need && (best < 0 || slots[i].cap < slots[best].cap))
+        best = i;
     if (best < 0) {
-      slots.push_back({round_up_sz(need, 1024), total, -1});
-      total += round_up_sz(need, 1024);
-      best = static_cast<int>(slots.size()) - 1;
+      slots[nslots] = {round_up_sz(need, 1024), V->total, -1};
+      V->total += round_up_sz(need, 1024);
+      best = nslots++;
     }
     slots[best].active = v;
-    P->value_off[v] = slots[best].off;
-    P->value_bytes[v] = need;
+    V->off[v] = slots[best].off;
+    V->bytes[v] = need;
   };
-  // a fused pair's intermediate map is never stored
-  bool stored[kLayers];
-  for (int l = 0; l < kLayers; ++l) stored[l] = true;
-  for (int i = 0; i < 2; ++i) {
-    P->fused[i] = pair_fusable(f, kPairs[i]);
-    if (P->fused[i]) stored[kPairs[i].first] = false;
-  }
-  allocate(V_IN, -1);
-  if (P->split_on[0]) allocate(V_INS, -1);
+  if (!io_external) place(V_IN, -1);
+  if (V->split_on[0]) place(V_INS, -1);
   for (int l = 0; l < kLayers; ++l) {
     // a fused pair reads the first layer's inputs while it writes the second
     // layer's outputs: place those as if the first layer wrote them
-    const int at = l > 0 && !stored[l - 1] ? l - 1 : l;
-    if (stored[l]) allocate(kDefs[l].dst, at);
+    const int at = l > 0 && !V->stored[l - 1] ? l - 1 : l;
+    if (V->stored[l] && !(io_external && kDefs[l].dst == V_OUT)) place(kDefs[l].dst, at);
     for (int i = 0; i < 4; ++i)
-      if (P->split_on[i] && kSplits[i].producer == l) allocate(kSplits[i].split, at);
+      if (V->split_on[i] && kSplits[i].producer == l) place(kSplits[i].split, at);
   }
-  P->arena_bytes = total;
-  cudaError_t e = cudaMalloc(&P->arena, total);
-  if (e != cudaSuccess)
-    return fail(OIDNX_ERR_OUT_OF_MEMORY, "activation arena of %zu bytes: %s", total,
-                cudaGetErrorString(e));
-  // Zero once so that padded lanes read as zero before any write.
-  e = cudaMemset(P->arena, 0, total);
-  if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "arena memset: %s", cudaGetErrorString(e));
-  e = cudaEventCreateWithFlags(&P->done, cudaEventDisableTiming);
-  if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "event: %s", cudaGetErrorString(e));
+}
 
+// The launches of one network pass over the values of V, in order, with
+// device pointers from ptr(value); emit(LayerLaunch&) receives each launch
+// (with its logical FLOPs and algorithmic bytes) and returns a status.
+template <class Ptr, class Emit>
+oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V, Ptr ptr, Emit emit) {
   const int bpe = f->precision == OIDNX_PRECISION_FP16 ? 2 : 4;
-  auto value_bytes = [&](int v) {
-    return static_cast<double>(P->value_ext[v].w) * P->value_ext[v].h * P->value_ch[v] * bpe;
+  auto logical_bytes = [&](int v) {
+    return static_cast<double>(V.ext[v].w) * V.ext[v].h * V.ch[v] * bpe;
   };
   for (int l = 0; l < kLayers; ++l) {
     const LayerDef& d = kDefs[l];
@@ -1447,77 +1452,114 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
     std::memset(&LL, 0, sizeof(LL));
     LL.layer = l;
     LL.name = kLayerNames[l];
-    const Extent conv = P->lvl[d.level];
+    const Extent conv = V.lvl[d.level];
+    const double px = static_cast<double>(conv.w) * conv.h;
     const int pi = l == kPairs[0].first ? 0 : (l == kPairs[1].first ? 1 : -1);
-    if (pi >= 0 && P->fused[pi]) {
+    if (pi >= 0 && V.fused[pi]) {
       const LayerDef& d2 = kDefs[l + 1];
       const DeviceLayer& L2 = f->layers[l + 1];
       void* out_split = nullptr;
       int out_split_pitch = 0;
       for (int i = 0; i < 4; ++i)
-        if (P->split_on[i] && kSplits[i].producer == l + 1) {
-          out_split = P->ptr(kSplits[i].split);
-          out_split_pitch = P->value_ext[kSplits[i].split].pitch;
+        if (V.split_on[i] && kSplits[i].producer == l + 1) {
+          out_split = ptr(kSplits[i].split);
+          out_split_pitch = V.ext[kSplits[i].split].pitch;
         }
       LL.pair = 1;
       LL.name = kPairs[pi].name;
-      OIDNX_TRY(build_pair_launch(L, L2, kPairs[pi].mode, P->ptr(d.src0), P->value_ext[d.src0],
-                                  conv.w, conv.h, P->ptr(d2.dst), P->value_ext[d2.dst].pitch,
-                                  out_split, out_split_pitch, f->status, &LL.pcl));
-      const double px = static_cast<double>(conv.w) * conv.h;
+      OIDNX_TRY(build_pair_launch(L, L2, kPairs[pi].mode, ptr(d.src0), V.ext[d.src0], conv.w, conv.h,
+                                  ptr(d2.dst), V.ext[d2.dst].pitch, out_split, out_split_pitch,
+                                  f->status, &LL.pcl));
       LL.flop = 2.0 * 9.0 * (L.cin * L.cout + L2.cin * L2.cout) * px;
-      const Extent oe = P->value_ext[d2.dst];
-      LL.bytes = value_bytes(d.src0) +
-                 (d2.kind == kFinal ? static_cast<double>(oe.w) * oe.h * 16 : value_bytes(d2.dst)) +
+      const Extent oe = V.ext[d2.dst];
+      LL.bytes = logical_bytes(d.src0) +
+                 (d2.kind == kFinal ? static_cast<double>(oe.w) * oe.h * 16 : logical_bytes(d2.dst)) +
                  static_cast<double>(L.weight_bytes + L2.weight_bytes);
-      P->launches.push_back(LL);
+      OIDNX_TRY(emit(LL));
       ++l;
       continue;
     }
     if (d.kind == kFinal && final_foldable(L)) {
       LL.final = 1;
-      OIDNX_TRY(build_final_launch(L, P->ptr(d.src0), P->value_ext[d.src0], conv.w, conv.h,
-                                   P->ptr(d.dst), f->status, &LL.fcl));
-      const double px = static_cast<double>(conv.w) * conv.h;
+      OIDNX_TRY(build_final_launch(L, ptr(d.src0), V.ext[d.src0], conv.w, conv.h, ptr(d.dst),
+                                   f->status, &LL.fcl));
       LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
-      LL.bytes = value_bytes(d.src0) + static_cast<double>(P->value_ext[d.dst].w) * P->value_ext[d.dst].h * 16 +
+      LL.bytes = logical_bytes(d.src0) + static_cast<double>(V.ext[d.dst].w) * V.ext[d.dst].h * 16 +
                  static_cast<double>(L.weight_bytes);
-      P->launches.push_back(LL);
+      OIDNX_TRY(emit(LL));
       continue;
     }
-    const void* s1 = d.src1 >= 0 ? P->ptr(d.src1) : nullptr;
-    Extent e1 = d.src1 >= 0 ? P->value_ext[d.src1] : Extent{0, 0, 0};
+    const void* s1 = d.src1 >= 0 ? ptr(d.src1) : nullptr;
+    Extent e1 = d.src1 >= 0 ? V.ext[d.src1] : Extent{0, 0, 0};
     bool subpixel = false;
     void* out_split = nullptr;
     int out_split_pitch = 0;
     for (int i = 0; i < 4; ++i) {
-      if (!P->split_on[i]) continue;
+      if (!V.split_on[i]) continue;
       if (kSplits[i].consumer == l) {
         subpixel = true;
-        s1 = P->ptr(kSplits[i].split);
-        e1 = P->value_ext[kSplits[i].split];
+        s1 = ptr(kSplits[i].split);
+        e1 = V.ext[kSplits[i].split];
       }
       if (kSplits[i].producer == l) {
-        out_split = P->ptr(kSplits[i].split);
-        out_split_pitch = P->value_ext[kSplits[i].split].pitch;
+        out_split = ptr(kSplits[i].split);
+        out_split_pitch = V.ext[kSplits[i].split].pitch;
       }
     }
-    OIDNX_TRY(build_tc_launch(L, d.kind, P->ptr(d.src0), P->value_ext[d.src0], s1, e1, conv.w,
-                              conv.h, P->ptr(d.dst), P->value_ext[d.dst].pitch, f->status,
-                              &LL.tcl, subpixel, out_split, out_split_pitch));
-    const double px = static_cast<double>(conv.w) * conv.h;
+    OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), V.ext[d.src0], s1, e1, conv.w, conv.h,
+                              ptr(d.dst), V.ext[d.dst].pitch, f->status, &LL.tcl, subpixel,
+                              out_split, out_split_pitch));
     LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
-    double in_bytes = static_cast<double>(P->value_ext[d.src0].w) * P->value_ext[d.src0].h *
-                      P->value_ch[d.src0] * bpe;
-    if (d.src1 >= 0)
-      in_bytes += static_cast<double>(P->value_ext[d.src1].w) * P->value_ext[d.src1].h *
-                  P->value_ch[d.src1] * bpe;
-    const Extent oe = P->value_ext[d.dst];
+    const Extent oe = V.ext[d.dst];
     const double out_bytes = d.kind == kFinal ? static_cast<double>(oe.w) * oe.h * 16
                                               : static_cast<double>(oe.w) * oe.h * L.cout * bpe;
-    LL.bytes = in_bytes + out_bytes + static_cast<double>(L.weight_bytes);
-    P->launches.push_back(LL);
+    LL.bytes = logical_bytes(d.src0) + (d.src1 >= 0 ? logical_bytes(d.src1) : 0.0) + out_bytes +
+               static_cast<double>(L.weight_bytes);
+    OIDNX_TRY(emit(LL));
   }
+  return ok();
+}
+
+// The cached plan for a w x h network input: its arena (zeroed once) and
+// its launch descriptors.
+oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* out) {
+  std::unique_ptr<Plan> P(new Plan());
+  // on any failure below, free what was already created (arena, event)
+  struct Release {
+    Plan* p;
+    ~Release() { destroy_plan(p); }
+  } release{P.get()};
+  P->w = w;
+  P->h = h;
+  ValueLayout V;
+  layout_values(f, w, h, false, f->keep_acts != 0, &V);
+  for (int l = 0; l < 5; ++l) P->lvl[l] = V.lvl[l];
+  for (int v = 0; v < V_COUNT; ++v) {
+    P->value_ext[v] = V.ext[v];
+    P->value_ch[v] = V.ch[v];
+    P->value_off[v] = V.off[v];
+    P->value_bytes[v] = V.bytes[v];
+  }
+  for (int i = 0; i < 4; ++i) P->split_on[i] = V.split_on[i];
+  for (int i = 0; i < 2; ++i) P->fused[i] = V.fused[i];
+  P->arena_bytes = V.total;
+  cudaError_t e = cudaMalloc(&P->arena, V.total);
+  if (e != cudaSuccess)
+    return fail(OIDNX_ERR_OUT_OF_MEMORY, "activation arena of %zu bytes: %s", V.total,
+                cudaGetErrorString(e));
+  // Zero once so that padded lanes read as zero before any write.
+  e = cudaMemset(P->arena, 0, V.total);
+  if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "arena memset: %s", cudaGetErrorString(e));
+  e = cudaEventCreateWithFlags(&P->done, cudaEventDisableTiming);
+  if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "event: %s", cudaGetErrorString(e));
+  Plan* plan = P.get();
+  OIDNX_TRY(build_network_launches(
+      f, V, [plan](int v) { return plan->ptr(v); },
+      [plan](const LayerLaunch& LL) {
+        plan->launches.push_back(LL);
+        return ok();
+      }));
+  release.p = nullptr;
   *out = std::move(P);
   return ok();
 }
@@ -1793,145 +1835,24 @@ oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, in
   if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16)
     return fail(OIDNX_ERR_INVALID_ARGUMENT,
                 "network_execute_noalloc: pointers must be 16-byte aligned");
-  Extent lvl[5];
-  lvl[0] = {w, h, w};
-  for (int l = 1; l < 5; ++l) {
-    const int lw = (lvl[l - 1].w + 1) / 2;
-    lvl[l] = {lw, (lvl[l - 1].h + 1) / 2, lw};
-  }
-  Extent ext[V_COUNT];
-  int ch[V_COUNT] = {};
-  ext[V_IN] = lvl[0];  // the caller's buffer, rows of w pixels
-  ch[V_IN] = f->in_channels;
-  for (int l = 0; l < kLayers; ++l) {
-    const LayerDef& d = kDefs[l];
-    ext[d.dst] = value_extent(f->precision, lvl[d.kind == kPool ? d.level + 1 : d.level],
-                              d.dst == V_OUT);
-    ch[d.dst] = f->layers[l].cout;
-  }
-  int last_use[V_COUNT];
-  for (int v = 0; v < V_COUNT; ++v) last_use[v] = -1;
-  for (int l = 0; l < kLayers; ++l) {
-    last_use[kDefs[l].src0] = l;
-    if (kDefs[l].src1 >= 0) last_use[kDefs[l].src1] = l;
-  }
-  bool split_on[4];
-  for (int i = 0; i < 4; ++i) {
-    const SplitCopy& sc = kSplits[i];
-    const LayerDef& d = kDefs[sc.consumer];
-    split_on[i] = f->subpixel && use_subpixel(lvl[d.level].w, lvl[d.level].h, ext[d.src0]);
-    ext[sc.split] = ext[sc.base];
-    ext[sc.split].pitch = split_pitch(ext[sc.base].w);
-    ch[sc.split] = ch[sc.base];
-    last_use[sc.split] = sc.consumer;
-  }
-  struct Slot { size_t cap, off; int active; };
-  Slot slots[V_COUNT];
-  int nslots = 0;
-  size_t total = 0, off[V_COUNT] = {};
-  auto place = [&](int v, int l) {
-    for (int i = 0; i < nslots; ++i)
-      if (slots[i].active >= 0 && last_use[slots[i].active] < l) slots[i].active = -1;
-    const size_t need = round_up_sz(act_bytes(f->precision, ext[v], ch[v], false), 1024);
-    int best = -1;
-    for (int i = 0; i < nslots; ++i)
-      if (slots[i].active < 0 && slots[i].cap >= need && (best < 0 || slots[i].cap < slots[best].cap))
-        best = i;
-    if (best < 0) {
-      slots[nslots] = {need, total, -1};
-      total += need;
-      best = nslots++;
-    }
-    slots[best].active = v;
-    off[v] = slots[best].off;
-  };
-  bool fused[2];
-  bool stored[kLayers];
-  for (int l = 0; l < kLayers; ++l) stored[l] = true;
-  for (int i = 0; i < 2; ++i) {
-    fused[i] = pair_fusable(f, kPairs[i]);
-    if (fused[i]) stored[kPairs[i].first] = false;
-  }
-  if (split_on[0]) place(V_INS, -1);
-  for (int l = 0; l < kLayers; ++l) {
-    const int v = kDefs[l].dst;
-    const int at = l > 0 && !stored[l - 1] ? l - 1 : l;  // see create_plan
-    // V_OUT is written straight into the caller's output
-    if (v != V_OUT && stored[l]) place(v, at);
-    for (int i = 0; i < 4; ++i)
-      if (split_on[i] && kSplits[i].producer == l) place(kSplits[i].split, at);
-  }
-  if (total > cap)
+  ValueLayout V;
+  layout_values(f, w, h, true, false, &V);
+  if (V.total > cap)
     return fail(OIDNX_ERR_INVALID_ARGUMENT,
                 "network_execute_noalloc: a %dx%d input needs %zu bytes of activation scratch; "
                 "the static arena holds %zu bytes",
-                w, h, total, cap);
+                w, h, V.total, cap);
   auto ptr = [&](int v) -> void* {
     if (v == V_IN) return const_cast<void*>(in);
     if (v == V_OUT) return out;
-    return static_cast<uint8_t*>(arena) + off[v];
+    return static_cast<uint8_t*>(arena) + V.off[v];
   };
-  if (split_on[0]) {
-    cudaError_t e = launch_split_copy(in, w, ptr(V_INS), ext[V_INS].pitch, w, h,
+  if (V.split_on[0]) {
+    cudaError_t e = launch_split_copy(in, w, ptr(V_INS), V.ext[V_INS].pitch, w, h,
                                       act_chunks(f->precision, f->in_channels), s);
     if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "split copy: %s", cudaGetErrorString(e));
   }
-  for (int l = 0; l < kLayers; ++l) {
-    const LayerDef& d = kDefs[l];
-    const DeviceLayer& L = f->layers[l];
-    LayerLaunch LL;
-    std::memset(&LL, 0, sizeof(LL));
-    LL.layer = l;
-    LL.name = kLayerNames[l];
-    const Extent conv = lvl[d.level];
-    const int pi = l == kPairs[0].first ? 0 : (l == kPairs[1].first ? 1 : -1);
-    if (pi >= 0 && fused[pi]) {
-      const LayerDef& d2 = kDefs[l + 1];
-      void* out_split = nullptr;
-      int out_split_pitch = 0;
-      for (int i = 0; i < 4; ++i)
-        if (split_on[i] && kSplits[i].producer == l + 1) {
-          out_split = ptr(kSplits[i].split);
-          out_split_pitch = ext[kSplits[i].split].pitch;
-        }
-      LL.pair = 1;
-      LL.name = kPairs[pi].name;
-      OIDNX_TRY(build_pair_launch(L, f->layers[l + 1], kPairs[pi].mode, ptr(d.src0), ext[d.src0],
-                                  conv.w, conv.h, ptr(d2.dst), ext[d2.dst].pitch, out_split,
-                                  out_split_pitch, f->status, &LL.pcl));
-      OIDNX_TRY(run_launch(LL, s));
-      ++l;
-      continue;
-    }
-    if (d.kind == kFinal && final_foldable(L)) {
-      LL.final = 1;
-      OIDNX_TRY(build_final_launch(L, ptr(d.src0), ext[d.src0], conv.w, conv.h, ptr(d.dst), f->status,
-                                   &LL.fcl));
-      OIDNX_TRY(run_launch(LL, s));
-      continue;
-    }
-    const void* s1 = d.src1 >= 0 ? ptr(d.src1) : nullptr;
-    Extent e1 = d.src1 >= 0 ? ext[d.src1] : Extent{0, 0, 0};
-    bool subpixel = false;
-    void* out_split = nullptr;
-    int out_split_pitch = 0;
-    for (int i = 0; i < 4; ++i) {
-      if (!split_on[i]) continue;
-      if (kSplits[i].consumer == l) {
-        subpixel = true;
-        s1 = ptr(kSplits[i].split);
-        e1 = ext[kSplits[i].split];
-      }
-      if (kSplits[i].producer == l) {
-        out_split = ptr(kSplits[i].split);
-        out_split_pitch = ext[kSplits[i].split].pitch;
-      }
-    }
-    OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), ext[d.src0], s1, e1, conv.w, conv.h,
-                              ptr(d.dst), ext[d.dst].pitch, f->status, &LL.tcl, subpixel,
-                              out_split, out_split_pitch));
-    OIDNX_TRY(run_launch(LL, s));
-  }
+  OIDNX_TRY(build_network_launches(f, V, ptr, [s](const LayerLaunch& LL) { return run_launch(LL, s); }));
   return ok();
 }
 
