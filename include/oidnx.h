@@ -256,7 +256,15 @@ void oidnx_filter_release(oidnx_filter* f);
  * weight: host OIHW float32 [cout][cin][3][3]; bias: host float32 [cout].
  * precision: OIDNX_PRECISION_FP16 (tensor cores, fp32 accumulate) or FP32.
  * in / out: device tensors in the activation layout above (cin / cout
- * channels, w x h pixels).  relu: 0 or 1.  */
+ * channels, w x h pixels, rows of w pixels), 16-byte aligned.  relu must be
+ * 1 (the hidden layers' form; the final layer runs inside the network).
+ * The caller owns in, out and the stream; the conv owns its packed weights
+ * and bias until oidnx_conv_release (NULL is ignored).  execute enqueues on
+ * `stream` and returns.
+ * Errors: create: INVALID_ARGUMENT (NULL or non-positive sizes, unknown
+ * precision), UNSUPPORTED (cout > 256), CUDA (allocation failures too); execute:
+ * INVALID_ARGUMENT (NULL, sizes, misaligned pointers), UNSUPPORTED
+ * (relu = 0), CUDA.  */
 oidnx_status oidnx_conv_create(const float* weight, const float* bias, int cout,
                                int cin, int precision, oidnx_conv** out);
 oidnx_status oidnx_conv_execute(oidnx_conv* c, const void* in, void* out, int w,
