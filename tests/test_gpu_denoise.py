@@ -127,6 +127,31 @@ def test_degenerate_image_shapes_match_oracle(w, h, precision):
         assert rel_l2(out[..., :3], ref[..., :3]) <= 3e-4   # 1e-4 on the network output x kappa
 
 
+@pytest.mark.parametrize("precision", ["fp16", "fp32"])
+def test_tiled_denoise_matches_oracle_tiled_denoise(precision):
+    """A ragged tile grid (500 x 300, maxTileSize 256, overlap 96) against the
+    oracle's own tiled denoise: the same tile rectangles, per-tile input and
+    output passes and stitching, with inputScale != 1."""
+    w, h = 500, 300
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True)
+    weights = synth.unet_weights(9, bias_scale=0.05)
+    prec = ox.PRECISION_FP16 if precision == "fp16" else ox.PRECISION_FP32
+    d = Denoiser(weights, prec, imgs, True, input_scale=0.8, max_tile_size=256, overlap=96)
+    try:
+        out = d.run()
+        tiles = ox.oidnx_filter_get_int(d.f, "tiles")
+    finally:
+        d.close()
+    ref = unet.denoise(imgs, weights, hdr=True, input_scale=0.8, max_tile_size=256, overlap=96,
+                       precision=precision)
+    assert tiles > 4
+    assert np.array_equal(out[..., 3].view(np.uint32), imgs[0][..., 3].view(np.uint32))
+    if precision == "fp16":
+        assert rel_l2(out[..., :3], ref[..., :3]) <= 2e-2
+    else:
+        assert rel_l2(out[..., :3], ref[..., :3]) <= 3e-4   # 1e-4 on the network output x kappa
+
+
 def test_8k_single_tile_with_activations_over_4gib():
     """8192 x 8192 as one tile: dec_conv1a's fp16 output alone is 8 GiB, so
     the 64-bit offsets of every kernel are exercised.  The output image is
