@@ -270,7 +270,9 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
     conv3x3_tc_kernel(const __grid_constant__ CUtensorMap map0,
                       const __grid_constant__ CUtensorMap map1, const TcConvParams p) {
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  // 128-byte alignment suffices: TMA tile destinations need 128 B, the
+  // unswizzled UMMA operands 16 B (every region below is a 1 KB multiple)
+  const uint32_t pad = (128u - (smem_u32(smem_raw) & 127u)) & 127u;
   uint8_t* smem = smem_raw + pad;
 
   const int S = p.S, R = p.R, N = p.N, KB0 = p.KB0;

@@ -987,7 +987,7 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   p.st_stage = 0;
   const int items = L.KB0 + 2 * L.KB1;
   const size_t max_smem = 227 * 1024;
-  const size_t fixed = 1024 + static_cast<size_t>((N + 31) / 32) * 32 * 4 + 256;
+  const size_t fixed = 128 + static_cast<size_t>((N + 31) / 32) * 32 * 4 + 256;
   // resident: one column parity's half of every upsampled block + the skip blocks
   const size_t wres = static_cast<size_t>(L.KB0) * (L.sub_ub / 2) +
                       (L.sub_bytes - static_cast<size_t>(L.KB0) * L.sub_ub);
@@ -1099,8 +1099,8 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   p.st_stage = static_cast<uint32_t>(round_up_sz(p.st_tx, 1024));
   const int KB = L.KB0 + L.KB1;
   const size_t max_smem = 227 * 1024;
-  // alignment slack + bias + barriers
-  const size_t fixed = 1024 + static_cast<size_t>((N + 31) / 32) * 32 * 4 + 256;
+  // alignment slack (128 B) + bias + barriers
+  const size_t fixed = 128 + static_cast<size_t>((N + 31) / 32) * 32 * 4 + 256;
   const size_t wbytes = static_cast<size_t>(KB) * p.b_stage;
   // per stage: A (and for tf32 its A_lo split), low-resolution staging
   const size_t a_st = static_cast<size_t>(p.a_stage) * (L.tf32 ? 2 : 1) + p.st_stage;
