@@ -713,7 +713,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
             if (two) tmem_st16(t0 + 16, bz[1]);
             // columns [W, pitch) are row padding: stored as zeros
             if (TF && x < p.pitch && y < p.H) {
-              const bool pad = x >= p.W;
+              const bool pad = x >= p.W || (p.period && y % p.period >= p.rows);
               float* row = static_cast<float*>(p.out) + (static_cast<size_t>(y) * p.out_c4 * p.pitch + x) * 4;
 #pragma unroll
               for (int b = 0; b < 2; ++b) {
@@ -732,7 +732,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
                 }
               }
             } else if (!TF && x < p.pitch && y < p.H) {
-              const bool pad = x >= p.W;
+              const bool pad = x >= p.W || (p.period && y % p.period >= p.rows);
               __half* row = out + (static_cast<size_t>(y) * C8 * p.pitch + x) * 8;
 #pragma unroll
               for (int b = 0; b < 2; ++b) {
@@ -761,6 +761,8 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
             const int ya = y0 + 2 * i;
             const bool va = x < p.W && ya < p.H;
             const bool vb = x < p.W && ya + 1 < p.H;
+            // stacked tiles: a pooled gap row (rows and period are even) is zero
+            const bool gap = p.period && ya % p.period >= p.rows;
             const int yp = ya >> 1;
             uint32_t v[2][16];
             const uint32_t t0 = tl + static_cast<uint32_t>((2 * i) * N + c * 16);
@@ -780,7 +782,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
             }
             // pooled columns [Wp, pitch) are row padding: stored as zeros
             if (TF && ((lane & 1) == 0) && yp < Hp) {
-              const bool pad = xp >= Wp;
+              const bool pad = xp >= Wp || gap;
               float* base = static_cast<float*>(p.out) + (static_cast<size_t>(yp) * p.out_c4 * p.pitch + xp) * 4;
               // split copy: plane xp & 1, index xp >> 1 (the split pitch is even)
               float* base2 = p.out_split == nullptr ? nullptr
@@ -797,7 +799,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
                   *reinterpret_cast<float4*>(base2 + c4 * static_cast<size_t>(p.split_pitch) * 4) = f;
               }
             } else if (!TF && ((lane & 1) == 0) && yp < Hp) {
-              const bool pad = xp >= Wp;
+              const bool pad = xp >= Wp || gap;
               uint32_t h[8];
 #pragma unroll
               for (int k = 0; k < 8; ++k) h[k] = pad ? 0u : pack_half2(mx[2 * k], mx[2 * k + 1]);

@@ -67,6 +67,9 @@ struct TcConvParams {
   int pitch;               // fp16 output row pitch in pixels (>= output width);
                            // columns [width, pitch) are written as zeros
   int up_pair;             // sub-pixel: upsampled K blocks per pipeline item (1 or 2)
+  // stacked tiles: rows y with y % period >= rows are the zero gap rows
+  // between tiles (stored as zeros); period 0: a single image
+  int period, rows;
   int out_c4;              // fp32 storage: 4-channel chunks of the output value
                            // (Cout rounded up to 4; may be fewer than N / 4)
   int xs0, xs1;            // log2 pixels per x unit of map0 / map1: 3 for
@@ -221,6 +224,8 @@ struct PackParams {
   void* out_split;         // optional parity-split copy [th][chunks][2][split_pitch/2][lanes]
   int split_pitch;         // its pitch (a multiple of 16), columns >= tw zero
   const float4* log2_tab;  // fp32 HDR: kLog2TabSize entries from fill_log2_table
+  int gap_rows;            // stacked tiles: rows th .. th + gap_rows - 1 of out and
+                           // out_split are written as zeros
 };
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 

@@ -134,8 +134,9 @@ __global__ void pack_kernel(const PackParams p) {
   const int ty = blockIdx.y;
   if (tx >= (p.out_split && p.split_pitch > p.pitch ? p.split_pitch : p.pitch)) return;
   const size_t pixel = static_cast<size_t>(ty) * p.chunks * p.pitch + tx;
-  if (tx >= p.tw) {
-    // row padding: zeros, so that 8-pixel TMA rows read zero past the tile
+  if (tx >= p.tw || ty >= p.th) {
+    // row padding, and the gap rows below a stacked tile: zeros, so that
+    // 8-pixel TMA rows read zero past the tile
     if (FP16) {
       uint4* out = static_cast<uint4*>(p.out);
       if (tx < p.pitch) {
@@ -309,7 +310,7 @@ cudaError_t launch_pitch_copy(const void* src, int src_pitch, void* dst, int dst
 template <int S, bool F16, bool HDR>
 cudaError_t launch_pack_t(const PackParams& p, cudaStream_t stream) {
   const int span = p.out_split && p.split_pitch > p.pitch ? p.split_pitch : p.pitch;
-  dim3 grid((span + 127) / 128, p.th);
+  dim3 grid((span + 127) / 128, p.th + p.gap_rows);
   return launch_pdl(pack_kernel<S, F16, HDR>, grid, dim3(128), 0, stream, p);
 }
 

@@ -714,6 +714,10 @@ struct Extent {
 
 int fp16_pitch(int w) { return (w + kGroupPx - 1) / kGroupPx * kGroupPx; }
 
+// Zero rows below each tile of a stacked frame at level 0 (one row at level
+// 4): the same padding for every conv as an image border gives.
+constexpr int kStackGap = 16;
+
 // Pitch of a column-parity split copy: 16-pixel multiple, so that each
 // parity plane (pitch / 2 entries) is a whole number of 8-entry TMA rows.
 int split_pitch(int w) { return (w + 2 * kGroupPx - 1) / (2 * kGroupPx) * (2 * kGroupPx); }
@@ -742,6 +746,12 @@ struct Plan {
   std::vector<LayerLaunch> launches;
   bool split_on[4] = {};  // kSplits[i] in use (its decoder runs in sub-pixel mode)
   bool fused[2] = {};     // kPairs[i] runs as one fused kernel
+  // stacked tiles: the frame's `stack` tiles (h rows each) sit one above the
+  // other in every value, each followed by kStackGap zero rows at level 0
+  // (kStackGap >> L at level L); the convs run once over the stack, the
+  // input pass and the final conv (final_tiles) once per tile
+  int stack = 1;
+  std::vector<LayerLaunch> final_tiles;
   // the last execution stored the network output (not so when the output
   // pass ran in the final conv's epilogue without keepActivations)
   bool out_stored = true;
@@ -1370,9 +1380,9 @@ struct ValueLayout {
 };
 
 void layout_values(const oidnx_filter* f, int w, int h, bool io_external, bool keep,
-                   ValueLayout* V) {
+                   ValueLayout* V, int stack = 1) {
   std::memset(V, 0, sizeof(*V));
-  V->lvl[0] = {w, h, w};
+  V->lvl[0] = {w, stack > 1 ? stack * (h + kStackGap) : h, w};
   for (int l = 1; l < 5; ++l) {
     const int lw = (V->lvl[l - 1].w + 1) / 2;
     V->lvl[l] = {lw, (V->lvl[l - 1].h + 1) / 2, lw};
@@ -1444,11 +1454,18 @@ void layout_values(const oidnx_filter* f, int w, int h, bool io_external, bool k
 // The launches of one network pass over the values of V, in order, with
 // device pointers from ptr(value); emit(LayerLaunch&) receives each launch
 // (with its logical FLOPs and algorithmic bytes) and returns a status.
+// stack_rows: tile rows of a stacked layout (0: one image): every conv
+// gets its level's gap period, the final conv is left to the caller (one
+// launch per tile), and FLOPs and bytes count the tiles' rows only.
 template <class Ptr, class Emit>
-oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V, Ptr ptr, Emit emit) {
+oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V, Ptr ptr, Emit emit,
+                                    int stack_rows = 0) {
   const int bpe = f->precision == OIDNX_PRECISION_FP16 ? 2 : 4;
+  // share of the stacked rows that are tile rows (the same at every level)
+  const double tile_share =
+      stack_rows ? static_cast<double>(stack_rows) / (stack_rows + kStackGap) : 1.0;
   auto logical_bytes = [&](int v) {
-    return static_cast<double>(V.ext[v].w) * V.ext[v].h * V.ch[v] * bpe;
+    return static_cast<double>(V.ext[v].w) * V.ext[v].h * V.ch[v] * bpe * tile_share;
   };
   for (int l = 0; l < kLayers; ++l) {
     const LayerDef& d = kDefs[l];
@@ -1458,7 +1475,7 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
     LL.layer = l;
     LL.name = kLayerNames[l];
     const Extent conv = V.lvl[d.level];
-    const double px = static_cast<double>(conv.w) * conv.h;
+    const double px = static_cast<double>(conv.w) * conv.h * tile_share;
     const int pi = l == kPairs[0].first ? 0 : (l == kPairs[1].first ? 1 : -1);
     if (pi >= 0 && V.fused[pi]) {
       const LayerDef& d2 = kDefs[l + 1];
@@ -1485,6 +1502,7 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
       continue;
     }
     if (d.kind == kFinal && final_foldable(L)) {
+      if (stack_rows) continue;  // one launch per tile, built by the caller
       LL.final = 1;
       OIDNX_TRY(build_final_launch(L, ptr(d.src0), V.ext[d.src0], conv.w, conv.h, ptr(d.dst),
                                    f->status, &LL.fcl));
@@ -1514,10 +1532,15 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
     OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), V.ext[d.src0], s1, e1, conv.w, conv.h,
                               ptr(d.dst), V.ext[d.dst].pitch, f->status, &LL.tcl, subpixel,
                               out_split, out_split_pitch));
+    if (stack_rows) {
+      LL.tcl.p.period = (stack_rows + kStackGap) >> d.level;
+      LL.tcl.p.rows = stack_rows >> d.level;
+    }
     LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
     const Extent oe = V.ext[d.dst];
-    const double out_bytes = d.kind == kFinal ? static_cast<double>(oe.w) * oe.h * 16
-                                              : static_cast<double>(oe.w) * oe.h * L.cout * bpe;
+    const double out_bytes = (d.kind == kFinal ? static_cast<double>(oe.w) * oe.h * 16
+                                               : static_cast<double>(oe.w) * oe.h * L.cout * bpe) *
+                             tile_share;
     LL.bytes = logical_bytes(d.src0) + (d.src1 >= 0 ? logical_bytes(d.src1) : 0.0) + out_bytes +
                static_cast<double>(L.weight_bytes);
     OIDNX_TRY(emit(LL));
@@ -1527,7 +1550,7 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
 
 // The cached plan for a w x h network input: its arena (zeroed once) and
 // its launch descriptors.
-oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* out) {
+oidnx_status create_plan(oidnx_filter* f, int w, int h, int stack, std::unique_ptr<Plan>* out) {
   std::unique_ptr<Plan> P(new Plan());
   // on any failure below, free what was already created (arena, event)
   struct Release {
@@ -1536,8 +1559,9 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
   } release{P.get()};
   P->w = w;
   P->h = h;
+  P->stack = stack;
   ValueLayout V;
-  layout_values(f, w, h, false, f->keep_acts != 0, &V);
+  layout_values(f, w, h, false, f->keep_acts != 0, &V, stack);
   for (int l = 0; l < 5; ++l) P->lvl[l] = V.lvl[l];
   for (int v = 0; v < V_COUNT; ++v) {
     P->value_ext[v] = V.ext[v];
@@ -1563,7 +1587,31 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
       [plan](const LayerLaunch& LL) {
         plan->launches.push_back(LL);
         return ok();
-      }));
+      },
+      stack > 1 ? h : 0));
+  if (stack > 1) {
+    // the final conv of each tile reads that tile's rows of dec_conv1b's
+    // output (its own halo rows beyond them read as zeros)
+    const int l = kLayers - 1;
+    const LayerDef& d = kDefs[l];
+    const DeviceLayer& L = f->layers[l];
+    const Extent se = V.ext[d.src0];
+    const size_t row_bytes = static_cast<size_t>(act_chunks(f->precision, V.ch[d.src0])) * se.pitch * 16;
+    for (int t = 0; t < stack; ++t) {
+      LayerLaunch LL;
+      std::memset(&LL, 0, sizeof(LL));
+      LL.layer = l;
+      LL.name = kLayerNames[l];
+      LL.final = 1;
+      const uint8_t* src = static_cast<const uint8_t*>(plan->ptr(d.src0)) +
+                           static_cast<size_t>(t) * (h + kStackGap) * row_bytes;
+      OIDNX_TRY(build_final_launch(L, src, Extent{w, h, se.pitch}, w, h, nullptr, f->status, &LL.fcl));
+      LL.flop = 2.0 * 9.0 * L.cin * L.cout * w * h;
+      LL.bytes = static_cast<double>(w) * h * (V.ch[d.src0] * (f->precision == OIDNX_PRECISION_FP16 ? 2 : 4) + 16) +
+                 static_cast<double>(L.weight_bytes);
+      plan->final_tiles.push_back(LL);
+    }
+  }
   release.p = nullptr;
   *out = std::move(P);
   return ok();
@@ -1571,7 +1619,7 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, std::unique_ptr<Plan>* o
 
 // LRU lookup/creation of the plan for a w x h network input ("nativeUNet.ts",
 // _execution): evicted plans are destroyed once their last use has finished.
-oidnx_status get_plan(oidnx_filter* f, int w, int h, Plan** out) {
+oidnx_status get_plan(oidnx_filter* f, int w, int h, Plan** out, int stack = 1) {
   for (auto it = f->retired.begin(); it != f->retired.end();) {
     if (cudaEventQuery((*it)->done) == cudaSuccess) {
       destroy_plan(it->get());
@@ -1581,13 +1629,13 @@ oidnx_status get_plan(oidnx_filter* f, int w, int h, Plan** out) {
     }
   }
   for (auto& p : f->plans)
-    if (p->w == w && p->h == h) {
+    if (p->w == w && p->h == h && p->stack == stack) {
       p->last_used = ++f->clock;
       *out = p.get();
       return ok();
     }
   std::unique_ptr<Plan> P;
-  OIDNX_TRY(create_plan(f, w, h, &P));
+  OIDNX_TRY(create_plan(f, w, h, stack, &P));
   P->last_used = ++f->clock;
   Plan* raw = P.get();
   f->plans.push_back(std::move(P));
@@ -1654,6 +1702,80 @@ bool output_fused(const oidnx_filter* f, const Plan* P) {
   return P && f->fuse_output && !P->launches.empty() && P->launches.back().final;
 }
 
+// Stacked frame: each tile's input pass into its block of the stack (gap
+// rows zeroed), the convs once over the stack, then each tile's final conv
+// with the output pass in its epilogue.
+oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const size_t stride[4],
+                             float scale, bool prof, cudaStream_t s) {
+  const int period = P->h + kStackGap;
+  const int chunks = act_chunks(f->precision, f->in_channels);
+  const size_t in_row = static_cast<size_t>(chunks) * P->value_ext[V_IN].pitch * 16;
+  const size_t split_row = static_cast<size_t>(chunks) * P->value_ext[V_INS].pitch * 16;
+  int t = 0;
+  for (const AxisTile& ty : f->ty)
+    for (const AxisTile& tx : f->tx) {
+      PackParams pp;
+      std::memset(&pp, 0, sizeof(pp));
+      for (int i = 0; i < 3; ++i) {
+        pp.img[i] = static_cast<const float4*>(img[i]);
+        pp.stride[i] = stride[i] / 16;
+      }
+      pp.sources = f->in_channels / 3;
+      pp.width = f->width;
+      pp.height = f->height;
+      pp.tx = tx.in_start;
+      pp.ty = ty.in_start;
+      pp.tw = tx.in_size;
+      pp.th = ty.in_size;
+      pp.gap_rows = kStackGap;
+      pp.hdr = f->hdr;
+      pp.scale = scale;
+      pp.fp16 = f->precision == OIDNX_PRECISION_FP16;
+      pp.out = static_cast<uint8_t*>(P->ptr(V_IN)) + static_cast<size_t>(t) * period * in_row;
+      pp.out_split = P->split_on[0]
+                         ? static_cast<uint8_t*>(P->ptr(V_INS)) + static_cast<size_t>(t) * period * split_row
+                         : nullptr;
+      pp.split_pitch = P->split_on[0] ? P->value_ext[V_INS].pitch : 0;
+      pp.chunks = chunks;
+      pp.pitch = P->value_ext[V_IN].pitch;
+      pp.log2_tab = static_cast<const float4*>(f->log2_tab);
+      (void)cudaGetLastError();
+      cudaError_t e = launch_pack(pp, s);
+      if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
+      OIDNX_TRY(prof_mark(f, prof, -1, s));
+      ++t;
+    }
+  for (const LayerLaunch& L : P->launches) {
+    OIDNX_TRY(run_launch(L, s));
+    OIDNX_TRY(prof_mark(f, prof, L.layer, s));
+  }
+  t = 0;
+  for (const AxisTile& ty : f->ty)
+    for (const AxisTile& tx : f->tx) {
+      LayerLaunch L = P->final_tiles[t++];
+      L.fcl.outpass = 1;
+      L.name = "dec_conv0+output";
+      FinalConvParams& fp = L.fcl.p;
+      fp.net = nullptr;
+      fp.color = static_cast<const float4*>(img[0]);
+      fp.color_stride = stride[0] / 16;
+      fp.out = static_cast<float4*>(img[3]);
+      fp.out_stride = stride[3] / 16;
+      fp.in_x = tx.out_start - tx.in_start;
+      fp.in_y = ty.out_start - ty.in_start;
+      fp.ox = tx.out_start;
+      fp.oy = ty.out_start;
+      fp.ow = tx.out_size;
+      fp.oh = ty.out_size;
+      fp.hdr = f->hdr;
+      fp.scale = scale;
+      OIDNX_TRY(run_launch(L, s));
+      OIDNX_TRY(prof_mark(f, prof, L.layer, s));
+    }
+  P->out_stored = false;
+  return ok();
+}
+
 // All tiles: input pass -> network -> output pass, on stream s.
 oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t stride[4],
                              bool prof, cudaStream_t s) {
@@ -1661,6 +1783,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
   const int sources = f->in_channels / 3;
   const float scale = f->input_scale == 0.0f ? 1.0f : f->input_scale;
   OIDNX_TRY(prof_mark(f, prof, -2, s));
+  if (P->stack > 1) return enqueue_stacked(f, P, img, stride, scale, prof, s);
   for (const AxisTile& ty : f->ty)
     for (const AxisTile& tx : f->tx) {
       PackParams pp;
@@ -1744,8 +1867,10 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
 
 size_t denoise_launches(const oidnx_filter* f) {
   // input pass, the plan's conv launches, output pass (folded into the final
-  // conv when fused)
+  // conv when fused); stacked: per tile the input pass and the final conv,
+  // once each of the other convs
   const Plan* P = f->current;
+  if (P && P->stack > 1) return 2 * static_cast<size_t>(P->stack) + P->launches.size();
   const size_t convs = P ? P->launches.size() : kLayers;
   return f->tx.size() * f->ty.size() * (convs + (output_fused(f, P) ? 1 : 2));
 }
@@ -2063,8 +2188,14 @@ oidnx_status oidnx_filter_commit(oidnx_filter* f) {
   if (!plan_axis(f->width, limit, overlap, &f->tx) || !plan_axis(f->height, limit, overlap, &f->ty))
     return fail(OIDNX_ERR_INVALID_ARGUMENT, "maxTileSize %d too small for overlap %d",
                 f->max_tile, overlap);
+  // Frames of several (equal) tiles are stacked: each conv layer runs once
+  // over all tiles.  Not with kept activations (per-tile debug reads), fused
+  // layer pairs, or a separate output pass.
+  const int tiles = static_cast<int>(f->tx.size() * f->ty.size());
+  const bool stack = tiles > 1 && f->fuse_output && !f->keep_acts && !f->fuse &&
+                     final_foldable(f->layers[kLayers - 1]);
   Plan* P = nullptr;
-  OIDNX_TRY(get_plan(f, f->tx[0].in_size, f->ty[0].in_size, &P));
+  OIDNX_TRY(get_plan(f, f->tx[0].in_size, f->ty[0].in_size, &P, stack ? tiles : 1));
   f->current = P;
   f->committed = true;
   return ok();
@@ -2272,6 +2403,11 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
           fused_out ? L.bytes - tile_px * 16 + out_bytes - out_px / tiles * 16 : L.bytes,
           mma_flop(L));
     }
+  if (plan && plan->stack > 1 && !plan->final_tiles.empty()) {
+    const LayerLaunch& L = plan->final_tiles[0];  // per tile, counted per launch
+    add("dec_conv0+output", L.layer + 2, L.flop, L.bytes - tile_px * 16 + out_bytes - out_px / tiles * 16,
+        mma_flop(L));
+  }
   add("output", kLayers + 2, 0, out_bytes);
   s += "]}";
   if (s.size() + 1 > cap) return fail(OIDNX_ERR_INVALID_ARGUMENT, "profile buffer too small");
