@@ -717,6 +717,10 @@ int fp16_pitch(int w) { return (w + kGroupPx - 1) / kGroupPx * kGroupPx; }
 // Zero rows below each tile of a stacked frame at level 0 (one row at level
 // 4): the same padding for every conv as an image border gives.
 constexpr int kStackGap = 16;
+// Activation bytes a stacked group of tiles may take; frames with more
+// tiles run in several groups.  (Groups of 8 + 7 tiles of a 3840 x 2160
+// frame ran 9% slower than one stack of 15: 4.4 GB of fp16 activations.)
+constexpr size_t kStackBudget = size_t(16) << 30;
 
 // Pitch of a column-parity split copy: 16-pixel multiple, so that each
 // parity plane (pitch / 2 entries) is a whole number of 8-entry TMA rows.
@@ -782,7 +786,7 @@ struct oidnx_filter {
   // parameters
   int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
       overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 1,
-      fuse = 0, fuse_output = 1;
+      fuse = 0, fuse_output = 1, stack_tiles = 0;
   float input_scale = 1.0f;
   void* img[4] = {};
   size_t img_stride[4] = {};
@@ -1702,18 +1706,24 @@ bool output_fused(const oidnx_filter* f, const Plan* P) {
   return P && f->fuse_output && !P->launches.empty() && P->launches.back().final;
 }
 
-// Stacked frame: each tile's input pass into its block of the stack (gap
-// rows zeroed), the convs once over the stack, then each tile's final conv
-// with the output pass in its epilogue.
+// Stacked frame, in groups of up to P->stack tiles: each tile's input pass
+// into its block of the stack (gap rows zeroed), the convs once over the
+// stack, then each tile's final conv with the output pass in its epilogue.
 oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const size_t stride[4],
                              float scale, bool prof, cudaStream_t s) {
   const int period = P->h + kStackGap;
   const int chunks = act_chunks(f->precision, f->in_channels);
   const size_t in_row = static_cast<size_t>(chunks) * P->value_ext[V_IN].pitch * 16;
   const size_t split_row = static_cast<size_t>(chunks) * P->value_ext[V_INS].pitch * 16;
-  int t = 0;
-  for (const AxisTile& ty : f->ty)
-    for (const AxisTile& tx : f->tx) {
+  const int nx = static_cast<int>(f->tx.size());
+  const int tiles = nx * static_cast<int>(f->ty.size());
+  // groups of up to P->stack tiles; a short last group leaves the blocks it
+  // does not fill with stale (finite) values, which no tile of it reads
+  for (int g0 = 0; g0 < tiles; g0 += P->stack) {
+    const int n = std::min(P->stack, tiles - g0);
+    for (int b = 0; b < n; ++b) {
+      const AxisTile& tx = f->tx[(g0 + b) % nx];
+      const AxisTile& ty = f->ty[(g0 + b) / nx];
       PackParams pp;
       std::memset(&pp, 0, sizeof(pp));
       for (int i = 0; i < 3; ++i) {
@@ -1731,9 +1741,9 @@ oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const
       pp.hdr = f->hdr;
       pp.scale = scale;
       pp.fp16 = f->precision == OIDNX_PRECISION_FP16;
-      pp.out = static_cast<uint8_t*>(P->ptr(V_IN)) + static_cast<size_t>(t) * period * in_row;
+      pp.out = static_cast<uint8_t*>(P->ptr(V_IN)) + static_cast<size_t>(b) * period * in_row;
       pp.out_split = P->split_on[0]
-                         ? static_cast<uint8_t*>(P->ptr(V_INS)) + static_cast<size_t>(t) * period * split_row
+                         ? static_cast<uint8_t*>(P->ptr(V_INS)) + static_cast<size_t>(b) * period * split_row
                          : nullptr;
       pp.split_pitch = P->split_on[0] ? P->value_ext[V_INS].pitch : 0;
       pp.chunks = chunks;
@@ -1743,16 +1753,15 @@ oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const
       cudaError_t e = launch_pack(pp, s);
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
       OIDNX_TRY(prof_mark(f, prof, -1, s));
-      ++t;
     }
-  for (const LayerLaunch& L : P->launches) {
-    OIDNX_TRY(run_launch(L, s));
-    OIDNX_TRY(prof_mark(f, prof, L.layer, s));
-  }
-  t = 0;
-  for (const AxisTile& ty : f->ty)
-    for (const AxisTile& tx : f->tx) {
-      LayerLaunch L = P->final_tiles[t++];
+    for (const LayerLaunch& L : P->launches) {
+      OIDNX_TRY(run_launch(L, s));
+      OIDNX_TRY(prof_mark(f, prof, L.layer, s));
+    }
+    for (int b = 0; b < n; ++b) {
+      const AxisTile& tx = f->tx[(g0 + b) % nx];
+      const AxisTile& ty = f->ty[(g0 + b) / nx];
+      LayerLaunch L = P->final_tiles[b];
       L.fcl.outpass = 1;
       L.name = "dec_conv0+output";
       FinalConvParams& fp = L.fcl.p;
@@ -1772,6 +1781,7 @@ oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const
       OIDNX_TRY(run_launch(L, s));
       OIDNX_TRY(prof_mark(f, prof, L.layer, s));
     }
+  }
   P->out_stored = false;
   return ok();
 }
@@ -1870,7 +1880,11 @@ size_t denoise_launches(const oidnx_filter* f) {
   // conv when fused); stacked: per tile the input pass and the final conv,
   // once each of the other convs
   const Plan* P = f->current;
-  if (P && P->stack > 1) return 2 * static_cast<size_t>(P->stack) + P->launches.size();
+  if (P && P->stack > 1) {
+    const size_t tiles = f->tx.size() * f->ty.size();
+    const size_t groups = (tiles + P->stack - 1) / P->stack;
+    return 2 * tiles + groups * P->launches.size();
+  }
   const size_t convs = P ? P->launches.size() : kLayers;
   return f->tx.size() * f->ty.size() * (convs + (output_fused(f, P) ? 1 : 2));
 }
@@ -2112,6 +2126,9 @@ oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value) 
     f->shape_cache = value;
   } else if (n == "fuseOutput") {
     f->fuse_output = value ? 1 : 0;  // the graph is re-recorded on commit
+  } else if (n == "stackTiles") {
+    if (value < 0) return fail(OIDNX_ERR_INVALID_ARGUMENT, "stackTiles must be >= 0");
+    f->stack_tiles = value;
   } else if (n == "keepActivations" || n == "subpixelDecoder" || n == "fuseLayers") {
     (n == "keepActivations" ? f->keep_acts : n == "subpixelDecoder" ? f->subpixel : f->fuse) =
         value ? 1 : 0;
@@ -2145,6 +2162,8 @@ oidnx_status oidnx_filter_get_int(oidnx_filter* f, const char* name, int* value)
   else if (n == "subpixelDecoder") *value = f->subpixel;
   else if (n == "fuseLayers") *value = f->fuse;
   else if (n == "fuseOutput") *value = f->fuse_output;
+  else if (n == "stackTiles") *value = f->stack_tiles;
+  else if (n == "stackedTiles") *value = f->committed && f->current ? f->current->stack : 0;
   else if (n == "profile") *value = f->profile_always;
   else if (n == "inputChannels") *value = f->in_channels;
   else if (n == "precision") *value = f->precision;
@@ -2192,10 +2211,22 @@ oidnx_status oidnx_filter_commit(oidnx_filter* f) {
   // over all tiles.  Not with kept activations (per-tile debug reads), fused
   // layer pairs, or a separate output pass.
   const int tiles = static_cast<int>(f->tx.size() * f->ty.size());
-  const bool stack = tiles > 1 && f->fuse_output && !f->keep_acts && !f->fuse &&
-                     final_foldable(f->layers[kLayers - 1]);
+  int stack = 1;
+  if (tiles > 1 && f->fuse_output && !f->keep_acts && !f->fuse &&
+      final_foldable(f->layers[kLayers - 1])) {
+    // groups of tiles whose stacked arena fits kStackBudget (tiles bound the
+    // memory a frame needs), as even as the group count allows
+    ValueLayout one;
+    layout_values(f, f->tx[0].in_size, f->ty[0].in_size, false, false, &one);
+    const size_t per_tile = std::max<size_t>(one.total, 1);
+    const int fit = f->stack_tiles > 0
+                        ? std::min(f->stack_tiles, tiles)
+                        : static_cast<int>(std::max<size_t>(1, std::min<size_t>(tiles, kStackBudget / per_tile)));
+    const int groups = (tiles + fit - 1) / fit;
+    stack = (tiles + groups - 1) / groups;
+  }
   Plan* P = nullptr;
-  OIDNX_TRY(get_plan(f, f->tx[0].in_size, f->ty[0].in_size, &P, stack ? tiles : 1));
+  OIDNX_TRY(get_plan(f, f->tx[0].in_size, f->ty[0].in_size, &P, stack));
   f->current = P;
   f->committed = true;
   return ok();

@@ -106,6 +106,14 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *                        on GB300 the separate kernels are faster (the MMAs
  *                        of these layers are bound by shared-memory operand
  *                        reads, which fusion does not reduce)
+ *   "stackTiles"         frames of several equal tiles stack them: each conv
+ *                        runs once over a group of tiles (zero rows between
+ *                        them), the input pass and the final conv per tile.
+ *                        0 = groups as large as 16 GiB of activations allow
+ *                        (default), 1 = tile by tile, n = at most n tiles.
+ *                        Off with keepActivations, fuseLayers or fuseOutput 0.
+ *                        get_int "stackedTiles": tiles per group of the
+ *                        committed plan
  *   "fuseOutput"         1 = the output pass runs in the final conv's
  *                        epilogue (the network output is then not stored
  *                        unless "keepActivations" is 1); default 1

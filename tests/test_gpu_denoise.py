@@ -152,6 +152,33 @@ def test_tiled_denoise_matches_oracle_tiled_denoise(precision):
         assert rel_l2(out[..., :3], ref[..., :3]) <= 3e-4   # 1e-4 on the network output x kappa
 
 
+@pytest.mark.parametrize("precision", ["fp16", "fp32"])
+def test_stacked_tile_groups_equal_tile_by_tile(precision):
+    """A 10-tile frame (ragged edges) denoised tile by tile (stackTiles 1), in
+    stacks of at most 4 and 3 tiles (a partial last group each: 4 + 4 + 2 and
+    3 + 3 + 3 + 1) and as one stack (0: the memory budget allows all ten):
+    the same bits, since every conv sees the same zero padding at a tile's
+    edges whether it comes from the image border or the gap rows."""
+    w, h = 300, 120
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True, nan_fraction=0.02)
+    weights = synth.unet_weights(9, bias_scale=0.05)
+    prec = ox.PRECISION_FP16 if precision == "fp16" else ox.PRECISION_FP32
+    outs = []
+    for stack, expect in ((1, 1), (4, 4), (3, 3), (0, 10)):
+        d = Denoiser(weights, prec, imgs, True, input_scale=0.9, max_tile_size=224, overlap=96)
+        try:
+            ox.oidnx_filter_set_int(d.f, "stackTiles", stack)
+            ox.oidnx_filter_commit(d.f)
+            assert ox.oidnx_filter_get_int(d.f, "tiles") == 10
+            assert ox.oidnx_filter_get_int(d.f, "stackedTiles") == expect
+            outs.append(d.run())
+            outs.append(d.run())   # graph replay
+        finally:
+            d.close()
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+
+
 def test_8k_single_tile_with_activations_over_4gib():
     """8192 x 8192 as one tile: dec_conv1a's fp16 output alone is 8 GiB, so
     the 64-bit offsets of every kernel are exercised.  The output image is
