@@ -417,8 +417,8 @@ def run_ours(args):
 # profiles/conv3x3_tc_dec_conv1a_dec_conv1b_1080p_fp16.md and
 # profiles/conv3x3_final_dec_conv0_output_1080p_fp16.md; emptied whenever the
 # kernels change after that capture (traffic reported null).
-TRAFFIC = {"dec_conv1a": 134.096384e6 + 207.474944e6,
-           "dec_conv1b": 267.566080e6 + 96.861952e6}
+TRAFFIC = {"dec_conv1a": 134.141440e6 + 207.531776e6,
+           "dec_conv1b": 267.567872e6 + 97.209600e6}
 
 
 def main():
