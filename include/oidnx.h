@@ -224,7 +224,8 @@ oidnx_status oidnx_profile_next(oidnx_filter* f);
 
 /* JSON of the last profiled execution:
  * {"totalMs":T,"layers":[{"id":"input-pack","ms":..,"flop":..,"bytes":..,
- *  "launches":..,"mmaFlop":..},...,{"id":"output",...}]} summed over tiles;
+ *  "launches":..,"mmaFlop":..},...,{"id":"output",...}]} summed over the
+ * launches (per tile; with stacked tiles each conv launches once per group);
  * flop and bytes are the algorithmic counts (logical channels; each input
  * activation read once, each output written once); mmaFlop is what the
  * tensor cores execute (padded tiles and channels; 4 of the 9 taps on the
