@@ -1706,6 +1706,36 @@ bool output_fused(const oidnx_filter* f, const Plan* P) {
   return P && f->fuse_output && !P->launches.empty() && P->launches.back().final;
 }
 
+// Input-pass parameters of one tile; out / out_split: where its packed
+// input and parity-split copy go (split null when unused).
+PackParams tile_pack_params(const oidnx_filter* f, const Plan* P, void* const img[4],
+                            const size_t stride[4], const AxisTile& tx, const AxisTile& ty,
+                            float scale, void* out, void* out_split) {
+  PackParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  for (int i = 0; i < 3; ++i) {
+    pp.img[i] = static_cast<const float4*>(img[i]);
+    pp.stride[i] = stride[i] / 16;
+  }
+  pp.sources = f->in_channels / 3;
+  pp.width = f->width;
+  pp.height = f->height;
+  pp.tx = tx.in_start;
+  pp.ty = ty.in_start;
+  pp.tw = tx.in_size;
+  pp.th = ty.in_size;
+  pp.hdr = f->hdr;
+  pp.scale = scale;
+  pp.fp16 = f->precision == OIDNX_PRECISION_FP16;
+  pp.out = out;
+  pp.out_split = out_split;
+  pp.split_pitch = out_split ? P->value_ext[V_INS].pitch : 0;
+  pp.chunks = act_chunks(f->precision, f->in_channels);
+  pp.pitch = P->value_ext[V_IN].pitch;
+  pp.log2_tab = static_cast<const float4*>(f->log2_tab);
+  return pp;
+}
+
 // Stacked frame, in groups of up to P->stack tiles: each tile's input pass
 // into its block of the stack (gap rows zeroed), the convs once over the
 // stack, then each tile's final conv with the output pass in its epilogue.
@@ -1724,31 +1754,12 @@ oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const
     for (int b = 0; b < n; ++b) {
       const AxisTile& tx = f->tx[(g0 + b) % nx];
       const AxisTile& ty = f->ty[(g0 + b) / nx];
-      PackParams pp;
-      std::memset(&pp, 0, sizeof(pp));
-      for (int i = 0; i < 3; ++i) {
-        pp.img[i] = static_cast<const float4*>(img[i]);
-        pp.stride[i] = stride[i] / 16;
-      }
-      pp.sources = f->in_channels / 3;
-      pp.width = f->width;
-      pp.height = f->height;
-      pp.tx = tx.in_start;
-      pp.ty = ty.in_start;
-      pp.tw = tx.in_size;
-      pp.th = ty.in_size;
+      PackParams pp = tile_pack_params(
+          f, P, img, stride, tx, ty, scale,
+          static_cast<uint8_t*>(P->ptr(V_IN)) + static_cast<size_t>(b) * period * in_row,
+          P->split_on[0] ? static_cast<uint8_t*>(P->ptr(V_INS)) + static_cast<size_t>(b) * period * split_row
+                         : nullptr);
       pp.gap_rows = kStackGap;
-      pp.hdr = f->hdr;
-      pp.scale = scale;
-      pp.fp16 = f->precision == OIDNX_PRECISION_FP16;
-      pp.out = static_cast<uint8_t*>(P->ptr(V_IN)) + static_cast<size_t>(b) * period * in_row;
-      pp.out_split = P->split_on[0]
-                         ? static_cast<uint8_t*>(P->ptr(V_INS)) + static_cast<size_t>(b) * period * split_row
-                         : nullptr;
-      pp.split_pitch = P->split_on[0] ? P->value_ext[V_INS].pitch : 0;
-      pp.chunks = chunks;
-      pp.pitch = P->value_ext[V_IN].pitch;
-      pp.log2_tab = static_cast<const float4*>(f->log2_tab);
       (void)cudaGetLastError();
       cudaError_t e = launch_pack(pp, s);
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
@@ -1790,34 +1801,13 @@ oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const
 oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t stride[4],
                              bool prof, cudaStream_t s) {
   Plan* P = f->current;
-  const int sources = f->in_channels / 3;
   const float scale = f->input_scale == 0.0f ? 1.0f : f->input_scale;
   OIDNX_TRY(prof_mark(f, prof, -2, s));
   if (P->stack > 1) return enqueue_stacked(f, P, img, stride, scale, prof, s);
   for (const AxisTile& ty : f->ty)
     for (const AxisTile& tx : f->tx) {
-      PackParams pp;
-      std::memset(&pp, 0, sizeof(pp));
-      for (int i = 0; i < 3; ++i) {
-        pp.img[i] = static_cast<const float4*>(img[i]);
-        pp.stride[i] = stride[i] / 16;
-      }
-      pp.sources = sources;
-      pp.width = f->width;
-      pp.height = f->height;
-      pp.tx = tx.in_start;
-      pp.ty = ty.in_start;
-      pp.tw = tx.in_size;
-      pp.th = ty.in_size;
-      pp.hdr = f->hdr;
-      pp.scale = scale;
-      pp.fp16 = f->precision == OIDNX_PRECISION_FP16;
-      pp.out = P->ptr(V_IN);
-      pp.out_split = P->split_on[0] ? P->ptr(V_INS) : nullptr;
-      pp.split_pitch = P->split_on[0] ? P->value_ext[V_INS].pitch : 0;
-      pp.chunks = act_chunks(f->precision, f->in_channels);
-      pp.pitch = P->value_ext[V_IN].pitch;
-      pp.log2_tab = static_cast<const float4*>(f->log2_tab);
+      PackParams pp = tile_pack_params(f, P, img, stride, tx, ty, scale, P->ptr(V_IN),
+                                       P->split_on[0] ? P->ptr(V_INS) : nullptr);
       (void)cudaGetLastError();
       cudaError_t e = launch_pack(pp, s);
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
