@@ -23,8 +23,9 @@ Sources (web pages, cited by title and function/section):
 * "oidn-webgpu 0.0.0-stage -> 0.6.0, src/native/denoise.ts" (input pass,
   output pass, tile grid use).
 
-Where the pages are silent the oracle takes the readings listed in
-DESIGN.md ("Readings of the pages"); each function names the one it uses.
+Where the pages are silent, ambiguous or garbled, the oracle takes a
+stated reading (R1, R2, ...); each function states the reading it uses in
+its own docstring.
 
 Parity status: every function here is pinned by `tests/test_oracle_*.py`
 against library routines (torch CPU float64 conv2d / max_pool2d /
