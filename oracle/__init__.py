@@ -24,8 +24,8 @@ Sources (web pages, cited by title and function/section):
   output pass, tile grid use).
 
 Where the pages are silent, ambiguous or garbled, the oracle takes a
-stated reading (R1, R2, ...); each function states the reading it uses in
-its own docstring.
+reading of them; each function states the reading it uses in its own
+docstring.
 
 Parity status: every function here is pinned by `tests/test_oracle_*.py`
 against library routines (torch CPU float64 conv2d / max_pool2d /
