@@ -412,11 +412,10 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of this workload with the current kernels, see
-# profiles/conv3x3_tc_dec_conv1a_dec_conv1b_1080p_fp16.md and
-# profiles/conv3x3_final_dec_conv0_output_1080p_fp16.md; emptied whenever the
-# kernels change after that capture (traffic reported null).
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# two largest layers, from one ncu capture of this workload with the current
+# kernels (its summary is kept under profiles/); to be emptied whenever these
+# kernels change after that capture (traffic is then reported null).
 TRAFFIC = {"dec_conv1a": 134.141440e6 + 207.531776e6,
            "dec_conv1b": 267.567872e6 + 97.209600e6}
 
