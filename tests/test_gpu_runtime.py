@@ -142,8 +142,9 @@ def test_execute_requires_commit_and_release_is_final(weights):
 
 
 def test_degenerate_dimensions_and_input_scale(weights):
-    """Non-positive image dimensions and a negative or non-finite inputScale
-    are rejected when set, leaving the committed filter as it was; an
+    """Non-positive image dimensions, other out-of-range integer parameters
+    and a negative or non-finite inputScale are rejected when set, leaving
+    the committed filter as it was; an
     inputScale of 0 stands for 1 (the pages' default): an HDR denoise with
     inputScale 0 gives the bits of one with inputScale 1."""
     w, h = 80, 48
@@ -157,7 +158,8 @@ def test_degenerate_dimensions_and_input_scale(weights):
                 with pytest.raises(ox.OidnxError) as e:
                     ox.oidnx_filter_set_float(d.f, "inputScale", bad)
                 assert e.value.status == ox.ERR_INVALID_ARGUMENT
-            for name, value in (("width", 0), ("height", -3)):
+            for name, value in (("width", 0), ("height", -3), ("stackTiles", -1),
+                                ("maxTileSize", -16), ("overlap", 40), ("shapeCacheSize", 0)):
                 with pytest.raises(ox.OidnxError) as e:
                     ox.oidnx_filter_set_int(d.f, name, value)
                 assert e.value.status == ox.ERR_INVALID_ARGUMENT
