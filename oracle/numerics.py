@@ -46,7 +46,10 @@ def hdr_forward_exact(x):
 
 
 def hdr_inverse_exact(y):
-    """F^-1(y) = 2^y - 1 in float64 for float32 inputs y >= 0."""
+    """F^-1(y) = 2^y - 1 in float64 for float32 inputs y >= 0.
+
+    2^y - 1 is taken as written for y >= 1 (2^y >= 2, so the subtraction
+    loses at most one bit); below 1, where it cancels, as expm1(y ln 2)."""
     y = np.asarray(y, dtype=np.float64)
-    with np.errstate(over="ignore"):
-        return np.expm1(y * np.log(2.0))
+    with np.errstate(over="ignore", invalid="ignore"):
+        return np.where(y < 1.0, np.expm1(y * np.log(2.0)), np.exp2(y) - 1.0)
