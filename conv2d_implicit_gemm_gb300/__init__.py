@@ -70,6 +70,7 @@ _sig("oidnx_filter_execute_host_async", _st, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("oidnx_filter_wait_host", _st, _vp)
 _sig("oidnx_network_execute", _st, _vp, _vp, _i, _i, _vp, _vp)
 _sig("oidnx_network_execute_noalloc", _st, _vp, _vp, _i, _i, _vp, _vp)
+_sig("oidnx_output_pass", _st, _vp, _vp, _i, _i, _vp, _sz, _vp, _sz, _i, ctypes.c_float, _vp)
 _sig("oidnx_filter_sync_status", _st, _vp)
 _sig("oidnx_debug_wait_probe", _st, _vp, ctypes.c_uint, _vp)
 _sig("oidnx_profile_next", _st, _vp)
@@ -175,8 +176,16 @@ def oidnx_network_execute(f, packed_in, w, h, out, stream=0):
 
 def oidnx_network_execute_noalloc(f, packed_in, w, h, out, stream=0):
     """Network forward without device allocation (intermediates in the
-    library's fixed 40 MiB device array; see oidnx.h)."""
+    library's fixed 48 MiB device array; limits in oidnx.h)."""
     _check(_lib.oidnx_network_execute_noalloc(f, packed_in, w, h, out, stream))
+
+
+def oidnx_output_pass(f, net, w, h, color, output, hdr, input_scale, stream=0,
+                      color_stride=0, output_stride=0):
+    """The output pass on device buffers (net [h][w] float4, colour and
+    output float4 images)."""
+    _check(_lib.oidnx_output_pass(f, net, w, h, color, color_stride, output, output_stride,
+                                  int(hdr), float(input_scale), stream))
 
 
 def oidnx_filter_sync_status(f):

@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(final_threads<TF>(), 1)
             const int xo = x - p.in_x, yo = y - p.in_y;
             if (xo >= 0 && xo < p.ow && yo >= 0 && yo < p.oh) {
               const size_t oi = static_cast<size_t>(p.oy + yo) * p.out_stride + p.ox + xo;
-              p.out[oi] = output_pixel(n[0], n[1], n[2], col[j], p.hdr, p.scale);
+              p.out[oi] = output_pixel(n[0], n[1], n[2], col[j], p.hdr, p.scale, p.exp2_tab);
             }
           }
         }

@@ -161,6 +161,7 @@ struct FinalConvParams {
   int in_x, in_y, ox, oy, ow, oh;
   int hdr;
   float scale;
+  const float4* exp2_tab;  // HDR: kExp2TabSize entries from fill_exp2_table
 };
 
 struct FinalConvLaunch {
@@ -236,6 +237,11 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 constexpr int kLog2TabSize = 512;
 void fill_log2_table(float (*tab)[4]);
 
+// Table of the output pass's inverse transfer: entry j holds 2^(j/32) and
+// 2^(j/32) - 1, each as a float pair (hi, lo): {Th, Tl, Dh, Dl}.
+constexpr int kExp2TabSize = 32;
+void fill_exp2_table(float (*tab)[4]);
+
 // Output pass of one tile.
 struct UnpackParams {
   const float4* net;       // [th][tw] network output of the tile
@@ -248,6 +254,7 @@ struct UnpackParams {
   int ox, oy, ow, oh;      // output rect in the image
   int hdr;
   float scale;
+  const float4* exp2_tab;  // HDR: kExp2TabSize entries from fill_exp2_table
 };
 cudaError_t launch_unpack(const UnpackParams& p, cudaStream_t stream);
 

@@ -8,11 +8,13 @@
 // Readings of the helpers the page imports without showing them:
 //  * sanitize(v, lo, hi): NaN becomes 0, then clamp by comparison;
 //  * 'log' transfer: F(x) = log2(1 + x), F^-1(y) = 2^y - 1.
-// The input pass stores F correctly rounded to the storage precision (see
-// hdr_forward_f16: float estimate, exact decision near rounding boundaries
+// The input pass stores F correctly rounded to the storage precision
+// (hdr_forward_f16: float estimate, exact decision near rounding boundaries
 // through the inverse, double precision only when that decision is too
 // close to call; hdr_forward_f32: a float-float evaluation of F that decides
 // the fp32 rounding unless it is too close to call, then double precision).
+// The output pass stores F^-1 / inputScale correctly rounded to fp32
+// (hdr_inverse_rn, passes.cuh).
 #include <cfloat>
 #include <cmath>
 
@@ -47,14 +49,6 @@ __device__ __forceinline__ __half hdr_forward_f16(float s) {
   if (s > c * (1.0f + 0x1p-18f)) return hi;
   if (s < c * (1.0f - 0x1p-18f)) return lo;
   return __double2half(log1p(static_cast<double>(s)) / kLn2);
-}
-
-// Error-free transformations on floats (Knuth's two-sum; the product
-// remainder via one fused multiply-add).
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
 __device__ __forceinline__ float pow2_neg(int k) {  // 2^-k, 0 <= k <= 126
@@ -243,7 +237,7 @@ __global__ void unpack_kernel(const UnpackParams p) {
   const float4 net = p.net[static_cast<size_t>(y + p.in_y) * p.tw + x + p.in_x];
   const float4 col = p.color[static_cast<size_t>(y + p.oy) * p.color_stride + x + p.ox];
   p.out[static_cast<size_t>(y + p.oy) * p.out_stride + x + p.ox] =
-      output_pixel(net.x, net.y, net.z, col, p.hdr, p.scale);
+      output_pixel(net.x, net.y, net.z, col, p.hdr, p.scale, p.exp2_tab);
 }
 
 __global__ void split_copy_kernel(const uint4* src, int src_pitch, uint4* dst, int dst_pitch,
@@ -343,7 +337,24 @@ void fill_log2_table(float (*tab)[4]) {
   }
 }
 
+void fill_exp2_table(float (*tab)[4]) {
+  for (int j = 0; j < kExp2TabSize; ++j) {
+    // 2^(j/32) and 2^(j/32) - 1 in double (expm1 keeps the small ones
+    // accurate to their last bit), each split into a float and the float
+    // nearest its remainder
+    const double t = std::exp2(j / static_cast<double>(kExp2TabSize));
+    const double d = std::expm1(j * 0.69314718055994530942 / kExp2TabSize);
+    const float th = static_cast<float>(t);
+    const float dh = static_cast<float>(d);
+    tab[j][0] = th;
+    tab[j][1] = static_cast<float>(t - static_cast<double>(th));
+    tab[j][2] = dh;
+    tab[j][3] = static_cast<float>(d - static_cast<double>(dh));
+  }
+}
+
 cudaError_t launch_unpack(const UnpackParams& p, cudaStream_t stream) {
+  if (p.hdr && !p.exp2_tab) return cudaErrorInvalidValue;
   dim3 grid((p.ow + 127) / 128, p.oh);
   return launch_pdl(unpack_kernel, grid, dim3(128), 0, stream, p);
 }

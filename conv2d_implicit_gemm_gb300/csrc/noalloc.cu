@@ -13,10 +13,15 @@
 // every intermediate activation lives in the array below.
 //
 // The array is a file-scope __device__ variable of kNoAllocScratchBytes
-// (48 MiB).  Every GPU that loads this library holds that much memory until
-// the process exits.  It is enough for fp16 inputs up to 384 x 384 pixels
-// and fp32 inputs up to 256 x 256; larger inputs are rejected with
-// OIDNX_ERR_INVALID_ARGUMENT and a message giving the bytes needed.
+// (48 MiB).  Every GPU that loads this library's device code holds that much
+// memory until the process exits.  The driver places it when it loads this
+// file's device code on a device; CUDA loads device code lazily (at first
+// use) by default, and the first use is the address look-up below, which
+// oidnx_filter_create makes on the device it creates the filter on.  So the
+// array is taken at set-up, not by the first frame.  It is enough for fp16
+// inputs up to 384 x 384 pixels and fp32 inputs up to 256 x 256; larger
+// inputs are rejected with OIDNX_ERR_INVALID_ARGUMENT and a message giving
+// the bytes needed.
 #include <mutex>
 
 #include "../../include/oidnx.h"
@@ -26,6 +31,7 @@ namespace oidnx {
 oidnx_status report_error(oidnx_status status, const char* message);
 oidnx_status network_enqueue_in_arena(oidnx_filter* f, const void* in, int w, int h, void* out,
                                       void* arena, size_t cap, cudaStream_t s);
+oidnx_status noalloc_scratch_address(void** out);
 }  // namespace oidnx
 
 namespace {
@@ -41,10 +47,13 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
+}  // namespace
+
 // Once per device, with that device current: look up the array's device
-// address.  This is the only set-up; it allocates nothing (the array is
-// created when the library's device code is loaded on the device).
-oidnx_status scratch_address(void** out) {
+// address (the driver loads this file's device code, and so places the
+// array, at the first look-up on a device).  oidnx_filter_create calls this
+// for its device; later calls on that device only read the cached address.
+oidnx_status oidnx::noalloc_scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess)
@@ -66,12 +75,10 @@ oidnx_status scratch_address(void** out) {
   return OIDNX_OK;
 }
 
-}  // namespace
-
 extern "C" oidnx_status oidnx_network_execute_noalloc(oidnx_filter* f, const void* packed_in,
                                                       int w, int h, void* out, void* stream) {
   void* scratch = nullptr;
-  oidnx_status st = scratch_address(&scratch);
+  oidnx_status st = oidnx::noalloc_scratch_address(&scratch);
   if (st != OIDNX_OK) return st;
   // Every intermediate activation is fully written before it is read, so
   // the array's contents from an earlier call need no clearing.

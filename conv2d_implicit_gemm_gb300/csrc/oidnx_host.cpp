@@ -11,6 +11,7 @@
 // (recordDenoiseExecution: overlap, tile grid, per-tile input pass ->
 // network -> output pass in order on one queue).
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -19,6 +20,7 @@
 #include <list>
 #include <map>
 #include <memory>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -783,6 +785,7 @@ struct oidnx_filter {
   size_t weight_bytes = 0;
   int* status = nullptr;  // device error word
   void* log2_tab = nullptr;  // fp32 log-transfer table (kLog2TabSize float4)
+  void* exp2_tab = nullptr;  // output pass's inverse-transfer table (kExp2TabSize float4)
   // parameters
   int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
       overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 1,
@@ -920,17 +923,48 @@ int act_chunks(int precision, int c) {
   return precision == OIDNX_PRECISION_FP16 ? round_up(c, 16) / 8 : round_up(c, 4) / 4;
 }
 
-int g_num_sms = 0;
+// Per-device facts and settings.  Kernel attributes (the raised shared-memory
+// limit) belong to the current device's context, so each is set once per
+// device, under a mutex, for up to kMaxDevices devices (beyond that on every
+// call).
+constexpr int kMaxDevices = 64;
+std::mutex g_device_mutex;
+int g_num_sms[kMaxDevices] = {};
+uint64_t g_smem_limit_set[3] = {};  // per kernel family: bit d for device d
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  return dev;
+}
 
 int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        g_num_sms <= 0)
-      g_num_sms = 148;
-  }
-  return g_num_sms;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(g_device_mutex);
+  if (dev < kMaxDevices && g_num_sms[dev] > 0) return g_num_sms[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < kMaxDevices) g_num_sms[dev] = n;
+  return n;
+}
+
+enum KernelFamily { kFamilyTc = 0, kFamilyPair = 1, kFamilyFinal = 2 };
+
+// Raise a kernel family's dynamic shared-memory limit to the 227 KB an SM
+// offers, on the current device.
+oidnx_status ensure_smem_limit(int family) {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(g_device_mutex);
+  const uint64_t bit = dev < kMaxDevices ? (uint64_t(1) << dev) : 0;
+  if (bit && (g_smem_limit_set[family] & bit)) return ok();
+  const size_t max_smem = 227 * 1024;
+  const cudaError_t e = family == kFamilyTc     ? conv_tc_set_smem_limit(max_smem)
+                        : family == kFamilyPair ? conv_pair_set_smem_limit(max_smem)
+                                                : conv_final_set_smem_limit(max_smem);
+  if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
+  g_smem_limit_set[family] |= bit;
+  return ok();
 }
 
 // Build the tensor-core launch of one conv.  src0/src1: device pointers of the
@@ -939,12 +973,7 @@ int num_sms() {
 // that CTAs sharing an SM never wait for tensor memory.
 oidnx_status bound_ctas_per_sm(size_t* smem, uint32_t tmem_cols, int* blocks) {
   const size_t max_smem = 227 * 1024;
-  static size_t limit_set = 0;
-  if (limit_set < max_smem) {
-    cudaError_t e = conv_tc_set_smem_limit(max_smem);
-    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
-    limit_set = max_smem;
-  }
+  OIDNX_TRY(ensure_smem_limit(kFamilyTc));
   const int allowed = static_cast<int>(512 / tmem_cols);
   for (;;) {
     cudaError_t e = conv_tc_occupancy(*smem, blocks);
@@ -1137,12 +1166,7 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
     if (p.S < 2) return fail(OIDNX_ERR_UNSUPPORTED, "conv stage does not fit shared memory");
     smem = fixed + p.S * stage;
   }
-  static size_t limit_set = 0;
-  if (limit_set < max_smem) {
-    cudaError_t e = conv_tc_set_smem_limit(max_smem);
-    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
-    limit_set = max_smem;
-  }
+  OIDNX_TRY(ensure_smem_limit(kFamilyTc));
   // CTAs resident on one SM must share the 512 TMEM columns without waiting:
   // pad the shared-memory request until the occupancy allows no more.
   const int allowed = static_cast<int>(512 / tmem_cols);
@@ -1245,12 +1269,7 @@ oidnx_status build_pair_launch(const DeviceLayer& A, const DeviceLayer& B, int m
     return fail(OIDNX_ERR_UNSUPPORTED, "fused conv does not fit shared memory");
   p.S = static_cast<int>(std::min<size_t>(4, (max_smem - fixed) / (16 + p.stage_bytes)));
   size_t smem = fixed + 16 * static_cast<size_t>(p.S) + static_cast<size_t>(p.S) * p.stage_bytes;
-  static bool limit_set = false;
-  if (!limit_set) {
-    cudaError_t e = conv_pair_set_smem_limit(max_smem);
-    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
-    limit_set = true;
-  }
+  OIDNX_TRY(ensure_smem_limit(kFamilyPair));
   // one CTA per SM: it allocates all 512 TMEM columns
   for (;;) {
     int blocks = 0;
@@ -1300,12 +1319,7 @@ oidnx_status build_final_launch(const DeviceLayer& L, const void* src, Extent ex
   p.S = static_cast<int>(std::min<size_t>(4, (max_smem - fixed) / per_stage));
   if (p.S < 2) return fail(OIDNX_ERR_UNSUPPORTED, "final conv stages do not fit");
   T->smem = fixed + static_cast<size_t>(p.S) * per_stage;
-  static bool limit_set = false;
-  if (!limit_set) {
-    cudaError_t e = conv_final_set_smem_limit(max_smem);
-    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
-    limit_set = true;
-  }
+  OIDNX_TRY(ensure_smem_limit(kFamilyFinal));
   const long tiles = static_cast<long>(p.tiles_x) * p.tiles_y;
   T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, num_sms())), 1, 1);
   return encode_act_map(&T->map, src, ext.w, ext.pitch, ext.h,
@@ -1364,12 +1378,16 @@ double mma_flop(const LayerLaunch& LL) {
 }
 
 // Shapes, liveness and arena placement of the network's values for a w x h
-// input, shared by the plan cache and the allocation-free path.  Values are
-// placed by liveness best-fit ("nativeUNet.ts", _createExecution: a value's
-// slot is free after its last use; each new value takes the smallest free
-// slot that fits, else a new one).  io_external: the network input (rows of
-// w pixels) and output are the caller's buffers and are not placed; keep:
-// no slot reuse.  Fixed-size arrays only: no allocation.
+// input, shared by the plan cache and the allocation-free path.  Memory is
+// reused by liveness, the rule of "nativeUNet.ts" (_createExecution): a
+// value's memory is free again once its last reader has run.  Here every
+// value is an interval in time (from the launch that writes it through its
+// last reader) and in address; values are placed in the order they are
+// written, each at the lowest offset where it overlaps, in address, no
+// placed value that is still live when it is written.  io_external: the
+// network input (rows of w pixels) and output are the caller's buffers and
+// are not placed; keep: nothing is reused.  Fixed-size arrays only: no
+// allocation.
 struct ValueLayout {
   Extent lvl[5];
   Extent ext[V_COUNT];
@@ -1420,28 +1438,31 @@ void layout_values(const oidnx_filter* f, int w, int h, bool io_external, bool k
     V->fused[i] = pair_fusable(f, kPairs[i]);
     if (V->fused[i]) V->stored[kPairs[i].first] = false;
   }
-  struct Slot {
-    size_t cap, off;
-    int active;
-  } slots[V_COUNT];
-  int nslots = 0;
+  struct Placed {
+    size_t lo, hi;  // byte range (1 KB multiples)
+    int until;      // index of the last launch that reads it
+  } placed[V_COUNT];
+  int nplaced = 0;
+  // v is written by launch `index`
   auto place = [&](int v, int index) {
-    if (!keep)
-      for (int i = 0; i < nslots; ++i)
-        if (slots[i].active >= 0 && V->last_use[slots[i].active] < index) slots[i].active = -1;
     const size_t need = act_bytes(f->precision, V->ext[v], V->ch[v], v == V_OUT);
-    int best = -1;
-    for (int i = 0; i < nslots; ++i)
-      if (slots[i].active < 0 && slots[i].cap >= need && (best < 0 || slots[i].cap < slots[best].cap))
-        best = i;
-    if (best < 0) {
-      slots[nslots] = {round_up_sz(need, 1024), V->total, -1};
-      V->total += round_up_sz(need, 1024);
-      best = nslots++;
+    const size_t span = round_up_sz(need, 1024);
+    // lowest offset clear of every value still read at or after `index`: a
+    // candidate that overlaps one moves past its end (no clear offset lies
+    // in between), until none overlaps
+    size_t off = 0;
+    for (bool moved = true; moved;) {
+      moved = false;
+      for (int i = 0; i < nplaced; ++i)
+        if (placed[i].until >= index && placed[i].lo < off + span && off < placed[i].hi) {
+          off = placed[i].hi;
+          moved = true;
+        }
     }
-    slots[best].active = v;
-    V->off[v] = slots[best].off;
+    placed[nplaced++] = {off, off + span, keep ? INT_MAX : V->last_use[v]};
+    V->off[v] = off;
     V->bytes[v] = need;
+    V->total = std::max(V->total, off + span);
   };
   if (!io_external) place(V_IN, -1);
   if (V->split_on[0]) place(V_INS, -1);
@@ -1789,6 +1810,7 @@ oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const
       fp.oh = ty.out_size;
       fp.hdr = f->hdr;
       fp.scale = scale;
+      fp.exp2_tab = static_cast<const float4*>(f->exp2_tab);
       OIDNX_TRY(run_launch(L, s));
       OIDNX_TRY(prof_mark(f, prof, L.layer, s));
     }
@@ -1836,6 +1858,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
         fp.oh = ty.out_size;
         fp.hdr = f->hdr;
         fp.scale = scale;
+        fp.exp2_tab = static_cast<const float4*>(f->exp2_tab);
         OIDNX_TRY(run_launch(L, s));
         OIDNX_TRY(prof_mark(f, prof, L.layer, s));
         continue;
@@ -1858,6 +1881,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
       up.oh = ty.out_size;
       up.hdr = f->hdr;
       up.scale = scale;
+      up.exp2_tab = static_cast<const float4*>(f->exp2_tab);
       e = launch_unpack(up, s);
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "output pass: %s", cudaGetErrorString(e));
       OIDNX_TRY(prof_mark(f, prof, kLayers, s));
@@ -1950,6 +1974,8 @@ oidnx_status execute_images(oidnx_filter* f, void* const img[4], const size_t st
 // network in caller-given scratch (no device allocation)
 // ======================================================================
 namespace oidnx {
+
+oidnx_status noalloc_scratch_address(void** out);
 
 oidnx_status report_error(oidnx_status status, const char* message) {
   return fail(status, "%s", message);
@@ -2062,11 +2088,23 @@ oidnx_status oidnx_filter_create(const void* blob, size_t bytes, int precision,
     fill_log2_table(tab);
     st = upload(tab, sizeof(tab), &f->log2_tab);
   }
+  if (st == OIDNX_OK) {
+    float tab[kExp2TabSize][4];
+    fill_exp2_table(tab);
+    st = upload(tab, sizeof(tab), &f->exp2_tab);
+  }
+  if (st == OIDNX_OK) {
+    // set-up of the allocation-free entry point on this device: the array
+    // it uses is placed here, not by its first call
+    void* scratch = nullptr;
+    st = noalloc_scratch_address(&scratch);
+  }
   if (st != OIDNX_OK) {
     std::string msg = g_last_error;
     for (DeviceLayer& L : f->layers) free_layer(L);
     cudaFree(f->status);
     cudaFree(f->log2_tab);
+    cudaFree(f->exp2_tab);
     g_last_error = msg;
     return st;
   }
@@ -2343,6 +2381,42 @@ oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w
   return ok();
 }
 
+oidnx_status oidnx_output_pass(oidnx_filter* f, const void* net, int w, int h, const void* color,
+                               size_t color_stride, void* output, size_t output_stride, int hdr,
+                               float input_scale, void* stream) {
+  oidnx_status st;
+  if (!filter_alive(f, &st)) return st;
+  if (!net || !color || !output || w <= 0 || h <= 0 || h > 65535)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "output_pass: bad arguments");
+  if (hdr != 0 && hdr != 1) return fail(OIDNX_ERR_INVALID_ARGUMENT, "output_pass: hdr must be 0 or 1");
+  if (!std::isfinite(input_scale) || input_scale < 0.0f)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "output_pass: inputScale must be finite and >= 0");
+  if ((reinterpret_cast<uintptr_t>(net) | reinterpret_cast<uintptr_t>(color) |
+       reinterpret_cast<uintptr_t>(output)) % 16 || color_stride % 16 || output_stride % 16)
+    return fail(OIDNX_ERR_INVALID_ARGUMENT,
+                "output_pass: pointers and row strides must be 16-byte aligned");
+  const size_t row = static_cast<size_t>(w) * 16;
+  if ((color_stride && color_stride < row) || (output_stride && output_stride < row))
+    return fail(OIDNX_ERR_INVALID_ARGUMENT, "output_pass: row stride below width*16");
+  UnpackParams up;
+  std::memset(&up, 0, sizeof(up));
+  up.net = static_cast<const float4*>(net);
+  up.tw = w;
+  up.color = static_cast<const float4*>(color);
+  up.color_stride = (color_stride ? color_stride : row) / 16;
+  up.out = static_cast<float4*>(output);
+  up.out_stride = (output_stride ? output_stride : row) / 16;
+  up.ow = w;
+  up.oh = h;
+  up.hdr = hdr;
+  up.scale = input_scale == 0.0f ? 1.0f : input_scale;
+  up.exp2_tab = static_cast<const float4*>(f->exp2_tab);
+  (void)cudaGetLastError();
+  cudaError_t e = launch_unpack(up, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "output pass: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 oidnx_status oidnx_filter_sync_status(oidnx_filter* f) {
   oidnx_status st;
   if (!filter_alive(f, &st)) return st;
@@ -2529,6 +2603,7 @@ void oidnx_filter_release(oidnx_filter* f) {
   if (f->capture_stream) cudaStreamDestroy(f->capture_stream);
   cudaFree(f->status);
   cudaFree(f->log2_tab);
+  cudaFree(f->exp2_tab);
   delete f;
 }
 

@@ -129,15 +129,22 @@ oidnx_status oidnx_filter_get_int(oidnx_filter* f, const char* name, int* value)
 oidnx_status oidnx_filter_set_float(oidnx_filter* f, const char* name, float value);
 
 /* Validate the parameters and images, plan the tile grid, create (or fetch
- * from the LRU cache) the per-tile-shape network plan.  Synchronous on the
+ * from the LRU cache) the per-tile-shape network plan: the set-up half of
+ * "denoise.ts", recordDenoiseExecution (its dimension checks, the overlap
+ * alignUp(receptiveField / 2, 16) and the planTileGrid call), with the plan
+ * lookup of "nativeUNet.ts", _execution / _createExecution, made ahead of
+ * the first run as NativeUNetExecutor.prewarm does.  Synchronous on the
  * host; allocates device memory.  Errors: INVALID_ARGUMENT, UNSUPPORTED,
  * OUT_OF_MEMORY, CUDA.  */
 oidnx_status oidnx_filter_commit(oidnx_filter* f);
 
 /* Run the denoise on `stream`: for every tile, in order, the input pass,
- * the network and the output pass into the tile's output rectangle.
- * Asynchronous; the first run of a configuration records a CUDA graph that
- * later runs replay.  Errors: NOT_COMMITTED, RELEASED, CUDA.  */
+ * the network and the output pass into the tile's output rectangle (the
+ * per-tile loop of "denoise.ts", recordDenoiseExecution: inputShader,
+ * executePacked, outputShader on one queue).  Asynchronous; the first run of
+ * a configuration records a CUDA graph that later runs replay, as
+ * "program.ts", recordNetwork records the second execution of a network.
+ * Errors: NOT_COMMITTED, RELEASED, CUDA.  */
 oidnx_status oidnx_filter_execute(oidnx_filter* f, void* stream);
 
 /* Same denoise with HOST images (float4 RGBA, width*16 bytes per row):
@@ -192,8 +199,12 @@ oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w
  *     INVALID_ARGUMENT and a message stating the bytes needed.
  *   - packed_in / out: as for oidnx_network_execute (the kernels read the
  *     input and write the output in place, without copies).
- *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *   - Set-up: oidnx_filter_create looks up the array's device address on
+ *     the device current at creation; that look-up is when the driver loads
+ *     the array (device code loads lazily by default), so its memory is
+ *     taken at set-up and calls on that device allocate nothing.  The first
+ *     call on any other device makes the look-up itself: make it before any
+ *     stream capture and off the frame path.
  *   - All calls on a device share the one array, and it keeps the previous
  *     call's contents (every activation is fully written before it is
  *     read, so nothing is cleared).  Calls that overlap on the GPU (on
@@ -204,9 +215,28 @@ oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w
 oidnx_status oidnx_network_execute_noalloc(oidnx_filter* f, const void* packed_in, int w,
                                            int h, void* out, void* stream);
 
+/* The output pass alone on one rectangle ("denoise.ts", outputShader): for
+ * every pixel, rgb = sanitize(net.rgb, 0, hdr ? FLT_MAX : 1); with hdr,
+ * rgb = (2^rgb - 1) / inputScale (the inverse 'log' transfer), correctly
+ * rounded to fp32; alpha = the colour's alpha, copied bit for bit.
+ *   net:    device, [h][w] float4 (the network output; lane 3 ignored);
+ *   color:  device, float4 RGBA rows of color_stride bytes (0: w*16);
+ *   output: device, float4 RGBA rows of output_stride bytes (0: w*16);
+ *   hdr 0 or 1; input_scale finite and >= 0 (0 means 1; used with hdr).
+ * w > 0, 0 < h <= 65535; pointers and strides 16-byte aligned.  The caller
+ * owns every buffer; enqueued on `stream`.  The denoise runs the same
+ * per-pixel code for each tile, inside the final conv's epilogue.
+ * Errors: INVALID_ARGUMENT, RELEASED, CUDA.  */
+oidnx_status oidnx_output_pass(oidnx_filter* f, const void* net, int w, int h, const void* color,
+                               size_t color_stride, void* output, size_t output_stride, int hdr,
+                               float input_scale, void* stream);
+
 /* Wait for the filter's work, then report and clear the device error word:
  * OK, or TIMEOUT if a kernel's bounded wait gave up (its output is then
- * undefined).  Errors: CUDA.  */
+ * undefined).  The device-side counterpart of the error packets of
+ * "program.ts" (an "ERRO" packet carries the failure of a recorded run);
+ * the pages have no device error word, since WebGPU reports failed work
+ * through its own error scopes.  Errors: CUDA.  */
 oidnx_status oidnx_filter_sync_status(oidnx_filter* f);
 
 /* Failure-detection probe: launch, on `stream`, one thread that waits on a
@@ -219,10 +249,13 @@ oidnx_status oidnx_filter_sync_status(oidnx_filter* f);
 oidnx_status oidnx_debug_wait_probe(oidnx_filter* f, unsigned int limit_us, void* stream);
 
 /* Per-kernel timing of the next execute (or network_execute) only, like
- * "nativeUNet.ts" profileNextExecution.  */
+ * "nativeUNet.ts" profileNextExecution (timestamp writes around every pass
+ * of the next execution only).  */
 oidnx_status oidnx_profile_next(oidnx_filter* f);
 
-/* JSON of the last profiled execution:
+/* JSON of the last profiled execution, the record of "nativeUNet.ts",
+ * getLastExecutionProfile ({totalMs, layers[{id, durationMs}]} with the ids
+ * "input-pack" and the node names), extended with counts:
  * {"totalMs":T,"layers":[{"id":"input-pack","ms":..,"flop":..,"bytes":..,
  *  "launches":..,"mmaFlop":..},...,{"id":"output",...}]} summed over the
  * launches (per tile; with stacked tiles each conv launches once per group);
@@ -240,7 +273,10 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap);
 oidnx_status oidnx_get_resource_info(oidnx_filter* f, char* json, size_t cap);
 
 /* Copy one stored activation of the last network run on this filter to
- * host memory as float32 [h_l][w_l][C_l] with logical channels.
+ * host memory as float32 [h_l][w_l][C_l] with logical channels: the value
+ * buffers of the plan built by "nativeUNet.ts", _createExecution (one per
+ * node output, the packed input at index -1), read back the way executeCPU
+ * reads the network output.  This is what the per-layer parity checks read.
  * layer: 0 = packed network input, 1..16 = outputs of enc_conv0 ..
  * dec_conv0 in network order (enc_conv1..enc_conv4 store their pooled
  * outputs).  Valid for every layer only with "keepActivations" = 1 and
@@ -257,7 +293,11 @@ oidnx_status oidnx_debug_read_activation(oidnx_filter* f, int layer, void* host_
 const char* oidnx_last_error(void);
 
 /* Release a filter and everything it owns, after the work it queued has
- * finished.  NULL is ignored.  Further calls on the handle are invalid.  */
+ * finished: "nativeUNet.ts", dispose (idempotent, destroys every tracked
+ * buffer), with the deferred destruction of _execution's evicted plans,
+ * which waits for onSubmittedWorkDone before destroying buffers that
+ * commands in flight may still use.  NULL is ignored.  Calls on the handle
+ * afterwards are invalid.  */
 void oidnx_filter_release(oidnx_filter* f);
 
 /* ---- one conv layer (3x3 same-padded conv + bias (+ReLU)) --------------

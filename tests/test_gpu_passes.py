@@ -9,7 +9,8 @@ pytestmark = pytest.mark.gpu
 
 import synth
 from oracle import passes, tiles
-from tests._gpu import Denoiser, ulp_diff_f32
+from oracle.numerics import hdr_inverse_exact
+from tests._gpu import Denoiser, empty_dev, stream, to_dev, to_host
 
 import conv2d_implicit_gemm_gb300 as ox
 
@@ -99,12 +100,9 @@ def test_pack_and_unpack_match_oracle(precision, sources, hdr):
         d.close()
     ref_out = passes.unpack_rect(net[:h, :w], imgs[0], hdr, scale)
     assert np.array_equal(out[..., 3].view(np.uint32), imgs[0][..., 3].view(np.uint32))
-    if hdr:
-        fin = np.isfinite(ref_out[..., :3])
-        assert np.array_equal(np.isfinite(out[..., :3]), fin)
-        assert ulp_diff_f32(out[..., :3][fin], ref_out[..., :3][fin]).max() <= 8
-    else:
-        assert np.array_equal(out.view(np.uint32), ref_out.view(np.uint32))
+    # HDR: (2^d - 1) / inputScale correctly rounded, as the oracle's single
+    # rounding of its float64 value; LDR and alpha: copies and clamps
+    assert np.array_equal(out.view(np.uint32), ref_out.view(np.uint32))
 
 
 def test_pack_hdr_transfer_is_correctly_rounded_everywhere():
@@ -124,3 +122,78 @@ def test_pack_hdr_transfer_is_correctly_rounded_everywhere():
     ref = passes.pack_tile(imgs, (0, 0, w, h), True, 1.0, "fp16")
     assert np.array_equal(packed[..., :3].view(np.uint32),
                           ref[..., :3].astype(np.float32).view(np.uint32))
+
+
+def _near_inverse_midpoints(n, scale, lo_rel, hi_rel, seed):
+    """Network outputs d whose (2^d - 1) / scale lies between lo_rel and
+    hi_rel (relative) from a rounding boundary between two fp32 values: the
+    inputs a pair evaluation must hand to its exact fallback.  lo_rel keeps
+    them far enough from the boundary that the oracle's float64 value
+    (within 2^-50) decides them."""
+    rng = np.random.default_rng(seed)
+    d = np.concatenate([2.0 ** rng.uniform(-60, 6.97, n), rng.uniform(0, 8, n)]).astype(np.float32)
+    with np.errstate(over="ignore"):
+        f = hdr_inverse_exact(d) / np.float64(scale)
+        y = f.astype(np.float32)
+    ok = np.isfinite(y) & (y > 0)
+    d, f, y = d[ok], f[ok], y[ok]
+    other = np.nextafter(y, np.where(f > y, np.float32(np.inf), np.float32(0)))
+    dist = np.abs(f - (y.astype(np.float64) + other.astype(np.float64)) / 2) / f
+    return d[(dist < hi_rel) & (dist > lo_rel)]
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.75, 3.0, 2.0 ** -20, 1e-30, 1e30, 0.0])
+def test_output_pass_hdr_is_correctly_rounded(scale):
+    """Output pass alone on a dense sweep of network outputs: every HDR value
+    must be the correctly rounded fp32 of (2^d - 1) / inputScale (the oracle's
+    float64 value rounded once), alpha copied bit for bit; specials (NaN,
+    +-Inf, negatives, -0, subnormals, FLT_MAX) sanitized first."""
+    f32max = np.finfo(np.float32).max
+    specials = np.array([np.nan, np.inf, -np.inf, -1.0, -0.0, 0.0, 2.0 ** -149, 2.0 ** -126,
+                         2.0 ** -61, 2.0 ** -60, 2.0 ** -9, 1.0 / 512, 0.5, 1.0, 2.0, 125.99,
+                         126.0, 127.0, 127.9999, 128.0, 150.0, 1023.0, 1025.0, f32max], np.float32)
+    eff = 1.0 if scale == 0.0 else scale
+    hard = _near_inverse_midpoints(1 << 20, np.float32(eff), 2.0 ** -46, 2.0 ** -36, 11)
+    assert hard.size > 50
+    rng = np.random.default_rng(5)
+    vals = np.concatenate([specials,
+                           np.logspace(-45, 2.2, 60000).astype(np.float32),
+                           rng.uniform(0, 1, 30000).astype(np.float32),
+                           rng.uniform(0, 20, 30000).astype(np.float32), hard])
+    w = 256
+    h = -(-vals.size // w)
+    net = np.zeros((h, w, 4), np.float32)
+    net.reshape(-1, 4)[:, 0] = np.resize(vals, h * w)
+    net.reshape(-1, 4)[:, 1] = np.resize(vals[::-1], h * w)
+    net.reshape(-1, 4)[:, 2] = np.resize(np.roll(vals, 7), h * w)
+    color = synth.hdr_color(w, h)
+    f = ox.oidnx_filter_create(ox.write_weight_blob(synth.unet_weights(9)), ox.PRECISION_FP16)
+    try:
+        d_net, d_col, d_out = to_dev(net), to_dev(color), empty_dev(w * h * 16)
+        for hdr in (1, 0):
+            d_out.fill_(0xFF)
+            ox.oidnx_output_pass(f, d_net.data_ptr(), w, h, d_col.data_ptr(), d_out.data_ptr(),
+                                 hdr, scale, stream())
+            ox.oidnx_filter_sync_status(f)
+            got = to_host(d_out, np.float32, (h, w, 4))
+            ref = passes.unpack_rect(net, color, bool(hdr), scale)
+            bad = np.flatnonzero(got.view(np.uint32) != ref.view(np.uint32))
+            assert bad.size == 0, (hdr, bad.size, net.reshape(-1)[bad[:4]], got.reshape(-1)[bad[:4]],
+                                   ref.reshape(-1)[bad[:4]])
+    finally:
+        ox.oidnx_filter_release(f)
+
+
+def test_output_pass_rejects_bad_arguments():
+    f = ox.oidnx_filter_create(ox.write_weight_blob(synth.unet_weights(9)), ox.PRECISION_FP16)
+    try:
+        buf = empty_dev(4096)
+        p = buf.data_ptr()
+        for args in [(0, 4, 0, 1, 1.0), (4, 4, 0, 2, 1.0), (4, 4, 0, 1, -1.0), (4, 4, 0, 1, float("nan")),
+                     (4, 4, 32, 1, 1.0), (4, 70000, 0, 1, 1.0)]:
+            w, h, stride, hdr, scale = args
+            with pytest.raises(ox.OidnxError) as e:
+                ox.oidnx_output_pass(f, p, w, h, p, p, hdr, scale, stream(), color_stride=stride)
+            assert e.value.status == ox.ERR_INVALID_ARGUMENT
+    finally:
+        ox.oidnx_filter_release(f)
