@@ -45,6 +45,75 @@ def _isolated(k, acts, weights, precision):
     return y
 
 
+def _fp16_code_diff(a, b):
+    ai = np.asarray(a).astype(np.float16).view(np.int16).astype(np.int32)
+    bi = np.asarray(b).astype(np.float16).view(np.int16).astype(np.int32)
+    return np.abs(ai - bi)
+
+
+def _magnitude(k, acts, weights, channels=None):
+    """|W| * |x| + |b| of layer k on the GPU's own inputs (the sum of the
+    absolute values of every term of each output), optionally over the
+    first `channels` input channels only (bias then left out); pooled like
+    the layer's output."""
+    s0, s1, op = LAYER_OPS[k]
+    w, b = weights[ox.LAYER_NAMES[k - 1]]
+    x = np.abs(acts[s0].astype(np.float64))
+    if op == "dec":
+        x = layers.decoder_input(x, np.abs(acts[s1].astype(np.float64)))
+    aw = np.abs(np.asarray(w, np.float64))
+    bias = np.abs(np.asarray(b, np.float64))
+    if channels is not None:
+        x, aw, bias = x[..., :channels], aw[:, :channels], np.zeros_like(bias)
+    m = layers.conv3x3(x, aw, bias, relu=False)
+    return layers.maxpool2x2(m) if op == "pool" else m
+
+
+def _subpixel_layer(k, acts, subpixel):
+    """Whether the GPU ran decoder layer k in sub-pixel form (even conv
+    extent, exactly twice the upsampled source's)."""
+    s0, _, op = LAYER_OPS[k]
+    if op != "dec" or not subpixel:
+        return False
+    h, w = acts[k].shape[:2]
+    h0, w0 = acts[s0].shape[:2]
+    return h % 2 == 0 and w % 2 == 0 and 2 * h0 == h and 2 * w0 == w
+
+
+def assert_layer_elementwise(k, got, ref, acts, weights, precision, subpixel):
+    """Every value of layer k against the oracle's layer on the GPU's inputs:
+      fp16 layers: within one fp16 step, or within 1e-4 absolute where the
+        sum cancels below the fp32 accumulation's rounding; a sub-pixel
+        decoder may add 2^-11 (|W_up| * |up(x)|) and one more fp16 step: it
+        sums the fp16 weights of the taps that read one low-resolution pixel
+        and rounds the sum to fp16 once more (relative error <= 2^-11 per
+        summed weight), before both sides round the result to fp16;
+      the fp16 network's final layer (fp32 output): within 2^-14 (|W| * |x| +
+        |b|), the fp32 accumulation of at most ~100 partial sums;
+      fp32 layers (3xTF32 products): within 2^-13 (|W| * |x| + |b|): each
+        product within 3 * 2^-22 (the dropped lo * lo term and the tf32
+        rounding of both lo parts), plus at most ~540 fp32 accumulation steps
+        of 2^-24 each."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    diff = np.abs(got - ref)
+    final = LAYER_OPS[k][2] == "final"
+    if precision == "fp16" and not final:
+        tol = 1e-4
+        if _subpixel_layer(k, acts, subpixel):
+            # the re-rounding bound, plus both sides' fp16 storage rounding
+            # (half an fp16 step each at the larger magnitude)
+            c0 = acts[LAYER_OPS[k][0]].shape[-1]
+            step = np.spacing(np.maximum(np.abs(got), np.abs(ref)).astype(np.float16)).astype(np.float64)
+            tol = tol + 2.0 ** -11 * _magnitude(k, acts, weights, channels=c0) + step
+        close = (_fp16_code_diff(got, ref) <= 1) | (diff <= tol)
+    else:
+        bound = 2.0 ** (-14 if precision == "fp16" else -13) * _magnitude(k, acts, weights)
+        close = diff <= bound + np.abs(ref) * 2.0 ** -23
+    assert close.all(), (VALUE_NAMES[k], int((~close).sum()), float(diff[~close].max()),
+                         np.argwhere(~close)[:3].tolist())
+
+
 def _run_network(weights, packed_logical, precision, subpixel=0, fuse=0):
     # fuse=1: the fused pairs' intermediate maps (activations 1 and 15) are
     # never stored and come back as None
@@ -68,7 +137,7 @@ def _run_network(weights, packed_logical, precision, subpixel=0, fuse=0):
 
 
 @pytest.mark.parametrize("precision,subpixel", [("fp16", 0), ("fp16", 1), ("fp32", 0), ("fp32", 1)])
-@pytest.mark.parametrize("w,h", [(64, 48), (80, 34), (130, 20), (512, 64)])
+@pytest.mark.parametrize("w,h", [(64, 48), (80, 34), (130, 20), (512, 64), (1, 1), (33, 17)])
 def test_network_layers_match_oracle(precision, subpixel, w, h):
     weights = synth.unet_weights(9, bias_scale=0.05)
     x = synth.uniform_activations(h, w, 9, seed=w + h, low=0.0, high=1.0)
@@ -85,6 +154,7 @@ def test_network_layers_match_oracle(precision, subpixel, w, h):
         iso = _isolated(k, acts, weights, precision)
         err = rel_l2(acts[k], iso)
         assert err <= tol, (VALUE_NAMES[k], err)
+        assert_layer_elementwise(k, acts[k], iso, acts, weights, precision, subpixel)
     # chained end to end
     out = ref["dec_conv0"]
     assert np.array_equal(final[..., :3], acts[16].astype(np.float32))
@@ -122,8 +192,10 @@ def test_colour_only_and_colour_albedo_models_match_oracle(precision, subpixel, 
         acts.append(acts_flat[k].reshape(shape))
     tol = 1e-2 if precision == "fp16" else 1e-4
     for k in range(1, 17):
-        err = rel_l2(acts[k], _isolated(k, acts, weights, precision))
+        iso = _isolated(k, acts, weights, precision)
+        err = rel_l2(acts[k], iso)
         assert err <= tol, (VALUE_NAMES[k], err)
+        assert_layer_elementwise(k, acts[k], iso, acts, weights, precision, subpixel)
     out = ref["dec_conv0"]
     if precision == "fp16":
         assert np.abs(final[..., :3] - out).max() <= 2e-2
