@@ -5,7 +5,8 @@ the library's fixed device array instead of a filter-allocated arena.
 
 Checked against oidnx_network_execute on two calls in a row with different
 shapes and data, so that contents left in the shared array by the first call
-cannot leak into the second.  This file is collected last on purpose."""
+cannot leak into the second, and checked to leave the device's free memory
+unchanged once set up.  This file is collected last on purpose."""
 
 import numpy as np
 import pytest
@@ -79,5 +80,36 @@ def test_noalloc_accepts_the_documented_maximum(precision, side):
         ox.oidnx_network_execute_noalloc(f, src.data_ptr(), side, side, got.data_ptr(), stream())
         ox.oidnx_filter_sync_status(f)
         assert np.isfinite(to_host(got, np.float32, (side, side, 4))).all()
+    finally:
+        ox.oidnx_filter_release(f)
+
+
+def test_noalloc_allocates_nothing_after_set_up():
+    """After one warm-up call (which also loads the kernels it launches),
+    further calls must not change the device's free memory, the filter's own
+    arena bytes or torch's allocator counters: the call's only memory is
+    the library's fixed array, placed when the filter was created."""
+    f = ox.oidnx_filter_create(ox.write_weight_blob(synth.unet_weights(9, bias_scale=0.05)),
+                               ox.PRECISION_FP16)
+    try:
+        w, h = 256, 160
+        src = _packed(w, h, 4, "fp16")
+        out = empty_dev(w * h * 16)
+        ox.oidnx_network_execute_noalloc(f, src.data_ptr(), w, h, out.data_ptr(), stream())
+        ox.oidnx_filter_sync_status(f)
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        arena0 = ox.oidnx_get_resource_info(f)
+        alloc0 = torch.cuda.memory_allocated()
+        reserved0 = torch.cuda.memory_reserved()
+        for _ in range(5):
+            ox.oidnx_network_execute_noalloc(f, src.data_ptr(), w, h, out.data_ptr(), stream())
+        ox.oidnx_filter_sync_status(f)
+        torch.cuda.synchronize()
+        free1, _ = torch.cuda.mem_get_info()
+        assert free1 == free0
+        assert ox.oidnx_get_resource_info(f) == arena0
+        assert torch.cuda.memory_allocated() == alloc0
+        assert torch.cuda.memory_reserved() == reserved0
     finally:
         ox.oidnx_filter_release(f)
