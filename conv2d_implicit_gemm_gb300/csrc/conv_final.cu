@@ -39,6 +39,7 @@ constexpr int kNc = 16;             // accumulator columns per output row (12 us
 constexpr int kR = kFinalRows;
 
 __device__ __forceinline__ void final_tile(const FinalConvParams& p, int tile, int* x0, int* y0) {
+  if (p.reverse) tile = p.tiles_x * p.tiles_y - 1 - tile;
   const int ty = tile / p.tiles_x;
   *x0 = (tile - ty * p.tiles_x) * kFinalSpan;
   *y0 = ty * kR;

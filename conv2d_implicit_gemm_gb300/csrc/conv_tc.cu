@@ -62,7 +62,17 @@ template <int KIND> __host__ __device__ constexpr bool kind_helpers() { return k
 
 namespace {
 
+// Tile index in walking order -> tile index in the image: last to first
+// when p.reverse is set.  A layer that walks its tiles in the opposite
+// order to the layer that wrote its input starts on the rows written last,
+// which are still in L2.  (Sub-pixel tiles alternate column parity and
+// their count is even, so reversing flips every CTA's parity.)
+__device__ __forceinline__ int tile_at(const TcConvParams& p, int tile) {
+  return p.reverse ? p.tiles_x * p.tiles_y - 1 - tile : tile;
+}
+
 __device__ __forceinline__ void tile_origin(const TcConvParams& p, int tile, int* x0, int* y0) {
+  tile = tile_at(p, tile);
   const int ty = tile / p.tiles_x;
   *x0 = (tile - ty * p.tiles_x) * kTileM;
   *y0 = ty * p.R;
@@ -73,6 +83,7 @@ __device__ __forceinline__ void tile_origin(const TcConvParams& p, int tile, int
 template <int KIND>
 __device__ __forceinline__ void tile_origin_k(const TcConvParams& p, int tile, int* x0, int* y0,
                                               int* px) {
+  tile = tile_at(p, tile);
   const int ty = tile / p.tiles_x;
   const int tx = tile - ty * p.tiles_x;
   *y0 = ty * p.R;
@@ -339,11 +350,12 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
       if (p.resident) {
         if (SP) {
           // This CTA's tiles all have column parity blockIdx.x & 1 (even
-          // grid): only that parity's half of each upsampled block stays
-          // resident, followed by the skip blocks.
+          // grid; flipped when the tiles are walked in reverse): only that
+          // parity's half of each upsampled block stays resident, followed
+          // by the skip blocks.
           const uint8_t* w = reinterpret_cast<const uint8_t*>(p.weights);
           const uint32_t half = p.b_tx / 2;
-          const uint32_t cpx = blockIdx.x & 1u;
+          const uint32_t cpx = (blockIdx.x ^ static_cast<uint32_t>(p.reverse)) & 1u;
           mbar_arrive_expect_tx(wbar, p.wres_bytes);
           for (int kb = 0; kb < KB0; ++kb)
             bulk_load(Wres + static_cast<size_t>(kb) * half,

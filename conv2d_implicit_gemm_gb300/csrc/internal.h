@@ -74,6 +74,7 @@ struct TcConvParams {
                            // (Cout rounded up to 4; may be fewer than N / 4)
   int xs0, xs1;            // log2 pixels per x unit of map0 / map1: 3 for
                            // 128-byte rows (pitch % 8 == 0), 0 for 16-byte rows
+  int reverse;             // walk the tiles last to first (see tile_at)
 };
 
 enum TcKind : int {
@@ -162,6 +163,7 @@ struct FinalConvParams {
   int hdr;
   float scale;
   const float4* exp2_tab;  // HDR: kExp2TabSize entries from fill_exp2_table
+  int reverse;             // walk the tiles last to first
 };
 
 struct FinalConvLaunch {
@@ -227,6 +229,7 @@ struct PackParams {
   const float4* log2_tab;  // fp32 HDR: kLog2TabSize entries from fill_log2_table
   int gap_rows;            // stacked tiles: rows th .. th + gap_rows - 1 of out and
                            // out_split are written as zeros
+  int reverse;             // row blocks in reverse order
 };
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 

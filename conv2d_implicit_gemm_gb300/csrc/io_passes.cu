@@ -125,7 +125,7 @@ __global__ void pack_kernel(const PackParams p) {
   griddep_wait();
   griddep_launch_dependents();
   const int tx = blockIdx.x * blockDim.x + threadIdx.x;
-  const int ty = blockIdx.y;
+  const int ty = p.reverse ? gridDim.y - 1 - blockIdx.y : blockIdx.y;
   if (tx >= (p.out_split && p.split_pitch > p.pitch ? p.split_pitch : p.pitch)) return;
   const size_t pixel = static_cast<size_t>(ty) * p.chunks * p.pitch + tx;
   if (tx >= p.tw || ty >= p.th) {

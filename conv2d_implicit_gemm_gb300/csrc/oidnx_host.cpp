@@ -1482,6 +1482,11 @@ void layout_values(const oidnx_filter* f, int w, int h, bool io_external, bool k
 // stack_rows: tile rows of a stacked layout (0: one image): every conv
 // gets its level's gap period, the final conv is left to the caller (one
 // launch per tile), and FLOPs and bytes count the tiles' rows only.
+// Launch k of a network pass (k = layer index + 1; the input pass is 0)
+// walks its tiles in reverse when k is odd: each layer then starts on the
+// rows its input's producer wrote last, which are still in L2.
+int walk_reverse(int layer) { return (layer + 1) & 1; }
+
 template <class Ptr, class Emit>
 oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V, Ptr ptr, Emit emit,
                                     int stack_rows = 0) {
@@ -1531,6 +1536,7 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
       LL.final = 1;
       OIDNX_TRY(build_final_launch(L, ptr(d.src0), V.ext[d.src0], conv.w, conv.h, ptr(d.dst),
                                    f->status, &LL.fcl));
+      LL.fcl.p.reverse = walk_reverse(l);
       LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
       LL.bytes = logical_bytes(d.src0) + static_cast<double>(V.ext[d.dst].w) * V.ext[d.dst].h * 16 +
                  static_cast<double>(L.weight_bytes);
@@ -1561,6 +1567,7 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
       LL.tcl.p.period = (stack_rows + kStackGap) >> d.level;
       LL.tcl.p.rows = stack_rows >> d.level;
     }
+    LL.tcl.p.reverse = walk_reverse(l);
     LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
     const Extent oe = V.ext[d.dst];
     const double out_bytes = (d.kind == kFinal ? static_cast<double>(oe.w) * oe.h * 16
@@ -1631,6 +1638,7 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, int stack, std::unique_p
       const uint8_t* src = static_cast<const uint8_t*>(plan->ptr(d.src0)) +
                            static_cast<size_t>(t) * (h + kStackGap) * row_bytes;
       OIDNX_TRY(build_final_launch(L, src, Extent{w, h, se.pitch}, w, h, nullptr, f->status, &LL.fcl));
+      LL.fcl.p.reverse = walk_reverse(l);
       LL.flop = 2.0 * 9.0 * L.cin * L.cout * w * h;
       LL.bytes = static_cast<double>(w) * h * (V.ch[d.src0] * (f->precision == OIDNX_PRECISION_FP16 ? 2 : 4) + 16) +
                  static_cast<double>(L.weight_bytes);

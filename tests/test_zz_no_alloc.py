@@ -8,6 +8,8 @@ shapes and data, so that contents left in the shared array by the first call
 cannot leak into the second, and checked to leave the device's free memory
 unchanged once set up.  This file is collected last on purpose."""
 
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -97,6 +99,9 @@ def test_noalloc_allocates_nothing_after_set_up():
         out = empty_dev(w * h * 16)
         ox.oidnx_network_execute_noalloc(f, src.data_ptr(), w, h, out.data_ptr(), stream())
         ox.oidnx_filter_sync_status(f)
+        # tensors left by earlier tests are collected now, not during the
+        # loop (torch's counters may still only go down, never up)
+        gc.collect()
         torch.cuda.synchronize()
         free0, _ = torch.cuda.mem_get_info()
         arena0 = ox.oidnx_get_resource_info(f)
@@ -109,7 +114,7 @@ def test_noalloc_allocates_nothing_after_set_up():
         free1, _ = torch.cuda.mem_get_info()
         assert free1 == free0
         assert ox.oidnx_get_resource_info(f) == arena0
-        assert torch.cuda.memory_allocated() == alloc0
-        assert torch.cuda.memory_reserved() == reserved0
+        assert torch.cuda.memory_allocated() <= alloc0
+        assert torch.cuda.memory_reserved() <= reserved0
     finally:
         ox.oidnx_filter_release(f)
