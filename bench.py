@@ -659,8 +659,8 @@ def run_ours(args):
 # two largest layers, from one ncu capture of this workload (its summary is
 # kept under profiles/), with sources_sha the hash of TRAFFIC_SOURCES at that
 # capture.
-TRAFFIC = {"sources_sha": "", "dec_conv1a": 134.141440e6 + 207.531776e6,
-           "dec_conv1b": 267.567872e6 + 97.209600e6}
+TRAFFIC = {"sources_sha": "966bbc1b11dd3d3b", "dec_conv1a": 134.052096e6 + 207.474688e6,
+           "dec_conv1b": 267.572992e6 + 96.472064e6}
 # the kernel sources those figures were taken with: traffic is reported
 # null once their hash differs from sources_sha
 TRAFFIC_SOURCES = ("conv_tc.cu", "ptx.cuh", "internal.h")
