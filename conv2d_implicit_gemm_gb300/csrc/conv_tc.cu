@@ -71,22 +71,25 @@ __device__ __forceinline__ int tile_at(const TcConvParams& p, int tile) {
   return p.reverse ? p.tiles_x * p.tiles_y - 1 - tile : tile;
 }
 
-__device__ __forceinline__ void tile_origin(const TcConvParams& p, int tile, int* x0, int* y0) {
-  tile = tile_at(p, tile);
-  const int ty = tile / p.tiles_x;
-  *x0 = (tile - ty * p.tiles_x) * kTileM;
-  *y0 = ty * p.R;
-}
-
-// Tile origin; sub-pixel decoder tiles span 256 columns and hold one column
-// parity px (tile index = 2 * 256-column block + px).
+// Step t of the walk -> origin and row count of its tile: a full tile of
+// p.R rows, or in the last wave a sub-tile (rows R / tail_split further down
+// per sub-index) of the walk step's parent tile.  Sub-pixel decoder tiles
+// span 256 columns and hold one column parity px (tile index = 2 * 256-column
+// block + px).
 template <int KIND>
-__device__ __forceinline__ void tile_origin_k(const TcConvParams& p, int tile, int* x0, int* y0,
-                                              int* px) {
-  tile = tile_at(p, tile);
+__device__ __forceinline__ int tile_origin_k(const TcConvParams& p, int t, int* x0, int* y0,
+                                             int* px) {
+  int rows = p.R, dy = 0;
+  if (t >= p.tail_first) {
+    const int u = t - p.tail_first;
+    rows = p.R / p.tail_split;
+    dy = (u % p.tail_split) * rows;
+    t = p.tail_first + u / p.tail_split;
+  }
+  const int tile = tile_at(p, t);
   const int ty = tile / p.tiles_x;
   const int tx = tile - ty * p.tiles_x;
-  *y0 = ty * p.R;
+  *y0 = ty * p.R + dy;
   if (kind_subpixel<KIND>()) {
     *x0 = (tx >> 1) * (2 * kTileM);
     *px = tx & 1;
@@ -94,6 +97,7 @@ __device__ __forceinline__ void tile_origin_k(const TcConvParams& p, int tile, i
     *x0 = tx * kTileM;
     *px = 0;
   }
+  return rows;
 }
 
 // Advance a pipeline position (stage s of S, phase parity ph) by one item.
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
 
   const int S = p.S, R = p.R, N = p.N, KB0 = p.KB0;
   const int KB = p.KB0 + p.KB1;
-  const int num_tiles = p.tiles_x * p.tiles_y;
+  const int num_tiles = p.walk_tiles;  // walk steps (tiles and tail sub-tiles)
   constexpr bool SP = kind_subpixel<KIND>();
   constexpr bool TF = kind_tf32<KIND>();
   constexpr bool EXP = kind_expand<KIND>();
@@ -503,7 +507,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
         tc_fence_after();
         const uint32_t d_base = tmem + buf * set_cols;
         int tx0, ty0, tpx;
-        tile_origin_k<KIND>(p, tile, &tx0, &ty0, &tpx);
+        const int R = tile_origin_k<KIND>(p, tile, &tx0, &ty0, &tpx);  // this tile's rows
         for (int kb = 0; kb < items; ++kb, ++it, next_stage(s, ph, S)) {
           bool w = mbar_wait_bounded(&full[s], ph, p.status, kErrTimeoutMma);
           if (HELP && w) w = mbar_wait_bounded(&xdone[s], ph, p.status, kErrTimeoutMma);
@@ -611,8 +615,8 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
       }
     }
     for (int tile = blockIdx.x; !SP && tile < num_tiles && ok; tile += gridDim.x) {
-      int x0, y0;
-      tile_origin(p, tile, &x0, &y0);
+      int x0, y0, px;
+      tile_origin_k<KIND>(p, tile, &x0, &y0, &px);
       const int ly0 = (y0 >> 1) - 1, lx0 = (x0 >> 1) - kGroupPx;
       for (int kb = 0; kb < KB; ++kb, ++it, next_stage(s, ph, S)) {
         // Waiting on every stage keeps this warp group at most one use of a
@@ -691,7 +695,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
       if (!mbar_wait_bounded(&tfull[buf], (tcount >> 1) & 1u, p.status, kErrTimeoutEpilogue)) break;
       tc_fence_after();
       int x0, y0, px;
-      tile_origin_k<KIND>(p, tile, &x0, &y0, &px);
+      const int R = tile_origin_k<KIND>(p, tile, &x0, &y0, &px);  // this tile's rows
       // sub-pixel tiles hold every other output column
       const int x = SP ? x0 + 2 * m + px : x0 + m;
       const uint32_t tl = tmem + lane_off + buf * set_cols;

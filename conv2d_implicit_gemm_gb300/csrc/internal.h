@@ -75,6 +75,11 @@ struct TcConvParams {
   int xs0, xs1;            // log2 pixels per x unit of map0 / map1: 3 for
                            // 128-byte rows (pitch % 8 == 0), 0 for 16-byte rows
   int reverse;             // walk the tiles last to first (see tile_at)
+  // Last wave: the walk's last (tiles_x * tiles_y - tail_first) tiles are
+  // split into tail_split sub-tiles of R / tail_split rows each, so that a
+  // short last wave spreads over more CTAs; walk_tiles counts the walk's
+  // steps (tail_first = tiles, tail_split = 1: no split)
+  int tail_first, tail_split, walk_tiles;
 };
 
 enum TcKind : int {

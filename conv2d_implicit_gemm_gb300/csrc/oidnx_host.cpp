@@ -967,6 +967,23 @@ oidnx_status ensure_smem_limit(int family) {
   return ok();
 }
 
+// Last wave of a persistent conv grid: when the tiles do not fill the
+// final wave and at most half of the grid would work in it, its tiles are
+// split into sub-tiles of fewer rows (a power of two, at least min_rows
+// rows each: even rows for pools and decoders), as many as the grid takes.
+// A sub-tile loads its parent tile's boxes and issues only its own rows.
+void plan_tail(TcConvParams* p, long grid, int min_rows, bool allowed) {
+  const long tiles = static_cast<long>(p->tiles_x) * p->tiles_y;
+  const long r = tiles % grid;
+  int split = 1;
+  if (allowed && r > 0 && 2 * r <= grid)
+    while (p->R % (2 * split) == 0 && p->R / (2 * split) >= min_rows && r * 2 * split <= grid)
+      split *= 2;
+  p->tail_first = static_cast<int>(split > 1 ? tiles - r : tiles);
+  p->tail_split = split;
+  p->walk_tiles = static_cast<int>(p->tail_first + (tiles - p->tail_first) * split);
+}
+
 // Build the tensor-core launch of one conv.  src0/src1: device pointers of the
 // sources (fp16 layout), ext0: extent of source 0, (W, H): conv extent.
 // Pad the shared-memory request until at most `allowed` CTAs fit one SM, so
@@ -1077,6 +1094,9 @@ oidnx_status build_tc_launch_subpixel(const DeviceLayer& L, const void* src0, Ex
   // an even grid keeps each CTA on one column parity (tiles alternate parity)
   if (grid > 1 && grid % 2) --grid;
   T->grid = dim3(static_cast<unsigned>(grid), 1, 1);
+  // (CTAs that keep one column parity's weights resident stay on their
+  // parity: no split for them)
+  plan_tail(&p, grid, 2, !p.resident);
   // 16-byte chunks per pixel of each source: 8 halves, or 4 floats
   auto chunks = [&](int c) { return L.tf32 ? round_up(c, 4) / 4 : round_up(c, 16) / 8; };
   const int c8_0 = chunks(L.c0);
@@ -1181,6 +1201,7 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   T->smem = smem;
   const long tiles = static_cast<long>(p.tiles_x) * p.tiles_y;
   T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, static_cast<long>(num_sms()) * blocks)), 1, 1);
+  plan_tail(&p, T->grid.x, minR, true);
 
   // 16-byte chunks per pixel of each source: 8 halves, or 4 floats
   auto chunks = [&](int c) { return L.tf32 ? round_up(c, 4) / 4 : round_up(c, 16) / 8; };

@@ -57,6 +57,9 @@ CASES = [  # (width, height, cin, cout)
     (128, 4, 16, 16), (130, 5, 32, 32), (1, 1, 16, 16), (37, 9, 9, 32),
     (257, 3, 64, 48), (64, 20, 80, 96), (200, 7, 112, 112), (50, 6, 160, 96),
     (300, 2, 73, 64), (17, 33, 32, 3),
+    # 184 tiles on a 152-CTA grid: the last wave's 32 tiles run as sub-tiles
+    # of 2 rows (R = 8) and of 1 row (R = 4)
+    (1024, 184, 32, 32), (1024, 92, 64, 64),
 ]
 
 
