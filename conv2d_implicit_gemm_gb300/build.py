@@ -17,7 +17,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liboidnx.so")
-SOURCES = ["oidnx_host.cpp", "conv_tc.cu", "conv_pair.cu", "conv_final.cu", "io_passes.cu", "noalloc.cu"]
+SOURCES = ["oidnx_host.cpp", "conv_tc.cu", "conv_pair.cu", "conv_final.cu", "conv_tail.cu",
+           "io_passes.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

@@ -50,6 +50,7 @@ __device__ __forceinline__ void final_tile(const FinalConvParams& p, int tile, i
 template <bool TF>
 __device__ __forceinline__ void final_kblock(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t id1,
                                              uint32_t id2, uint32_t id3) {
+  if (!elect_one()) return;  // one lane issues the K block's MMAs
 #pragma unroll
   for (int h = 0; h < kR + 2; ++h) {
     const int lo = h - 2 > 0 ? h - 2 : 0;
@@ -59,10 +60,8 @@ __device__ __forceinline__ void final_kblock(uint64_t ad, uint64_t bd, uint32_t 
     const uint64_t a = ad + static_cast<uint32_t>(h * 2 * kHaloW);
     const uint64_t b = bd + static_cast<uint32_t>((2 - h + lo) * kNc);
     const uint32_t id = n == 1 ? id1 : (n == 2 ? id2 : id3);
-    if (elect_one()) {
-      if (TF) mma_tf32_ss(d, a, b, id);
-      else mma_f16_ss(d, a, b, id, 1u);
-    }
+    if (TF) mma_tf32_ss(d, a, b, id);
+    else mma_f16_ss(d, a, b, id, 1u);
   }
 }
 

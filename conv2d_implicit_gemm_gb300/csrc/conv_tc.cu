@@ -108,20 +108,18 @@ __device__ __forceinline__ void next_stage(uint32_t& s, uint32_t& ph, uint32_t S
   }
 }
 
-// One MMA issued by the elected lane of the (converged) MMA warp.  Every MMA
-// accumulates: the epilogue refills each accumulator with the bias after
-// reading it (and before the first tile), so no MMA has to overwrite one.
-// An overwriting MMA issued amid accumulating ones stalled the tensor pipe
-// (~200 cycles each in a microbenchmark of this issue sequence).
-__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
-  if (elect_one()) mma_f16_ss(d, a, b, idesc, 1u);
-}
-
-// fp16 (kind::f16) or tf32 (kind::tf32) MMA by the elected lane.
+// One fp16 (kind::f16) or tf32 (kind::tf32) MMA, issued by the thread that
+// runs it: the issue functions below elect one lane of the (converged) MMA
+// warp once and let it issue a whole K block, with no branch per MMA.
+// Every MMA accumulates: the epilogue refills each accumulator with the
+// bias after reading it (and before the first tile), so no MMA has to
+// overwrite one.  An overwriting MMA issued amid accumulating ones stalled
+// the tensor pipe (~200 cycles each in a microbenchmark of this issue
+// sequence).
 template <bool TF>
 __device__ __forceinline__ void umma_k(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
-  if (!TF) umma(d, a, b, idesc);
-  else if (elect_one()) mma_tf32_ss(d, a, b, idesc);
+  if (!TF) mma_f16_ss(d, a, b, idesc, 1u);
+  else mma_tf32_ss(d, a, b, idesc);
 }
 
 // All MMAs of one K block for a tile of R rows, fully unrolled so that the
@@ -133,6 +131,7 @@ template <int R, int G, bool TF>
 __device__ __forceinline__ void issue_kblock(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
                                              uint32_t kx_b16, uint32_t id1, uint32_t id2,
                                              uint32_t id3) {
+  if (!elect_one()) return;
   const uint32_t idn[4] = {0u, id1, id2, id3};
 #pragma unroll
   for (int kx = 0; kx < 3; ++kx) {
@@ -198,6 +197,7 @@ template <int R, int G, bool TF>
 __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
                                          int px, int pxb, uint32_t row16, uint32_t id1,
                                          uint32_t id2, uint32_t id3, uint32_t id4) {
+  if (!elect_one()) return;
 #pragma unroll
   for (int d = 0; d < 2; ++d) {
     const uint64_t adk = ad + static_cast<uint32_t>(d + px);
@@ -225,6 +225,7 @@ __device__ __forceinline__ void issue_up(uint64_t ad, uint64_t bd, uint32_t dbas
 template <int R, int G, bool TF>
 __device__ __forceinline__ void issue_skip(uint64_t ad, uint64_t bd, uint32_t dbase, uint32_t N,
                                            uint32_t row16, uint32_t id1, uint32_t id2, uint32_t id3) {
+  if (!elect_one()) return;
 #pragma unroll
   for (int h = 0; h < R + 2; ++h) {
     const int lo = h - 2 > 0 ? h - 2 : 0;

@@ -183,6 +183,54 @@ struct FinalConvLaunch {
 cudaError_t launch_conv_final(const FinalConvLaunch& L, cudaStream_t stream);
 cudaError_t conv_final_set_smem_limit(size_t bytes);
 
+// dec_conv1b (64 -> 32, ReLU, fp16) and dec_conv0 (32 -> 3, folded) in one
+// kernel, fp16 storage: output tiles of kTailOut rows x kFinalSpan pixels,
+// conv 1 over the kTailMid rows x 128 pixels around each, its output kept in
+// tensor memory as conv 2's A operand; CTAs take groups of `run` row tiles
+// of one column strip round robin, carrying two conv-1 rows from tile to
+// tile of a group; optionally the output pass in the epilogue (as
+// FinalConvParams).
+constexpr int kTailOut = 6;
+constexpr int kTailMid = kTailOut + 2;
+
+struct TailConvParams {
+  const __half* w1;        // conv-1 B operand, [kb][kx][2][3 x 32][8] (the plain packing)
+  const __half* w2;        // conv-2 B operand, kx folded: [kb][2][3 x 16][8]
+  const float* bias1;      // [32]
+  const float* bias2;      // [16]: b0, b1, b2, zeros
+  float4* net;             // [H][W] network output (lane 3 zero), or null
+  int* status;
+  int W, H;                // conv extent
+  int KB1;                 // 16-channel K blocks of conv 1's input
+  int tiles_x, tiles_y;    // tiles of kTailOut rows x kFinalSpan pixels
+  int S;                   // input stages (one K block's halo box each)
+  uint32_t stage_tx, stage_bytes;  // bytes of a kTailMid + 2 row box; stage size
+  uint32_t stage_tx8;      // bytes of a kTailMid row box (six new conv-1 rows)
+  int xs;                  // log2 pixels per x unit of the input maps
+  int run, groups;         // row tiles per group; groups (ceil(tiles_y / run) x tiles_x)
+  // output pass (when fused): as FinalConvParams
+  const float4* color;
+  size_t color_stride;
+  float4* out;
+  size_t out_stride;
+  int in_x, in_y, ox, oy, ow, oh;
+  int hdr;
+  float scale;
+  const float4* exp2_tab;
+};
+
+struct TailConvLaunch {
+  CUtensorMap map10;       // conv-1 input: boxes of kTailMid + 2 rows x kHaloW pixels x 2 chunks
+  CUtensorMap map8;        // the same with boxes of kTailMid rows
+  TailConvParams p;
+  int outpass;
+  dim3 grid;
+  size_t smem;
+};
+
+cudaError_t launch_conv_tail(const TailConvLaunch& L, cudaStream_t stream);
+cudaError_t conv_tail_set_smem_limit(size_t bytes);
+
 struct TcConvLaunch {
   CUtensorMap map0;        // source 0 (full-res halo box, or low-res box)
   CUtensorMap map1;        // source 1 (full-res halo box, or stride-2 box); unused if KB1 == 0

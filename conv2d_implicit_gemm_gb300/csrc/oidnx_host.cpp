@@ -732,10 +732,12 @@ struct LayerLaunch {
   int layer;               // first layer of the launch
   int pair;                // 1: layers `layer` and `layer + 1` fused (pcl)
   int final;               // 1: the final conv with kx folded (fcl)
+  int tail;                // 1: the last two layers in one kernel (tlcl)
   const char* name;
   TcConvLaunch tcl;
   PairConvLaunch pcl;
   FinalConvLaunch fcl;
+  TailConvLaunch tlcl;
   double flop;   // logical conv FLOPs
   double bytes;  // algorithmic bytes: inputs read once, output written once
 };
@@ -761,6 +763,8 @@ struct Plan {
   // the last execution stored the network output (not so when the output
   // pass ran in the final conv's epilogue without keepActivations)
   bool out_stored = true;
+  // the last execution ran the output pass in the last conv's epilogue
+  bool outpass_fused = false;
   uint64_t last_used = 0;
   cudaEvent_t done = nullptr;  // recorded after each use
   bool used = false;
@@ -789,7 +793,7 @@ struct oidnx_filter {
   // parameters
   int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
       overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 1,
-      fuse = 0, fuse_output = 1, stack_tiles = 0;
+      fuse = 0, fuse_output = 1, fuse_tail = 1, stack_tiles = 0;
   float input_scale = 1.0f;
   void* img[4] = {};
   size_t img_stride[4] = {};
@@ -930,7 +934,7 @@ int act_chunks(int precision, int c) {
 constexpr int kMaxDevices = 64;
 std::mutex g_device_mutex;
 int g_num_sms[kMaxDevices] = {};
-uint64_t g_smem_limit_set[3] = {};  // per kernel family: bit d for device d
+uint64_t g_smem_limit_set[4] = {};  // per kernel family: bit d for device d
 
 int current_device() {
   int dev = 0;
@@ -949,7 +953,7 @@ int num_sms() {
   return n;
 }
 
-enum KernelFamily { kFamilyTc = 0, kFamilyPair = 1, kFamilyFinal = 2 };
+enum KernelFamily { kFamilyTc = 0, kFamilyPair = 1, kFamilyFinal = 2, kFamilyTail = 3 };
 
 // Raise a kernel family's dynamic shared-memory limit to the 227 KB an SM
 // offers, on the current device.
@@ -959,9 +963,10 @@ oidnx_status ensure_smem_limit(int family) {
   const uint64_t bit = dev < kMaxDevices ? (uint64_t(1) << dev) : 0;
   if (bit && (g_smem_limit_set[family] & bit)) return ok();
   const size_t max_smem = 227 * 1024;
-  const cudaError_t e = family == kFamilyTc     ? conv_tc_set_smem_limit(max_smem)
-                        : family == kFamilyPair ? conv_pair_set_smem_limit(max_smem)
-                                                : conv_final_set_smem_limit(max_smem);
+  const cudaError_t e = family == kFamilyTc      ? conv_tc_set_smem_limit(max_smem)
+                        : family == kFamilyPair  ? conv_pair_set_smem_limit(max_smem)
+                        : family == kFamilyFinal ? conv_final_set_smem_limit(max_smem)
+                                                 : conv_tail_set_smem_limit(max_smem);
   if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
   g_smem_limit_set[family] |= bit;
   return ok();
@@ -1348,10 +1353,85 @@ oidnx_status build_final_launch(const DeviceLayer& L, const void* src, Extent ex
                         kFinalRows + 2, true, &p.xs);
 }
 
+// dec_conv1b and dec_conv0 as one kernel ("fuseTail", fp16, one image per
+// plan, activations not kept): dec_conv1b's 32-channel map stays in tensor
+// memory.  Not with the fused pairs ("fuseLayers"), which take these layers.
+bool tail_fusable(const oidnx_filter* f, int stack) {
+  if (!f->fuse_tail || f->fuse || f->keep_acts || stack > 1 || f->precision != OIDNX_PRECISION_FP16)
+    return false;
+  const DeviceLayer& a = f->layers[kLayers - 2];
+  return a.c1 == 0 && a.cout == 32 && a.N == 32 && a.KB0 >= 1 && a.KB0 <= 4 &&
+         final_foldable(f->layers[kLayers - 1]);
+}
+
+// Launch of the fused last two layers over a W x H extent: A = dec_conv1b
+// reading `src` (fp16, extent ext), B = dec_conv0 writing `net` (f32
+// [H][W][4]; may be null when the output pass runs in the epilogue).
+oidnx_status build_tail_launch(const DeviceLayer& A, const DeviceLayer& B, const void* src, Extent ext,
+                               int W, int H, void* net, int* status, TailConvLaunch* T) {
+  T->outpass = 0;
+  TailConvParams& p = T->p;
+  std::memset(&p, 0, sizeof(p));
+  p.w1 = static_cast<const __half*>(A.wtc);
+  p.w2 = static_cast<const __half*>(B.wfold);
+  p.bias1 = A.bias;
+  p.bias2 = B.bias;
+  p.net = static_cast<float4*>(net);
+  p.status = status;
+  p.W = W;
+  p.H = H;
+  p.KB1 = A.KB0;
+  p.tiles_x = (W + kFinalSpan - 1) / kFinalSpan;
+  p.tiles_y = (H + kTailOut - 1) / kTailOut;
+  // one stage: one K block's halo box, kTailMid + 2 rows x kHaloW pixels x 2
+  // chunks (kTailMid rows when six conv-1 rows are computed)
+  p.stage_tx = static_cast<uint32_t>((kTailMid + 2) * 2 * kHaloW * kChunkBytes);
+  p.stage_tx8 = static_cast<uint32_t>(kTailMid * 2 * kHaloW * kChunkBytes);
+  p.stage_bytes = static_cast<uint32_t>(round_up_sz(p.stage_tx, 1024));
+  // alignment slack, weights of both convs, boundary exchange (2 sub x 2 x 4
+  // quarters x 3 rows x 3 float4), both biases, 14 barriers + 2 per stage,
+  // the TMEM address
+  const size_t fixed = 128 + static_cast<size_t>(p.KB1) * 3 * 2 * 3 * 32 * kChunkBytes + B.fold_bytes +
+                       2 * 2 * 4 * (kTailOut / 2) * 3 * 16 + (32 + 16) * 4 + 14 * 8 + 16;
+  const size_t per_stage = static_cast<size_t>(p.stage_bytes) + 16;
+  const size_t max_smem = 227 * 1024;
+  if (fixed + 2 * per_stage > max_smem) return fail(OIDNX_ERR_UNSUPPORTED, "tail conv does not fit");
+  p.S = static_cast<int>(std::min<size_t>(4, (max_smem - fixed) / per_stage));
+  // one CTA per SM (it allocates all 512 TMEM columns): more than half the
+  // shared memory of an SM
+  T->smem = std::max<size_t>(fixed + static_cast<size_t>(p.S) * per_stage, 120 * 1024);
+  OIDNX_TRY(ensure_smem_limit(kFamilyTail));
+  // Groups of `run` row tiles of one strip, taken round robin: the run that
+  // gives the busiest CTA the fewest conv-1 rows (rounds of groups x
+  // (6 run + 2)), the shortest among equals (the frame is then read closest
+  // to the walk's order).
+  const long sms = num_sms();
+  long best = LONG_MAX;
+  for (int run = 1; run <= p.tiles_y; ++run) {
+    const long groups = static_cast<long>((p.tiles_y + run - 1) / run) * p.tiles_x;
+    const long cost = (groups + sms - 1) / sms * ((kTailMid - 2) * static_cast<long>(run) + 2);
+    if (cost < best) {
+      best = cost;
+      p.run = run;
+      p.groups = static_cast<int>(groups);
+    }
+  }
+  T->grid = dim3(static_cast<unsigned>(std::min<long>(p.groups, sms)), 1, 1);
+  OIDNX_TRY(encode_act_map(&T->map8, src, ext.w, ext.pitch, ext.h, 2 * p.KB1, kHaloW, kTailMid, true,
+                           &p.xs));
+  return encode_act_map(&T->map10, src, ext.w, ext.pitch, ext.h, 2 * p.KB1, kHaloW, kTailMid + 2, true,
+                        &p.xs);
+}
+
 oidnx_status run_launch(const LayerLaunch& L, cudaStream_t s) {
   (void)cudaGetLastError();  // drop a stale, non-sticky error of an earlier call
   if (L.final) {
     cudaError_t e = launch_conv_final(L.fcl, s);
+    if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "%s launch: %s", L.name, cudaGetErrorString(e));
+    return ok();
+  }
+  if (L.tail) {
+    cudaError_t e = launch_conv_tail(L.tlcl, s);
     if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "%s launch: %s", L.name, cudaGetErrorString(e));
     return ok();
   }
@@ -1380,10 +1460,19 @@ void destroy_plan(Plan* p) {
 // rows and channels padded as the kernels run them): per tile, K blocks x
 // taps x R rows x N x 128 pixels x K x 2, with 4 taps on the upsampled
 // channels of a sub-pixel decoder, three passes for 3xTF32, and for the
-// folded final conv 3 R rows of N = 16 (three kx taps) per K block.  0 for
-// fused pairs.
+// folded final conv 3 R rows of N = 16 (three kx taps) per K block.  The
+// fused tail: conv 1 over the rows each tile computes (kTailMid in a
+// group's first tile, else kTailMid - 2; 3 ky each) of N = 32 per
+// K block and kx, conv 2 over kTailOut rows of N = 16 per K block and ky.
+// 0 for fused pairs.
 double mma_flop(const LayerLaunch& LL) {
   if (LL.pair) return 0;
+  if (LL.tail) {
+    const TailConvParams& p = LL.tlcl.p;
+    const double T = static_cast<double>(p.tiles_x) * p.tiles_y;
+    const double rows = (kTailMid - 2) * T + 2.0 * p.groups;  // 8 rows in a group's first tile
+    return 128.0 * 16 * 2 * (rows * p.KB1 * 3 * 3 * 32 + T * 2 * 3 * kTailOut * 16);
+  }
   if (LL.final) {  // 32 input channels: 2 K blocks of 16, or 4 of 8 x 3 tf32 passes
     const FinalConvParams& p = LL.fcl.p;
     return static_cast<double>(p.tiles_x) * p.tiles_y * 3 * kFinalRows * 16 * 128.0 * 32 * 2 *
@@ -1416,6 +1505,7 @@ struct ValueLayout {
   int last_use[V_COUNT];
   bool split_on[4];       // kSplits[i] in use (its decoder runs in sub-pixel mode)
   bool fused[2];          // kPairs[i] runs as one fused kernel
+  bool tail;              // the last two layers run as one kernel
   bool stored[kLayers];   // layer l's output is stored (not fused away)
   size_t off[V_COUNT];    // arena offset of each placed value
   size_t bytes[V_COUNT];  // its bytes; 0 if not placed
@@ -1459,6 +1549,8 @@ void layout_values(const oidnx_filter* f, int w, int h, bool io_external, bool k
     V->fused[i] = pair_fusable(f, kPairs[i]);
     if (V->fused[i]) V->stored[kPairs[i].first] = false;
   }
+  V->tail = !keep && tail_fusable(f, stack);
+  if (V->tail) V->stored[kLayers - 2] = false;
   struct Placed {
     size_t lo, hi;  // byte range (1 KB multiples)
     int until;      // index of the last launch that reads it
@@ -1547,6 +1639,20 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
       const Extent oe = V.ext[d2.dst];
       LL.bytes = logical_bytes(d.src0) +
                  (d2.kind == kFinal ? static_cast<double>(oe.w) * oe.h * 16 : logical_bytes(d2.dst)) +
+                 static_cast<double>(L.weight_bytes + L2.weight_bytes);
+      OIDNX_TRY(emit(LL));
+      ++l;
+      continue;
+    }
+    if (l == kLayers - 2 && V.tail) {
+      const LayerDef& d2 = kDefs[l + 1];
+      const DeviceLayer& L2 = f->layers[l + 1];
+      LL.tail = 1;
+      LL.name = "dec_conv1b+dec_conv0";
+      OIDNX_TRY(build_tail_launch(L, L2, ptr(d.src0), V.ext[d.src0], conv.w, conv.h, ptr(d2.dst),
+                                  f->status, &LL.tlcl));
+      LL.flop = 2.0 * 9.0 * (L.cin * L.cout + L2.cin * L2.cout) * px;
+      LL.bytes = logical_bytes(d.src0) + static_cast<double>(V.ext[d2.dst].w) * V.ext[d2.dst].h * 16 +
                  static_cast<double>(L.weight_bytes + L2.weight_bytes);
       OIDNX_TRY(emit(LL));
       ++l;
@@ -1750,10 +1856,30 @@ oidnx_status enqueue_network(oidnx_filter* f, Plan* P, bool prof, cudaStream_t s
   return ok();
 }
 
-// The output pass runs in the final conv's epilogue (kx-folded final conv,
-// "fuseOutput" on).
+// The output pass runs in the final conv's epilogue (kx-folded final conv
+// or the fused tail, "fuseOutput" on).
 bool output_fused(const oidnx_filter* f, const Plan* P) {
-  return P && f->fuse_output && !P->launches.empty() && P->launches.back().final;
+  return P && f->fuse_output && !P->launches.empty() &&
+         (P->launches.back().final || P->launches.back().tail);
+}
+
+// Output-pass parameters of one tile in a final-conv or tail epilogue.
+template <class Params>
+void set_output_pass(const oidnx_filter* f, void* const img[4], const size_t stride[4],
+                     const AxisTile& tx, const AxisTile& ty, float scale, Params* fp) {
+  fp->color = static_cast<const float4*>(img[0]);
+  fp->color_stride = stride[0] / 16;
+  fp->out = static_cast<float4*>(img[3]);
+  fp->out_stride = stride[3] / 16;
+  fp->in_x = tx.out_start - tx.in_start;
+  fp->in_y = ty.out_start - ty.in_start;
+  fp->ox = tx.out_start;
+  fp->oy = ty.out_start;
+  fp->ow = tx.out_size;
+  fp->oh = ty.out_size;
+  fp->hdr = f->hdr;
+  fp->scale = scale;
+  fp->exp2_tab = static_cast<const float4*>(f->exp2_tab);
 }
 
 // Input-pass parameters of one tile; out / out_split: where its packed
@@ -1825,26 +1951,14 @@ oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const
       LayerLaunch L = P->final_tiles[b];
       L.fcl.outpass = 1;
       L.name = "dec_conv0+output";
-      FinalConvParams& fp = L.fcl.p;
-      fp.net = nullptr;
-      fp.color = static_cast<const float4*>(img[0]);
-      fp.color_stride = stride[0] / 16;
-      fp.out = static_cast<float4*>(img[3]);
-      fp.out_stride = stride[3] / 16;
-      fp.in_x = tx.out_start - tx.in_start;
-      fp.in_y = ty.out_start - ty.in_start;
-      fp.ox = tx.out_start;
-      fp.oy = ty.out_start;
-      fp.ow = tx.out_size;
-      fp.oh = ty.out_size;
-      fp.hdr = f->hdr;
-      fp.scale = scale;
-      fp.exp2_tab = static_cast<const float4*>(f->exp2_tab);
+      L.fcl.p.net = nullptr;
+      set_output_pass(f, img, stride, tx, ty, scale, &L.fcl.p);
       OIDNX_TRY(run_launch(L, s));
       OIDNX_TRY(prof_mark(f, prof, L.layer, s));
     }
   }
   P->out_stored = false;
+  P->outpass_fused = true;
   return ok();
 }
 
@@ -1855,6 +1969,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
   const float scale = f->input_scale == 0.0f ? 1.0f : f->input_scale;
   OIDNX_TRY(prof_mark(f, prof, -2, s));
   if (P->stack > 1) return enqueue_stacked(f, P, img, stride, scale, prof, s);
+  P->outpass_fused = output_fused(f, P);
   for (const AxisTile& ty : f->ty)
     for (const AxisTile& tx : f->tx) {
       PackParams pp = tile_pack_params(f, P, img, stride, tx, ty, scale, P->ptr(V_IN),
@@ -1870,24 +1985,19 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
           OIDNX_TRY(prof_mark(f, prof, P->launches[i].layer, s));
         }
         LayerLaunch L = P->launches.back();
-        L.fcl.outpass = 1;
-        L.name = "dec_conv0+output";
-        FinalConvParams& fp = L.fcl.p;
-        fp.net = f->keep_acts ? static_cast<float4*>(P->ptr(V_OUT)) : nullptr;
+        float4* net = f->keep_acts ? static_cast<float4*>(P->ptr(V_OUT)) : nullptr;
         P->out_stored = f->keep_acts != 0;
-        fp.color = static_cast<const float4*>(img[0]);
-        fp.color_stride = stride[0] / 16;
-        fp.out = static_cast<float4*>(img[3]);
-        fp.out_stride = stride[3] / 16;
-        fp.in_x = tx.out_start - tx.in_start;
-        fp.in_y = ty.out_start - ty.in_start;
-        fp.ox = tx.out_start;
-        fp.oy = ty.out_start;
-        fp.ow = tx.out_size;
-        fp.oh = ty.out_size;
-        fp.hdr = f->hdr;
-        fp.scale = scale;
-        fp.exp2_tab = static_cast<const float4*>(f->exp2_tab);
+        if (L.tail) {
+          L.tlcl.outpass = 1;
+          L.name = "dec_conv1b+dec_conv0+output";
+          L.tlcl.p.net = net;
+          set_output_pass(f, img, stride, tx, ty, scale, &L.tlcl.p);
+        } else {
+          L.fcl.outpass = 1;
+          L.name = "dec_conv0+output";
+          L.fcl.p.net = net;
+          set_output_pass(f, img, stride, tx, ty, scale, &L.fcl.p);
+        }
         OIDNX_TRY(run_launch(L, s));
         OIDNX_TRY(prof_mark(f, prof, L.layer, s));
         continue;
@@ -2186,9 +2296,12 @@ oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value) 
   } else if (n == "stackTiles") {
     if (value < 0) return fail(OIDNX_ERR_INVALID_ARGUMENT, "stackTiles must be >= 0");
     f->stack_tiles = value;
-  } else if (n == "keepActivations" || n == "subpixelDecoder" || n == "fuseLayers") {
-    (n == "keepActivations" ? f->keep_acts : n == "subpixelDecoder" ? f->subpixel : f->fuse) =
-        value ? 1 : 0;
+  } else if (n == "keepActivations" || n == "subpixelDecoder" || n == "fuseLayers" ||
+             n == "fuseTail") {
+    (n == "keepActivations"   ? f->keep_acts
+     : n == "subpixelDecoder" ? f->subpixel
+     : n == "fuseLayers"      ? f->fuse
+                              : f->fuse_tail) = value ? 1 : 0;
     for (auto& p : f->plans) f->retired.push_back(std::move(p));
     f->plans.clear();
     f->current = nullptr;
@@ -2219,6 +2332,7 @@ oidnx_status oidnx_filter_get_int(oidnx_filter* f, const char* name, int* value)
   else if (n == "subpixelDecoder") *value = f->subpixel;
   else if (n == "fuseLayers") *value = f->fuse;
   else if (n == "fuseOutput") *value = f->fuse_output;
+  else if (n == "fuseTail") *value = f->fuse_tail;
   else if (n == "stackTiles") *value = f->stack_tiles;
   else if (n == "stackedTiles") *value = f->committed && f->current ? f->current->stack : 0;
   else if (n == "profile") *value = f->profile_always;
@@ -2402,6 +2516,7 @@ oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w
     if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "split copy: %s", cudaGetErrorString(e));
   }
   P->out_stored = true;
+  P->outpass_fused = false;
   OIDNX_TRY(prof_mark(f, prof, -2, s));
   OIDNX_TRY(enqueue_network(f, P, prof, s));
   OIDNX_CUDA(cudaMemcpyAsync(out, P->ptr(V_OUT), P->value_bytes[V_OUT], cudaMemcpyDeviceToDevice, s));
@@ -2520,10 +2635,12 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
   const double out_bytes = out_px / tiles * 48.0;  // per tile: net + colour read, image written
   if (plan)
     for (const LayerLaunch& L : plan->launches) {
-      const bool fused_out = &L == &plan->launches.back() && output_fused(f, plan);
+      const bool fused_out =
+          &L == &plan->launches.back() && plan->outpass_fused && (L.final || L.tail);
       // with the output pass fused the network output is not stored: the
       // kernel reads the colour and writes the image instead
-      add(fused_out ? "dec_conv0+output" : L.name, L.layer + 2, L.flop,
+      add(fused_out ? (L.tail ? "dec_conv1b+dec_conv0+output" : "dec_conv0+output") : L.name,
+          L.layer + 2, L.flop,
           fused_out ? L.bytes - tile_px * 16 + out_bytes - out_px / tiles * 16 : L.bytes,
           mma_flop(L));
     }

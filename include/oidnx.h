@@ -106,6 +106,13 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *                        on GB300 the separate kernels are faster (the MMAs
  *                        of these layers are bound by shared-memory operand
  *                        reads, which fusion does not reduce)
+ *   "fuseTail"           1 = with fp16 storage and a frame of one tile,
+ *                        dec_conv1b and dec_conv0 (and the output pass when
+ *                        "fuseOutput" is 1) run as one kernel: dec_conv1b's
+ *                        32-channel map stays in tensor memory and is never
+ *                        stored; the results equal the separate kernels' bit
+ *                        for bit (default).  Off with keepActivations or
+ *                        fuseLayers 1.
  *   "stackTiles"         frames of several equal tiles stack them: each conv
  *                        runs once over a group of tiles (zero rows between
  *                        them), the input pass and the final conv per tile.
@@ -279,8 +286,8 @@ oidnx_status oidnx_get_resource_info(oidnx_filter* f, char* json, size_t cap);
  * reads the network output.  This is what the per-layer parity checks read.
  * layer: 0 = packed network input, 1..16 = outputs of enc_conv0 ..
  * dec_conv0 in network order (enc_conv1..enc_conv4 store their pooled
- * outputs).  Valid for every layer only with "keepActivations" = 1 and
- * "fuseLayers" = 0 (the output of a layer fused with the next one is never
+ * outputs).  Valid for every layer only with "keepActivations" = 1 (which
+ * turns "fuseTail" off) and "fuseLayers" = 0 (the output of a layer fused with the next one is never
  * stored, nor is the network output of a denoise whose output pass ran in
  * the final conv's epilogue without "keepActivations": such reads fail
  * with INVALID_ARGUMENT); the required size is returned in *bytes_needed.

@@ -66,7 +66,10 @@ def test_profile_every_execution_through_the_graph(weights):
     finally:
         d.close()
     assert np.array_equal(plain.view(np.uint32), profiled.view(np.uint32))
-    assert len(prof["layers"]) == 17
+    # input pass, 14 convs, then dec_conv1b + dec_conv0 + the output pass as
+    # one kernel (the fused tail, on by default for a one-tile frame)
+    ids = [l["id"] for l in prof["layers"]]
+    assert len(ids) == 16 and ids[-1] == "dec_conv1b+dec_conv0+output", ids
 
 
 @pytest.mark.parametrize("precision", ["fp16", "fp32"])
@@ -94,6 +97,14 @@ def test_profile_counts_executed_tensor_flops(weights, precision):
     assert prof["dec_conv1a"]["flop"] == 2 * 9 * 73 * 64 * px
     assert prof["dec_conv1a"]["mmaFlop"] == passes * 2 * (4 * 64 + 9 * 16) * 64 * px
     assert prof["input-pack"]["mmaFlop"] == 0
+    if precision == "fp16":
+        # the fused tail: 3 x 22 tiles of 126 x 6 outputs, each its own group
+        # at this size (all 8 conv-1 rows computed); per tile conv 1 issues
+        # 8 rows x 3 ky x 3 kx x 4 K blocks at N 32, conv 2 6 rows x 3 ky x
+        # 2 K blocks at N 16, each M 128 x K 16
+        tail = prof["dec_conv1b+dec_conv0+output"]
+        assert tail["flop"] == 2 * 9 * (64 * 32 + 32 * 3) * px
+        assert tail["mmaFlop"] == 66 * 2 * 128 * 16 * (8 * 3 * 3 * 4 * 32 + 6 * 3 * 2 * 16)
 
 
 def test_shape_cache_eviction_with_work_in_flight(weights):
