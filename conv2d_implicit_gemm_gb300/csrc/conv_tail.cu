@@ -24,17 +24,19 @@
 //    and the row accumulators start from the bias, in the per-row order (K
 //    block, kx, ky) of the plain conv kernel, so the values equal that
 //    kernel's bit for bit.
-//  * Tensor memory holds two tile buffers of kTailMid slots x 32 columns.
-//    Slot r first accumulates conv-1 row r; the epilogue reads it, applies
-//    ReLU, rounds to fp16 and writes the row back into the slot's first 16
-//    columns as packed fp16 pairs (zero for rows and pixels outside the
-//    image: conv 2's same padding), and for r < kTailOut sets the last 16
-//    columns to conv 2's bias.  Conv 2 takes the fp16 rows straight from
+//  * Tensor memory holds two tile buffers of 256 columns.  Conv 1
+//    accumulates row r in the 32 columns of slot r (slot r + 2 when rows 6
+//    and 7 are carried).  The conversion warps read each row, apply ReLU,
+//    round to fp16 and write it back as 16 columns of packed fp16 pairs
+//    (zero for rows and pixels outside the image: conv 2's same padding):
+//    rows 0..5 at columns 32 + 16 r, rows 6 and 7 at columns 0 and 16 (where
+//    the previous tile of the group put its carried rows); then conv 2's
+//    bias into columns 128..223.  Conv 2 takes the fp16 rows straight from
 //    tensor memory as its A operand (tcgen05.mma with A in TMEM), with the
-//    three kx taps folded into N = 16 as in the final-conv kernel: output
-//    row r accumulates in slot r's last 16 columns, in the final-conv
-//    kernel's order (K block, ky); the kx partial sums of pixels m, m + 1,
-//    m + 2 are added in the epilogue.
+//    three kx taps folded into N = 16 as in the final-conv kernel and ky
+//    stacked along N: output row r accumulates in columns 128 + 16 r, in the
+//    final-conv kernel's order (K block, ky); the kx partial sums of pixels
+//    m, m + 1, m + 2 are added in the epilogue.
 //  * Overlap: while the epilogue turns tile t's conv-1 rows into fp16 and
 //    later finishes its output, the tensor cores run conv 1 of tile t + 1
 //    in the other buffer; conv 2 of tile t is issued between two K blocks
@@ -57,8 +59,14 @@ constexpr int kTailSubs = 2;         // output warps per lane quarter
 constexpr int kTailThreads = 32 * (2 + kTailMidWarps + kTailOutWarps);
 constexpr int kMidC = 32;            // conv-1 output channels
 constexpr int kC2 = 16;              // conv-2 accumulator columns per row (12 used)
-constexpr uint32_t kSlot = 32;                  // columns per row slot
+constexpr uint32_t kSlot = 32;                  // columns per conv-1 row slot
 constexpr uint32_t kBufCols = kTailMid * kSlot; // 256: one tile buffer
+constexpr uint32_t kC2Col = 128;                // conv-2 accumulators: 6 rows x 16 columns
+
+// Column of fp16 row r (of kTailMid) in a tile buffer.
+__host__ __device__ constexpr uint32_t mid_col(int r) {
+  return r < kTailOut ? 32u + 16u * static_cast<uint32_t>(r) : 16u * static_cast<uint32_t>(r - kTailOut);
+}
 constexpr uint32_t kTmemCols = 2 * kBufCols;
 constexpr uint32_t kW1Block = 3u * 2u * 3u * kMidC * kChunkBytes;  // [kx][half][ky][32][8]: 9216 B
 constexpr uint32_t kW2Block = 2u * 3u * kC2 * kChunkBytes;          // [half][ky][16][8]: 1536 B
@@ -222,7 +230,8 @@ __global__ void __launch_bounds__(kTailThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     const uint32_t i1[4] = {0u, idesc_f16_f32(kTileM, kMidC), idesc_f16_f32(kTileM, 2 * kMidC),
                             idesc_f16_f32(kTileM, 3 * kMidC)};
-    const uint32_t i2 = idesc_f16_f32(kTileM, kC2);
+    const uint32_t i2[4] = {0u, idesc_f16_f32(kTileM, kC2), idesc_f16_f32(kTileM, 2 * kC2),
+                            idesc_f16_f32(kTileM, 3 * kC2)};
     // stage box rows are kHaloW pixels; A row i of conv 1 is image pixel
     // x0 - 2 + i + kx, o pixels past the box start
     const uint64_t a0 = smem_desc_noswizzle(smem_u32(A), kHaloW * kChunkBytes, 128);
@@ -230,23 +239,24 @@ __global__ void __launch_bounds__(kTailThreads, 1)
     // per K block [8-lane half][ky stack][16][8] (kx folded into the 16)
     const uint64_t w1d = smem_desc_noswizzle(smem_u32(W1), 3u * kMidC * kChunkBytes, 128);
     const uint64_t w2d = smem_desc_noswizzle(smem_u32(W2), 3u * kC2 * kChunkBytes, 128);
-    // conv 2 of the tile in buffer b: output row r (slot r, columns 16..31)
-    // gets mid row r + ky (slot r + ky, K block kb = columns kb * 8 .. + 7)
-    // with B rows (2 - ky) * 16 .., in the order (K block, ky)
+    // conv 2 of the tile in buffer b: fp16 row h (A, K block kb = its
+    // columns kb * 8 .. + 7) updates output rows max(0, h - 2) .. min(5, h)
+    // with the ky-stacked B block
     auto conv2 = [&](uint32_t b) {
       const uint32_t base = tmem + b * kBufCols;
       if (elect_one()) {
 #pragma unroll
-      for (int r = 0; r < kTailOut; ++r)
-#pragma unroll
         for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-          for (int ky = 0; ky < 3; ++ky)
-              mma_f16_ts(base + static_cast<uint32_t>(r) * kSlot + kC2,
-                         base + static_cast<uint32_t>(r + ky) * kSlot + static_cast<uint32_t>(kb * 8),
-                         w2d + static_cast<uint32_t>(kb) * (kW2Block >> 4) +
-                             static_cast<uint32_t>((2 - ky) * kC2),
-                         i2);
+          for (int h = 0; h < kTailMid; ++h) {
+            const int lo = h - 2 > 0 ? h - 2 : 0;
+            const int hi = h < kTailOut - 1 ? h : kTailOut - 1;
+            mma_f16_ts(base + kC2Col + static_cast<uint32_t>(lo * kC2),
+                       base + mid_col(h) + static_cast<uint32_t>(kb * 8),
+                       w2d + static_cast<uint32_t>(kb) * (kW2Block >> 4) +
+                           static_cast<uint32_t>((2 - h + lo) * kC2),
+                       i2[hi - lo + 1]);
+          }
         mma_commit(&c2full[b]);
       }
       __syncwarp();
@@ -293,7 +303,7 @@ __global__ void __launch_bounds__(kTailThreads, 1)
           const uint64_t adk = ad + static_cast<uint32_t>(kx);
           const uint64_t bdk = bd + static_cast<uint32_t>(kx * 6 * kMidC);
           if (st.r1 == kTailMid) conv1_kx<kTailMid>(d1, adk, bdk, i1);
-          else conv1_kx<kTailMid - 2>(d1, adk, bdk, i1);
+          else conv1_kx<kTailMid - 2>(d1 + 2 * kSlot, adk, bdk, i1);
         }
         if (elect_one()) mma_commit(&empty[s]);
         if (++s == static_cast<uint32_t>(S)) {
@@ -329,9 +339,10 @@ __global__ void __launch_bounds__(kTailThreads, 1)
     named_barrier_sync(1, 32 * (kTailMidWarps + kTailOutWarps));
     if (warp < 2 + kTailMidWarps) {
       // -------- conversion warps: conv-1 row r (image row y0 - 1 + r) ->
-      // ReLU -> fp16 pairs in slot r's columns 0..15 (channel 2c in the low
-      // half of column c), conv-2 bias in columns 16..31 of slots 0..5;
-      // rows 0 and 1 also go to slots 6 and 7 of the next tile's buffer
+      // ReLU -> fp16 pairs at mid_col(r) (channel 2c in the low half of
+      // column c), each row written over columns already read; rows 0 and 1
+      // also go to the next tile's buffer as its rows 6 and 7; then conv 2's
+      // bias
       uint32_t tcount = 0;
       TailWalk w;
       for (w.begin(p); w.valid(p); w.next(p), ++tcount) {
@@ -340,13 +351,14 @@ __global__ void __launch_bounds__(kTailThreads, 1)
         const uint32_t nb = tmem + lane_off + (buf ^ 1u) * kBufCols;
         const TailStep st = w.step(p);
         const int xm = st.x0 - 1 + m;
+        const int sb = st.r1 == kTailMid ? 0 : 2;  // slot of conv-1 row 0
         if (!mbar_wait_bounded(&c1full[buf], (tcount >> 1) & 1u, p.status, kErrTimeoutEpilogue)) break;
         tc_fence_after();
         for (int r2 = 0; r2 < st.r1; r2 += 2) {
           uint32_t v[2][2][16];
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            const uint32_t t0 = tb + static_cast<uint32_t>(r2 + i) * kSlot;
+            const uint32_t t0 = tb + static_cast<uint32_t>(sb + r2 + i) * kSlot;
             tmem_ld16_nowait(t0, v[i][0]);
             tmem_ld16_nowait(t0 + 16, v[i][1]);
           }
@@ -362,16 +374,14 @@ __global__ void __launch_bounds__(kTailThreads, 1)
               h[k] = inside ? pack_half2(fmaxf(__uint_as_float(v[i][k >> 3][2 * (k & 7)]), 0.0f),
                                          fmaxf(__uint_as_float(v[i][k >> 3][2 * (k & 7) + 1]), 0.0f))
                             : 0u;
-            const uint32_t t0 = tb + static_cast<uint32_t>(r) * kSlot;
-            tmem_st16(t0, h);
-            if (r < kTailOut) {
-              uint32_t b2[16];
-              bias16_regs(bias2_s, b2);
-              tmem_st16(t0 + kC2, b2);
-            }
-            if (st.carry && r < 2) tmem_st16(nb + static_cast<uint32_t>(r + kTailOut) * kSlot, h);
+            tmem_st16(tb + mid_col(r), h);
+            if (st.carry && r < 2) tmem_st16(nb + mid_col(r + kTailOut), h);
           }
         }
+        uint32_t b2[16];
+        bias16_regs(bias2_s, b2);
+#pragma unroll
+        for (int r = 0; r < kTailOut; ++r) tmem_st16(tb + kC2Col + static_cast<uint32_t>(r * kC2), b2);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&midready[buf]);
@@ -385,19 +395,17 @@ __global__ void __launch_bounds__(kTailThreads, 1)
       // with the bias for the tile after next (its six new rows, or all
       // eight when it starts a group).
       const int sub = (warp - 2 - kTailMidWarps) >> 2;
-      // conv-1 bias into rows sub, sub + 2, .. < rows of a buffer
-      auto fill_bias1 = [&](uint32_t tb, int rows) {
-        uint32_t b1[2][16];
-        bias16_regs(bias1_s, b1[0]);
-        bias16_regs(bias1_s + 16, b1[1]);
-        for (int r = sub; r < rows; r += kTailSubs) {
-          const uint32_t t0 = tb + static_cast<uint32_t>(r) * kSlot;
-          tmem_st16(t0, b1[0]);
-          tmem_st16(t0 + 16, b1[1]);
-        }
+      // conv-1 bias into slots first .. 7 of a buffer, this warp taking
+      // columns 16 sub .. 16 sub + 15 of each slot (channels 16 sub ..): in
+      // columns 128..223 those hold exactly the conv-2 rows it has read, so
+      // it never overwrites a row the other warp of its quarter still reads
+      auto fill_bias1 = [&](uint32_t tb, int first) {
+        uint32_t b1[16];
+        bias16_regs(bias1_s + 16 * sub, b1);
+        for (int r = first; r < kTailMid; ++r) tmem_st16(tb + static_cast<uint32_t>(r) * kSlot + 16u * sub, b1);
       };
-      fill_bias1(tmem + lane_off, kTailMid);
-      fill_bias1(tmem + lane_off + kBufCols, kTailMid);
+      fill_bias1(tmem + lane_off, 0);
+      fill_bias1(tmem + lane_off + kBufCols, 0);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&c1empty[0]);  // completion 0 of each: conv 1 starts from the bias
@@ -414,7 +422,9 @@ __global__ void __launch_bounds__(kTailThreads, 1)
         const uint32_t tb = tmem + lane_off + buf * kBufCols;
         const TailStep st = w.step(p);
         const int x0 = st.x0, y0 = st.y0;
-        const int refill = w2.valid(p) ? w2.step(p).r1 : 0;
+        // the buffer's next tile accumulates in slots 0..7, or 2..7 when it
+        // takes two carried rows (slots 0 and 1 then hold them)
+        const int refill = !w2.valid(p) ? kTailMid : (w2.step(p).r1 == kTailMid ? 0 : 2);
         // fused output pass: the input colour of this warp's output pixels is
         // loaded before the accumulators are waited for
         const int x = x0 + m;
@@ -433,7 +443,7 @@ __global__ void __launch_bounds__(kTailThreads, 1)
         uint32_t d[kJ2][16];
 #pragma unroll
         for (int j = 0; j < kJ2; ++j)
-          tmem_ld16_nowait(tb + static_cast<uint32_t>(sub + kTailSubs * j) * kSlot + kC2, d[j]);
+          tmem_ld16_nowait(tb + kC2Col + static_cast<uint32_t>((sub + kTailSubs * j) * kC2), d[j]);
         tmem_wait_ld();
         fill_bias1(tb, refill);
         tmem_wait_st();
