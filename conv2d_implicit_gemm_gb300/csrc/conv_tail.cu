@@ -80,6 +80,14 @@ struct TailStep {
   bool carry;
 };
 
+// The output pass of one pixel, out of line: the output warps call it three
+// times per tile row, and inlined copies crowded the instruction cache that
+// the MMA warp shares.
+__device__ __noinline__ float4 tail_output_pixel(float n0, float n1, float n2, float4 col, int hdr,
+                                                 float scale, const float4* exp2_tab) {
+  return output_pixel(n0, n1, n2, col, hdr, scale, exp2_tab);
+}
+
 __device__ __forceinline__ TailStep tail_step(const TailConvParams& p, int sx, int k, int k0, int k1) {
   TailStep st;
   st.x0 = sx * kFinalSpan;
@@ -298,7 +306,9 @@ __global__ void __launch_bounds__(kTailThreads, 1)
         }
         const uint64_t ad = a0 + ((s * p.stage_bytes) >> 4) + o;
         const uint64_t bd = w1d + static_cast<uint32_t>(kb) * (kW1Block >> 4);
-#pragma unroll
+        // (not unrolled: the kernel's four warp roles run different code,
+        // and a smaller MMA loop stays in the instruction cache)
+#pragma unroll 1
         for (int kx = 0; kx < 3; ++kx) {
           const uint64_t adk = ad + static_cast<uint32_t>(kx);
           const uint64_t bdk = bd + static_cast<uint32_t>(kx * 6 * kMidC);
@@ -484,7 +494,7 @@ __global__ void __launch_bounds__(kTailThreads, 1)
               const int xo = x - p.in_x, yo = y - p.in_y;
               if (xo >= 0 && xo < p.ow && yo >= 0 && yo < p.oh) {
                 const size_t oi = static_cast<size_t>(p.oy + yo) * p.out_stride + p.ox + xo;
-                p.out[oi] = output_pixel(n[0], n[1], n[2], col[j], p.hdr, p.scale, p.exp2_tab);
+                p.out[oi] = tail_output_pixel(n[0], n[1], n[2], col[j], p.hdr, p.scale, p.exp2_tab);
               }
             }
           }
