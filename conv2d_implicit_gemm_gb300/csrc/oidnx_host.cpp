@@ -1353,11 +1353,12 @@ oidnx_status build_final_launch(const DeviceLayer& L, const void* src, Extent ex
                         kFinalRows + 2, true, &p.xs);
 }
 
-// dec_conv1b and dec_conv0 as one kernel ("fuseTail", fp16, one image per
-// plan, activations not kept): dec_conv1b's 32-channel map stays in tensor
-// memory.  Not with the fused pairs ("fuseLayers"), which take these layers.
-bool tail_fusable(const oidnx_filter* f, int stack) {
-  if (!f->fuse_tail || f->fuse || f->keep_acts || stack > 1 || f->precision != OIDNX_PRECISION_FP16)
+// dec_conv1b and dec_conv0 as one kernel ("fuseTail", fp16, activations not
+// kept): dec_conv1b's 32-channel map stays in tensor memory.  Stacked tiles
+// run it once per tile.  Not with the fused pairs ("fuseLayers"), which take
+// these layers.
+bool tail_fusable(const oidnx_filter* f) {
+  if (!f->fuse_tail || f->fuse || f->keep_acts || f->precision != OIDNX_PRECISION_FP16)
     return false;
   const DeviceLayer& a = f->layers[kLayers - 2];
   return a.c1 == 0 && a.cout == 32 && a.N == 32 && a.KB0 >= 1 && a.KB0 <= 4 &&
@@ -1549,7 +1550,7 @@ void layout_values(const oidnx_filter* f, int w, int h, bool io_external, bool k
     V->fused[i] = pair_fusable(f, kPairs[i]);
     if (V->fused[i]) V->stored[kPairs[i].first] = false;
   }
-  V->tail = !keep && tail_fusable(f, stack);
+  V->tail = !keep && tail_fusable(f);
   if (V->tail) V->stored[kLayers - 2] = false;
   struct Placed {
     size_t lo, hi;  // byte range (1 KB multiples)
@@ -1645,6 +1646,7 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
       continue;
     }
     if (l == kLayers - 2 && V.tail) {
+      if (stack_rows) break;  // one launch per tile, built by the caller
       const LayerDef& d2 = kDefs[l + 1];
       const DeviceLayer& L2 = f->layers[l + 1];
       LL.tail = 1;
@@ -1749,26 +1751,37 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, int stack, std::unique_p
       },
       stack > 1 ? h : 0));
   if (stack > 1) {
-    // the final conv of each tile reads that tile's rows of dec_conv1b's
-    // output (its own halo rows beyond them read as zeros)
-    const int l = kLayers - 1;
+    // the final conv of each tile (or the fused tail) reads that tile's rows
+    // of its source (its own halo rows beyond them read as zeros, as the
+    // gap rows give the stacked layers)
+    const int l = V.tail ? kLayers - 2 : kLayers - 1;
     const LayerDef& d = kDefs[l];
     const DeviceLayer& L = f->layers[l];
+    const DeviceLayer& L2 = f->layers[kLayers - 1];
     const Extent se = V.ext[d.src0];
     const size_t row_bytes = static_cast<size_t>(act_chunks(f->precision, V.ch[d.src0])) * se.pitch * 16;
+    const int bpe = f->precision == OIDNX_PRECISION_FP16 ? 2 : 4;
     for (int t = 0; t < stack; ++t) {
       LayerLaunch LL;
       std::memset(&LL, 0, sizeof(LL));
       LL.layer = l;
-      LL.name = kLayerNames[l];
-      LL.final = 1;
       const uint8_t* src = static_cast<const uint8_t*>(plan->ptr(d.src0)) +
                            static_cast<size_t>(t) * (h + kStackGap) * row_bytes;
-      OIDNX_TRY(build_final_launch(L, src, Extent{w, h, se.pitch}, w, h, nullptr, f->status, &LL.fcl));
-      LL.fcl.p.reverse = walk_reverse(l);
-      LL.flop = 2.0 * 9.0 * L.cin * L.cout * w * h;
-      LL.bytes = static_cast<double>(w) * h * (V.ch[d.src0] * (f->precision == OIDNX_PRECISION_FP16 ? 2 : 4) + 16) +
-                 static_cast<double>(L.weight_bytes);
+      if (V.tail) {
+        LL.tail = 1;
+        LL.name = "dec_conv1b+dec_conv0";
+        OIDNX_TRY(build_tail_launch(L, L2, src, Extent{w, h, se.pitch}, w, h, nullptr, f->status, &LL.tlcl));
+        LL.flop = 2.0 * 9.0 * (L.cin * L.cout + L2.cin * L2.cout) * w * h;
+        LL.bytes = static_cast<double>(w) * h * (V.ch[d.src0] * bpe + 16) +
+                   static_cast<double>(L.weight_bytes + L2.weight_bytes);
+      } else {
+        LL.name = kLayerNames[l];
+        LL.final = 1;
+        OIDNX_TRY(build_final_launch(L, src, Extent{w, h, se.pitch}, w, h, nullptr, f->status, &LL.fcl));
+        LL.fcl.p.reverse = walk_reverse(l);
+        LL.flop = 2.0 * 9.0 * L.cin * L.cout * w * h;
+        LL.bytes = static_cast<double>(w) * h * (V.ch[d.src0] * bpe + 16) + static_cast<double>(L.weight_bytes);
+      }
       plan->final_tiles.push_back(LL);
     }
   }
@@ -1949,10 +1962,16 @@ oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const
       const AxisTile& tx = f->tx[(g0 + b) % nx];
       const AxisTile& ty = f->ty[(g0 + b) / nx];
       LayerLaunch L = P->final_tiles[b];
-      L.fcl.outpass = 1;
-      L.name = "dec_conv0+output";
-      L.fcl.p.net = nullptr;
-      set_output_pass(f, img, stride, tx, ty, scale, &L.fcl.p);
+      if (L.tail) {
+        L.tlcl.outpass = 1;
+        L.name = "dec_conv1b+dec_conv0+output";
+        set_output_pass(f, img, stride, tx, ty, scale, &L.tlcl.p);
+      } else {
+        L.fcl.outpass = 1;
+        L.name = "dec_conv0+output";
+        L.fcl.p.net = nullptr;
+        set_output_pass(f, img, stride, tx, ty, scale, &L.fcl.p);
+      }
       OIDNX_TRY(run_launch(L, s));
       OIDNX_TRY(prof_mark(f, prof, L.layer, s));
     }
@@ -2646,8 +2665,8 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
     }
   if (plan && plan->stack > 1 && !plan->final_tiles.empty()) {
     const LayerLaunch& L = plan->final_tiles[0];  // per tile, counted per launch
-    add("dec_conv0+output", L.layer + 2, L.flop, L.bytes - tile_px * 16 + out_bytes - out_px / tiles * 16,
-        mma_flop(L));
+    add(L.tail ? "dec_conv1b+dec_conv0+output" : "dec_conv0+output", L.layer + 2, L.flop,
+        L.bytes - tile_px * 16 + out_bytes - out_px / tiles * 16, mma_flop(L));
   }
   add("output", kLayers + 2, 0, out_bytes);
   s += "]}";

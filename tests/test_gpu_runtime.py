@@ -42,12 +42,14 @@ def test_graph_replay_equals_eager_and_host_path(weights):
     assert np.array_equal(graph1.view(np.uint32), graph2.view(np.uint32))
     assert np.array_equal(graph1.view(np.uint32), host_out.view(np.uint32))
     ids = [l["id"] for l in prof["layers"]]
-    # input pass, 15 convs, the final conv with the output pass in its epilogue
-    assert ids[0] == "input-pack" and ids[-1] == "dec_conv0+output" and len(ids) == 17
-    # the 10 tiles are stacked: one input pass and one final conv per tile,
-    # each other conv once over the stack
+    # input pass, 14 convs, then dec_conv1b + dec_conv0 with the output pass
+    # in one kernel (the fused tail)
+    last = "dec_conv1b+dec_conv0+output"
+    assert ids[0] == "input-pack" and ids[-1] == last and len(ids) == 16
+    # the 10 tiles are stacked: one input pass and one tail per tile, each
+    # other conv once over the stack
     for l in prof["layers"]:
-        assert l["launches"] == (10 if l["id"] in ("input-pack", "dec_conv0+output") else 1), l
+        assert l["launches"] == (10 if l["id"] in ("input-pack", last) else 1), l
     assert all(l["ms"] > 0 for l in prof["layers"])
     assert prof["totalMs"] >= sum(l["ms"] for l in prof["layers"]) * 0.99
     # one graph for the bound device images, one for the host path's staging set

@@ -169,3 +169,32 @@ def test_tail_1080p_frame_equals_unfused():
     ref = unet.denoise([im[592:848, 1504:1760] for im in imgs], weights, hdr=True)
     got = outs[0][592 + m:848 - m, 1504 + m:1760 - m, :3]
     assert rel_l2(got, ref[m:-m, m:-m, :3]) <= 2e-2
+
+
+@pytest.mark.parametrize("stack", [0, 3])
+def test_tail_stacked_tiles_equal_unfused(stack):
+    """A frame of several tiles, stacked (one group, or groups of 3 with a
+    short last one): each tile's fused tail reads that tile's rows of
+    dec_conv1a's output, its halo beyond them read as zeros like the gap rows
+    the separate dec_conv1b sees, so the bits equal the separate kernels'."""
+    w, h = 700, 430
+    imgs = synth.denoise_inputs(w, h, 3, hdr=True, nan_fraction=0.02)
+    weights = synth.unet_weights(9, bias_scale=0.05)
+    outs = []
+    for tail in (1, 0):
+        d = Denoiser(weights, ox.PRECISION_FP16, imgs, True, input_scale=0.7, max_tile_size=256, overlap=96)
+        try:
+            ox.oidnx_filter_set_int(d.f, "fuseTail", tail)
+            ox.oidnx_filter_set_int(d.f, "stackTiles", stack)
+            ox.oidnx_filter_commit(d.f)
+            assert ox.oidnx_filter_get_int(d.f, "tiles") > 4
+            assert ox.oidnx_filter_get_int(d.f, "stackedTiles") > 1
+            if tail:
+                ox.oidnx_profile_next(d.f)
+            outs.append(d.run())
+            if tail:
+                ids = [l["id"] for l in ox.oidnx_get_profile(d.f)["layers"]]
+                assert ids[-1] == "dec_conv1b+dec_conv0+output" and "dec_conv1b" not in ids
+        finally:
+            d.close()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
