@@ -19,6 +19,7 @@
 #include <cmath>
 
 #include "internal.h"
+#include "pack.cuh"
 #include "passes.cuh"
 #include "ptx.cuh"
 
@@ -27,29 +28,6 @@ namespace oidnx {
 namespace {
 
 constexpr double kLn2 = 0.69314718055994530942;
-
-// F(s) = log2(1 + s), s in [0, FLT_MAX], correctly rounded to fp16.
-// The float estimate y is within 2^-22 (relative) of F(s): log1pf is within
-// 1 ulp (2^-23), the rounded constant log2(e) and the product add 2^-24
-// each.  y decides the code unless y(1 -+ 1.5 * 2^-22) round differently
-// (the bracket also covers the rounding of those two products).  Then the
-// rounding boundary b between the two candidate codes (exact in float) is
-// compared through the monotone inverse instead: F(s) >= b <=> s >= 2^b - 1,
-// with 2^b - 1 from exp2f/expm1f (a few ulp).  Only when s lies within
-// 2^-18 (relative) of that value is F evaluated in double precision.  The
-// bracket is kept tight because FP64 is slow on this GPU and one lane on
-// the double path holds up its whole warp.
-__device__ __forceinline__ __half hdr_forward_f16(float s) {
-  const float y = log1pf(s) * 1.44269504088896341f;
-  const __half lo = __float2half_rn(y * (1.0f - 0x1.8p-22f));
-  const __half hi = __float2half_rn(y * (1.0f + 0x1.8p-22f));
-  if (__half_as_ushort(lo) == __half_as_ushort(hi)) return lo;
-  const float b = 0.5f * (__half2float(lo) + __half2float(hi));
-  const float c = b < 1.0f ? expm1f(b * 0.693147180559945309f) : exp2f(b) - 1.0f;
-  if (s > c * (1.0f + 0x1p-18f)) return hi;
-  if (s < c * (1.0f - 0x1p-18f)) return lo;
-  return __double2half(log1p(static_cast<double>(s)) / kLn2);
-}
 
 __device__ __forceinline__ float pow2_neg(int k) {  // 2^-k, 0 <= k <= 126
   return __int_as_float((127 - k) << 23);
@@ -160,44 +138,14 @@ __global__ void pack_kernel(const PackParams p) {
   const int iy = min(max(p.ty + ty, 0), p.height - 1);
   constexpr int kCh = 3 * SOURCES;
   float ch[kCh];
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4 c = p.img[0][static_cast<size_t>(iy) * p.stride[0] + ix];
-  if (HDR) {
-    ch[0] = sanitize(__fmul_rn(c.x, p.scale), 0.0f, FLT_MAX);
-    ch[1] = sanitize(__fmul_rn(c.y, p.scale), 0.0f, FLT_MAX);
-    ch[2] = sanitize(__fmul_rn(c.z, p.scale), 0.0f, FLT_MAX);
-  } else {
-    ch[0] = sanitize(c.x, 0.0f, 1.0f);
-    ch[1] = sanitize(c.y, 0.0f, 1.0f);
-    ch[2] = sanitize(c.z, 0.0f, 1.0f);
-  }
-  if (SOURCES > 1) {
-    const float4 a = p.img[1][static_cast<size_t>(iy) * p.stride[1] + ix];
-    ch[3 % kCh] = sanitize(a.x, 0.0f, 1.0f);
-    ch[4 % kCh] = sanitize(a.y, 0.0f, 1.0f);
-    ch[5 % kCh] = sanitize(a.z, 0.0f, 1.0f);
-  }
-  if (SOURCES > 2) {
-    const float4 n = p.img[2][static_cast<size_t>(iy) * p.stride[2] + ix];
-    ch[6 % kCh] = __fadd_rn(__fmul_rn(sanitize(n.x, -1.0f, 1.0f), 0.5f), 0.5f);
-    ch[7 % kCh] = __fadd_rn(__fmul_rn(sanitize(n.y, -1.0f, 1.0f), 0.5f), 0.5f);
-    ch[8 % kCh] = __fadd_rn(__fmul_rn(sanitize(n.z, -1.0f, 1.0f), 0.5f), 0.5f);
-  }
+  const float4 a = SOURCES > 1 ? p.img[1][static_cast<size_t>(iy) * p.stride[1] + ix] : zero;
+  const float4 n = SOURCES > 2 ? p.img[2][static_cast<size_t>(iy) * p.stride[2] + ix] : zero;
+  input_channels<SOURCES, HDR>(c, a, n, p.scale, ch);
   if (FP16) {
-    // 16 lanes = 2 chunks of 8 halves; lanes past 3*SOURCES are zero
     uint32_t w[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      uint32_t pair = 0;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int lane = 2 * k + e;
-        if (lane < kCh) {
-          const __half hv = (HDR && lane < 3) ? hdr_forward_f16(ch[lane]) : __float2half_rn(ch[lane]);
-          pair |= static_cast<uint32_t>(__half_as_ushort(hv)) << (16 * e);
-        }
-      }
-      w[k] = pair;
-    }
+    pack_f16<SOURCES, HDR>(ch, w);
     uint4* out = static_cast<uint4*>(p.out);
     out[pixel] = make_uint4(w[0], w[1], w[2], w[3]);
     out[pixel + p.pitch] = make_uint4(w[4], w[5], w[6], w[7]);

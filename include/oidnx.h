@@ -106,13 +106,13 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *                        on GB300 the separate kernels are faster (the MMAs
  *                        of these layers are bound by shared-memory operand
  *                        reads, which fusion does not reduce)
- *   "fuseTail"           1 = with fp16 storage and a frame of one tile,
- *                        dec_conv1b and dec_conv0 (and the output pass when
- *                        "fuseOutput" is 1) run as one kernel: dec_conv1b's
- *                        32-channel map stays in tensor memory and is never
- *                        stored; the results equal the separate kernels' bit
- *                        for bit (default).  Off with keepActivations or
- *                        fuseLayers 1.
+ *   "fuseTail"           1 = with fp16 storage, dec_conv1b and dec_conv0 (and
+ *                        the output pass when "fuseOutput" is 1) run as one
+ *                        kernel, once per tile of a stacked frame:
+ *                        dec_conv1b's 32-channel map stays in tensor memory
+ *                        and is never stored; the results equal the
+ *                        separate kernels' bit for bit (default).  Off with
+ *                        keepActivations or fuseLayers 1.
  *   "stackTiles"         frames of several equal tiles stack them: each conv
  *                        runs once over a group of tiles (zero rows between
  *                        them), the input pass and the final conv per tile.
