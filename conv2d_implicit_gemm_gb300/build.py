@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liboidnx.so")
 SOURCES = ["oidnx_host.cpp", "conv_tc.cu", "conv_pair.cu", "conv_final.cu", "conv_tail.cu",
-           "io_passes.cu", "noalloc.cu"]
+           "conv_head.cu", "io_passes.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

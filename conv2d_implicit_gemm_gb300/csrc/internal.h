@@ -231,6 +231,44 @@ struct TailConvLaunch {
 cudaError_t launch_conv_tail(const TailConvLaunch& L, cudaStream_t stream);
 cudaError_t conv_tail_set_smem_limit(size_t bytes);
 
+// The input pass and enc_conv0 (16 input lanes -> 32, bias + ReLU) in one
+// kernel, fp16 storage: conv tiles of kHeadRows rows x 128 pixels whose
+// packed input halo is computed in shared memory from TMA-staged boxes of
+// the source images.  Writes enc_conv0's output and the packed input's
+// column-parity copy (not the plain packed input).
+constexpr int kHeadRows = 8;
+
+struct HeadParams {
+  // input pass (as PackParams)
+  int sources;             // 1..3
+  int width, height;       // image extent
+  int tx, ty, tw, th;      // tile input rect (= enc_conv0's extent)
+  int hdr;
+  float scale;
+  // outputs
+  void* split;             // packed input, column-parity copy [th][2][2][split_pitch/2][8]
+  int split_pitch;
+  __half* out;             // enc_conv0 output [th][4][pitch][8]; columns [tw, pitch) zero
+  int pitch;
+  // enc_conv0
+  const __half* weights;   // B operand, one K block: [kx][2][3 x 32][8]
+  const float* bias;       // [32]
+  int* status;
+  int tiles_x, tiles_y;    // tiles of kHeadRows rows x 128 pixels
+  int SI, SA;              // image stages, packed-input stages
+  uint32_t img_stage, a_stage;  // their bytes
+};
+
+struct HeadLaunch {
+  CUtensorMap map[3];      // colour, albedo, normal: float4 pixels, boxes of kHeadRows + 2 rows x 130
+  HeadParams p;
+  dim3 grid;
+  size_t smem;
+};
+
+cudaError_t launch_conv_head(const HeadLaunch& L, cudaStream_t stream);
+cudaError_t conv_head_set_smem_limit(size_t bytes);
+
 struct TcConvLaunch {
   CUtensorMap map0;        // source 0 (full-res halo box, or low-res box)
   CUtensorMap map1;        // source 1 (full-res halo box, or stride-2 box); unused if KB1 == 0

@@ -694,6 +694,24 @@ oidnx_status encode_split_map(CUtensorMap* map, const void* base, int W, int pit
 // ======================================================================
 // device-side model and plans
 // ======================================================================
+// A float4 image [height][width] with row stride `stride` bytes as a 2-D
+// tensor {4 * width floats, height}; boxes of kHeadRows + 2 rows x 176
+// floats (44 pixels): the fused input pass stages 132 pixels as three.
+oidnx_status encode_image_map(CUtensorMap* map, const void* base, int width, int height, size_t stride) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[2] = {4 * static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(height)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride)};
+  cuuint32_t box[2] = {4 * 44, static_cast<cuuint32_t>(kHeadRows + 2)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(OIDNX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a %dx%d image", int(r), width, height);
+  return ok();
+}
+
 struct DeviceLayer {
   int cout = 0, cin = 0, c0 = 0, c1 = 0;
   // B operands, each fp16 or (fp32 storage) tf32 hi/lo
@@ -765,6 +783,11 @@ struct Plan {
   bool out_stored = true;
   // the last execution ran the output pass in the last conv's epilogue
   bool outpass_fused = false;
+  // one-tile-at-a-time frames: the input pass and enc_conv0 as one kernel
+  // (head: built when the plan allows it; head_used: the last execution
+  // ran it)
+  bool head_on = false, head_used = false;
+  HeadLaunch head;
   uint64_t last_used = 0;
   cudaEvent_t done = nullptr;  // recorded after each use
   bool used = false;
@@ -793,7 +816,7 @@ struct oidnx_filter {
   // parameters
   int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
       overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 1,
-      fuse = 0, fuse_output = 1, fuse_tail = 1, stack_tiles = 0;
+      fuse = 0, fuse_output = 1, fuse_tail = 1, fuse_input = 0, stack_tiles = 0;
   float input_scale = 1.0f;
   void* img[4] = {};
   size_t img_stride[4] = {};
@@ -934,7 +957,7 @@ int act_chunks(int precision, int c) {
 constexpr int kMaxDevices = 64;
 std::mutex g_device_mutex;
 int g_num_sms[kMaxDevices] = {};
-uint64_t g_smem_limit_set[4] = {};  // per kernel family: bit d for device d
+uint64_t g_smem_limit_set[5] = {};  // per kernel family: bit d for device d
 
 int current_device() {
   int dev = 0;
@@ -953,7 +976,7 @@ int num_sms() {
   return n;
 }
 
-enum KernelFamily { kFamilyTc = 0, kFamilyPair = 1, kFamilyFinal = 2, kFamilyTail = 3 };
+enum KernelFamily { kFamilyTc = 0, kFamilyPair = 1, kFamilyFinal = 2, kFamilyTail = 3, kFamilyHead = 4 };
 
 // Raise a kernel family's dynamic shared-memory limit to the 227 KB an SM
 // offers, on the current device.
@@ -966,7 +989,8 @@ oidnx_status ensure_smem_limit(int family) {
   const cudaError_t e = family == kFamilyTc      ? conv_tc_set_smem_limit(max_smem)
                         : family == kFamilyPair  ? conv_pair_set_smem_limit(max_smem)
                         : family == kFamilyFinal ? conv_final_set_smem_limit(max_smem)
-                                                 : conv_tail_set_smem_limit(max_smem);
+                        : family == kFamilyTail  ? conv_tail_set_smem_limit(max_smem)
+                                                 : conv_head_set_smem_limit(max_smem);
   if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "smem limit: %s", cudaGetErrorString(e));
   g_smem_limit_set[family] |= bit;
   return ok();
@@ -1424,6 +1448,56 @@ oidnx_status build_tail_launch(const DeviceLayer& A, const DeviceLayer& B, const
                         &p.xs);
 }
 
+// The input pass and enc_conv0 as one kernel ("fuseInput", off by default:
+// inside the replayed graph it is not faster; fp16, frames run
+// one tile at a time, activations not kept, the sub-pixel dec_conv1a
+// reading the packed input's column-parity copy): the plain packed input is
+// then neither written nor read.
+bool head_fusable(const oidnx_filter* f) {
+  if (!f->fuse_input || f->keep_acts || f->precision != OIDNX_PRECISION_FP16) return false;
+  const DeviceLayer& L = f->layers[0];
+  return L.c1 == 0 && L.KB0 == 1 && L.N == 32 && L.cout == 32 && L.wtc != nullptr;
+}
+
+// The head launch over a W x H tile: enc_conv0's weights and the value
+// buffers; the tile's image fields are filled per tile when it is enqueued.
+oidnx_status build_head_launch(const DeviceLayer& L, int W, int H, void* out, int pitch, void* split,
+                               int split_pitch, int* status, HeadLaunch* T) {
+  HeadParams& p = T->p;
+  std::memset(&p, 0, sizeof(p));
+  p.weights = static_cast<const __half*>(L.wtc);
+  p.bias = L.bias;
+  p.status = status;
+  p.out = static_cast<__half*>(out);
+  p.pitch = pitch;
+  p.split = split;
+  p.split_pitch = split_pitch;
+  p.tw = W;
+  p.th = H;
+  p.tiles_x = (W + kTileM - 1) / kTileM;
+  p.tiles_y = (H + kHeadRows - 1) / kHeadRows;
+  // image stage: per image kHeadRows + 2 rows x 132 float4 pixels (three
+  // boxes of 44); packed stage: kHeadRows + 2 halo rows x 2 halves
+  // x 130 pixels x 16 bytes
+  const size_t img_box = static_cast<size_t>(kHeadRows + 2) * 3 * 44 * 16;  // 132 pixels
+  p.img_stage = static_cast<uint32_t>(3 * img_box);
+  p.a_stage = static_cast<uint32_t>(round_up_sz((kHeadRows + 2) * 2 * (kTileM + 2) * kChunkBytes, 128));
+  p.SI = 2;
+  p.SA = 2;
+  // alignment slack, stages, weights (one K block), bias, 6 barriers + 2
+  // per stage, the TMEM address
+  const size_t smem = 128 + static_cast<size_t>(p.SI) * p.img_stage + static_cast<size_t>(p.SA) * p.a_stage +
+                      3 * 2 * 3 * 32 * kChunkBytes + 32 * 4 + (6 + 2 * p.SI + 2 * p.SA) * 8 + 16;
+  if (smem > 227 * 1024) return fail(OIDNX_ERR_UNSUPPORTED, "input conv stages do not fit");
+  // one CTA per SM (it allocates all 512 TMEM columns): more than half the
+  // shared memory of an SM
+  T->smem = std::max<size_t>(smem, 120 * 1024);
+  OIDNX_TRY(ensure_smem_limit(kFamilyHead));
+  const long tiles = static_cast<long>(p.tiles_x) * p.tiles_y;
+  T->grid = dim3(static_cast<unsigned>(std::min<long>(tiles, num_sms())), 1, 1);
+  return ok();
+}
+
 oidnx_status run_launch(const LayerLaunch& L, cudaStream_t s) {
   (void)cudaGetLastError();  // drop a stale, non-sticky error of an earlier call
   if (L.final) {
@@ -1750,6 +1824,12 @@ oidnx_status create_plan(oidnx_filter* f, int w, int h, int stack, std::unique_p
         return ok();
       },
       stack > 1 ? h : 0));
+  if (stack == 1 && V.split_on[0] && head_fusable(f)) {
+    const LayerDef& d = kDefs[0];
+    OIDNX_TRY(build_head_launch(f->layers[0], V.lvl[0].w, V.lvl[0].h, plan->ptr(d.dst), V.ext[d.dst].pitch,
+                                plan->ptr(V_INS), V.ext[V_INS].pitch, f->status, &plan->head));
+    plan->head_on = true;
+  }
   if (stack > 1) {
     // the final conv of each tile (or the fused tail) reads that tile's rows
     // of its source (its own halo rows beyond them read as zeros, as the
@@ -1978,6 +2058,7 @@ oidnx_status enqueue_stacked(oidnx_filter* f, Plan* P, void* const img[4], const
   }
   P->out_stored = false;
   P->outpass_fused = true;
+  P->head_used = false;
   return ok();
 }
 
@@ -1989,17 +2070,37 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
   OIDNX_TRY(prof_mark(f, prof, -2, s));
   if (P->stack > 1) return enqueue_stacked(f, P, img, stride, scale, prof, s);
   P->outpass_fused = output_fused(f, P);
+  P->head_used = P->head_on;
+  // with the head kernel the plan's enc_conv0 launch is skipped
+  const size_t first = P->head_used ? 1 : 0;
   for (const AxisTile& ty : f->ty)
     for (const AxisTile& tx : f->tx) {
       PackParams pp = tile_pack_params(f, P, img, stride, tx, ty, scale, P->ptr(V_IN),
                                        P->split_on[0] ? P->ptr(V_INS) : nullptr);
       (void)cudaGetLastError();
-      cudaError_t e = launch_pack(pp, s);
-      if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
-      OIDNX_TRY(prof_mark(f, prof, -1, s));
+      if (P->head_used) {
+        HeadLaunch H = P->head;
+        for (int i = 0; i < 3; ++i)
+          OIDNX_TRY(encode_image_map(&H.map[i], img[i < pp.sources ? i : 0], f->width, f->height,
+                                     stride[i < pp.sources ? i : 0]));
+        H.p.sources = pp.sources;
+        H.p.width = pp.width;
+        H.p.height = pp.height;
+        H.p.tx = pp.tx;
+        H.p.ty = pp.ty;
+        H.p.hdr = pp.hdr;
+        H.p.scale = pp.scale;
+        cudaError_t e = launch_conv_head(H, s);
+        if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass + enc_conv0: %s", cudaGetErrorString(e));
+        OIDNX_TRY(prof_mark(f, prof, 0, s));
+      } else {
+        cudaError_t e = launch_pack(pp, s);
+        if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "input pass: %s", cudaGetErrorString(e));
+        OIDNX_TRY(prof_mark(f, prof, -1, s));
+      }
       if (output_fused(f, P)) {
         // the final conv's epilogue runs the output pass for this tile
-        for (size_t i = 0; i + 1 < P->launches.size(); ++i) {
+        for (size_t i = first; i + 1 < P->launches.size(); ++i) {
           OIDNX_TRY(run_launch(P->launches[i], s));
           OIDNX_TRY(prof_mark(f, prof, P->launches[i].layer, s));
         }
@@ -2021,7 +2122,10 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
         OIDNX_TRY(prof_mark(f, prof, L.layer, s));
         continue;
       }
-      OIDNX_TRY(enqueue_network(f, P, prof, s));
+      for (size_t i = first; i < P->launches.size(); ++i) {
+        OIDNX_TRY(run_launch(P->launches[i], s));
+        OIDNX_TRY(prof_mark(f, prof, P->launches[i].layer, s));
+      }
       P->out_stored = true;
       UnpackParams up;
       std::memset(&up, 0, sizeof(up));
@@ -2040,7 +2144,7 @@ oidnx_status enqueue_denoise(oidnx_filter* f, void* const img[4], const size_t s
       up.hdr = f->hdr;
       up.scale = scale;
       up.exp2_tab = static_cast<const float4*>(f->exp2_tab);
-      e = launch_unpack(up, s);
+      cudaError_t e = launch_unpack(up, s);
       if (e != cudaSuccess) return fail(OIDNX_ERR_CUDA, "output pass: %s", cudaGetErrorString(e));
       OIDNX_TRY(prof_mark(f, prof, kLayers, s));
     }
@@ -2316,11 +2420,12 @@ oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value) 
     if (value < 0) return fail(OIDNX_ERR_INVALID_ARGUMENT, "stackTiles must be >= 0");
     f->stack_tiles = value;
   } else if (n == "keepActivations" || n == "subpixelDecoder" || n == "fuseLayers" ||
-             n == "fuseTail") {
+             n == "fuseTail" || n == "fuseInput") {
     (n == "keepActivations"   ? f->keep_acts
      : n == "subpixelDecoder" ? f->subpixel
      : n == "fuseLayers"      ? f->fuse
-                              : f->fuse_tail) = value ? 1 : 0;
+     : n == "fuseTail"        ? f->fuse_tail
+                              : f->fuse_input) = value ? 1 : 0;
     for (auto& p : f->plans) f->retired.push_back(std::move(p));
     f->plans.clear();
     f->current = nullptr;
@@ -2352,6 +2457,7 @@ oidnx_status oidnx_filter_get_int(oidnx_filter* f, const char* name, int* value)
   else if (n == "fuseLayers") *value = f->fuse;
   else if (n == "fuseOutput") *value = f->fuse_output;
   else if (n == "fuseTail") *value = f->fuse_tail;
+  else if (n == "fuseInput") *value = f->fuse_input;
   else if (n == "stackTiles") *value = f->stack_tiles;
   else if (n == "stackedTiles") *value = f->committed && f->current ? f->current->stack : 0;
   else if (n == "profile") *value = f->profile_always;
@@ -2536,6 +2642,7 @@ oidnx_status oidnx_network_execute(oidnx_filter* f, const void* packed_in, int w
   }
   P->out_stored = true;
   P->outpass_fused = false;
+  P->head_used = false;
   OIDNX_TRY(prof_mark(f, prof, -2, s));
   OIDNX_TRY(enqueue_network(f, P, prof, s));
   OIDNX_CUDA(cudaMemcpyAsync(out, P->ptr(V_OUT), P->value_bytes[V_OUT], cudaMemcpyDeviceToDevice, s));
@@ -2654,6 +2761,17 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
   const double out_bytes = out_px / tiles * 48.0;  // per tile: net + colour read, image written
   if (plan)
     for (const LayerLaunch& L : plan->launches) {
+      if (&L == &plan->launches[0] && plan->head_used) {
+        // the input pass and enc_conv0 ran as one kernel: the images read
+        // once, the packed input's parity copy and enc_conv0's output
+        // written once; its MMAs: per tile of kHeadRows rows, 3 kx x 3 ky
+        // row updates of N = 32 per row
+        const HeadParams& h = plan->head.p;
+        const double mma = static_cast<double>(h.tiles_x) * h.tiles_y * 3.0 * 3 * kHeadRows * 32 * 128 * 16 * 2;
+        add("input-pack+enc_conv0", L.layer + 2, L.flop,
+            tile_px * (16.0 * sources + 2 * 16 + 2.0 * 32) + static_cast<double>(f->layers[0].weight_bytes), mma);
+        continue;
+      }
       const bool fused_out =
           &L == &plan->launches.back() && plan->outpass_fused && (L.final || L.tail);
       // with the output pass fused the network output is not stored: the

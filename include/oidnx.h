@@ -106,6 +106,14 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *                        on GB300 the separate kernels are faster (the MMAs
  *                        of these layers are bound by shared-memory operand
  *                        reads, which fusion does not reduce)
+ *   "fuseInput"          1 = with fp16 storage, frames run one tile at a time
+ *                        and the sub-pixel dec_conv1a, the input pass runs
+ *                        inside enc_conv0's kernel: the packed input is
+ *                        built in shared memory from the source images and
+ *                        only its column-parity copy is stored; the results
+ *                        equal the separate kernels' bit for bit.  Default
+ *                        0 (on GB300 the separate kernels, which overlap
+ *                        each other, are as fast).  Off with keepActivations.
  *   "fuseTail"           1 = with fp16 storage, dec_conv1b and dec_conv0 (and
  *                        the output pass when "fuseOutput" is 1) run as one
  *                        kernel, once per tile of a stacked frame:
