@@ -828,12 +828,14 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
               }
               if (p.out_split && xp < p.split_pitch) {
                 // plane xp & 1, index xp >> 1 (the split pitch is even)
+                // (read by a decoder only: evict-first)
                 __half* o2 = static_cast<__half*>(p.out_split);
                 const size_t s0 =
                     ((((static_cast<size_t>(yp) * C8 + 2 * c) * 2 + (xp & 1)) * (p.split_pitch >> 1)) + (xp >> 1)) * 8;
                 const size_t s1 = s0 + static_cast<size_t>(p.split_pitch) * 8;
-                *reinterpret_cast<uint4*>(o2 + s0) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(o2 + s1) = make_uint4(h[4], h[5], h[6], h[7]);
+                const uint64_t pol = l2_evict_first();
+                st_global_hint(o2 + s0, make_uint4(h[0], h[1], h[2], h[3]), pol);
+                st_global_hint(o2 + s1, make_uint4(h[4], h[5], h[6], h[7]), pol);
               }
             }
           }

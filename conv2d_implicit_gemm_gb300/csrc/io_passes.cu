@@ -139,9 +139,12 @@ __global__ void pack_kernel(const PackParams p) {
   constexpr int kCh = 3 * SOURCES;
   float ch[kCh];
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4 c = p.img[0][static_cast<size_t>(iy) * p.stride[0] + ix];
-  const float4 a = SOURCES > 1 ? p.img[1][static_cast<size_t>(iy) * p.stride[1] + ix] : zero;
-  const float4 n = SOURCES > 2 ? p.img[2][static_cast<size_t>(iy) * p.stride[2] + ix] : zero;
+  // the images are read once here (the output pass re-reads only the colour,
+  // at the end of the step)
+  const uint64_t pol = l2_evict_first();
+  const float4 c = ld_global_hint(p.img[0] + static_cast<size_t>(iy) * p.stride[0] + ix, pol);
+  const float4 a = SOURCES > 1 ? ld_global_hint(p.img[1] + static_cast<size_t>(iy) * p.stride[1] + ix, pol) : zero;
+  const float4 n = SOURCES > 2 ? ld_global_hint(p.img[2] + static_cast<size_t>(iy) * p.stride[2] + ix, pol) : zero;
   input_channels<SOURCES, HDR>(c, a, n, p.scale, ch);
   if (FP16) {
     uint32_t w[8];
@@ -150,12 +153,13 @@ __global__ void pack_kernel(const PackParams p) {
     out[pixel] = make_uint4(w[0], w[1], w[2], w[3]);
     out[pixel + p.pitch] = make_uint4(w[4], w[5], w[6], w[7]);
     if (p.out_split) {
-      // column-parity split copy: plane tx & 1, index tx >> 1
+      // column-parity split copy: plane tx & 1, index tx >> 1 (read by the
+      // last decoder only: evict-first)
       uint4* o2 = static_cast<uint4*>(p.out_split);
       const size_t half = static_cast<size_t>(p.split_pitch) >> 1;
       const size_t s0 = (static_cast<size_t>(ty) * p.chunks * 2 + (tx & 1)) * half + (tx >> 1);
-      o2[s0] = make_uint4(w[0], w[1], w[2], w[3]);
-      o2[s0 + 2 * half] = make_uint4(w[4], w[5], w[6], w[7]);
+      st_global_hint(o2 + s0, make_uint4(w[0], w[1], w[2], w[3]), pol);
+      st_global_hint(o2 + s0 + 2 * half, make_uint4(w[4], w[5], w[6], w[7]), pol);
     }
   } else {
     float v[12];
