@@ -174,15 +174,15 @@ __device__ __forceinline__ void issue_kblock_r(int R, uint64_t ad, uint64_t bd, 
                                                uint32_t N, uint32_t kx_b16, uint32_t id1,
                                                uint32_t id2, uint32_t id3, uint32_t alo16,
                                                uint32_t blo16) {
-  if (!TF) {
+  if constexpr (!TF) {
     issue_kblock_r1<G, TF>(R, ad, bd, dbase, N, kx_b16, id1, id2, id3);
-    return;
-  }
+  } else {
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const uint64_t a = ad + (pass == 2 ? alo16 : 0u);
-    const uint64_t b = bd + (pass == 1 ? blo16 : 0u);
-    issue_kblock_r1<G, TF>(R, a, b, dbase, N, kx_b16, id1, id2, id3);
+    for (int pass = 0; pass < 3; ++pass) {
+      const uint64_t a = ad + (pass == 2 ? alo16 : 0u);
+      const uint64_t b = bd + (pass == 1 ? blo16 : 0u);
+      issue_kblock_r1<G, TF>(R, a, b, dbase, N, kx_b16, id1, id2, id3);
+    }
   }
 }
 
@@ -267,6 +267,17 @@ __device__ __forceinline__ void issue_subpixel_item(int R, bool up, uint64_t ad,
   }
 }
 
+// One sub-pixel item of a compile-time shape SPEC = 100 + 10 R + G4 (every
+// walk step a whole tile of R rows).
+template <int SPEC, bool TF>
+__device__ __forceinline__ void issue_subpixel_spec(bool up, uint64_t ad, uint64_t bd, uint32_t dbase,
+                                                    uint32_t N, int px, int pxb, uint32_t row16,
+                                                    uint32_t id1, uint32_t id2, uint32_t id3,
+                                                    uint32_t id4) {
+  constexpr int SR = (SPEC - 100) / 10, SG4 = SPEC % 10, SG3 = SG4 < 3 ? SG4 : 3;
+  issue_subpixel_r<SR, SG4, SG3, TF>(up, ad, bd, dbase, N, px, pxb, row16, id1, id2, id3, id4);
+}
+
 // One sub-pixel item with the row grouping G4 = min(4, 256 / N) (upsampled
 // part; the skip part groups min(3, G4) rows).
 template <bool TF>
@@ -281,7 +292,18 @@ __device__ __forceinline__ void issue_subpixel_g(int g4, int R, bool up, uint64_
 
 }  // namespace
 
-template <int KIND>
+// SPEC fixes the issue sequence at compile time for the common shapes, so
+// that the MMA warp's loop holds one or two unrolled sequences instead of one
+// per (rows, grouping) pair: 0 = chosen at run time; 10 R + G = plain tiles
+// of R rows (R / 2 in a last wave split in two), G rows stacked per MMA;
+// 100 + 10 R + G = sub-pixel tiles of R rows (no split), G row classes
+// stacked.  (A smaller MMA loop is an instruction-cache matter: the 1080p
+// step went from 494 to 478 us.)
+constexpr int kSpecAny = 0;
+constexpr int spec_plain(int r, int g) { return 10 * r + g; }
+constexpr int spec_sub(int r, int g) { return 100 + 10 * r + g; }
+
+template <int KIND, int SPEC>
 __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTcThreads, 1)
     conv3x3_tc_kernel(const __grid_constant__ CUtensorMap map0,
                       const __grid_constant__ CUtensorMap map1, const TcConvParams p) {
@@ -542,7 +564,10 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
                 for (int jj = 0; jj < nkb; ++jj) {
                   const uint64_t adj = ap + static_cast<uint32_t>(jj * 2 * kHaloW);
                   const uint64_t bdj = bp + static_cast<uint32_t>(jj) * (half >> 4);
-                  issue_subpixel_g<TF>(g4, R, true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
+                  if constexpr (SPEC >= 100)
+                    issue_subpixel_spec<SPEC, TF>(true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
+                  else
+                    issue_subpixel_g<TF>(g4, R, true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
                 }
               }
               if (elect_one()) mma_commit(&empty[s]);
@@ -564,18 +589,32 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
             const uint64_t bd = b_sk0 + (woff >> 4);
             const uint32_t row16 = static_cast<uint32_t>(2 * kHaloW);
 #pragma unroll 1
-            for (int pass = 0; pass < kPasses; ++pass)
-              issue_subpixel_g<TF>(g4, R, false, ad + (pass == 2 ? alo16 : 0u),
-                                   bd + (pass == 1 ? blo_sk16 : 0u), d_base, N, tpx, pxb, row16, id1,
-                                   id2, id3, id4);
+            for (int pass = 0; pass < kPasses; ++pass) {
+              if constexpr (SPEC >= 100)
+                issue_subpixel_spec<SPEC, TF>(false, ad + (pass == 2 ? alo16 : 0u),
+                                              bd + (pass == 1 ? blo_sk16 : 0u), d_base, N, tpx, pxb,
+                                              row16, id1, id2, id3, id4);
+              else
+                issue_subpixel_g<TF>(g4, R, false, ad + (pass == 2 ? alo16 : 0u),
+                                     bd + (pass == 1 ? blo_sk16 : 0u), d_base, N, tpx, pxb, row16, id1,
+                                     id2, id3, id4);
+            }
             if (elect_one()) mma_commit(&empty[s]);
             continue;
           }
           const uint64_t ad = a_desc0 + ((s * p.a_stage) >> 4);
           const uint64_t bd = b_desc0 + ((static_cast<uint32_t>(p.resident ? kb : s) * p.b_stage) >> 4);
-          if (g == 3) issue_kblock_r<3, TF>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, alo16, blo16);
-          else if (g == 2) issue_kblock_r<2, TF>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, alo16, blo16);
-          else issue_kblock_r<1, TF>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, alo16, blo16);
+          if constexpr (SPEC > 0 && SPEC < 100) {
+            constexpr int SR = SPEC / 10, SG = SPEC % 10;
+            if (R == SR) issue_kblock<SR, SG, TF>(ad, bd, d_base, N, kx_b16, id1, id2, id3);
+            else issue_kblock<(SR > 1 ? SR / 2 : 1), SG, TF>(ad, bd, d_base, N, kx_b16, id1, id2, id3);
+          } else if (g == 3) {
+            issue_kblock_r<3, TF>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, alo16, blo16);
+          } else if (g == 2) {
+            issue_kblock_r<2, TF>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, alo16, blo16);
+          } else {
+            issue_kblock_r<1, TF>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, alo16, blo16);
+          }
           if (elect_one()) mma_commit(&empty[s]);
         }
         if (!ok) break;
@@ -875,50 +914,92 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
   }
 }
 
-cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
-  if (L.kind == kTcPlain32)
-    return launch_pdl(conv3x3_tc_kernel<kTcPlain32>, L.grid, dim3(kTcThreadsDecoder), L.smem,
-                      stream, L.map0, L.map1, L.p);
-  if (L.kind == kTcExpand32)
-    return launch_pdl(conv3x3_tc_kernel<kTcExpand32>, L.grid, dim3(kTcThreadsDecoder), L.smem,
-                      stream, L.map0, L.map1, L.p);
-  if (L.kind == kTcExpand)
-    return launch_pdl(conv3x3_tc_kernel<kTcExpand>, L.grid, dim3(kTcThreadsDecoder), L.smem,
-                      stream, L.map0, L.map1, L.p);
-  if (L.kind == kTcSubpixel)
-    return launch_pdl(conv3x3_tc_kernel<kTcSubpixel>, L.grid, dim3(kTcThreads), L.smem, stream,
-                      L.map0, L.map1, L.p);
-  if (L.kind == kTcSubpixel32)
-    return launch_pdl(conv3x3_tc_kernel<kTcSubpixel32>, L.grid, dim3(kTcThreadsDecoder), L.smem,
-                      stream, L.map0, L.map1, L.p);
-  return launch_pdl(conv3x3_tc_kernel<kTcPlain>, L.grid, dim3(kTcThreads), L.smem, stream, L.map0,
+namespace {
+
+// The compile-time shapes instantiated for the fp16 kinds (the shapes of
+// the 1080p and 4K U-Net layers); other shapes run the run-time form.
+template <int KIND, int SPEC>
+cudaError_t launch_tc(const TcConvLaunch& L, cudaStream_t stream) {
+  return launch_pdl(conv3x3_tc_kernel<KIND, SPEC>, L.grid,
+                    dim3(kind_helpers<KIND>() ? kTcThreadsDecoder : kTcThreads), L.smem, stream, L.map0,
                     L.map1, L.p);
 }
 
+#define OIDNX_PLAIN_SPECS(X) X(8, 3) X(4, 3) X(2, 3) X(2, 2) X(1, 2) X(1, 3)
+#define OIDNX_SUB_SPECS(X) X(4, 4) X(2, 2)
+
+// The spec of a launch: its tile rows and the stacking factor, when every
+// walk step has those rows or half of them.
+int tc_spec(const TcConvLaunch& L) {
+  const TcConvParams& p = L.p;
+  if (L.kind == kTcSubpixel) {
+    const int g4 = std::min(4, 256 / p.N);
+    // (a split last wave runs the run-time form: dec_conv2a at 1080p, whose
+    // split tiles took 54.9 us specialised against 53.0)
+    const bool steps = p.tail_split == 1;
+#define X(r, g) if (steps && p.R == r && g4 == g) return spec_sub(r, g);
+    OIDNX_SUB_SPECS(X)
+#undef X
+    return kSpecAny;
+  }
+  if (L.kind == kTcPlain) {
+    const int g = std::min(3, 256 / p.N);
+    if (p.tail_split > 2) return kSpecAny;
+#define X(r, gg) if (p.R == r && g == gg) return spec_plain(r, gg);
+    OIDNX_PLAIN_SPECS(X)
+#undef X
+  }
+  return kSpecAny;
+}
+
+}  // namespace
+
+cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
+  const int spec = tc_spec(L);
+  switch (L.kind) {
+    case kTcPlain32: return launch_tc<kTcPlain32, kSpecAny>(L, stream);
+    case kTcExpand32: return launch_tc<kTcExpand32, kSpecAny>(L, stream);
+    case kTcExpand: return launch_tc<kTcExpand, kSpecAny>(L, stream);
+    case kTcSubpixel32: return launch_tc<kTcSubpixel32, kSpecAny>(L, stream);
+    case kTcSubpixel:
+#define X(r, g) if (spec == spec_sub(r, g)) return launch_tc<kTcSubpixel, spec_sub(r, g)>(L, stream);
+      OIDNX_SUB_SPECS(X)
+#undef X
+      return launch_tc<kTcSubpixel, kSpecAny>(L, stream);
+    default:
+#define X(r, g) if (spec == spec_plain(r, g)) return launch_tc<kTcPlain, spec_plain(r, g)>(L, stream);
+      OIDNX_PLAIN_SPECS(X)
+#undef X
+      return launch_tc<kTcPlain, kSpecAny>(L, stream);
+  }
+}
+
 cudaError_t conv_tc_set_smem_limit(size_t bytes) {
-  cudaError_t e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcExpand>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bytes));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcSubpixel>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcPlain32>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcExpand32>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(conv3x3_tc_kernel<kTcSubpixel32>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(conv3x3_tc_kernel<kTcPlain>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  const int b = static_cast<int>(bytes);
+  const void* fns[] = {
+      reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcExpand, kSpecAny>),
+      reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcSubpixel, kSpecAny>),
+      reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcPlain32, kSpecAny>),
+      reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcExpand32, kSpecAny>),
+      reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcSubpixel32, kSpecAny>),
+      reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcPlain, kSpecAny>),
+#define X(r, g) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcPlain, spec_plain(r, g)>),
+      OIDNX_PLAIN_SPECS(X)
+#undef X
+#define X(r, g) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcSubpixel, spec_sub(r, g)>),
+      OIDNX_SUB_SPECS(X)
+#undef X
+  };
+  for (const void* fn : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t conv_tc_occupancy(size_t smem, int* blocks_per_sm) {
   // the plain variant has fewer threads and so the higher occupancy bound
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, conv3x3_tc_kernel<kTcPlain>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, conv3x3_tc_kernel<kTcPlain, kSpecAny>,
                                                        kTcThreads, smem);
 }
 
