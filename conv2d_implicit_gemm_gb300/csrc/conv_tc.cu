@@ -606,8 +606,14 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
           const uint64_t bd = b_desc0 + ((static_cast<uint32_t>(p.resident ? kb : s) * p.b_stage) >> 4);
           if constexpr (SPEC > 0 && SPEC < 100) {
             constexpr int SR = SPEC / 10, SG = SPEC % 10;
-            if (R == SR) issue_kblock<SR, SG, TF>(ad, bd, d_base, N, kx_b16, id1, id2, id3);
-            else issue_kblock<(SR > 1 ? SR / 2 : 1), SG, TF>(ad, bd, d_base, N, kx_b16, id1, id2, id3);
+            // tf32: passes A_hi B_hi, A_hi B_lo, A_lo B_hi
+#pragma unroll 1
+            for (int pass = 0; pass < kPasses; ++pass) {
+              const uint64_t ap = ad + (pass == 2 ? alo16 : 0u);
+              const uint64_t bp = bd + (pass == 1 ? blo16 : 0u);
+              if (R == SR) issue_kblock<SR, SG, TF>(ap, bp, d_base, N, kx_b16, id1, id2, id3);
+              else issue_kblock<(SR > 1 ? SR / 2 : 1), SG, TF>(ap, bp, d_base, N, kx_b16, id1, id2, id3);
+            }
           } else if (g == 3) {
             issue_kblock_r<3, TF>(R, ad, bd, d_base, N, kx_b16, id1, id2, id3, alo16, blo16);
           } else if (g == 2) {
@@ -926,13 +932,15 @@ cudaError_t launch_tc(const TcConvLaunch& L, cudaStream_t stream) {
 }
 
 #define OIDNX_PLAIN_SPECS(X) X(8, 3) X(4, 3) X(2, 3) X(2, 2) X(1, 2) X(1, 3)
+// (the fp32 kind's 8-row form spills: it keeps the run-time form)
+#define OIDNX_PLAIN32_SPECS(X) X(4, 3) X(2, 3) X(2, 2) X(1, 2) X(1, 3)
 #define OIDNX_SUB_SPECS(X) X(4, 4) X(2, 2)
 
 // The spec of a launch: its tile rows and the stacking factor, when every
 // walk step has those rows or half of them.
 int tc_spec(const TcConvLaunch& L) {
   const TcConvParams& p = L.p;
-  if (L.kind == kTcSubpixel) {
+  if (L.kind == kTcSubpixel || L.kind == kTcSubpixel32) {
     const int g4 = std::min(4, 256 / p.N);
     // (a split last wave runs the run-time form: dec_conv2a at 1080p, whose
     // split tiles took 54.9 us specialised against 53.0)
@@ -942,11 +950,15 @@ int tc_spec(const TcConvLaunch& L) {
 #undef X
     return kSpecAny;
   }
-  if (L.kind == kTcPlain) {
+  if (L.kind == kTcPlain || L.kind == kTcPlain32) {
     const int g = std::min(3, 256 / p.N);
     if (p.tail_split > 2) return kSpecAny;
 #define X(r, gg) if (p.R == r && g == gg) return spec_plain(r, gg);
-    OIDNX_PLAIN_SPECS(X)
+    if (L.kind == kTcPlain) {
+      OIDNX_PLAIN_SPECS(X)
+    } else {
+      OIDNX_PLAIN32_SPECS(X)
+    }
 #undef X
   }
   return kSpecAny;
@@ -957,10 +969,18 @@ int tc_spec(const TcConvLaunch& L) {
 cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
   const int spec = tc_spec(L);
   switch (L.kind) {
-    case kTcPlain32: return launch_tc<kTcPlain32, kSpecAny>(L, stream);
+    case kTcPlain32:
+#define X(r, g) if (spec == spec_plain(r, g)) return launch_tc<kTcPlain32, spec_plain(r, g)>(L, stream);
+      OIDNX_PLAIN32_SPECS(X)
+#undef X
+      return launch_tc<kTcPlain32, kSpecAny>(L, stream);
     case kTcExpand32: return launch_tc<kTcExpand32, kSpecAny>(L, stream);
     case kTcExpand: return launch_tc<kTcExpand, kSpecAny>(L, stream);
-    case kTcSubpixel32: return launch_tc<kTcSubpixel32, kSpecAny>(L, stream);
+    case kTcSubpixel32:
+#define X(r, g) if (spec == spec_sub(r, g)) return launch_tc<kTcSubpixel32, spec_sub(r, g)>(L, stream);
+      OIDNX_SUB_SPECS(X)
+#undef X
+      return launch_tc<kTcSubpixel32, kSpecAny>(L, stream);
     case kTcSubpixel:
 #define X(r, g) if (spec == spec_sub(r, g)) return launch_tc<kTcSubpixel, spec_sub(r, g)>(L, stream);
       OIDNX_SUB_SPECS(X)
@@ -987,6 +1007,12 @@ cudaError_t conv_tc_set_smem_limit(size_t bytes) {
       OIDNX_PLAIN_SPECS(X)
 #undef X
 #define X(r, g) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcSubpixel, spec_sub(r, g)>),
+      OIDNX_SUB_SPECS(X)
+#undef X
+#define X(r, g) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcPlain32, spec_plain(r, g)>),
+      OIDNX_PLAIN32_SPECS(X)
+#undef X
+#define X(r, g) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcSubpixel32, spec_sub(r, g)>),
       OIDNX_SUB_SPECS(X)
 #undef X
   };
