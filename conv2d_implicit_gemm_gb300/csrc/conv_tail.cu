@@ -308,12 +308,15 @@ __global__ void __launch_bounds__(kTailThreads, 1)
         const uint64_t bd = w1d + static_cast<uint32_t>(kb) * (kW1Block >> 4);
         // (not unrolled: the kernel's four warp roles run different code,
         // and a smaller MMA loop stays in the instruction cache)
+        if (st.r1 == kTailMid) {
 #pragma unroll 1
-        for (int kx = 0; kx < 3; ++kx) {
-          const uint64_t adk = ad + static_cast<uint32_t>(kx);
-          const uint64_t bdk = bd + static_cast<uint32_t>(kx * 6 * kMidC);
-          if (st.r1 == kTailMid) conv1_kx<kTailMid>(d1, adk, bdk, i1);
-          else conv1_kx<kTailMid - 2>(d1 + 2 * kSlot, adk, bdk, i1);
+          for (int kx = 0; kx < 3; ++kx)
+            conv1_kx<kTailMid>(d1, ad + static_cast<uint32_t>(kx), bd + static_cast<uint32_t>(kx * 6 * kMidC), i1);
+        } else {
+#pragma unroll 1
+          for (int kx = 0; kx < 3; ++kx)
+            conv1_kx<kTailMid - 2>(d1 + 2 * kSlot, ad + static_cast<uint32_t>(kx),
+                                   bd + static_cast<uint32_t>(kx * 6 * kMidC), i1);
         }
         if (elect_one()) mma_commit(&empty[s]);
         if (++s == static_cast<uint32_t>(S)) {
