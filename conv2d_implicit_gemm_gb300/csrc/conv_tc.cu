@@ -297,10 +297,11 @@ __device__ __forceinline__ void issue_subpixel_g(int g4, int R, bool up, uint64_
 // per (rows, grouping) pair: 0 = chosen at run time; 10 R + G = plain tiles
 // of R rows (R / 2 in a last wave split in two), G rows stacked per MMA;
 // 100 + 10 R + G = sub-pixel tiles of R rows (no split), G row classes
-// stacked.  (A smaller MMA loop is an instruction-cache matter: the 1080p
-// step went from 494 to 478 us.)
+// stacked.  Plain shapes also fix the epilogue mode: + 1000 (mode + 1).
+// (A smaller MMA loop is an instruction-cache matter: the 1080p step went
+// from 494 to 478 us.)
 constexpr int kSpecAny = 0;
-constexpr int spec_plain(int r, int g) { return 10 * r + g; }
+constexpr int spec_plain(int r, int g, int mode) { return 1000 * (mode + 1) + 10 * r + g; }
 constexpr int spec_sub(int r, int g) { return 100 + 10 * r + g; }
 
 template <int KIND, int SPEC>
@@ -320,6 +321,8 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
   constexpr bool TF = kind_tf32<KIND>();
   constexpr bool EXP = kind_expand<KIND>();
   constexpr bool HELP = kind_helpers<KIND>();
+  constexpr int SRG = SPEC % 1000;                         // the shape part of SPEC
+  constexpr int SMODE = SPEC >= 1000 ? SPEC / 1000 - 1 : -1;  // the epilogue mode, or -1
   // pipeline items per tile: K blocks, or (sub-pixel) upsampled K blocks plus
   // one item per (skip K block, kx)
   // sub-pixel: items are groups of up_pair upsampled K blocks (one TMA box
@@ -564,8 +567,8 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
                 for (int jj = 0; jj < nkb; ++jj) {
                   const uint64_t adj = ap + static_cast<uint32_t>(jj * 2 * kHaloW);
                   const uint64_t bdj = bp + static_cast<uint32_t>(jj) * (half >> 4);
-                  if constexpr (SPEC >= 100)
-                    issue_subpixel_spec<SPEC, TF>(true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
+                  if constexpr (SRG >= 100)
+                    issue_subpixel_spec<SRG, TF>(true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
                   else
                     issue_subpixel_g<TF>(g4, R, true, adj, bdj, d_base, N, tpx, 0, row16, id1, id2, id3, id4);
                 }
@@ -590,8 +593,8 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
             const uint32_t row16 = static_cast<uint32_t>(2 * kHaloW);
 #pragma unroll 1
             for (int pass = 0; pass < kPasses; ++pass) {
-              if constexpr (SPEC >= 100)
-                issue_subpixel_spec<SPEC, TF>(false, ad + (pass == 2 ? alo16 : 0u),
+              if constexpr (SRG >= 100)
+                issue_subpixel_spec<SRG, TF>(false, ad + (pass == 2 ? alo16 : 0u),
                                               bd + (pass == 1 ? blo_sk16 : 0u), d_base, N, tpx, pxb,
                                               row16, id1, id2, id3, id4);
               else
@@ -604,8 +607,8 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
           }
           const uint64_t ad = a_desc0 + ((s * p.a_stage) >> 4);
           const uint64_t bd = b_desc0 + ((static_cast<uint32_t>(p.resident ? kb : s) * p.b_stage) >> 4);
-          if constexpr (SPEC > 0 && SPEC < 100) {
-            constexpr int SR = SPEC / 10, SG = SPEC % 10;
+          if constexpr (SRG > 0 && SRG < 100) {
+            constexpr int SR = SRG / 10, SG = SRG % 10;
             // tf32: passes A_hi B_hi, A_hi B_lo, A_lo B_hi
 #pragma unroll 1
             for (int pass = 0; pass < kPasses; ++pass) {
@@ -747,7 +750,8 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
       const uint32_t tl = tmem + lane_off + buf * set_cols;
 
       // decoders (expansion, sub-pixel) always take the ReLU epilogue
-      if (EXP || SP || p.mode == kEpiRelu) {
+      const int mode = SMODE >= 0 ? SMODE : p.mode;
+      if (EXP || SP || mode == kEpiRelu) {
         __half* out = static_cast<__half*>(p.out);
         for (int c0 = 0; c0 < nc; c0 += 2) {
           const bool two = c0 + 1 < nc;
@@ -812,7 +816,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
             }
           }
         }
-      } else if (p.mode == kEpiReluPool) {
+      } else if (mode == kEpiReluPool) {
         __half* out = static_cast<__half*>(p.out);
         const int Wp = (p.W + 1) >> 1, Hp = (p.H + 1) >> 1;
         const int xp = x >> 1;
@@ -931,9 +935,12 @@ cudaError_t launch_tc(const TcConvLaunch& L, cudaStream_t stream) {
                     L.map1, L.p);
 }
 
-#define OIDNX_PLAIN_SPECS(X) X(8, 3) X(4, 3) X(2, 3) X(2, 2) X(1, 2) X(1, 3)
-// (the fp32 kind's 8-row form spills: it keeps the run-time form)
-#define OIDNX_PLAIN32_SPECS(X) X(4, 3) X(2, 3) X(2, 2) X(1, 2) X(1, 3)
+// (rows, stacking, epilogue mode); the fp32 kind's 8-row form spills, so it
+// keeps the run-time form
+#define OIDNX_PLAIN_SPECS(X) \
+  X(8, 3, 0) X(4, 3, 0) X(2, 3, 0) X(2, 2, 0) X(1, 2, 0) X(1, 3, 0) X(8, 3, 1) X(4, 3, 1) X(2, 3, 1)
+#define OIDNX_PLAIN32_SPECS(X) \
+  X(4, 3, 0) X(2, 3, 0) X(2, 2, 0) X(1, 2, 0) X(1, 3, 0) X(4, 3, 1) X(2, 3, 1)
 #define OIDNX_SUB_SPECS(X) X(4, 4) X(2, 2)
 
 // The spec of a launch: its tile rows and the stacking factor, when every
@@ -953,7 +960,7 @@ int tc_spec(const TcConvLaunch& L) {
   if (L.kind == kTcPlain || L.kind == kTcPlain32) {
     const int g = std::min(3, 256 / p.N);
     if (p.tail_split > 2) return kSpecAny;
-#define X(r, gg) if (p.R == r && g == gg) return spec_plain(r, gg);
+#define X(r, gg, m) if (p.R == r && g == gg && p.mode == m) return spec_plain(r, gg, m);
     if (L.kind == kTcPlain) {
       OIDNX_PLAIN_SPECS(X)
     } else {
@@ -970,7 +977,7 @@ cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
   const int spec = tc_spec(L);
   switch (L.kind) {
     case kTcPlain32:
-#define X(r, g) if (spec == spec_plain(r, g)) return launch_tc<kTcPlain32, spec_plain(r, g)>(L, stream);
+#define X(r, g, m) if (spec == spec_plain(r, g, m)) return launch_tc<kTcPlain32, spec_plain(r, g, m)>(L, stream);
       OIDNX_PLAIN32_SPECS(X)
 #undef X
       return launch_tc<kTcPlain32, kSpecAny>(L, stream);
@@ -987,7 +994,7 @@ cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
 #undef X
       return launch_tc<kTcSubpixel, kSpecAny>(L, stream);
     default:
-#define X(r, g) if (spec == spec_plain(r, g)) return launch_tc<kTcPlain, spec_plain(r, g)>(L, stream);
+#define X(r, g, m) if (spec == spec_plain(r, g, m)) return launch_tc<kTcPlain, spec_plain(r, g, m)>(L, stream);
       OIDNX_PLAIN_SPECS(X)
 #undef X
       return launch_tc<kTcPlain, kSpecAny>(L, stream);
@@ -1003,13 +1010,13 @@ cudaError_t conv_tc_set_smem_limit(size_t bytes) {
       reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcExpand32, kSpecAny>),
       reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcSubpixel32, kSpecAny>),
       reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcPlain, kSpecAny>),
-#define X(r, g) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcPlain, spec_plain(r, g)>),
+#define X(r, g, m) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcPlain, spec_plain(r, g, m)>),
       OIDNX_PLAIN_SPECS(X)
 #undef X
 #define X(r, g) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcSubpixel, spec_sub(r, g)>),
       OIDNX_SUB_SPECS(X)
 #undef X
-#define X(r, g) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcPlain32, spec_plain(r, g)>),
+#define X(r, g, m) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcPlain32, spec_plain(r, g, m)>),
       OIDNX_PLAIN32_SPECS(X)
 #undef X
 #define X(r, g) reinterpret_cast<const void*>(conv3x3_tc_kernel<kTcSubpixel32, spec_sub(r, g)>),
