@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(final_threads<TF>(), 1)
       mbar_arrive_expect_tx(wbar, kWBytes);
       bulk_load(Wsm, p.w, kWBytes, wbar);
       griddep_wait();
+      const uint64_t pol = p.l2_first ? l2_evict_first() : l2_evict_normal();
       uint32_t it = 0, s = 0, ph = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(final_threads<TF>(), 1)
           }
           mbar_arrive_expect_tx(&full[s], p.stage_tx);
           tma_load_4d(A + static_cast<size_t>(s) * p.stage_bytes, &map, &full[s], 0, bx >> p.xs, 2 * kb,
-                      y0 - 1);
+                      y0 - 1, pol);
           if (++s == static_cast<uint32_t>(S)) {
             s = 0;
             ph ^= 1u;

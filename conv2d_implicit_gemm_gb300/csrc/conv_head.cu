@@ -184,9 +184,12 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 #pragma unroll
         for (int b = 0; b < 3; ++b) {
           const int xf = 4 * (col0 + b * kHeadSubPx);
-          tma_load_2d(st + b * kHeadSubBox, &map0, &ifull[s], xf, row0);
-          if (SOURCES > 1) tma_load_2d(st + kHeadImgSlot + b * kHeadSubBox, &map1, &ifull[s], xf, row0);
-          if (SOURCES > 2) tma_load_2d(st + 2 * kHeadImgSlot + b * kHeadSubBox, &map2, &ifull[s], xf, row0);
+          // (one-tile frames only: the images read once, evict-first)
+          tma_load_2d(st + b * kHeadSubBox, &map0, &ifull[s], xf, row0, l2_evict_first());
+          if (SOURCES > 1)
+            tma_load_2d(st + kHeadImgSlot + b * kHeadSubBox, &map1, &ifull[s], xf, row0, l2_evict_first());
+          if (SOURCES > 2)
+            tma_load_2d(st + 2 * kHeadImgSlot + b * kHeadSubBox, &map2, &ifull[s], xf, row0, l2_evict_first());
         }
         if (++s == static_cast<uint32_t>(SI)) {
           s = 0;

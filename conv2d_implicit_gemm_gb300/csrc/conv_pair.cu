@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           }
           mbar_arrive_expect_tx(&full[s], p.stage_tx);
           tma_load_4d(IN + static_cast<size_t>(s) * p.stage_bytes, &map, &full[s], 0, bx >> p.xs, 0,
-                      g.ya - 2 + t0);
+                      g.ya - 2 + t0, l2_evict_first());  // (fused pairs: one-tile frames)
         }
       }
       for (uint32_t j = it > static_cast<uint32_t>(S) ? it - S : 0u; j < it; ++j)

@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(kTailThreads, 1)
       bulk_load(W2, p.w2, 2u * kW2Block, wbar);
       // weights and bias are constants; the input comes from the previous kernel
       griddep_wait();
+      const uint64_t pol = p.l2_first ? l2_evict_first() : l2_evict_normal();
       uint32_t it = 0, s = 0, ph = 0;
       bool ok = true;
       TailWalk w;
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kTailThreads, 1)
           }
           mbar_arrive_expect_tx(&full[s], all ? p.stage_tx : p.stage_tx8);
           tma_load_4d(A + static_cast<size_t>(s) * p.stage_bytes, all ? &map10 : &map8, &full[s], 0,
-                      bx >> p.xs, 2 * kb, st.y0 - 2);
+                      bx >> p.xs, 2 * kb, st.y0 - 2, pol);
           if (++s == static_cast<uint32_t>(S)) {
             s = 0;
             ph ^= 1u;

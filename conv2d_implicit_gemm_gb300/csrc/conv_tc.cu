@@ -405,6 +405,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
       // Weights and bias are constants; the activations come from the
       // previous kernel in the stream.
       griddep_wait();
+      const uint64_t pol = p.l2_first ? l2_evict_first() : l2_evict_normal();
       uint32_t it = 0, s = 0, ph = 0;  // item count, its stage and phase
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
               // pixel (up_pair K blocks; a box reaching past the last chunk
               // reads zeros there, and no MMA uses them)
               tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map0, &full[s], 0,
-                          ((x0 >> 1) - kGroupPx) >> p.xs0, 2 * p.up_pair * kb, (y0 >> 1) - 1);
+                          ((x0 >> 1) - kGroupPx) >> p.xs0, 2 * p.up_pair * kb, (y0 >> 1) - 1, pol);
               if (!p.resident)
                 bulk_load(B + static_cast<size_t>(s) * p.b_stage,
                           wsrc + static_cast<size_t>(kb) * p.b_tx + static_cast<size_t>(px) * half,
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
               const uint32_t wb = part ? p.b_tx2 : 2u * p.b_tx2;
               mbar_arrive_expect_tx(&full[s], p.st_tx + (p.resident ? 0u : wb));
               tma_load_5d(A + static_cast<size_t>(s) * p.a_stage, &map1, &full[s], 0, i0, plane,
-                          2 * j, y0 - 1);
+                          2 * j, y0 - 1, pol);
               if (!p.resident) {
                 const size_t kb_off = static_cast<size_t>(KB0) * p.b_tx + static_cast<size_t>(3 * j) * p.b_tx2;
                 if (part) {
@@ -462,13 +463,13 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
             // so 128-byte-row maps address it in 8-pixel units)
             if (low)
               tma_load_4d(ST + static_cast<size_t>(s) * p.st_stage, &map0, &full[s], 0,
-                          ((x0 >> 1) - kGroupPx) >> p.xs0, 2 * kb, (y0 >> 1) - 1);
+                          ((x0 >> 1) - kGroupPx) >> p.xs0, 2 * kb, (y0 >> 1) - 1, pol);
             else
               tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map0, &full[s], 0,
-                          (x0 - kGroupPx) >> p.xs0, 2 * kb, y0 - 1);
+                          (x0 - kGroupPx) >> p.xs0, 2 * kb, y0 - 1, pol);
           } else {
             tma_load_4d(A + static_cast<size_t>(s) * p.a_stage, &map1, &full[s], 0,
-                        (x0 - kGroupPx) >> p.xs1, 2 * (kb - KB0), y0 - 1);
+                        (x0 - kGroupPx) >> p.xs1, 2 * (kb - KB0), y0 - 1, pol);
           }
           if (!p.resident)
             bulk_load(B + static_cast<size_t>(s) * p.b_stage,

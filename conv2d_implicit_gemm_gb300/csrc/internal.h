@@ -80,6 +80,7 @@ struct TcConvParams {
   // short last wave spreads over more CTAs; walk_tiles counts the walk's
   // steps (tail_first = tiles, tail_split = 1: no split)
   int tail_first, tail_split, walk_tiles;
+  int l2_first;            // activation loads evict-first in L2 (one-tile frames)
 };
 
 enum TcKind : int {
@@ -169,6 +170,7 @@ struct FinalConvParams {
   float scale;
   const float4* exp2_tab;  // HDR: kExp2TabSize entries from fill_exp2_table
   int reverse;             // walk the tiles last to first
+  int l2_first;            // activation loads evict-first in L2 (one-tile frames)
 };
 
 struct FinalConvLaunch {
@@ -217,6 +219,7 @@ struct TailConvParams {
   int hdr;
   float scale;
   const float4* exp2_tab;
+  int l2_first;            // activation loads evict-first in L2 (one-tile frames)
 };
 
 struct TailConvLaunch {

@@ -1727,6 +1727,7 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
       LL.name = "dec_conv1b+dec_conv0";
       OIDNX_TRY(build_tail_launch(L, L2, ptr(d.src0), V.ext[d.src0], conv.w, conv.h, ptr(d2.dst),
                                   f->status, &LL.tlcl));
+      LL.tlcl.p.l2_first = 1;  // one image: evict-first activation loads
       LL.flop = 2.0 * 9.0 * (L.cin * L.cout + L2.cin * L2.cout) * px;
       LL.bytes = logical_bytes(d.src0) + static_cast<double>(V.ext[d2.dst].w) * V.ext[d2.dst].h * 16 +
                  static_cast<double>(L.weight_bytes + L2.weight_bytes);
@@ -1740,6 +1741,7 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
       OIDNX_TRY(build_final_launch(L, ptr(d.src0), V.ext[d.src0], conv.w, conv.h, ptr(d.dst),
                                    f->status, &LL.fcl));
       LL.fcl.p.reverse = walk_reverse(l);
+      LL.fcl.p.l2_first = 1;  // one image: evict-first activation loads
       LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
       LL.bytes = logical_bytes(d.src0) + static_cast<double>(V.ext[d.dst].w) * V.ext[d.dst].h * 16 +
                  static_cast<double>(L.weight_bytes);
@@ -1770,6 +1772,10 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
       LL.tcl.p.period = (stack_rows + kStackGap) >> d.level;
       LL.tcl.p.rows = stack_rows >> d.level;
     }
+    // Evict-first activation loads pay in one image, not in a stack of tiles,
+    // whose neighbouring tiles' shared halo rows they pushed out to DRAM
+    // (3840x2160 in 15 tiles: 3.25 ms with them, 2.86 without).
+    LL.tcl.p.l2_first = stack_rows ? 0 : 1;
     LL.tcl.p.reverse = walk_reverse(l);
     LL.flop = 2.0 * 9.0 * L.cin * L.cout * px;
     const Extent oe = V.ext[d.dst];

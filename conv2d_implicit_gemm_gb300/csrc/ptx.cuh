@@ -125,6 +125,11 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+__device__ __forceinline__ uint64_t l2_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 __device__ __forceinline__ float4 ld_global_hint(const float4* p, uint64_t pol) {
   float4 v;
   asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
@@ -143,52 +148,54 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// Tiled tensor loads into shared memory, completion on `bar` (tx bytes).
-// They carry the L2 evict-first policy: every activation map (and input
-// image) is read by one kernel only, so its lines should give way to the
-// lines that kernel writes for the next.  (The halo rows that neighbouring
-// tiles share are re-read soon after; measured in the 1080p step: enc_conv0
-// 36.6 -> 32.8 us, the others unchanged.)
+// Tiled tensor loads into shared memory, completion on `bar` (tx bytes),
+// with an L2 policy `pol`.  Every activation map (and input image) is read
+// by one kernel only; evict-first lets its lines give way to the lines that
+// kernel writes for the next one.  That pays in a one-tile 1080p frame
+// (enc_conv0 36.6 -> 32.8 us) but not in a stack of tiles, whose halo rows
+// shared by neighbouring tiles were then re-read from DRAM (3840x2160 in 15
+// tiles: 2.86 -> 3.25 ms): the kernels take the policy from their launch.
 //
 // 2-D.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(l2_evict_first())
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 
 // 3-D.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int c0, int c1, int c2) {
+                                            int c0, int c1, int c2, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
-      "l"(l2_evict_first())
+      "l"(pol)
       : "memory");
 }
 
 // 4-D.
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int c0, int c1, int c2, int c3) {
+                                            int c0, int c1, int c2, int c3, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-      "r"(smem_u32(bar)), "l"(l2_evict_first())
+      "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 
 // 5-D.
 __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int c0, int c1, int c2, int c3, int c4) {
+                                            int c0, int c1, int c2, int c3, int c4, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-      "r"(smem_u32(bar)), "l"(l2_evict_first())
+      "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 
