@@ -1160,7 +1160,33 @@ oidnx_status build_tc_launch(const DeviceLayer& L, int kind, const void* src0, E
   while (R > minR && R * N > 256) R /= 2;
   if (2 * R * N > 512) return fail(OIDNX_ERR_UNSUPPORTED, "accumulators exceed tensor memory");
   const int tiles_x = (W + kTileM - 1) / kTileM;
-  while (R > minR && static_cast<long>(tiles_x) * ((H + R - 1) / R) < num_sms()) R /= 2;
+  // Fewer tiles than SMs: the tile height that finishes first, by rounds of
+  // tiles x estimated cycles per tile (K blocks x (~600 cycles of per-item
+  // synchronisation + the MMAs of the cost model: max(45.7, N / 2, operand
+  // bytes / 128 B per clock) each)).  dec_conv4b at 1080p: 2 rows, one
+  // round of 136 tiles, not 1 row in two rounds (14.4 against 15.0 us).
+  if (static_cast<long>(tiles_x) * ((H + R - 1) / R) < num_sms()) {
+    auto mma = [](int n) { return std::max(45.7, std::max(n / 2.0, (4096.0 + 32.0 * n) / 128.0)); };
+    const int G = std::min(3, 256 / N);
+    double best = 0.0;
+    int best_r = R;
+    for (int r = R; r >= minR; r /= 2) {
+      double kx = 0.0;  // cycles of the MMAs of one kx over the halo rows
+      for (int h = 0; h < r + 2; ++h) {
+        const int lo = std::max(0, h - 2), hi = std::min(r - 1, h);
+        for (int c = lo; c <= hi; c += G) kx += mma(N * (std::min(hi, c + G - 1) - c + 1));
+      }
+      const long tiles = static_cast<long>(tiles_x) * ((H + r - 1) / r);
+      const double est = static_cast<double>((tiles + num_sms() - 1) / num_sms()) *
+                         (L.KB0 + L.KB1) * (600.0 + 3.0 * kx);
+      if (r == R || est < best) {
+        best = est;
+        best_r = r;
+      }
+      if (r == 1) break;
+    }
+    R = best_r;
+  }
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(2 * R * N)) tmem_cols *= 2;
 
