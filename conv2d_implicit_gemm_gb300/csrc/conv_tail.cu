@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kTailThreads, 1)
           for (int kx = 0; kx < 3; ++kx)
             conv1_kx<kTailMid>(d1, ad + static_cast<uint32_t>(kx), bd + static_cast<uint32_t>(kx * 6 * kMidC), i1);
         } else {
-#pragma unroll 1
+#pragma unroll
           for (int kx = 0; kx < 3; ++kx)
             conv1_kx<kTailMid - 2>(d1 + 2 * kSlot, ad + static_cast<uint32_t>(kx),
                                    bd + static_cast<uint32_t>(kx * 6 * kMidC), i1);
