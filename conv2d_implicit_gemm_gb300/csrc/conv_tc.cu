@@ -948,6 +948,7 @@ cudaError_t launch_tc(const TcConvLaunch& L, cudaStream_t stream) {
 // walk step has those rows or half of them.
 int tc_spec(const TcConvLaunch& L) {
   const TcConvParams& p = L.p;
+  if (L.any_shape) return kSpecAny;
   if (L.kind == kTcSubpixel || L.kind == kTcSubpixel32) {
     const int g4 = std::min(4, 256 / p.N);
     // (a split last wave runs the run-time form: dec_conv2a at 1080p, whose
@@ -973,6 +974,8 @@ int tc_spec(const TcConvLaunch& L) {
 }
 
 }  // namespace
+
+int conv_tc_shape(const TcConvLaunch& L) { return tc_spec(L); }
 
 cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream) {
   const int spec = tc_spec(L);

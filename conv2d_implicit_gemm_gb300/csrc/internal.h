@@ -277,6 +277,7 @@ struct TcConvLaunch {
   CUtensorMap map1;        // source 1 (full-res halo box, or stride-2 box); unused if KB1 == 0
   TcConvParams p;
   int kind;                // TcKind
+  int any_shape;           // 1: the run-time issue form even for a compile-time shape
   dim3 grid;
   size_t smem;
 };
@@ -301,6 +302,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 cudaError_t launch_conv_tc(const TcConvLaunch& L, cudaStream_t stream);
+// The compile-time shape the launch runs (0: the run-time issue form).
+int conv_tc_shape(const TcConvLaunch& L);
 cudaError_t conv_tc_set_smem_limit(size_t bytes);
 cudaError_t conv_tc_occupancy(size_t smem, int* blocks_per_sm);
 

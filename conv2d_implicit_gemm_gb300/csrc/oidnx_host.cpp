@@ -816,7 +816,8 @@ struct oidnx_filter {
   // parameters
   int width = 0, height = 0, hdr = 0, transfer = OIDNX_TRANSFER_LOG, max_tile = 0,
       overlap = -1, shape_cache = 2, keep_acts = 0, profile_always = 0, subpixel = 1,
-      fuse = 0, fuse_output = 1, fuse_tail = 1, fuse_input = 0, stack_tiles = 0;
+      fuse = 0, fuse_output = 1, fuse_tail = 1, fuse_input = 0, stack_tiles = 0,
+      shape_kernels = 1;
   float input_scale = 1.0f;
   void* img[4] = {};
   size_t img_stride[4] = {};
@@ -1794,6 +1795,7 @@ oidnx_status build_network_launches(const oidnx_filter* f, const ValueLayout& V,
     OIDNX_TRY(build_tc_launch(L, d.kind, ptr(d.src0), V.ext[d.src0], s1, e1, conv.w, conv.h,
                               ptr(d.dst), V.ext[d.dst].pitch, f->status, &LL.tcl, subpixel,
                               out_split, out_split_pitch));
+    LL.tcl.any_shape = f->shape_kernels ? 0 : 1;
     if (stack_rows) {
       LL.tcl.p.period = (stack_rows + kStackGap) >> d.level;
       LL.tcl.p.rows = stack_rows >> d.level;
@@ -2452,12 +2454,13 @@ oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value) 
     if (value < 0) return fail(OIDNX_ERR_INVALID_ARGUMENT, "stackTiles must be >= 0");
     f->stack_tiles = value;
   } else if (n == "keepActivations" || n == "subpixelDecoder" || n == "fuseLayers" ||
-             n == "fuseTail" || n == "fuseInput") {
+             n == "fuseTail" || n == "fuseInput" || n == "shapeKernels") {
     (n == "keepActivations"   ? f->keep_acts
      : n == "subpixelDecoder" ? f->subpixel
      : n == "fuseLayers"      ? f->fuse
      : n == "fuseTail"        ? f->fuse_tail
-                              : f->fuse_input) = value ? 1 : 0;
+     : n == "fuseInput"       ? f->fuse_input
+                              : f->shape_kernels) = value ? 1 : 0;
     for (auto& p : f->plans) f->retired.push_back(std::move(p));
     f->plans.clear();
     f->current = nullptr;
@@ -2490,6 +2493,7 @@ oidnx_status oidnx_filter_get_int(oidnx_filter* f, const char* name, int* value)
   else if (n == "fuseOutput") *value = f->fuse_output;
   else if (n == "fuseTail") *value = f->fuse_tail;
   else if (n == "fuseInput") *value = f->fuse_input;
+  else if (n == "shapeKernels") *value = f->shape_kernels;
   else if (n == "stackTiles") *value = f->stack_tiles;
   else if (n == "stackedTiles") *value = f->committed && f->current ? f->current->stack : 0;
   else if (n == "profile") *value = f->profile_always;
@@ -2772,13 +2776,15 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
   const Plan* plan = f->last_plan;
   std::string s = "{\"totalMs\":" + std::to_string(total) + ",\"layers\":[";
   bool first = true;
-  auto add = [&](const char* id, int idx, double flop, double bytes, double mma = 0) {
+  // shape: the compile-time shape of a conv3x3_tc launch (0: run-time form)
+  auto add = [&](const char* id, int idx, double flop, double bytes, double mma = 0, int shape = 0) {
     if (count[idx] == 0) return;
-    char buf[320];
+    char buf[352];
     snprintf(buf, sizeof(buf),
-             "%s{\"id\":\"%s\",\"ms\":%.6f,\"launches\":%d,\"flop\":%.0f,\"bytes\":%.0f,\"mmaFlop\":%.0f}",
+             "%s{\"id\":\"%s\",\"ms\":%.6f,\"launches\":%d,\"flop\":%.0f,\"bytes\":%.0f,\"mmaFlop\":%.0f,"
+             "\"shape\":%d}",
              first ? "" : ",", id, ms[idx], count[idx], flop * count[idx], bytes * count[idx],
-             mma * count[idx]);
+             mma * count[idx], shape);
     s += buf;
     first = false;
   };
@@ -2811,7 +2817,7 @@ oidnx_status oidnx_get_profile(oidnx_filter* f, char* json, size_t cap) {
       add(fused_out ? (L.tail ? "dec_conv1b+dec_conv0+output" : "dec_conv0+output") : L.name,
           L.layer + 2, L.flop,
           fused_out ? L.bytes - tile_px * 16 + out_bytes - out_px / tiles * 16 : L.bytes,
-          mma_flop(L));
+          mma_flop(L), L.pair || L.final || L.tail ? 0 : conv_tc_shape(L.tcl));
     }
   if (plan && plan->stack > 1 && !plan->final_tiles.empty()) {
     const LayerLaunch& L = plan->final_tiles[0];  // per tile, counted per launch

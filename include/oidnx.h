@@ -132,6 +132,12 @@ oidnx_status oidnx_filter_set_image(oidnx_filter* f, int which, void* device_ptr
  *   "fuseOutput"         1 = the output pass runs in the final conv's
  *                        epilogue (the network output is then not stored
  *                        unless "keepActivations" is 1); default 1
+ *   "shapeKernels"       1 = conv layers of the common tile shapes (rows per
+ *                        tile, rows stacked per MMA, epilogue) run kernels
+ *                        compiled for that shape (default); 0 = every conv
+ *                        runs the form that selects its issue sequence at
+ *                        run time.  Both issue the same MMAs in the same
+ *                        order, so the results are the same bits.
  *   "profile"            1 = record per-kernel events on every execute
  * Errors: INVALID_ARGUMENT for unknown names or out-of-range values.  */
 oidnx_status oidnx_filter_set_int(oidnx_filter* f, const char* name, int value);
