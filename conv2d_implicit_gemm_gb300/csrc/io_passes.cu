@@ -139,8 +139,9 @@ __global__ void pack_kernel(const PackParams p) {
   constexpr int kCh = 3 * SOURCES;
   float ch[kCh];
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  // the images are read once here (the output pass re-reads only the colour,
-  // at the end of the step)
+  // the images are read once per tile here (the output pass re-reads only the
+  // colour, at the end of the step; the overlaps of neighbouring tiles read
+  // the same rows again, measured no slower with this policy)
   const uint64_t pol = l2_evict_first();
   const float4 c = ld_global_hint(p.img[0] + static_cast<size_t>(iy) * p.stride[0] + ix, pol);
   const float4 a = SOURCES > 1 ? ld_global_hint(p.img[1] + static_cast<size_t>(iy) * p.stride[1] + ix, pol) : zero;
