@@ -927,8 +927,9 @@ __global__ void __launch_bounds__(kind_helpers<KIND>() ? kTcThreadsDecoder : kTc
 
 namespace {
 
-// The compile-time shapes instantiated for the fp16 kinds (the shapes of
-// the 1080p and 4K U-Net layers); other shapes run the run-time form.
+// The compile-time shapes instantiated for the plain and sub-pixel kinds,
+// fp16 and fp32 (the shapes of the 1080p and 4K U-Net layers); other
+// shapes, and the expansion kinds, run the run-time form.
 template <int KIND, int SPEC>
 cudaError_t launch_tc(const TcConvLaunch& L, cudaStream_t stream) {
   return launch_pdl(conv3x3_tc_kernel<KIND, SPEC>, L.grid,
@@ -944,8 +945,10 @@ cudaError_t launch_tc(const TcConvLaunch& L, cudaStream_t stream) {
   X(4, 3, 0) X(2, 3, 0) X(2, 2, 0) X(1, 2, 0) X(1, 3, 0) X(4, 3, 1) X(2, 3, 1)
 #define OIDNX_SUB_SPECS(X) X(4, 4) X(2, 2)
 
-// The spec of a launch: its tile rows and the stacking factor, when every
-// walk step has those rows or half of them.
+// The spec of a launch: its tile rows, stacking factor and (plain kinds)
+// epilogue mode, when every walk step has those rows (plain kinds: or half
+// of them); kSpecAny otherwise, or when the filter asks for the run-time
+// form ("shapeKernels" 0).
 int tc_spec(const TcConvLaunch& L) {
   const TcConvParams& p = L.p;
   if (L.any_shape) return kSpecAny;
